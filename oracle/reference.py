@@ -1,0 +1,292 @@
+"""fp64 numpy oracle of the causal video-VAE decoder hot path (test infrastructure only).
+
+Tensor conventions (the pages' channels-last video layout, NDHWC):
+  activations  [N, T, H, W, C]       bf16 bit patterns (uint16) at the boundary
+  conv weights [Cout, 3, 3, 3, Cin]  (kt, kh, kw) taps, bf16 bits
+  GN gamma/beta [C]                  fp32
+  conv bias    [Cout]                bf16 bits
+  3x3 weights  [Cout, 3, 3, Cin]     bf16 bits (the spatial conv of the upsampler)
+  phase weights [4, Cout, 2, 2, Cin] bf16 bits, phase p = 2a + b for output row parity a and
+                                     column parity b
+Inside each operation the oracle computes in fp64 and rounds once, directly from fp64 to bf16
+(round to nearest, ties to even), wherever the library writes a bf16 tensor.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = [
+    "round_to_bf16", "bf16_to_f64", "bf16_to_f32", "ulp_distance_bf16",
+    "silu_f64", "gn_silu_f64", "gn_silu",
+    "causal_conv3d_f64", "causal_conv3d", "conv_at_points_f64",
+    "resblock",
+    "phase_tap_sources", "phase_weights", "phase_weights_f64",
+    "phase_conv_f64", "phase_conv", "upsample_nearest_conv_f64", "upsample_nearest_conv",
+]
+
+_BF16_OVERFLOW = 2.0 ** 128  # |value| rounded to 2^128 or above is out of bf16 range
+
+
+def bf16_to_f64(bits) -> np.ndarray:
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    with np.errstate(invalid="ignore"):
+        return b.view(np.float32).astype(np.float64)
+
+
+def bf16_to_f32(bits) -> np.ndarray:
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return b.view(np.float32)
+
+
+def round_to_bf16(x) -> np.ndarray:
+    """fp64 -> bf16 bits with ONE rounding (nearest, ties to even), not via fp32.
+
+    bf16 keeps 8 significant bits and fp32's exponent range: a finite x = m 2^e (0.5 <= |m| < 1)
+    is rounded to a multiple of 2^(e-8), or of 2^-133 (the subnormal spacing) below 2^-126.
+    Results of magnitude 2^128 or more become infinities; NaN becomes the quiet NaN 0x7FC0."""
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)
+    step = np.maximum(e - 8, -133)
+    q = np.round(np.ldexp(x, -step))          # exact scaling by a power of two, then RNE
+    val = np.ldexp(q, step)
+    val = np.where(np.abs(val) >= _BF16_OVERFLOW, np.copysign(np.inf, x), val)
+    with np.errstate(over="ignore", invalid="ignore"):
+        f32 = val.astype(np.float32)            # exact: val has <= 8 significant bits
+    bits = (f32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
+    return np.where(np.isnan(x), np.uint16(0x7FC0), bits)
+
+
+def ulp_distance_bf16(a_bits, b_bits) -> np.ndarray:
+    """Distance in bf16 units in the last place between two bf16 bit arrays: both are mapped to
+    integers ordered like the reals (negative values mirrored, +0 and -0 equal)."""
+    def ordered(bits):
+        b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+        mag = b & 0x7FFF
+        return np.where(b & 0x8000, -mag, mag)
+    return np.abs(ordered(a_bits) - ordered(b_bits))
+
+
+# ----------------------------------------------------------------------------------------------
+# GroupNorm + SiLU  (WanGP group_norm_silu.py: module docstring, `_group_stats`, `_apply_kernel`)
+# ----------------------------------------------------------------------------------------------
+
+def silu_f64(z) -> np.ndarray:
+    """z * sigmoid(z) = z / (1 + e^-z); written as z e^z / (1 + e^z) for z < 0 so that e^-z
+    cannot overflow."""
+    z = np.asarray(z, dtype=np.float64)
+    ez = np.exp(-np.abs(z))
+    return np.where(z >= 0, z / (1.0 + ez), z * ez / (1.0 + ez))
+
+
+def gn_silu_f64(x, gamma, beta, groups: int, eps: float) -> np.ndarray:
+    """silu(group_norm(x)) in fp64, x float [N, T, H, W, C].
+
+    Statistics are taken per (n, t, group) over the group's C/groups channels of all H*W pixels
+    of one frame (the per-image GroupNorm of the pages applied to every frame). Two passes:
+    m = sum(x)/L, var = sum((x - m)^2)/L (population variance, divided by the length L as the
+    pages do), z = (x - m)/sqrt(var + eps) * gamma_c + beta_c, output silu(z)."""
+    x = np.asarray(x, dtype=np.float64)
+    N, T, H, W, C = x.shape
+    assert C % groups == 0
+    cg = C // groups
+    L = H * W * cg
+    xg = x.reshape(N, T, H * W, groups, cg)
+    mean = xg.sum(axis=(2, 4)) / L
+    d = xg - mean[:, :, None, :, None]
+    var = (d * d).sum(axis=(2, 4)) / L
+    rstd = 1.0 / np.sqrt(var + float(eps))
+    g = np.asarray(gamma, dtype=np.float64).reshape(groups, cg)
+    b = np.asarray(beta, dtype=np.float64).reshape(groups, cg)
+    z = d * rstd[:, :, None, :, None] * g + b
+    return silu_f64(z).reshape(N, T, H, W, C)
+
+
+def gn_silu(x_bits, gamma, beta, groups: int, eps: float) -> np.ndarray:
+    """bf16 in, bf16 out: silu(group_norm(x)) rounded once."""
+    return round_to_bf16(gn_silu_f64(bf16_to_f64(x_bits), gamma, beta, groups, eps))
+
+
+# ----------------------------------------------------------------------------------------------
+# Causal 3x3x3 convolution with the carried temporal cache  (binding.cpp, `Decoder::conv`)
+# ----------------------------------------------------------------------------------------------
+
+def _padded_input(a, cache):
+    """P = [cache (2 frames, zeros if absent); a] along T, zero-padded by one pixel in H and W."""
+    N, T, H, W, C = a.shape
+    if cache is None:
+        cache = np.zeros((N, 2, H, W, C), dtype=np.float64)
+    p = np.concatenate([cache, a], axis=1)
+    return np.pad(p, ((0, 0), (0, 0), (1, 1), (1, 1), (0, 0)))
+
+
+def causal_conv3d_f64(a, w, bias=None, residual=None, cache=None) -> np.ndarray:
+    """y[n,t,h,w,co] = bias[co] + residual[n,t,h,w,co]
+                      + sum_{kt,kh,kw,ci} w[co,kt,kh,kw,ci] * P[n, t+kt, h+kh, w+kw, ci]
+    with P from `_padded_input`: tap kt = 0 meets frame t-2 of the sequence, kt = 2 frame t
+    (the conv of the front-padded input, as the decoder pads two history frames in front)."""
+    a = np.asarray(a, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    N, T, H, W, _ = a.shape
+    Co = w.shape[0]
+    P = _padded_input(a, None if cache is None else np.asarray(cache, dtype=np.float64))
+    y = np.zeros((N, T, H, W, Co), dtype=np.float64)
+    for kt in range(3):
+        for kh in range(3):
+            for kw in range(3):
+                win = P[:, kt:kt + T, kh:kh + H, kw:kw + W, :]
+                y += win @ w[:, kt, kh, kw, :].T
+    if bias is not None:
+        y += np.asarray(bias, dtype=np.float64)
+    if residual is not None:
+        y += np.asarray(residual, dtype=np.float64)
+    return y
+
+
+def causal_conv3d(a_bits, w_bits, bias_bits=None, residual_bits=None, cache_bits=None):
+    """bf16 causal conv: returns (y bits rounded once, cache_out bits).
+
+    cache_out holds the last two frames of [cache_in; a] (the conv's padded input history that
+    the next chunk continues from), bit-for-bit copies."""
+    a = bf16_to_f64(a_bits)
+    cache = None if cache_bits is None else bf16_to_f64(cache_bits)
+    y = causal_conv3d_f64(a, bf16_to_f64(w_bits),
+                          None if bias_bits is None else bf16_to_f64(bias_bits),
+                          None if residual_bits is None else bf16_to_f64(residual_bits),
+                          cache)
+    N, T, H, W, C = np.asarray(a_bits).shape
+    prev = np.zeros((N, 2, H, W, C), np.uint16) if cache_bits is None else np.asarray(cache_bits)
+    cache_out = np.concatenate([prev, np.asarray(a_bits, dtype=np.uint16)], axis=1)[:, -2:]
+    return round_to_bf16(y), np.ascontiguousarray(cache_out)
+
+
+def conv_at_points_f64(patches, w, bias=None, residual=None) -> np.ndarray:
+    """The same sum at isolated output points: patches [P, 3, 3, 3, Cin] are the padded-input
+    neighbourhoods P[t:t+3, h:h+3, w:w+3] of each point; returns [P, Cout] in fp64."""
+    patches = np.asarray(patches, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    y = patches.reshape(patches.shape[0], -1) @ w.reshape(w.shape[0], -1).T
+    if bias is not None:
+        y += np.asarray(bias, dtype=np.float64)
+    if residual is not None:
+        y += np.asarray(residual, dtype=np.float64)
+    return y
+
+
+# ----------------------------------------------------------------------------------------------
+# Causal ResBlock  (binding.cpp, `Decoder::resnet`)
+# ----------------------------------------------------------------------------------------------
+
+def resblock(x_bits, p: dict, groups: int, eps: float, cache1=None, cache2=None):
+    """out = conv2(silu(gn2(h))) + x with h = conv1(silu(gn1(x))); each conv carries its own
+    cache of its activated input. Every tensor the library writes in bf16 (the two activations,
+    h and out) is rounded once here too. Returns (out, cache1_out, cache2_out)."""
+    a1 = gn_silu(x_bits, p["gamma1"], p["beta1"], groups, eps)
+    h, c1 = causal_conv3d(a1, p["w1"], p["b1"], None, cache1)
+    a2 = gn_silu(h, p["gamma2"], p["beta2"], groups, eps)
+    out, c2 = causal_conv3d(a2, p["w2"], p["b2"], x_bits, cache2)
+    return out, c1, c2
+
+
+# ----------------------------------------------------------------------------------------------
+# Nearest-x2 + 3x3 as four 2x2 phase convolutions  (binding.cpp, `prepare()` phase transform,
+# and `Decoder::up` / resample_upsample)
+# ----------------------------------------------------------------------------------------------
+
+def phase_tap_sources(a: int, u: int) -> list:
+    """The 3x3 kernel rows r that land on low-resolution offset u of output parity a.
+
+    Output row 2i + a of the nearest-x2 image reads high-resolution row 2i + a + r - 1, which is
+    low-resolution row i + floor((a + r - 1)/2) (the pages write the floor as -1 for a negative
+    dy and dy/2 otherwise). Tap u of phase a sits at low-resolution offset u + a - 1, so it
+    collects the rows r with floor((a + r - 1)/2) == u + a - 1. Columns follow the same rule."""
+    out = []
+    for r in range(3):
+        dy = a + r - 1
+        iy = -1 if dy < 0 else dy // 2
+        if iy == u + a - 1:
+            out.append(r)
+    return out
+
+
+def phase_weights(w3_bits) -> np.ndarray:
+    """[Cout, 3, 3, Cin] bf16 -> [4, Cout, 2, 2, Cin] bf16: each phase tap is the fp32 sum of its
+    source taps, added in the order the pages loop (r outer, c inner, starting from zero), then
+    rounded once to bf16."""
+    w = bf16_to_f32(w3_bits)
+    Co, _, _, Ci = w.shape
+    out = np.zeros((4, Co, 2, 2, Ci), dtype=np.float32)
+    for a in range(2):
+        for b in range(2):
+            for u in range(2):
+                for v in range(2):
+                    s = np.zeros((Co, Ci), dtype=np.float32)
+                    for r in phase_tap_sources(a, u):
+                        for c in phase_tap_sources(b, v):
+                            s = (s + w[:, r, c, :]).astype(np.float32)
+                    out[2 * a + b, :, u, v, :] = s
+    return round_to_bf16(out.astype(np.float64))
+
+
+def phase_weights_f64(w3) -> np.ndarray:
+    """The same transform with exact (fp64) sums, for the fp64 identity with the definition."""
+    w = np.asarray(w3, dtype=np.float64)
+    Co, _, _, Ci = w.shape
+    out = np.zeros((4, Co, 2, 2, Ci), dtype=np.float64)
+    for a in range(2):
+        for b in range(2):
+            for u in range(2):
+                for v in range(2):
+                    for r in phase_tap_sources(a, u):
+                        for c in phase_tap_sources(b, v):
+                            out[2 * a + b, :, u, v, :] += w[:, r, c, :]
+    return out
+
+
+def phase_conv_f64(x, wp, bias=None) -> np.ndarray:
+    """y[n, t, 2i+a, 2j+b, co] = bias[co] + sum_{u,v,ci} wp[2a+b, co, u, v, ci]
+                                  * x[n, t, i+a-1+u, j+b-1+v, ci]   (x zero outside the frame)."""
+    x = np.asarray(x, dtype=np.float64)
+    wp = np.asarray(wp, dtype=np.float64)
+    N, T, H, W, _ = x.shape
+    Co = wp.shape[1]
+    xp = np.pad(x, ((0, 0), (0, 0), (1, 1), (1, 1), (0, 0)))
+    y = np.zeros((N, T, 2 * H, 2 * W, Co), dtype=np.float64)
+    for a in range(2):
+        for b in range(2):
+            acc = np.zeros((N, T, H, W, Co), dtype=np.float64)
+            for u in range(2):
+                for v in range(2):
+                    # padded index (i + a - 1 + u) + 1
+                    win = xp[:, :, a + u:a + u + H, b + v:b + v + W, :]
+                    acc += win @ wp[2 * a + b, :, u, v, :].T
+            y[:, :, a::2, b::2, :] = acc
+    if bias is not None:
+        y += np.asarray(bias, dtype=np.float64)
+    return y
+
+
+def phase_conv(x_bits, wp_bits, bias_bits=None) -> np.ndarray:
+    return round_to_bf16(phase_conv_f64(bf16_to_f64(x_bits), bf16_to_f64(wp_bits),
+                                        None if bias_bits is None else bf16_to_f64(bias_bits)))
+
+
+def upsample_nearest_conv_f64(x, w3, bias=None) -> np.ndarray:
+    """The definition: nearest-neighbour x2 in H and W, then a 3x3 convolution, zero padding 1."""
+    x = np.asarray(x, dtype=np.float64)
+    w3 = np.asarray(w3, dtype=np.float64)
+    N, T, H, W, _ = x.shape
+    Co = w3.shape[0]
+    x2 = np.repeat(np.repeat(x, 2, axis=2), 2, axis=3)
+    xp = np.pad(x2, ((0, 0), (0, 0), (1, 1), (1, 1), (0, 0)))
+    y = np.zeros((N, T, 2 * H, 2 * W, Co), dtype=np.float64)
+    for r in range(3):
+        for c in range(3):
+            y += xp[:, :, r:r + 2 * H, c:c + 2 * W, :] @ w3[:, r, c, :].T
+    if bias is not None:
+        y += np.asarray(bias, dtype=np.float64)
+    return y
+
+
+def upsample_nearest_conv(x_bits, w3_bits, bias_bits=None) -> np.ndarray:
+    return round_to_bf16(upsample_nearest_conv_f64(bf16_to_f64(x_bits), bf16_to_f64(w3_bits),
+                                                   None if bias_bits is None else bf16_to_f64(bias_bits)))
