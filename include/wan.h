@@ -1,0 +1,196 @@
+/*
+ * wan.h - C ABI of the GB300 (sm_103a) causal video-VAE decoder hot path.
+ *
+ * What the library computes, and where the method is stated:
+ *   - GroupNorm + SiLU with FP32 arithmetic and one rounding to bf16:
+ *     WanGP, shared/kernels/group_norm_silu.py (module docstring; `_apply_kernel`).
+ *   - The causal 3x3x3 convolution whose two leading frames come from a carried temporal
+ *     cache, the cache update, bias and residual:
+ *     FastVideo, wan22_vae_decode/solution/binding.cpp (`Decoder::conv`, `Decoder::resnet`).
+ *   - Nearest-x2 + 3x3 convolution as four 2x2 phase convolutions, and the phase-weight
+ *     transform: binding.cpp (`prepare()`, `Decoder::up`).
+ *
+ * Conventions shared by every entry point
+ *   - bf16 tensors are passed as `wan_bf16*` (16-bit patterns of bfloat16 values) and are
+ *     channels-last video tensors [N, T, H, W, C] (NDHWC), dense, C innermost.
+ *   - Every pointer is a DEVICE pointer, owned by the caller, 16-byte aligned (else
+ *     WAN_ERR_MISALIGNED). The library allocates no device memory: scratch comes from the
+ *     caller's workspace `ws` of `ws_bytes` bytes (query the size with wan_workspace_size;
+ *     too small -> WAN_ERR_WORKSPACE). Inputs are only read; outputs must not overlap inputs
+ *     unless an argument says otherwise.
+ *   - `stream` is a cudaStream_t (0 = the legacy default stream). Work is enqueued
+ *     asynchronously on it; the call returns once the work is enqueued.
+ *   - Arguments are validated on the host before anything is enqueued: a call that returns an
+ *     error status has launched nothing and written nothing. A launch failure returns
+ *     WAN_ERR_CUDA. Faults that happen later on the device surface at the caller's next
+ *     synchronisation; kernels that give up a bounded wait record WAN_ERR_TIMEOUT in a device
+ *     word read by wan_device_status().
+ *   - Results are deterministic: the same inputs on the same GPU give the same bits, whatever
+ *     the chunking of the frame axis (see wan_causal_conv3d).
+ */
+#ifndef WAN_H
+#define WAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t wan_bf16;
+
+typedef enum wan_status {
+  WAN_OK = 0,
+  WAN_ERR_INVALID_ARG = 1,       /* null pointer, non-positive size, groups not dividing C ... */
+  WAN_ERR_UNSUPPORTED_SHAPE = 2, /* a size this build has no kernel for (see each call) */
+  WAN_ERR_MISALIGNED = 3,        /* a pointer is not 16-byte aligned */
+  WAN_ERR_WORKSPACE = 4,         /* ws is NULL or ws_bytes below wan_workspace_size() */
+  WAN_ERR_CUDA = 5,              /* a CUDA runtime call or kernel launch failed */
+  WAN_ERR_TIMEOUT = 6            /* a kernel gave up a bounded wait (wan_device_status) */
+} wan_status;
+
+typedef enum wan_op {
+  WAN_OP_GN_SILU = 0,
+  WAN_OP_CAUSAL_CONV3D = 1,
+  WAN_OP_RESBLOCK = 2,
+  WAN_OP_UPSAMPLE_PHASE_CONV = 3
+} wan_op;
+
+/* Human-readable name of a status (static storage, never NULL). */
+const char* wan_status_string(wan_status status);
+
+/* Bytes of workspace `ws` the call `op` needs for these sizes (0 if it needs none).
+ * Arguments that an op does not use are ignored (e.g. Cout and groups for the conv). */
+size_t wan_workspace_size(wan_op op, int N, int T, int H, int W, int Cin, int Cout, int groups);
+
+/*
+ * y = silu(group_norm(x)), rounded once to bf16.
+ *
+ * Source: WanGP group_norm_silu.py (module docstring, `_group_stats`, `_apply_kernel`).
+ * Statistics are per (n, t, group): each frame of the video is normalised as the pages'
+ * NCHW image, over its C/groups channels of all H*W pixels; mean and POPULATION variance
+ * (divided by the element count), eps inside the square root:
+ *     z = (x - mean) / sqrt(var + eps) * gamma[c] + beta[c],   y = z * sigmoid(z).
+ * The statistics are accumulated with error-free (two-sum) fp32 partials per pixel span and
+ * merged in a fixed order, so they stay exact however large the mean is against the spread.
+ *
+ *   x, y         [N, T, H, W, C] bf16, device; y may not overlap x.
+ *   gamma, beta  [C] fp32, device.
+ *   groups       divides C; C % 8 == 0; C/8 <= 1024; (C/groups) % 8 == 0 or 8 % (C/groups) == 0.
+ *   eps          > 0.
+ *   ws           >= wan_workspace_size(WAN_OP_GN_SILU, N, T, H, W, C, 0, groups) bytes.
+ * Values are supported for |x| < 2^60 (the squares of deviations stay finite in fp32).
+ */
+wan_status wan_gn_silu(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta,
+                       int N, int T, int H, int W, int C, int groups, float eps,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Causal 3x3x3 convolution with a carried two-frame temporal cache (implicit GEMM on the
+ * tcgen05 tensor cores, bf16 operands, fp32 accumulation, one rounding to bf16).
+ *
+ * Source: binding.cpp, `Decoder::conv` (the padded input is the cache frames followed by the
+ * chunk; the cache then keeps the last two frames of that padded input) and `Decoder::resnet`.
+ *     P = [cache_in (2 frames, or zeros if cache_in == NULL); a]   along T, per batch item,
+ *     y[n,t,h,w,co] = bias[co] + residual[n,t,h,w,co]
+ *                   + sum_{kt,kh,kw,ci} w[co,kt,kh,kw,ci] * P[n, t+kt, h+kh-1, w+kw-1, ci]
+ * with P zero outside the frame in H and W (padding 1). Tap kt = 2 is the current frame.
+ * cache_out (if not NULL) receives the last two frames of P, bit-for-bit: calling this on
+ * consecutive chunks of a video with cache_out of one call passed as cache_in of the next
+ * gives the same bits as one call on the whole video.
+ *
+ *   a          [N, T, H, W, Cin] bf16.
+ *   cache_in   [N, 2, H, W, Cin] bf16 or NULL (zero history: the first chunk).
+ *   cache_out  [N, 2, H, W, Cin] bf16 or NULL; MAY alias cache_in (updated after the conv
+ *              has read it); must not overlap a or y.
+ *   w          [Cout, 3, 3, 3, Cin] bf16 (taps kt, kh, kw; Cin innermost).
+ *   bias       [Cout] bf16 or NULL.   residual  [N, T, H, W, Cout] bf16 or NULL (may not
+ *              overlap y).
+ *   y          [N, T, H, W, Cout] bf16.
+ *   Cin % 64 == 0; 1 <= Cout; Cout % 2 == 0.
+ *   ws         unused by this build (wan_workspace_size returns 0); may be NULL.
+ */
+wan_status wan_causal_conv3d(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out,
+                             const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual,
+                             wan_bf16* y, int N, int T, int H, int W, int Cin, int Cout,
+                             void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Phase-weight transform of the nearest-x2 upsampler.
+ *
+ * Source: binding.cpp, `prepare()` (nearest-x2 + 3x3 equals four 2x2 low-resolution phases;
+ * sums formed in fp32, stored in bf16). For output parity (a, b), phase p = 2a + b, and phase
+ * tap (u, v):
+ *     wp[p, co, u, v, ci] = bf16( sum over r in R(a,u), c in R(b,v) of fp32(w3[co, r, c, ci]) )
+ * where R(a, u) = { r in 0..2 : floor((a + r - 1) / 2) == u + a - 1 }, added in the order r
+ * outer, c inner, starting from zero, rounded once to nearest even.
+ *
+ *   w3  [Cout, 3, 3, Cin] bf16.    wp  [4, Cout, 2, 2, Cin] bf16 (may not overlap w3).
+ */
+wan_status wan_upsample_phase_weights(const wan_bf16* w3, wan_bf16* wp, int Cin, int Cout,
+                                      void* stream);
+
+/*
+ * Nearest-x2 spatial upsample followed by a 3x3 convolution (padding 1), executed as four 2x2
+ * phase convolutions on the low-resolution input, written interleaved into the output.
+ *
+ * Source: binding.cpp, `Decoder::up` (the four phase convolutions of the resampler) with the
+ * weights of wan_upsample_phase_weights:
+ *     y[n, t, 2i+a, 2j+b, co] = bias[co]
+ *         + sum_{u,v,ci} wp[2a+b, co, u, v, ci] * x[n, t, i+a-1+u, j+b-1+v, ci]
+ * with x zero outside the frame. bf16 operands, fp32 accumulation, one rounding.
+ *
+ *   x     [N, T, H, W, Cin] bf16.       wp  [4, Cout, 2, 2, Cin] bf16.
+ *   bias  [Cout] bf16 or NULL.          y   [N, T, 2H, 2W, Cout] bf16.
+ *   Cin % 64 == 0; Cout % 2 == 0.
+ */
+wan_status wan_upsample_phase_conv(const wan_bf16* x, const wan_bf16* wp, const wan_bf16* bias,
+                                   wan_bf16* y, int N, int T, int H, int W, int Cin, int Cout,
+                                   void* stream);
+
+/* Parameters of one causal ResBlock (C -> C). All device pointers. */
+typedef struct wan_resblock_params {
+  const float* gamma1;   /* [C] fp32, GroupNorm 1 scale */
+  const float* beta1;    /* [C] fp32, GroupNorm 1 shift */
+  const wan_bf16* w1;    /* [C, 3, 3, 3, C] bf16, conv 1 */
+  const wan_bf16* b1;    /* [C] bf16 or NULL */
+  const float* gamma2;   /* [C] fp32 */
+  const float* beta2;    /* [C] fp32 */
+  const wan_bf16* w2;    /* [C, 3, 3, 3, C] bf16, conv 2 */
+  const wan_bf16* b2;    /* [C] bf16 or NULL */
+  int groups;            /* GroupNorm groups, divides C */
+  float eps;             /* GroupNorm eps, > 0 */
+} wan_resblock_params;
+
+/*
+ * One causal ResBlock on one chunk of frames:
+ *     a1 = silu(gn1(x));  h = conv1(a1; cache1) + b1;
+ *     a2 = silu(gn2(h));  out = conv2(a2; cache2) + b2 + x
+ * Source: binding.cpp, `Decoder::resnet` (residual x, each conv with its own cache of its
+ * activated input). a1, h and a2 are rounded to bf16 as the standalone calls round them.
+ *
+ *   x, out       [N, T, H, W, C] bf16; out may not overlap x.
+ *   cache1/2     [N, 2, H, W, C] bf16, in/out (the history of conv 1 / conv 2's input).
+ *   cache_valid  0: the caches' contents are ignored (zero history, the first chunk) and
+ *                overwritten; 1: they hold the history left by the previous chunk.
+ *   C % 64 == 0 and the GroupNorm conditions of wan_gn_silu.
+ *   ws           >= wan_workspace_size(WAN_OP_RESBLOCK, N, T, H, W, C, C, groups) bytes.
+ */
+wan_status wan_resblock(const wan_bf16* x, wan_bf16* out, const wan_resblock_params* p,
+                        wan_bf16* cache1, wan_bf16* cache2, int cache_valid,
+                        int N, int T, int H, int W, int C, void* ws, size_t ws_bytes,
+                        void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device error word on the
+ * current device. Returns WAN_ERR_TIMEOUT if a kernel gave up a bounded wait since the last
+ * call, WAN_ERR_CUDA if the synchronisation failed, else WAN_OK.
+ */
+wan_status wan_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WAN_H */

@@ -1,0 +1,103 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every entry point
+include/wan.h declares, and rejects invalid arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "wan.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(wan_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from video_vae_decoder_gb300 import build, binding
+    build.build()
+    return binding.lib()
+
+
+def test_exports_every_declared_symbol(L):
+    syms = declared_symbols()
+    assert "wan_resblock" in syms and "wan_gn_silu" in syms
+    for s in syms:
+        assert hasattr(L, s), f"{s} declared in wan.h but not exported"
+    from video_vae_decoder_gb300 import binding
+    assert set(binding.EXPORTS) == set(syms)
+
+
+def test_status_strings(L):
+    from video_vae_decoder_gb300 import binding
+    for code, name in binding.STATUS.items():
+        assert binding.wan_status_string(code).startswith(name)
+    assert binding.wan_status_string(99) == "WAN_ERR_UNKNOWN"
+
+
+def test_workspace_sizes(L):
+    from video_vae_decoder_gb300 import binding as b
+    assert b.wan_workspace_size(b.WAN_OP_CAUSAL_CONV3D, 1, 4, 8, 8, 64, 64) == 0
+    gn = b.wan_workspace_size(b.WAN_OP_GN_SILU, 1, 4, 88, 156, 512, 0, 32)
+    assert gn >= 4 * 512 * 16  # per-frame per-channel coefficients at least
+    rb = b.wan_workspace_size(b.WAN_OP_RESBLOCK, 1, 4, 16, 16, 64, 64, 32)
+    assert rb >= 2 * 4 * 16 * 16 * 64 * 2
+    assert b.wan_workspace_size(b.WAN_OP_GN_SILU, 1, 4, 8, 8, 60, 0, 32) == 0   # groups do not divide C
+
+
+# Fake, never-dereferenced device addresses: every call below must be rejected on the host.
+A = 1 << 20          # 16-byte aligned
+MIS = (1 << 20) + 2  # misaligned
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers are only passed where no GPU exists")
+def test_gn_rejects_invalid(L):
+    f = L.wan_gn_silu
+    args = dict(x=A, y=A * 3, g=A * 5, b=A * 7, N=1, T=2, H=4, W=4, C=64, G=32, eps=1e-6)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(a["x"], a["y"], a["g"], a["b"], a["N"], a["T"], a["H"], a["W"], a["C"], a["G"],
+                 ctypes.c_float(a["eps"]), A * 9, 1 << 30, None)
+    assert call(x=None) == 1
+    assert call(T=0) == 1
+    assert call(G=24) == 1            # does not divide 64
+    assert call(C=60, G=4) == 2       # C % 8 != 0
+    assert call(eps=0.0) == 1
+    assert call(x=MIS) == 3
+    assert call(y=A) == 1             # y overlaps x
+    assert f(A, A * 3, A * 5, A * 7, 1, 2, 4, 4, 64, 32, ctypes.c_float(1e-6), A * 9, 8, None) == 4
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers are only passed where no GPU exists")
+def test_conv_rejects_invalid(L):
+    f = L.wan_causal_conv3d
+    ok = (A, None, None, A * 5, None, None, A * 9)
+    assert f(*ok, 1, 2, 4, 4, 48, 64, None, 0, None) == 2      # Cin % 64 != 0
+    assert f(*ok, 1, 2, 4, 4, 64, 63, None, 0, None) == 2      # odd Cout
+    assert f(*ok, 1, 0, 4, 4, 64, 64, None, 0, None) == 1      # T = 0
+    assert f(None, None, None, A * 5, None, None, A * 9, 1, 2, 4, 4, 64, 64, None, 0, None) == 1
+    assert f(MIS, None, None, A * 5, None, None, A * 9, 1, 2, 4, 4, 64, 64, None, 0, None) == 3
+    # y overlapping a
+    assert f(A, None, None, A * 5, None, None, A + 64, 1, 2, 4, 4, 64, 64, None, 0, None) == 1
+    # cache_out overlapping a
+    assert f(A, None, A + 128, A * 5, None, None, A * 9, 1, 2, 4, 4, 64, 64, None, 0, None) == 1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers are only passed where no GPU exists")
+def test_resblock_and_upsample_reject_invalid(L):
+    from video_vae_decoder_gb300.binding import ResblockParams
+    p = ResblockParams(A * 2, A * 3, A * 4, None, A * 5, A * 6, A * 7, None, 32, 1e-6)
+    f = L.wan_resblock
+    assert f(A, A * 40, None, A * 50, A * 60, 0, 1, 2, 4, 4, 64, A * 70, 1 << 30, None) == 1   # no params
+    assert f(A, A * 40, ctypes.byref(p), A * 50, A * 50, 0, 1, 2, 4, 4, 64, A * 70, 1 << 30, None) == 1  # caches alias
+    assert f(A, A * 40, ctypes.byref(p), A * 50, A * 60, 0, 1, 2, 4, 4, 64, A * 70, 16, None) == 4      # workspace
+    p.groups = 48
+    assert f(A, A * 40, ctypes.byref(p), A * 50, A * 60, 0, 1, 2, 4, 4, 64, A * 70, 1 << 30, None) == 1
+    assert L.wan_upsample_phase_weights(None, A, 64, 64, None) == 1
+    assert L.wan_upsample_phase_weights(MIS, A * 8, 64, 64, None) == 3
+    assert L.wan_upsample_phase_conv(A, A * 3, None, A * 9, 1, 1, 4, 4, 32, 64, None) == 2

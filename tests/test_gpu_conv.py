@@ -1,0 +1,97 @@
+"""Causal 3x3x3 convolution on the GPU against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from util import to_dev, bits, conv_close, padded, sample_points
+from video_vae_decoder_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def make(shape, Cout, name, bias=True, residual=False, cache=False, seed=0):
+    N, T, H, W, Cin = shape
+    a = synth.normal_bf16(shape, seed, f"{name}/a")
+    w = synth.normal_bf16((Cout, 3, 3, 3, Cin), seed, f"{name}/w", 0.0, float(np.sqrt(1.0 / (27 * Cin))))
+    b = synth.normal_bf16((Cout,), seed, f"{name}/b", 0.0, 0.01) if bias else None
+    r = synth.normal_bf16((N, T, H, W, Cout), seed, f"{name}/r") if residual else None
+    c = synth.normal_bf16((N, 2, H, W, Cin), seed, f"{name}/c") if cache else None
+    return a, w, b, r, c
+
+
+def run(wan, a, w, b, r, c, with_cache_out=True):
+    N, T, H, W, Cin = a.shape
+    cout = torch.empty((N, 2, H, W, Cin), dtype=torch.bfloat16, device="cuda") if with_cache_out else None
+    y = wan.wan_causal_conv3d(to_dev(a), to_dev(w), None if b is None else to_dev(b),
+                              None if r is None else to_dev(r), None if c is None else to_dev(c), cout)
+    torch.cuda.synchronize()
+    assert wan.wan_device_status() == 0
+    return bits(y), (bits(cout) if with_cache_out else None)
+
+
+@pytest.mark.parametrize("shape,Cout,bias,residual,cache", [
+    ((1, 3, 16, 16, 64), 64, True, False, False),     # the tiny ResBlock's conv
+    ((1, 3, 16, 16, 64), 64, True, True, True),
+    ((1, 5, 11, 21, 128), 96, True, False, True),     # ragged pixel tiles, N block wider than Cout
+    ((2, 3, 9, 14, 64), 320, False, True, True),      # batch 2, two N blocks (second ragged)
+    ((1, 4, 10, 24, 64), 12, False, False, False),    # head-like: 12 output channels
+    ((1, 1, 8, 8, 64), 64, True, False, True),        # a single frame: both history frames from the cache
+    ((1, 2, 5, 5, 192), 256, True, True, False),
+])
+def test_conv_small(wan, shape, Cout, bias, residual, cache):
+    a, w, b, r, c = make(shape, Cout, f"conv/{shape}/{Cout}", bias, residual, cache)
+    got, cout = run(wan, a, w, b, r, c)
+    ref, ref_cache = oracle.causal_conv3d(a, w, b, r, c)
+    conv_close(got, oracle.causal_conv3d_f64(oracle.bf16_to_f64(a), oracle.bf16_to_f64(w),
+                                             None if b is None else oracle.bf16_to_f64(b),
+                                             None if r is None else oracle.bf16_to_f64(r),
+                                             None if c is None else oracle.bf16_to_f64(c)), "conv")
+    assert np.array_equal(cout, ref_cache)
+
+
+def test_conv_chunked_equals_unchunked(wan):
+    shape = (1, 12, 12, 20, 128)
+    a, w, b, _, _ = make(shape, 128, "conv/chunks")
+    full, full_cache = run(wan, a, w, b, None, None)
+    parts, cache = [], None
+    for s in range(0, 12, 4):
+        y, cache = run(wan, a[:, s:s + 4], w, b, None, cache)
+        parts.append(y)
+    assert np.array_equal(np.concatenate(parts, 1), full)
+    assert np.array_equal(cache, full_cache)
+
+
+def test_conv_cache_aliasing_in_place(wan):
+    # cache_out may be cache_in: it is updated after the convolution has read it (T = 1 and 3).
+    for T in (1, 3):
+        a, w, b, _, c = make((1, T, 6, 8, 64), 64, f"conv/alias{T}", cache=True)
+        ref, ref_cache = oracle.causal_conv3d(a, w, b, None, c)
+        cd = to_dev(c)
+        y = wan.wan_causal_conv3d(to_dev(a), to_dev(w), to_dev(b), None, cd, cd)
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(cd), ref_cache)
+        conv_close(bits(y), ref, "alias")
+
+
+def _sampled_check(wan, shape, Cout, name, count=160):
+    rng = np.random.default_rng(0)
+    a, w, b, _, _ = make(shape, Cout, name)
+    got, _ = run(wan, a, w, b, None, None, with_cache_out=False)
+    P = padded(a)
+    N, T, H, W, _ = shape
+    pts = sample_points(rng, N, T, H, W, count)
+    patches = np.stack([P[n, t:t + 3, h:h + 3, x:x + 3] for n, t, h, x in pts])
+    ref = oracle.conv_at_points_f64(patches, oracle.bf16_to_f64(w), oracle.bf16_to_f64(b))
+    sel = np.stack([got[n, t, h, x] for n, t, h, x in pts])
+    conv_close(sel, ref, name)
+
+
+def test_conv_full_size_c256(wan):
+    # One 4-frame chunk of the C=256 decoder stage: [1, 4, 176, 312, 256], sampled outputs.
+    _sampled_check(wan, (1, 4, 176, 312, 256), 256, "conv/cfg4")
+
+
+def test_conv_full_size_c1024(wan):
+    # The widest stage: [1, 4, 44, 78, 1024] -> 1024 channels, sampled outputs.
+    _sampled_check(wan, (1, 4, 44, 78, 1024), 1024, "conv/cfg5")

@@ -1,0 +1,67 @@
+"""GroupNorm + SiLU on the GPU against the oracle: every element within one bf16 ulp."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from util import to_dev, f32_dev, bits
+from video_vae_decoder_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+EPS = float(np.float32(1e-6))
+
+
+def run_case(wan, shape, groups, mean, std, name, seed=0):
+    x = synth.normal_bf16(shape, seed, f"{name}/x", mean, std)
+    C = shape[-1]
+    g = synth.normal_f32((C,), seed, f"{name}/gamma", 1.0, 0.1)
+    b = synth.normal_f32((C,), seed, f"{name}/beta", 0.0, 0.1)
+    y = wan.wan_gn_silu(to_dev(x), f32_dev(g), f32_dev(b), groups, EPS)
+    got = bits(y)
+    ref = oracle.gn_silu(x, g, b, groups, EPS)
+    ulp = oracle.ulp_distance_bf16(got, ref)
+    assert wan.wan_device_status() == 0
+    return int(ulp.max()), got, (x, g, b)
+
+
+@pytest.mark.parametrize("shape,groups", [
+    ((1, 3, 16, 16, 64), 32),      # 2 channels per group (4 groups per 16-byte vector)
+    ((1, 3, 7, 13, 256), 32),      # 8 per group, ragged spans
+    ((2, 2, 5, 9, 128), 16),       # batch of 2, 8 per group
+    ((1, 2, 9, 11, 32), 32),       # 1 channel per group
+    ((1, 2, 10, 10, 64), 16),      # 4 per group
+    ((1, 1, 1, 1, 512), 32),       # a single pixel
+    ((1, 2, 33, 47, 1024), 32),    # 32 per group
+])
+def test_gn_small(wan, shape, groups):
+    mx, _, _ = run_case(wan, shape, groups, 0.5, np.sqrt(2.0), f"gn/{shape}")
+    assert mx <= 1
+
+
+def test_gn_decode_mid_full_size(wan):
+    # [1, C=512, T=4, H=88, W=156] stored channels-last, x ~ N(0.5, variance 2)
+    mx, got, _ = run_case(wan, (1, 4, 88, 156, 512), 32, 0.5, np.sqrt(2.0), "gn/cfg2")
+    assert mx <= 1
+
+
+def test_gn_stress_degenerate_mean_1e3(wan):
+    # mean 1e3, std 1e-2: every bf16 value rounds to 1000 (ulp 4 there), variance 0, so the
+    # output is silu(beta) per channel exactly.
+    mx, got, (x, g, b) = run_case(wan, (1, 4, 88, 156, 512), 32, 1e3, 1e-2, "gn/stress")
+    assert np.all(x == x.flat[0])
+    assert mx <= 1
+
+
+def test_gn_stress_large_mean_small_spread(wan):
+    # mean 1e4 with a spread of about one bf16 ulp: naive E[x^2] - E[x]^2 in fp32 fails here.
+    mx, _, _ = run_case(wan, (1, 2, 44, 78, 512), 32, 1e4, 64.0, "gn/stress2")
+    assert mx <= 1
+
+
+def test_gn_deterministic(wan):
+    x = to_dev(synth.normal_bf16((1, 4, 30, 40, 256), 1, "gn/det/x"))
+    g = f32_dev(np.ones(256))
+    b = f32_dev(np.zeros(256))
+    y1 = bits(wan.wan_gn_silu(x, g, b, 32, EPS))
+    y2 = bits(wan.wan_gn_silu(x, g, b, 32, EPS))
+    assert np.array_equal(y1, y2)

@@ -1,0 +1,192 @@
+"""Python binding of the C ABI in include/wan.h (ctypes; argument marshalling only).
+
+Every function here has the name of the C entry point it calls. Device memory comes from torch
+(tensors must be CUDA, contiguous, bf16 where the ABI says bf16, fp32 for GroupNorm's gamma and
+beta); work is enqueued on torch's current CUDA stream. The shared library is the in-tree build
+`lib/libwan.so`; if it is missing, loading raises instead of falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "lib", "libwan.so")
+
+WAN_OP_GN_SILU = 0
+WAN_OP_CAUSAL_CONV3D = 1
+WAN_OP_RESBLOCK = 2
+WAN_OP_UPSAMPLE_PHASE_CONV = 3
+
+STATUS = {0: "WAN_OK", 1: "WAN_ERR_INVALID_ARG", 2: "WAN_ERR_UNSUPPORTED_SHAPE", 3: "WAN_ERR_MISALIGNED",
+          4: "WAN_ERR_WORKSPACE", 5: "WAN_ERR_CUDA", 6: "WAN_ERR_TIMEOUT"}
+
+EXPORTS = ("wan_status_string", "wan_workspace_size", "wan_gn_silu", "wan_causal_conv3d",
+           "wan_upsample_phase_weights", "wan_upsample_phase_conv", "wan_resblock", "wan_device_status")
+
+
+class WanError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+
+
+class ResblockParams(ctypes.Structure):
+    _fields_ = [("gamma1", ctypes.c_void_p), ("beta1", ctypes.c_void_p), ("w1", ctypes.c_void_p),
+                ("b1", ctypes.c_void_p), ("gamma2", ctypes.c_void_p), ("beta2", ctypes.c_void_p),
+                ("w2", ctypes.c_void_p), ("b2", ctypes.c_void_p), ("groups", ctypes.c_int),
+                ("eps", ctypes.c_float)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library with argument types declared. Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                           "(there is no fallback implementation)")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.wan_status_string.restype = ctypes.c_char_p
+    L.wan_status_string.argtypes = [I]
+    L.wan_workspace_size.restype = S
+    L.wan_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
+    L.wan_gn_silu.restype = I
+    L.wan_gn_silu.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, S, P]
+    L.wan_causal_conv3d.restype = I
+    L.wan_causal_conv3d.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, S, P]
+    L.wan_upsample_phase_weights.restype = I
+    L.wan_upsample_phase_weights.argtypes = [P, P, I, I, P]
+    L.wan_upsample_phase_conv.restype = I
+    L.wan_upsample_phase_conv.argtypes = [P, P, P, P, I, I, I, I, I, I, P]
+    L.wan_resblock.restype = I
+    L.wan_resblock.argtypes = [P, P, ctypes.POINTER(ResblockParams), P, P, I, I, I, I, I, I, P, S, P]
+    L.wan_device_status.restype = I
+    L.wan_device_status.argtypes = [P]
+    _lib = L
+    return L
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise WanError(status, where)
+
+
+def _need(t, dtype, name):
+    if t is None:
+        return
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor, got "
+                         f"{t.device} {t.dtype} contiguous={t.is_contiguous()}")
+
+
+def wan_status_string(status: int) -> str:
+    return lib().wan_status_string(status).decode()
+
+
+def wan_workspace_size(op: int, N: int, T: int, H: int, W: int, Cin: int, Cout: int = 0, groups: int = 0) -> int:
+    return int(lib().wan_workspace_size(op, N, T, H, W, Cin, Cout, groups))
+
+
+def _workspace(nbytes: int, device, ws=None):
+    if nbytes == 0:
+        return None
+    if ws is not None and ws.numel() * ws.element_size() >= nbytes:
+        return ws
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def wan_gn_silu(x, gamma, beta, groups: int, eps: float, y=None, ws=None, stream=None):
+    """y = silu(group_norm(x)) per (n, t, group); x [N, T, H, W, C] bf16."""
+    _need(x, torch.bfloat16, "x")
+    _need(gamma, torch.float32, "gamma")
+    _need(beta, torch.float32, "beta")
+    N, T, H, W, C = x.shape
+    y = torch.empty_like(x) if y is None else y
+    _need(y, torch.bfloat16, "y")
+    need = wan_workspace_size(WAN_OP_GN_SILU, N, T, H, W, C, 0, groups)
+    ws = _workspace(need, x.device, ws)
+    _check(lib().wan_gn_silu(_ptr(x), _ptr(y), _ptr(gamma), _ptr(beta), N, T, H, W, C, groups, eps,
+                             _ptr(ws), need if ws is not None else 0, _stream(stream)), "wan_gn_silu")
+    return y
+
+
+def wan_causal_conv3d(a, w, bias=None, residual=None, cache_in=None, cache_out=None, y=None, stream=None):
+    """Causal 3x3x3 conv of a [N, T, H, W, Cin] with weights [Cout, 3, 3, 3, Cin] (bf16)."""
+    for t, n in ((a, "a"), (w, "w"), (bias, "bias"), (residual, "residual"), (cache_in, "cache_in"),
+                 (cache_out, "cache_out")):
+        _need(t, torch.bfloat16, n)
+    N, T, H, W, Cin = a.shape
+    Cout = w.shape[0]
+    y = torch.empty((N, T, H, W, Cout), dtype=torch.bfloat16, device=a.device) if y is None else y
+    _need(y, torch.bfloat16, "y")
+    _check(lib().wan_causal_conv3d(_ptr(a), _ptr(cache_in), _ptr(cache_out), _ptr(w), _ptr(bias), _ptr(residual),
+                                   _ptr(y), N, T, H, W, Cin, Cout, None, 0, _stream(stream)), "wan_causal_conv3d")
+    return y
+
+
+def wan_upsample_phase_weights(w3, wp=None, stream=None):
+    """[Cout, 3, 3, Cin] bf16 -> [4, Cout, 2, 2, Cin] bf16 phase weights."""
+    _need(w3, torch.bfloat16, "w3")
+    Cout, _, _, Cin = w3.shape
+    wp = torch.empty((4, Cout, 2, 2, Cin), dtype=torch.bfloat16, device=w3.device) if wp is None else wp
+    _need(wp, torch.bfloat16, "wp")
+    _check(lib().wan_upsample_phase_weights(_ptr(w3), _ptr(wp), Cin, Cout, _stream(stream)),
+           "wan_upsample_phase_weights")
+    return wp
+
+
+def wan_upsample_phase_conv(x, wp, bias=None, y=None, stream=None):
+    """Nearest-x2 + 3x3 conv as four phase convs: x [N, T, H, W, Cin] -> [N, T, 2H, 2W, Cout]."""
+    _need(x, torch.bfloat16, "x")
+    _need(wp, torch.bfloat16, "wp")
+    _need(bias, torch.bfloat16, "bias")
+    N, T, H, W, Cin = x.shape
+    Cout = wp.shape[1]
+    y = torch.empty((N, T, 2 * H, 2 * W, Cout), dtype=torch.bfloat16, device=x.device) if y is None else y
+    _need(y, torch.bfloat16, "y")
+    _check(lib().wan_upsample_phase_conv(_ptr(x), _ptr(wp), _ptr(bias), _ptr(y), N, T, H, W, Cin, Cout,
+                                         _stream(stream)), "wan_upsample_phase_conv")
+    return y
+
+
+def wan_resblock(x, params: dict, cache1, cache2, cache_valid: bool, groups: int, eps: float, out=None, ws=None,
+                 stream=None):
+    """One causal ResBlock on a chunk; params holds gamma1, beta1, w1, b1, gamma2, beta2, w2, b2."""
+    _need(x, torch.bfloat16, "x")
+    _need(cache1, torch.bfloat16, "cache1")
+    _need(cache2, torch.bfloat16, "cache2")
+    for k in ("gamma1", "beta1", "gamma2", "beta2"):
+        _need(params[k], torch.float32, k)
+    for k in ("w1", "b1", "w2", "b2"):
+        _need(params.get(k), torch.bfloat16, k)
+    N, T, H, W, C = x.shape
+    out = torch.empty_like(x) if out is None else out
+    _need(out, torch.bfloat16, "out")
+    need = wan_workspace_size(WAN_OP_RESBLOCK, N, T, H, W, C, C, groups)
+    ws = _workspace(need, x.device, ws)
+    p = ResblockParams(_ptr(params["gamma1"]), _ptr(params["beta1"]), _ptr(params["w1"]), _ptr(params.get("b1")),
+                       _ptr(params["gamma2"]), _ptr(params["beta2"]), _ptr(params["w2"]), _ptr(params.get("b2")),
+                       groups, eps)
+    _check(lib().wan_resblock(_ptr(x), _ptr(out), ctypes.byref(p), _ptr(cache1), _ptr(cache2), int(bool(cache_valid)),
+                              N, T, H, W, C, _ptr(ws), need, _stream(stream)), "wan_resblock")
+    return out
+
+
+def wan_device_status(stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the library's device error status."""
+    return int(lib().wan_device_status(_stream(stream)))

@@ -1,0 +1,242 @@
+// The extern "C" entry points of include/wan.h: host-side validation, workspace layout and the
+// ordering of the kernels on the caller's stream. Nothing here allocates device memory.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "conv_tc.h"
+#include "gn_silu.h"
+#include "wan.h"
+
+namespace wan {
+
+// Device error word: kernels that give up a bounded wait set bits here.
+__device__ unsigned g_device_error = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return -1;
+  return d;
+}
+
+int sm_count() {
+  static int cached[kMaxDevices] = {0};
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return 148;
+  if (!cached[d]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n <= 0) n = 148;
+    cached[d] = n;
+  }
+  return cached[d];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlap(const void* a, size_t abytes, const void* b, size_t bbytes) {
+  if (!a || !b || !abytes || !bbytes) return false;
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + bbytes && b0 < a0 + abytes;
+}
+
+size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+bool positive(int a, int b, int c, int d, int e) { return a > 0 && b > 0 && c > 0 && d > 0 && e > 0; }
+
+// Sizes the kernels index with 32-bit integers stay below 2^31.
+bool fits(int N, int T, int H, int W, int C) {
+  const long long px = (long long)H * W;
+  return px * C < (1LL << 31) && (long long)N * T * 4 < (1LL << 31) && C <= 65536;
+}
+
+wan_status cuda_status(cudaError_t e) { return e == cudaSuccess ? WAN_OK : WAN_ERR_CUDA; }
+
+wan_status check_gn(const void* x, const void* y, const float* gamma, const float* beta, int N, int T,
+                    int H, int W, int C, int groups, float eps) {
+  if (!x || !y || !gamma || !beta) return WAN_ERR_INVALID_ARG;
+  if (!positive(N, T, H, W, C) || groups <= 0 || C % groups != 0) return WAN_ERR_INVALID_ARG;
+  if (!(eps > 0.0f) || eps != eps || eps > 3.0e38f) return WAN_ERR_INVALID_ARG;
+  if (!gn_silu_supported(C, groups) || !fits(N, T, H, W, C)) return WAN_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(gamma) || !aligned16(beta)) return WAN_ERR_MISALIGNED;
+  return WAN_OK;
+}
+
+wan_status check_conv(const void* a, const void* w, const void* y, int N, int T, int H, int W, int Cin,
+                      int Cout) {
+  if (!a || !w || !y) return WAN_ERR_INVALID_ARG;
+  if (!positive(N, T, H, W, Cin) || Cout <= 0) return WAN_ERR_INVALID_ARG;
+  if (Cin % 64 != 0 || Cout % 2 != 0 || !fits(N, T, H, W, Cin) || !fits(N, T, H, W, Cout))
+    return WAN_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(a) || !aligned16(w) || !aligned16(y)) return WAN_ERR_MISALIGNED;
+  return WAN_OK;
+}
+
+}  // namespace
+
+unsigned* device_error_word() {
+  static unsigned* cached[kMaxDevices] = {nullptr};
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return nullptr;
+  if (!cached[d]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    cached[d] = static_cast<unsigned*>(p);
+  }
+  return cached[d];
+}
+
+}  // namespace wan
+
+using namespace wan;
+
+extern "C" {
+
+const char* wan_status_string(wan_status s) {
+  switch (s) {
+    case WAN_OK: return "WAN_OK";
+    case WAN_ERR_INVALID_ARG: return "WAN_ERR_INVALID_ARG: a pointer is NULL or a size/parameter is invalid";
+    case WAN_ERR_UNSUPPORTED_SHAPE: return "WAN_ERR_UNSUPPORTED_SHAPE: no kernel for these sizes";
+    case WAN_ERR_MISALIGNED: return "WAN_ERR_MISALIGNED: a pointer is not 16-byte aligned";
+    case WAN_ERR_WORKSPACE: return "WAN_ERR_WORKSPACE: workspace missing or too small";
+    case WAN_ERR_CUDA: return "WAN_ERR_CUDA: a CUDA call or kernel launch failed";
+    case WAN_ERR_TIMEOUT: return "WAN_ERR_TIMEOUT: a kernel gave up a bounded wait";
+  }
+  return "WAN_ERR_UNKNOWN";
+}
+
+size_t wan_workspace_size(wan_op op, int N, int T, int H, int W, int Cin, int Cout, int groups) {
+  if (!positive(N, T, H, W, Cin)) return 0;
+  switch (op) {
+    case WAN_OP_GN_SILU:
+      if (groups <= 0 || Cin % groups || !gn_silu_supported(Cin, groups)) return 0;
+      return gn_silu_workspace(N, T, H, W, Cin, groups, sm_count());
+    case WAN_OP_CAUSAL_CONV3D:
+    case WAN_OP_UPSAMPLE_PHASE_CONV:
+      return 0;
+    case WAN_OP_RESBLOCK: {
+      if (groups <= 0 || Cin % groups || !gn_silu_supported(Cin, groups)) return 0;
+      const size_t act = (size_t)N * T * H * W * Cin * sizeof(wan_bf16);
+      return 2 * align256(act) + align256(gn_silu_workspace(N, T, H, W, Cin, groups, sm_count()));
+    }
+  }
+  return 0;
+}
+
+wan_status wan_gn_silu(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta, int N, int T,
+                       int H, int W, int C, int groups, float eps, void* ws, size_t ws_bytes, void* stream) {
+  wan_status st = check_gn(x, y, gamma, beta, N, T, H, W, C, groups, eps);
+  if (st != WAN_OK) return st;
+  const size_t bytes = (size_t)N * T * H * W * C * sizeof(wan_bf16);
+  if (overlap(x, bytes, y, bytes)) return WAN_ERR_INVALID_ARG;
+  const size_t need = wan_workspace_size(WAN_OP_GN_SILU, N, T, H, W, C, 0, groups);
+  if (!ws || ws_bytes < need) return WAN_ERR_WORKSPACE;
+  if (!aligned16(ws)) return WAN_ERR_MISALIGNED;
+  return cuda_status(gn_silu_launch(x, y, gamma, beta, N, T, H, W, C, groups, eps, ws, sm_count(),
+                                    static_cast<cudaStream_t>(stream)));
+}
+
+wan_status wan_causal_conv3d(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out,
+                             const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y,
+                             int N, int T, int H, int W, int Cin, int Cout, void* ws, size_t ws_bytes,
+                             void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  wan_status st = check_conv(a, w, y, N, T, H, W, Cin, Cout);
+  if (st != WAN_OK) return st;
+  if (!aligned16(cache_in) && cache_in) return WAN_ERR_MISALIGNED;
+  if (!aligned16(cache_out) && cache_out) return WAN_ERR_MISALIGNED;
+  if (!aligned16(bias) && bias) return WAN_ERR_MISALIGNED;
+  if (!aligned16(residual) && residual) return WAN_ERR_MISALIGNED;
+  const size_t abytes = (size_t)N * T * H * W * Cin * 2, ybytes = (size_t)N * T * H * W * Cout * 2;
+  const size_t cbytes = (size_t)N * 2 * H * W * Cin * 2;
+  if (overlap(a, abytes, y, ybytes) || overlap(residual, ybytes, y, ybytes) || overlap(cache_in, cbytes, y, ybytes) ||
+      overlap(cache_out, cbytes, y, ybytes) || overlap(cache_out, cbytes, a, abytes))
+    return WAN_ERR_INVALID_ARG;
+  unsigned* err = device_error_word();
+  if (!err) return WAN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = cuda_status(conv_launch(0, a, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, sm_count(), err, s));
+  if (st != WAN_OK || !cache_out) return st;
+  return cuda_status(cache_update_launch(a, cache_in, cache_out, N, T, H, W, Cin, sm_count(), s));
+}
+
+wan_status wan_upsample_phase_weights(const wan_bf16* w3, wan_bf16* wp, int Cin, int Cout, void* stream) {
+  if (!w3 || !wp || Cin <= 0 || Cout <= 0) return WAN_ERR_INVALID_ARG;
+  if ((long long)Cin * Cout * 16 >= (1LL << 40)) return WAN_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(w3) || !aligned16(wp)) return WAN_ERR_MISALIGNED;
+  if (overlap(w3, (size_t)Cout * 9 * Cin * 2, wp, (size_t)Cout * 16 * Cin * 2)) return WAN_ERR_INVALID_ARG;
+  return cuda_status(phase_weights_launch(w3, wp, Cin, Cout, sm_count(), static_cast<cudaStream_t>(stream)));
+}
+
+wan_status wan_upsample_phase_conv(const wan_bf16* x, const wan_bf16* wp, const wan_bf16* bias, wan_bf16* y,
+                                   int N, int T, int H, int W, int Cin, int Cout, void* stream) {
+  wan_status st = check_conv(x, wp, y, N, T, 2 * H, 2 * W, Cin, Cout);
+  if (st != WAN_OK) return st;
+  if (bias && !aligned16(bias)) return WAN_ERR_MISALIGNED;
+  const size_t xbytes = (size_t)N * T * H * W * Cin * 2, ybytes = (size_t)N * T * 4 * H * W * Cout * 2;
+  if (overlap(x, xbytes, y, ybytes) || overlap(wp, (size_t)16 * Cout * Cin * 2, y, ybytes)) return WAN_ERR_INVALID_ARG;
+  unsigned* err = device_error_word();
+  if (!err) return WAN_ERR_CUDA;
+  return cuda_status(conv_launch(1, x, nullptr, wp, bias, nullptr, y, N, T, H, W, Cin, Cout, sm_count(), err,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+wan_status wan_resblock(const wan_bf16* x, wan_bf16* out, const wan_resblock_params* p, wan_bf16* cache1,
+                        wan_bf16* cache2, int cache_valid, int N, int T, int H, int W, int C, void* ws,
+                        size_t ws_bytes, void* stream) {
+  if (!p || !cache1 || !cache2) return WAN_ERR_INVALID_ARG;
+  wan_status st = check_gn(x, out, p->gamma1, p->beta1, N, T, H, W, C, p->groups, p->eps);
+  if (st != WAN_OK) return st;
+  st = check_gn(x, out, p->gamma2, p->beta2, N, T, H, W, C, p->groups, p->eps);
+  if (st != WAN_OK) return st;
+  st = check_conv(x, p->w1, out, N, T, H, W, C, C);
+  if (st != WAN_OK) return st;
+  st = check_conv(x, p->w2, out, N, T, H, W, C, C);
+  if (st != WAN_OK) return st;
+  if (!aligned16(cache1) || !aligned16(cache2) || (p->b1 && !aligned16(p->b1)) || (p->b2 && !aligned16(p->b2)))
+    return WAN_ERR_MISALIGNED;
+  const size_t bytes = (size_t)N * T * H * W * C * 2, cbytes = (size_t)N * 2 * H * W * C * 2;
+  if (overlap(x, bytes, out, bytes) || overlap(cache1, cbytes, cache2, cbytes) || overlap(cache1, cbytes, out, bytes) ||
+      overlap(cache2, cbytes, out, bytes) || overlap(cache1, cbytes, x, bytes) || overlap(cache2, cbytes, x, bytes))
+    return WAN_ERR_INVALID_ARG;
+  const size_t need = wan_workspace_size(WAN_OP_RESBLOCK, N, T, H, W, C, C, p->groups);
+  if (!ws || ws_bytes < need) return WAN_ERR_WORKSPACE;
+  if (!aligned16(ws)) return WAN_ERR_MISALIGNED;
+  unsigned* err = device_error_word();
+  if (!err) return WAN_ERR_CUDA;
+  const int sms = sm_count();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(ws);
+  wan_bf16* act = reinterpret_cast<wan_bf16*>(base);
+  wan_bf16* h = reinterpret_cast<wan_bf16*>(base + align256(bytes));
+  void* gn_ws = base + 2 * align256(bytes);
+  const wan_bf16* c1_in = cache_valid ? cache1 : nullptr;
+  const wan_bf16* c2_in = cache_valid ? cache2 : nullptr;
+
+  cudaError_t e = gn_silu_launch(x, act, p->gamma1, p->beta1, N, T, H, W, C, p->groups, p->eps, gn_ws, sms, s);
+  if (e == cudaSuccess) e = conv_launch(0, act, c1_in, p->w1, p->b1, nullptr, h, N, T, H, W, C, C, sms, err, s);
+  if (e == cudaSuccess) e = cache_update_launch(act, c1_in, cache1, N, T, H, W, C, sms, s);
+  if (e == cudaSuccess) e = gn_silu_launch(h, act, p->gamma2, p->beta2, N, T, H, W, C, p->groups, p->eps, gn_ws, sms, s);
+  if (e == cudaSuccess) e = conv_launch(0, act, c2_in, p->w2, p->b2, x, out, N, T, H, W, C, C, sms, err, s);
+  if (e == cudaSuccess) e = cache_update_launch(act, c2_in, cache2, N, T, H, W, C, sms, s);
+  return cuda_status(e);
+}
+
+wan_status wan_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return WAN_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return WAN_ERR_CUDA;
+  if (v) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return WAN_ERR_CUDA;
+    return WAN_ERR_TIMEOUT;
+  }
+  return WAN_OK;
+}
+
+}  // extern "C"

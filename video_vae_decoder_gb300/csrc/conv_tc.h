@@ -1,0 +1,17 @@
+// Internal interface of the tensor-core convolutions and their helpers (conv_tc.cu).
+#pragma once
+#include <cuda_runtime.h>
+
+#include "wan.h"
+
+namespace wan {
+// mode 0: causal 3x3x3 conv (w [Cout, 27, Cin]); mode 1: 2x2 phase convs (w [4, Cout, 4, Cin]).
+cudaError_t conv_launch(int mode, const wan_bf16* a, const wan_bf16* cache_in, const wan_bf16* w,
+                        const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T,
+                        int H, int W, int Cin, int Cout, int sms, unsigned* err, cudaStream_t stream);
+// cache_out[n, j] = ([cache_in or zeros; a])[n, T + j], j = 0, 1.
+cudaError_t cache_update_launch(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out,
+                                int N, int T, int H, int W, int C, int sms, cudaStream_t stream);
+cudaError_t phase_weights_launch(const wan_bf16* w3, wan_bf16* wp, int Cin, int Cout, int sms,
+                                 cudaStream_t stream);
+}  // namespace wan
