@@ -1,0 +1,519 @@
+#!/usr/bin/env python
+"""Benchmark of the causal video-VAE decoder hot path on GB300 (one JSON line on stdout).
+
+A step is one steady-state pass of every op of the path over one batch of synthetic input,
+each op at the decoder shape it is quoted on:
+  gn      GroupNorm+SiLU standalone, x [1, 4, 88, 156, 512] ~ N(0.5, var 2), 32 groups
+  c256    three causal ResBlocks at C=256 on a 4-frame chunk [1, 4, 176, 312, 256] with the
+          two-frame caches carried from the previous chunk (GN+SiLU, causal conv, cache update,
+          GN+SiLU, causal conv + residual, cache update, per block)
+  up      phase-weight transform [512, 3, 3, 512] and the nearest-x2 + 3x3 upsample as four phase
+          convs, [1, 4, 44, 78, 512] -> [1, 4, 88, 156, 512]
+  c1024   two causal ResBlocks at C=1024 on [1, 4, 44, 78, 1024] with carried caches
+  head    causal 3x3x3 conv 256 -> 12 channels on [1, 16, 704, 1248, 256] (zero history)
+value = useful convolution FLOPs of the step / step time (TFLOP/s); the per-op times, GN GB/s,
+ResBlock ms and the dominant kernel's roofline fraction are reported beside it. The step's
+working set (about 8 GB) is far larger than L2, so no flush is inserted between steps.
+
+--impl reference times the fp64 CPU oracle on the host cores (a bounded sample of the C=256
+ResBlock workload per step), in the same unit.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal conv3d TFLOP/s (% bf16 peak); GN+SiLU GB/s (% HBM); ResBlock ms"
+EPS = 1e-6
+GROUPS = 32
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def conv_flops(N, T, H, W, Cin, Cout):
+    return 2.0 * N * T * H * W * Cout * 27 * Cin
+
+
+def phase_flops(N, T, H, W, Cin, Cout):
+    return 2.0 * N * T * H * W * 4 * Cout * 4 * Cin
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.uuid and parts[0] != self.uuid:
+                continue
+            rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        load = [s for s in sm]
+        return {"sm_mhz": statistics.median(load) if load else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------------------------------------------
+# the GPU workload
+# ------------------------------------------------------------------------------------------------
+CASES = ("all", "gn", "c256", "up", "c1024", "head")
+
+
+class Workload:
+    def __init__(self, dev, case="all", seed=0):
+        import numpy as np
+        import torch
+        from video_vae_decoder_gb300 import synth
+        self.dev = dev
+        bf = torch.bfloat16
+
+        def n(shape, name, mean=0.0, std=1.0, dtype=bf):
+            return synth.normal_torch(shape, seed, name, mean, std, device=dev, dtype=dtype)
+
+        def block(C, prefix):
+            wstd = float(np.sqrt(1.0 / (27 * C)))
+            p = {}
+            for k in (1, 2):
+                p[f"gamma{k}"] = n((C,), f"{prefix}/gamma{k}", 1.0, 0.1, torch.float32)
+                p[f"beta{k}"] = n((C,), f"{prefix}/beta{k}", 0.0, 0.1, torch.float32)
+                p[f"w{k}"] = n((C, 3, 3, 3, C), f"{prefix}/w{k}", 0.0, wstd)
+                p[f"b{k}"] = n((C,), f"{prefix}/b{k}", 0.0, 0.01)
+            return p
+
+        self.case = case
+        want = (lambda part: case in ("all", part))
+        # gn: standalone GroupNorm+SiLU at decode-mid scale (its gamma/beta also serve the e2e leg)
+        self.gn_x = n((1, 4, 88, 156, 512), "bench/gn/x", 0.5, float(np.sqrt(2.0)))
+        self.gn_g = n((512,), "bench/gn/gamma", 1.0, 0.1, torch.float32)
+        self.gn_b = n((512,), "bench/gn/beta", 0.0, 0.1, torch.float32)
+        self.gn_y = torch.empty_like(self.gn_x)
+        # c256: decoder stage
+        small = (1, 1, 8, 8)
+        self.x4 = n((1, 4, 176, 312, 256) if want("c256") else small + (256,), "bench/c256/x")
+        self.blocks4 = [block(256, f"bench/c256/block{i}") for i in range(3 if want("c256") else 0)]
+        # up: spatial upsample
+        self.x3 = n((1, 4, 44, 78, 512) if want("up") else small + (512,), "bench/up/x")
+        self.w3 = n((512, 3, 3, 512), "bench/up/w3", 0.0, float(np.sqrt(1.0 / (9 * 512))))
+        self.wp = torch.empty((4, 512, 2, 2, 512), dtype=bf, device=dev)
+        self.y3 = torch.empty((1, 4, 88, 156, 512), dtype=bf, device=dev)
+        # c1024: widest stage
+        self.x5 = n((1, 4, 44, 78, 1024) if want("c1024") else small + (1024,), "bench/c1024/x")
+        self.blocks5 = [block(1024, f"bench/c1024/block{i}") for i in range(2 if want("c1024") else 0)]
+        # head
+        hshape = (1, 16, 704, 1248, 256) if want("head") else (1, 1, 8, 8, 256)
+        self.xh = n(hshape, "bench/head/x")
+        self.wh = n((12, 3, 3, 3, 256), "bench/head/w", 0.0, float(np.sqrt(1.0 / (27 * 256))))
+        self.yh = torch.empty(hshape[:-1] + (12,), dtype=bf, device=dev)
+
+        def stage_bufs(x, nblk):
+            N, T, H, W, C = x.shape
+            caches = [(torch.zeros((N, 2, H, W, C), dtype=bf, device=dev),
+                       torch.zeros((N, 2, H, W, C), dtype=bf, device=dev)) for _ in range(nblk)]
+            outs = [torch.empty_like(x) for _ in range(nblk)]
+            return caches, outs, torch.empty_like(x), torch.empty_like(x)
+        self.c4, self.o4, self.a4, self.h4 = stage_bufs(self.x4, 3)
+        self.c5, self.o5, self.a5, self.h5 = stage_bufs(self.x5, 2)
+        from video_vae_decoder_gb300 import binding as wan
+        need = max(wan.wan_workspace_size(wan.WAN_OP_GN_SILU, *t.shape, 0, GROUPS)
+                   for t in (self.gn_x, self.x4, self.x5))
+        self.gn_ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        need_rb = max(wan.wan_workspace_size(wan.WAN_OP_RESBLOCK, *t.shape, t.shape[-1], GROUPS)
+                      for t in (self.x4, self.x5))
+        self.rb_ws = torch.empty(need_rb, dtype=torch.uint8, device=dev)
+
+        # useful FLOPs / bytes of the parts in the step
+        self.flops = {}
+        if want("c256"):
+            self.flops["c256"] = 6 * conv_flops(1, 4, 176, 312, 256, 256)
+        if want("c1024"):
+            self.flops["c1024"] = 4 * conv_flops(1, 4, 44, 78, 1024, 1024)
+        if want("up"):
+            self.flops["up"] = phase_flops(1, 4, 44, 78, 512, 512)
+        if want("head"):
+            self.flops["head"] = conv_flops(1, 16, 704, 1248, 256, 12)
+        self.gn_bytes = 4.0 * self.gn_x.numel()
+
+    # ---- one step as the sequence of C-ABI calls, each bracketed by events -----------------
+    def step_calls(self):
+        """[(tag, kernels launched, callable)] for one step."""
+        from video_vae_decoder_gb300 import binding as wan
+        want = (lambda part: self.case in ("all", part))
+        calls = []
+        if want("gn"):
+            calls.append(("gn", 3, lambda: wan.wan_gn_silu(self.gn_x, self.gn_g, self.gn_b, GROUPS, EPS, self.gn_y,
+                                                           self.gn_ws)))
+
+        def stage(tag, x, blocks, caches, outs, act, h):
+            cur = x
+            for i, (p, (c1, c2), out) in enumerate(zip(blocks, caches, outs)):
+                def g1(cur=cur, p=p):
+                    wan.wan_gn_silu(cur, p["gamma1"], p["beta1"], GROUPS, EPS, act, self.gn_ws)
+
+                def k1(p=p, c1=c1):
+                    wan.wan_causal_conv3d(act, p["w1"], p["b1"], None, c1, None, h)
+
+                def u1(c1=c1):
+                    wan.wan_cache_update(act, c1, c1)
+
+                def g2(p=p):
+                    wan.wan_gn_silu(h, p["gamma2"], p["beta2"], GROUPS, EPS, act, self.gn_ws)
+
+                def k2(cur=cur, p=p, c2=c2, out=out):
+                    wan.wan_causal_conv3d(act, p["w2"], p["b2"], cur, c2, None, out)
+
+                def u2(c2=c2):
+                    wan.wan_cache_update(act, c2, c2)
+                calls.extend([(f"{tag}.gn", 3, g1), (f"{tag}.conv", 1, k1), (f"{tag}.cache", 2, u1),
+                              (f"{tag}.gn", 3, g2), (f"{tag}.conv", 1, k2), (f"{tag}.cache", 2, u2)])
+                cur = out
+
+        if want("c256"):
+            stage("c256", self.x4, self.blocks4, self.c4, self.o4, self.a4, self.h4)
+        if want("up"):
+            calls.append(("up.weights", 1, lambda: wan.wan_upsample_phase_weights(self.w3, self.wp)))
+            calls.append(("up.conv", 1, lambda: wan.wan_upsample_phase_conv(self.x3, self.wp, None, self.y3)))
+        if want("c1024"):
+            stage("c1024", self.x5, self.blocks5, self.c5, self.o5, self.a5, self.h5)
+        if want("head"):
+            calls.append(("head.conv", 1, lambda: wan.wan_causal_conv3d(self.xh, self.wh, None, None, None, None,
+                                                                        self.yh)))
+        return calls
+
+    # ---- the same step through the public calls a user makes (wan_resblock etc.) ------------
+    def public_step(self, x2, x4, x3, x5, xh):
+        from video_vae_decoder_gb300 import binding as wan
+        wan.wan_gn_silu(x2, self.gn_g, self.gn_b, GROUPS, EPS, self.gn_y, self.gn_ws)
+        cur = x4
+        for p, (c1, c2), out in zip(self.blocks4, self.c4, self.o4):
+            wan.wan_resblock(cur, p, c1, c2, True, GROUPS, EPS, out, self.rb_ws)
+            cur = out
+        wan.wan_upsample_phase_weights(self.w3, self.wp)
+        wan.wan_upsample_phase_conv(x3, self.wp, None, self.y3)
+        cur = x5
+        for p, (c1, c2), out in zip(self.blocks5, self.c5, self.o5):
+            wan.wan_resblock(cur, p, c1, c2, True, GROUPS, EPS, out, self.rb_ws)
+            cur = out
+        wan.wan_causal_conv3d(xh, self.wh, None, None, None, None, self.yh)
+        return (self.gn_y, self.o4[-1], self.y3, self.o5[-1], self.yh)
+
+
+def run_ours(args, rank, world, dev):
+    import torch
+    from video_vae_decoder_gb300 import binding as wan
+    torch.cuda.set_device(dev)
+    wl = Workload(dev, args.case)
+    calls = wl.step_calls()
+    stream = torch.cuda.current_stream()
+    # warm-up (also fills the caches: the timed steps are steady-state chunks with history)
+    for _ in range(max(args.warmup, 0)):
+        for _, _, fn in calls:
+            fn()
+    torch.cuda.synchronize()
+    assert wan.wan_device_status() == 0
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        ev[s][0].record(stream)
+        for i, (_, _, fn) in enumerate(calls):
+            fn()
+            ev[s][i + 1].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    assert wan.wan_device_status() == 0
+
+    per_tag = {}
+    step_ms = []
+    for s in range(args.steps):
+        step_ms.append(ev[s][0].elapsed_time(ev[s][-1]))
+        for i, (tag, _, _) in enumerate(calls):
+            per_tag.setdefault(tag, []).append(ev[s][i].elapsed_time(ev[s][i + 1]))
+    ms = statistics.mean(step_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    flops = sum(wl.flops.values())
+    pk = peaks()
+
+    def tot(prefix):  # mean total ms per step of the calls with this tag
+        return sum(statistics.mean(v) * (len(v) // args.steps) for k, v in per_tag.items() if k == prefix)
+
+    def per_launch(prefix):
+        v = per_tag.get(prefix, [])
+        return statistics.mean(v) if v else 0.0
+
+    pk_tf = pk["bf16_tflops_sustained"]
+    kernels = {}
+    shares = {}
+    if "c256.conv" in per_tag:
+        f4 = conv_flops(1, 4, 176, 312, 256, 256)
+        kernels["conv_c256"] = {"ms": per_launch("c256.conv"), "tflops": f4 / per_launch("c256.conv") / 1e9,
+                                "total_ms": tot("c256.conv")}
+        kernels["gn_silu_c256"] = {"ms": per_launch("c256.gn"), "gbs": 4.0 * wl.x4.numel() / per_launch("c256.gn") / 1e6}
+        kernels["resblock_c256_ms"] = (tot("c256.gn") + tot("c256.conv") + tot("c256.cache")) / 3.0
+        shares["conv_c256"] = tot("c256.conv")
+    if "c1024.conv" in per_tag:
+        f5 = conv_flops(1, 4, 44, 78, 1024, 1024)
+        kernels["conv_c1024"] = {"ms": per_launch("c1024.conv"), "tflops": f5 / per_launch("c1024.conv") / 1e9,
+                                 "total_ms": tot("c1024.conv")}
+        kernels["resblock_c1024_ms"] = (tot("c1024.gn") + tot("c1024.conv") + tot("c1024.cache")) / 2.0
+        shares["conv_c1024"] = tot("c1024.conv")
+    if "head.conv" in per_tag:
+        hm = per_launch("head.conv")
+        kernels["head_256_to_12"] = {"ms": hm, "tflops": wl.flops["head"] / hm / 1e9,
+                                     "hbm_gbs_in_out": (wl.xh.numel() + wl.yh.numel()) * 2 / hm / 1e6}
+        shares["head_256_to_12"] = hm
+    if "up.conv" in per_tag:
+        um = per_launch("up.conv")
+        kernels["upsample_phase_conv"] = {"ms": um, "tflops": wl.flops["up"] / um / 1e9}
+        shares["upsample_phase_conv"] = um
+    if "gn" in per_tag:
+        gm = per_launch("gn")
+        kernels["gn_silu_decode_mid"] = {"ms": gm, "gbs": wl.gn_bytes / gm / 1e6,
+                                         "frac_hbm": wl.gn_bytes / gm / 1e6 / pk["hbm_gbs"]}
+    gn_total = tot("gn") + tot("c256.gn") + tot("c1024.gn")
+    if gn_total:
+        shares["gn_silu"] = gn_total
+    dom = max(shares, key=shares.get)
+    if dom == "gn_silu":
+        k = kernels.get("gn_silu_c256") or kernels["gn_silu_decode_mid"]
+        roof = {"kernel": "gn_silu", "bound": "hbm", "achieved": k["gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": k["gbs"] / pk["hbm_gbs"], "peak_source": f"{pk['source']} HBM copy"}
+    else:
+        roof = {"kernel": dom, "bound": "tensor", "achieved": kernels[dom]["tflops"], "peak": pk_tf,
+                "unit": "TFLOP/s", "frac": kernels[dom]["tflops"] / pk_tf,
+                "peak_source": f"{pk['source']} sustained bf16 (kernel timed inside a long step)"}
+    roof["traffic"] = None
+    roof["share_of_step"] = shares[dom] / ms
+    launches = sum(k for _, k, _ in calls) * args.steps
+
+    out = {
+        "metric": METRIC, "value": world * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded counter-based normals; random-init weights of the decoder shapes)",
+        "config": {"workload": "decoder hot path, one steady-state 4-frame chunk: GN+SiLU [1,4,88,156,512]; "
+                               "3 causal ResBlocks C=256 [1,4,176,312,256]; nearest-x2+3x3 upsample as 4 phase convs "
+                               "[1,4,44,78,512]->[1,4,88,156,512]; 2 causal ResBlocks C=1024 [1,4,44,78,1024]; "
+                               "head conv 256->12 [1,16,704,1248,256]",
+                   "useful_tflop_per_step": flops / 1e12, "l2": "no flush: the step's working set (~8 GB) exceeds L2",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "kernels": kernels, "wall_s_timed": wall, "clocks": clocks, "gpu_launches": launches, "roofline": roof,
+    }
+    if not args.no_e2e and args.case == "all":
+        out["e2e"] = run_e2e(args, wl, dev, flops)
+    return out
+
+
+def run_e2e(args, wl, dev, flops):
+    """The same step through the public calls with HOST buffers: pinned inputs copied in and the
+    results copied out inside the timed region."""
+    import torch
+    ins = [wl.gn_x, wl.x4, wl.x3, wl.x5, wl.xh]
+    host_in = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in ins]
+    for h, d in zip(host_in, ins):
+        h.copy_(d)
+    dev_in = [torch.empty_like(t) for t in ins]
+    outs = wl.public_step(*dev_in)
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for h, d in zip(host_in, dev_in):
+            d.copy_(h, non_blocking=True)
+        o = wl.public_step(*dev_in)
+        for h, d in zip(host_out, o):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = max(1, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "api": "wan_gn_silu, wan_resblock x5, wan_upsample_phase_weights, wan_upsample_phase_conv, "
+                   "wan_causal_conv3d from pinned host buffers"}
+
+
+# ------------------------------------------------------------------------------------------------
+# the oracle on the host cores
+# ------------------------------------------------------------------------------------------------
+SAMPLE_SHAPE = (1, 4, 32, 312, 256)
+
+
+def oracle_sample():
+    import numpy as np
+    import oracle
+    from video_vae_decoder_gb300 import synth
+    x = synth.normal_bf16(SAMPLE_SHAPE, 0, "bench/c256/x")
+    p = synth.resblock_params(256, 0, "bench/cpu/block")
+    flops = 2 * conv_flops(*SAMPLE_SHAPE, 256)
+
+    def run():
+        t = time.perf_counter()
+        oracle.resblock(x, p, GROUPS, float(np.float32(EPS)))
+        return time.perf_counter() - t
+    return run, flops
+
+
+def cpu_threads():
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        v = os.environ.get(k)
+        if v and v.isdigit():
+            return int(v)
+    return os.cpu_count() or 1
+
+
+def cpu_baseline(reps=1):
+    run, flops = oracle_sample()
+    secs = [run() for _ in range(reps)]
+    s = min(secs)
+    return {"value": flops / s / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle ResBlock (GN+SiLU, 2 causal convs C=256) on {list(SAMPLE_SHAPE)}, "
+                      f"{flops / 1e9:.0f} GFLOP of conv work, {s:.2f} s"}
+
+
+def run_reference(args):
+    run, flops = oracle_sample()
+    for _ in range(max(args.warmup, 0)):
+        run()
+    secs = [run() for _ in range(args.steps)]
+    ms = 1e3 * statistics.mean(secs)
+    v = flops / (ms * 1e-3) / 1e12
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"fp64 CPU oracle: causal ResBlock C=256 on {list(SAMPLE_SHAPE)} "
+                                   "(a bounded slice of the [1,4,176,312,256] chunk)"},
+            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
+                             "sample": f"ResBlock on {list(SAMPLE_SHAPE)} per step"},
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default="all", choices=CASES,
+                    help="time one part of the step only (profiling captures); the default is the whole step")
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    import torch
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    from video_vae_decoder_gb300 import binding
+    binding.lib()
+    out = run_ours(args, rank, world, dev)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            out["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

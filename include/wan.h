@@ -117,6 +117,23 @@ wan_status wan_causal_conv3d(const wan_bf16* a, const wan_bf16* cache_in, wan_bf
                              void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Temporal-cache update (the cache manager of the causal convolutions), on its own.
+ *
+ * Source: binding.cpp, `Decoder::conv` (`cache[idx] = last_frames(p, ...)`: after a chunk the
+ * cache keeps the last two frames of the conv's padded input P = [cache_in; a]):
+ *     cache_out[n, j] = P[n, T + j],  j = 0, 1   (bit-for-bit copies; zeros where P comes
+ *                                                from a NULL cache_in)
+ * wan_causal_conv3d does this itself when given cache_out; this call is the same copy for
+ * callers that schedule it separately (it must run after every reader of cache_in).
+ *
+ *   a          [N, T, H, W, C] bf16.      cache_in  [N, 2, H, W, C] bf16 or NULL.
+ *   cache_out  [N, 2, H, W, C] bf16; MAY alias cache_in; must not overlap a.
+ *   C % 8 == 0.
+ */
+wan_status wan_cache_update(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out,
+                            int N, int T, int H, int W, int C, void* stream);
+
+/*
  * Phase-weight transform of the nearest-x2 upsampler.
  *
  * Source: binding.cpp, `prepare()` (nearest-x2 + 3x3 equals four 2x2 low-resolution phases;

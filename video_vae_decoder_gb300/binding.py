@@ -22,7 +22,7 @@ WAN_OP_UPSAMPLE_PHASE_CONV = 3
 STATUS = {0: "WAN_OK", 1: "WAN_ERR_INVALID_ARG", 2: "WAN_ERR_UNSUPPORTED_SHAPE", 3: "WAN_ERR_MISALIGNED",
           4: "WAN_ERR_WORKSPACE", 5: "WAN_ERR_CUDA", 6: "WAN_ERR_TIMEOUT"}
 
-EXPORTS = ("wan_status_string", "wan_workspace_size", "wan_gn_silu", "wan_causal_conv3d",
+EXPORTS = ("wan_status_string", "wan_workspace_size", "wan_gn_silu", "wan_causal_conv3d", "wan_cache_update",
            "wan_upsample_phase_weights", "wan_upsample_phase_conv", "wan_resblock", "wan_device_status")
 
 
@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
     L.wan_gn_silu.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, S, P]
     L.wan_causal_conv3d.restype = I
     L.wan_causal_conv3d.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, S, P]
+    L.wan_cache_update.restype = I
+    L.wan_cache_update.argtypes = [P, P, P, I, I, I, I, I, P]
     L.wan_upsample_phase_weights.restype = I
     L.wan_upsample_phase_weights.argtypes = [P, P, I, I, P]
     L.wan_upsample_phase_conv.restype = I
@@ -137,6 +139,17 @@ def wan_causal_conv3d(a, w, bias=None, residual=None, cache_in=None, cache_out=N
     _check(lib().wan_causal_conv3d(_ptr(a), _ptr(cache_in), _ptr(cache_out), _ptr(w), _ptr(bias), _ptr(residual),
                                    _ptr(y), N, T, H, W, Cin, Cout, None, 0, _stream(stream)), "wan_causal_conv3d")
     return y
+
+
+def wan_cache_update(a, cache_out, cache_in=None, stream=None):
+    """cache_out = last two frames of [cache_in (or zeros); a]; cache_out may be cache_in."""
+    _need(a, torch.bfloat16, "a")
+    _need(cache_out, torch.bfloat16, "cache_out")
+    _need(cache_in, torch.bfloat16, "cache_in")
+    N, T, H, W, C = a.shape
+    _check(lib().wan_cache_update(_ptr(a), _ptr(cache_in), _ptr(cache_out), N, T, H, W, C, _stream(stream)),
+           "wan_cache_update")
+    return cache_out
 
 
 def wan_upsample_phase_weights(w3, wp=None, stream=None):

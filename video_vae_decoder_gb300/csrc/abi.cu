@@ -165,6 +165,19 @@ wan_status wan_causal_conv3d(const wan_bf16* a, const wan_bf16* cache_in, wan_bf
   return cuda_status(cache_update_launch(a, cache_in, cache_out, N, T, H, W, Cin, sm_count(), s));
 }
 
+wan_status wan_cache_update(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out, int N, int T, int H,
+                            int W, int C, void* stream) {
+  if (!a || !cache_out) return WAN_ERR_INVALID_ARG;
+  if (!positive(N, T, H, W, C)) return WAN_ERR_INVALID_ARG;
+  if (C % 8 != 0 || !fits(N, T, H, W, C)) return WAN_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(a) || !aligned16(cache_out) || (cache_in && !aligned16(cache_in))) return WAN_ERR_MISALIGNED;
+  const size_t abytes = (size_t)N * T * H * W * C * 2, cbytes = (size_t)N * 2 * H * W * C * 2;
+  if (overlap(cache_out, cbytes, a, abytes)) return WAN_ERR_INVALID_ARG;
+  if (cache_in && cache_in != cache_out && overlap(cache_in, cbytes, cache_out, cbytes)) return WAN_ERR_INVALID_ARG;
+  return cuda_status(cache_update_launch(a, cache_in, cache_out, N, T, H, W, C, sm_count(),
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 wan_status wan_upsample_phase_weights(const wan_bf16* w3, wan_bf16* wp, int Cin, int Cout, void* stream) {
   if (!w3 || !wp || Cin <= 0 || Cout <= 0) return WAN_ERR_INVALID_ARG;
   if ((long long)Cin * Cout * 16 >= (1LL << 40)) return WAN_ERR_UNSUPPORTED_SHAPE;
