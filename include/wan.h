@@ -87,6 +87,31 @@ wan_status wan_gn_silu(const wan_bf16* x, wan_bf16* y, const float* gamma, const
                        void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * wan_gn_silu for callers that cannot allocate device memory. (The pages have no counterpart:
+ * this is an interface of this library only.)
+ *
+ * Some hosts give a library only the tensors it works on: an application that has reserved all
+ * device memory for its own pool and offers plug-ins no allocator, or a latency-bound loop that
+ * may not call cudaMalloc and cannot hand over a workspace either. This call computes exactly
+ * what wan_gn_silu computes, with the same kernels, but takes no workspace: its scratch is a
+ * fixed 4 MiB array in the library's device memory, which every GPU that loads the library holds
+ * until the process exits. The call allocates nothing.
+ *   - Sizes whose scratch exceeds 4 MiB are refused with WAN_ERR_WORKSPACE (nothing is
+ *     launched). The scratch needed is wan_workspace_size(WAN_OP_GN_SILU, ...); for example
+ *     [1, 4, 88, 156, 512] with 32 groups needs about 0.7 MiB.
+ *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream capture.
+ *   - All calls share the one array: calls that may overlap on the GPU (on different streams,
+ *     or from different threads without ordering) race on it and must be serialised by the
+ *     caller. Each call writes every scratch word it later reads, so the array needs no
+ *     clearing between calls.
+ * Arguments and their conditions are those of wan_gn_silu.
+ */
+wan_status wan_gn_silu_noalloc(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta,
+                               int N, int T, int H, int W, int C, int groups, float eps,
+                               void* stream);
+
+/*
  * Causal 3x3x3 convolution with a carried two-frame temporal cache (implicit GEMM on the
  * tcgen05 tensor cores, bf16 operands, fp32 accumulation, one rounding to bf16).
  *

@@ -101,3 +101,16 @@ def test_resblock_and_upsample_reject_invalid(L):
     assert L.wan_upsample_phase_weights(None, A, 64, 64, None) == 1
     assert L.wan_upsample_phase_weights(MIS, A * 8, 64, 64, None) == 3
     assert L.wan_upsample_phase_conv(A, A * 3, None, A * 9, 1, 1, 4, 4, 32, 64, None) == 2
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers are only passed where no GPU exists")
+def test_gn_noalloc_refuses_sizes_beyond_its_static_scratch(L):
+    # [1, 64, 176, 312, 256] with 32 groups needs more scratch than the fixed 4 MiB: refused on
+    # the host with WAN_ERR_WORKSPACE, before any device work.
+    from video_vae_decoder_gb300 import binding as b
+    assert b.wan_workspace_size(b.WAN_OP_GN_SILU, 1, 64, 176, 312, 256, 0, 32) > 4 << 20
+    f = L.wan_gn_silu_noalloc
+    x, y = A, A << 12
+    assert f(x, y, A * 5, A * 7, 1, 64, 176, 312, 256, 32, ctypes.c_float(1e-6), None) == 4
+    assert f(None, y, A * 5, A * 7, 1, 4, 8, 8, 256, 32, ctypes.c_float(1e-6), None) == 1
+    assert f(MIS, y, A * 5, A * 7, 1, 4, 8, 8, 256, 32, ctypes.c_float(1e-6), None) == 3

@@ -22,7 +22,8 @@ WAN_OP_UPSAMPLE_PHASE_CONV = 3
 STATUS = {0: "WAN_OK", 1: "WAN_ERR_INVALID_ARG", 2: "WAN_ERR_UNSUPPORTED_SHAPE", 3: "WAN_ERR_MISALIGNED",
           4: "WAN_ERR_WORKSPACE", 5: "WAN_ERR_CUDA", 6: "WAN_ERR_TIMEOUT"}
 
-EXPORTS = ("wan_status_string", "wan_workspace_size", "wan_gn_silu", "wan_causal_conv3d", "wan_cache_update",
+EXPORTS = ("wan_status_string", "wan_workspace_size", "wan_gn_silu", "wan_gn_silu_noalloc", "wan_causal_conv3d",
+           "wan_cache_update",
            "wan_upsample_phase_weights", "wan_upsample_phase_conv", "wan_resblock", "wan_device_status")
 
 
@@ -58,6 +59,8 @@ def lib() -> ctypes.CDLL:
     L.wan_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
     L.wan_gn_silu.restype = I
     L.wan_gn_silu.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, S, P]
+    L.wan_gn_silu_noalloc.restype = I
+    L.wan_gn_silu_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P]
     L.wan_causal_conv3d.restype = I
     L.wan_causal_conv3d.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, S, P]
     L.wan_cache_update.restype = I
@@ -124,6 +127,20 @@ def wan_gn_silu(x, gamma, beta, groups: int, eps: float, y=None, ws=None, stream
     ws = _workspace(need, x.device, ws)
     _check(lib().wan_gn_silu(_ptr(x), _ptr(y), _ptr(gamma), _ptr(beta), N, T, H, W, C, groups, eps,
                              _ptr(ws), need if ws is not None else 0, _stream(stream)), "wan_gn_silu")
+    return y
+
+
+def wan_gn_silu_noalloc(x, gamma, beta, groups: int, eps: float, y=None, stream=None):
+    """wan_gn_silu without a workspace: the library's fixed device scratch is used instead (for
+    callers that cannot allocate). Calls that overlap on the GPU race on that scratch."""
+    _need(x, torch.bfloat16, "x")
+    _need(gamma, torch.float32, "gamma")
+    _need(beta, torch.float32, "beta")
+    N, T, H, W, C = x.shape
+    y = torch.empty_like(x) if y is None else y
+    _need(y, torch.bfloat16, "y")
+    _check(lib().wan_gn_silu_noalloc(_ptr(x), _ptr(y), _ptr(gamma), _ptr(beta), N, T, H, W, C, groups, eps,
+                                     _stream(stream)), "wan_gn_silu_noalloc")
     return y
 
 
