@@ -160,7 +160,10 @@ wan_status wan_causal_conv3d(const wan_bf16* a, const wan_bf16* cache_in, wan_bf
   unsigned* err = device_error_word();
   if (!err) return WAN_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = cuda_status(conv_launch(0, a, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, sm_count(), err, s));
+  if (head_supported(Cin, Cout))
+    st = cuda_status(head_launch(a, cache_in, w, bias, residual, y, N, T, H, W, Cin, sm_count(), err, s));
+  else
+    st = cuda_status(conv_launch(0, a, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, sm_count(), err, s));
   if (st != WAN_OK || !cache_out) return st;
   return cuda_status(cache_update_launch(a, cache_in, cache_out, N, T, H, W, Cin, sm_count(), s));
 }

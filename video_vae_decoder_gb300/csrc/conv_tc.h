@@ -12,6 +12,11 @@ cudaError_t conv_launch(int mode, const wan_bf16* a, const wan_bf16* cache_in, c
 // cache_out[n, j] = ([cache_in or zeros; a])[n, T + j], j = 0, 1.
 cudaError_t cache_update_launch(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out,
                                 int N, int T, int H, int W, int C, int sms, cudaStream_t stream);
+// Causal conv to exactly 12 output channels (the output head), Cin % 64 == 0 and Cin <= 256.
+bool head_supported(int Cin, int Cout);
+cudaError_t head_launch(const wan_bf16* a, const wan_bf16* cache_in, const wan_bf16* w, const wan_bf16* bias,
+                        const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W, int Cin, int sms,
+                        unsigned* err, cudaStream_t stream);
 cudaError_t phase_weights_launch(const wan_bf16* w3, wan_bf16* wp, int Cin, int Cout, int sms,
                                  cudaStream_t stream);
 }  // namespace wan
