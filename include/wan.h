@@ -77,7 +77,7 @@ size_t wan_workspace_size(wan_op op, int N, int T, int H, int W, int Cin, int Co
  *
  *   x, y         [N, T, H, W, C] bf16, device; y may not overlap x.
  *   gamma, beta  [C] fp32, device.
- *   groups       divides C; C % 8 == 0; C/8 <= 1024; (C/groups) % 8 == 0 or 8 % (C/groups) == 0.
+ *   groups       divides C; C % 8 == 0; C <= 2048; (C/groups) % 8 == 0 or 8 % (C/groups) == 0.
  *   eps          > 0.
  *   ws           >= wan_workspace_size(WAN_OP_GN_SILU, N, T, H, W, C, 0, groups) bytes.
  * Values are supported for |x| < 2^60 (the squares of deviations stay finite in fp32).
@@ -103,8 +103,9 @@ wan_status wan_gn_silu(const wan_bf16* x, wan_bf16* y, const float* gamma, const
  *     with that device current; make that first call before any stream capture.
  *   - All calls share the one array: calls that may overlap on the GPU (on different streams,
  *     or from different threads without ordering) race on it and must be serialised by the
- *     caller. Each call writes every scratch word it later reads, so the array needs no
- *     clearing between calls.
+ *     caller. Each call clears, on its stream, the one scratch word that must start at zero
+ *     (a grid-barrier counter) and writes every other word before reading it, so the array
+ *     needs no clearing by the caller between calls.
  * Arguments and their conditions are those of wan_gn_silu.
  */
 wan_status wan_gn_silu_noalloc(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta,

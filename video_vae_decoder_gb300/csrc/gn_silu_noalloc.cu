@@ -69,8 +69,9 @@ extern "C" wan_status wan_gn_silu_noalloc(const wan_bf16* x, wan_bf16* y, const 
   if (gn_silu_workspace(N, T, H, W, C, groups, sms) > kNoAllocScratchBytes) return WAN_ERR_WORKSPACE;
   void* scratch = scratch_address();
   if (!scratch) return WAN_ERR_CUDA;
-  // Every word of the scratch that the kernels read is written earlier in the same call (the
-  // per-span partial sums, then the per-channel coefficients), so nothing needs clearing.
+  // The launcher clears the one scratch word that must start at zero (a grid-barrier counter)
+  // at the start of every call; every other word the kernel reads it has written earlier in the
+  // same call (the per-span partial sums, then the per-channel coefficients).
   return gn_silu_launch(x, y, gamma, beta, N, T, H, W, C, groups, eps, scratch, sms,
                         static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? WAN_OK
