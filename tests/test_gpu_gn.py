@@ -65,3 +65,20 @@ def test_gn_deterministic(wan):
     y1 = bits(wan.wan_gn_silu(x, g, b, 32, EPS))
     y2 = bits(wan.wan_gn_silu(x, g, b, 32, EPS))
     assert np.array_equal(y1, y2)
+
+
+def test_gn_very_negative_z(wan):
+    # One outlier per group and large gammas put z in [-100, -80], where e^-|z| is subnormal in
+    # fp32 but z*sigmoid(z) is still a representable (tiny) bf16: the exact-range path.
+    N, T, H, W, C, G = 1, 2, 8, 8, 64, 32
+    x = synth.normal_f32((N, T, H, W, C), 0, "gn/negz/x")
+    x[:, :, 0, 0, :] = -30.0
+    xb = synth.f32_to_bf16_bits(x)
+    g = np.linspace(6.0, 11.0, C).astype(np.float32)
+    b = np.zeros(C, np.float32)
+    y = wan.wan_gn_silu(to_dev(xb), f32_dev(g), f32_dev(b), G, EPS)
+    ref = oracle.gn_silu(xb, g, b, G, EPS)
+    got = bits(y)
+    assert int(oracle.ulp_distance_bf16(got, ref).max()) <= 1
+    tiny = oracle.bf16_to_f64(ref[:, :, 0, 0, :])
+    assert np.any((tiny < 0) & (tiny > -1e-30)), "the case must reach the tiny-output range"

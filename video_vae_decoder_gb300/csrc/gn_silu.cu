@@ -8,6 +8,9 @@
 // GB300 layout of the work: ONE cooperative, persistent kernel in three phases separated by
 // two grid barriers (bounded waits; a barrier that times out records an error and the kernel
 // winds down):
+//   x streams through shared memory: each CTA keeps four 16 KB pieces of its work in flight with
+//   bulk async copies (cp.async.bulk, completion on an mbarrier), from the statistics items
+//   straight on into the apply items, so the apply pass's first pieces load during the barriers.
 //   A  statistics: work items are (frame, pixel span of ~64 KB). Every thread owns one 16-byte
 //      vector of 8 channels (so its groups are fixed) and accumulates, per channel, sum(d) and
 //      sum(d^2) of d = x - s, where s is one value of the channel's group in the frame (its
@@ -15,8 +18,8 @@
 //      (non-negative terms) with Dekker's Fast2Sum, two channels per packed fp32x2 instruction.
 //      The CTA merges its threads' pairs per group (float-float adds, fixed order) and writes
 //      one partial per (frame, span, group).
-//   B  finalize: one warp per (frame, group) adds the span partials in fp64 in a fixed order
-//      (lane-strided, then a butterfly), gets mean = s + S1/L and the population variance
+//   B  finalize: one warp per (frame, group) adds the span partials as float-float pairs in a
+//      fixed order (lane-strided, then a butterfly), gets in fp64 mean = s + S1/L and the variance
 //      S2/L - (S1/L)^2, and writes per channel the scale S = gamma/sqrt(var + eps) and shift
 //      B = beta - mean*S, each as an fp32 (hi, lo) pair.
 //   C  apply: z = (x*S_hi + B_hi) + (x*S_lo + B_lo) (two FMAs: z is accurate to fp32 rounding
@@ -46,13 +49,16 @@ struct GnPartial {  // one (frame, span, group): float-float sums of d and d^2
   float s1_hi, s1_lo, s2_hi, s2_lo;
 };
 
+// a - b on float2 in one packed instruction: b * (-1) + a with one rounding equals the rounded
+// difference (there is no packed subtract).
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __ffma2_rn(b, make_float2(-1.f, -1.f), a); }
+
 // Knuth TwoSum: s + e == a + b exactly (round-to-nearest, no overflow). Packed on float2.
 __device__ __forceinline__ void two_sum2(float2& hi, float2& lo, float2 x) {
   const float2 s = __fadd2_rn(hi, x);
-  const float2 bb = __fadd2_rn(s, make_float2(-hi.x, -hi.y));
-  const float2 t1 = __fadd2_rn(s, make_float2(-bb.x, -bb.y));   // s - bb
-  const float2 e1 = __fadd2_rn(hi, make_float2(-t1.x, -t1.y));  // hi - (s - bb)
-  const float2 e2 = __fadd2_rn(x, make_float2(-bb.x, -bb.y));   // x - bb
+  const float2 bb = sub2(s, hi);
+  const float2 e1 = sub2(hi, sub2(s, bb));  // hi - (s - bb)
+  const float2 e2 = sub2(x, bb);            // x - bb
   lo = __fadd2_rn(lo, __fadd2_rn(e1, e2));
   hi = s;
 }
@@ -61,8 +67,7 @@ __device__ __forceinline__ void two_sum2(float2& hi, float2& lo, float2 x) {
 // most the rounding of the smaller (earlier) partial sum.
 __device__ __forceinline__ void fast_two_sum2(float2& hi, float2& lo, float2 x) {
   const float2 s = __fadd2_rn(hi, x);
-  const float2 z = __fadd2_rn(s, make_float2(-hi.x, -hi.y));
-  lo = __fadd2_rn(lo, __fadd2_rn(x, make_float2(-z.x, -z.y)));
+  lo = __fadd2_rn(lo, sub2(x, sub2(s, hi)));
   hi = s;
 }
 
@@ -76,14 +81,6 @@ __device__ __forceinline__ void ff_add(float& hi, float& lo, float bhi, float bl
   lo = __fsub_rn(t, __fsub_rn(hi, s));
 }
 
-__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-
 __device__ __forceinline__ void stg_v4(void* p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
@@ -95,21 +92,33 @@ __device__ __forceinline__ float2 unpack2(uint32_t w) {
 
 __device__ __forceinline__ float bf16_at(const wan_bf16* p) { return __uint_as_float(((uint32_t)*p) << 16); }
 
-__device__ __forceinline__ float ex2_approx(float x) {
+__device__ __forceinline__ float ex2_approx(float x) {  // subnormal results kept
   float y;
   asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ float rcp_approx(float x) {
+__device__ __forceinline__ float ex2_approx_ftz(float x) {
   float y;
-  asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float rcp_approx_ftz(float x) {  // used on [1, 2] only
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
-// z * sigmoid(z): t = e^-|z| (never overflows), sigmoid = 1/(1+t) or t/(1+t).
-__device__ __forceinline__ float silu_f32(float z) {
-  const float t = ex2_approx(-fabsf(z) * 1.4426950408889634f);
-  const float r = rcp_approx(1.0f + t);
+// z * sigmoid(z): t = e^-|z| (never overflows), sigmoid = 1/(1+t) or t/(1+t). The fast form
+// flushes t to zero once it is subnormal (|z| > 87); vectors holding a z < -80 take the exact
+// form, whose result there is still a representable bf16.
+__device__ __forceinline__ float silu_fast(float z) {
+  const float t = ex2_approx_ftz(fminf(z, -z) * 1.4426950408889634f);
+  const float r = rcp_approx_ftz(1.0f + t);
+  return z < 0.f ? (z * t) * r : z * r;
+}
+__device__ __forceinline__ float silu_exact_range(float z) {
+  const float t = ex2_approx(fminf(z, -z) * 1.4426950408889634f);
+  const float r = rcp_approx_ftz(1.0f + t);
   return z < 0.f ? (z * t) * r : z * r;
 }
 
@@ -141,6 +150,10 @@ __device__ bool grid_barrier(unsigned* ctr, unsigned target, unsigned* err, int*
   return *s_flag != 0;
 }
 
+constexpr int kSlots = 6;          // 16 KB pieces of x in flight per CTA
+constexpr int kVecPerThread = 4;   // 16-byte vectors per thread per piece
+constexpr int kPiecesPerSpan = 4;  // a statistics partial covers 4 pieces (about 64 KB)
+
 struct GnArgs {
   const wan_bf16* x;
   wan_bf16* y;
@@ -150,30 +163,75 @@ struct GnArgs {
   float4* coef;     // [F][C]: (S_hi, S_lo, B_hi, B_lo)
   unsigned* bar;    // grid-barrier arrival counter, zero at launch
   unsigned* err;
-  int P, C, G, F, span_px, spans;
+  int P, C, G, F, piece_px, spans, items;
   float eps;
   double inv_len;   // 1 / (H * W * C / G)
 };
 
+// The CTA's stream of pieces: first its statistics items (item = blockIdx + k * grid), then its
+// apply items in the reverse global order, kPiecesPerSpan pieces each. Piece n -> frame f and
+// pixel range [q0, q1) (empty past the end of a frame). False past the end of the stream.
+__device__ __forceinline__ bool piece_of(const GnArgs& a, int n, int cnt, int& f, int& q0, int& q1) {
+  const int per = cnt * kPiecesPerSpan;
+  if (n >= 2 * per) return false;
+  const bool apply = n >= per;
+  const int m = apply ? n - per : n;
+  const int k = m / kPiecesPerSpan, j = m - k * kPiecesPerSpan;
+  int item = blockIdx.x + k * gridDim.x;
+  if (apply) item = a.items - 1 - item;
+  f = item / a.spans;
+  const int piece = (item - f * a.spans) * kPiecesPerSpan + j;
+  q0 = min(a.P, piece * a.piece_px);
+  q1 = min(a.P, q0 + a.piece_px);
+  return true;
+}
+
 __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
-  extern __shared__ float red[];  // [blockDim][slots][4] float-float partial sums
-  __shared__ int s_flag;
+  extern __shared__ __align__(128) uint8_t gsm[];
+  uint8_t* slots = gsm;                                                  // kSlots x piece bytes
   const int vpp = a.C >> 3;
   const int ppi = blockDim.x / vpp;
+  const int piece_bytes = a.piece_px * a.C * 2;
+  float* red = reinterpret_cast<float*>(gsm + kSlots * piece_bytes);   // [blockDim][slots][4]
+  __shared__ uint64_t full[kSlots];
+  __shared__ int s_flag;
   const int tid = threadIdx.x;
   const int j = tid % vpp;
   const int lp = tid / vpp;
   const bool active = lp < ppi;
   const int cg = a.C / a.G;
-  const int slots = cg >= 8 ? 1 : 8 / cg;
-  const int items = a.F * a.spans;
-  const size_t pstride = (size_t)a.C * 2;
-  constexpr int U = 4;
+  const int nslot = cg >= 8 ? 1 : 8 / cg;
+  const int cnt = (a.items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;  // items of this CTA
+
+  auto issue = [&](int n) {  // thread 0: start loading piece n of the stream
+    int f, q0, q1;
+    if (!piece_of(a, n, cnt, f, q0, q1)) return;
+    uint64_t* bar = &full[n % kSlots];
+    const uint32_t bytes = (uint32_t)(q1 - q0) * a.C * 2;
+    if (bytes) {
+      mbar_arrive_expect_tx(bar, bytes);
+      bulk_load(slots + (n % kSlots) * piece_bytes, a.x + ((size_t)f * a.P + q0) * a.C, bytes, bar);
+    } else {
+      mbar_arrive(bar);
+    }
+  };
+  if (tid == 0) {
+    for (int s = 0; s < kSlots; ++s) mbar_init(&full[s], 1);
+    fence_mbarrier_init();
+    for (int n = 0; n < kSlots; ++n) issue(n);
+  }
+  __syncthreads();
+  int n = 0;  // next piece of the stream to consume
+
+  // Waits for piece n (all threads), bounded; the failure is made CTA-uniform by the caller.
+  auto wait_piece = [&](int nn) -> bool {
+    return mbar_wait(&full[nn % kSlots], (uint32_t)((nn / kSlots) & 1), a.err, kDevErrTimeoutGrid);
+  };
 
   // ---------------------------------------------------------------- A: statistics
-  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+  for (int k = 0; k < cnt; ++k) {
+    const int item = blockIdx.x + k * gridDim.x;
     const int f = item / a.spans, span = item - f * a.spans;
-    const int p0 = span * a.span_px, p1 = min(a.P, p0 + a.span_px);
     const wan_bf16* xf = a.x + (size_t)f * a.P * a.C;
     float2 s1h[4], s1l[4], s2h[4], s2l[4], sh[4];
 #pragma unroll
@@ -183,39 +241,34 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
       sh[w] = active ? make_float2(bf16_at(xf + (c0 / cg) * cg), bf16_at(xf + ((c0 + 1) / cg) * cg))
                      : make_float2(0.f, 0.f);
     }
-    if (active) {
-      const char* base = reinterpret_cast<const char*>(xf) + (size_t)j * 16;
-      int p = p0 + lp;
-      for (; p + (U - 1) * ppi < p1; p += U * ppi) {
-        uint4 v[U];
+    for (int pj = 0; pj < kPiecesPerSpan; ++pj, ++n) {
+      bool ok = wait_piece(n);
+      int f2, q0, q1;
+      piece_of(a, n, cnt, f2, q0, q1);
+      if (ok && active) {
+        const uint8_t* src = slots + (n % kSlots) * piece_bytes + (size_t)j * 16;
 #pragma unroll
-        for (int u = 0; u < U; ++u) v[u] = ldg_nc_v4(base + (size_t)(p + u * ppi) * pstride);
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        for (int i = 0; i < kVecPerThread; ++i) {
+          const int pl = lp + i * ppi;
+          if (q0 + pl >= q1) break;
+          const uint4 v = *reinterpret_cast<const uint4*>(src + (size_t)pl * vpp * 16);
+          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
-            const float2 d = __fadd2_rn(unpack2(wv[w]), make_float2(-sh[w].x, -sh[w].y));
+            const float2 d = sub2(unpack2(wv[w]), sh[w]);
             two_sum2(s1h[w], s1l[w], d);
             fast_two_sum2(s2h[w], s2l[w], __fmul2_rn(d, d));
           }
         }
       }
-      for (; p < p1; p += ppi) {
-        const uint4 v = ldg_nc_v4(base + (size_t)p * pstride);
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const float2 d = __fadd2_rn(unpack2(wv[w]), make_float2(-sh[w].x, -sh[w].y));
-          two_sum2(s1h[w], s1l[w], d);
-          fast_two_sum2(s2h[w], s2l[w], __fmul2_rn(d, d));
-        }
-      }
+      if (__syncthreads_or(!ok)) return;  // every thread is done with the slot
+      if (tid == 0) issue(n + kSlots);
     }
+    (void)span;
     // Fold this thread's 8 channel partials by group slot (channels of a group are consecutive:
     // a vector holds 8/cg groups when cg < 8, else part of one group).
-    float* mine = red + (size_t)tid * slots * 4;
-    for (int q = 0; q < slots; ++q) {
+    float* mine = red + (size_t)tid * nslot * 4;
+    for (int q = 0; q < nslot; ++q) {
       float ah = 0.f, al = 0.f, bh = 0.f, bl = 0.f;
       if (active) {
 #pragma unroll
@@ -239,7 +292,7 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
       const int q = cg >= 8 ? 0 : (c_first % 8) / cg;
       for (int jj = c_first / 8; jj <= c_last / 8; ++jj)
         for (int l = 0; l < ppi; ++l) {
-          const float* r = red + ((size_t)(l * vpp + jj) * slots + q) * 4;
+          const float* r = red + ((size_t)(l * vpp + jj) * nslot + q) * 4;
           ff_add(ah, al, r[0], r[1]);
           ff_add(bh, bl, r[2], r[3]);
         }
@@ -257,19 +310,26 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
   // ---------------------------------------------------------------- B: finalize per (frame, group)
   {
     const int warps = blockDim.x >> 5, warp = tid >> 5, lane = tid & 31;
-    for (int pr = blockIdx.x * warps + warp; pr < a.F * a.G; pr += gridDim.x * warps) {
+    // pair p -> CTA p % grid, warp (p / grid) % warps: the few pairs spread over many SMs.
+    for (int pr = warp * gridDim.x + blockIdx.x; pr < a.F * a.G; pr += gridDim.x * warps) {
       const int f = pr / a.G, g = pr - f * a.G;
-      double s1 = 0.0, s2 = 0.0;
-      for (int s = lane; s < a.spans; s += 32) {
-        const GnPartial q = a.part[((size_t)f * a.spans + s) * a.G + g];
-        s1 += (double)q.s1_hi + (double)q.s1_lo;
-        s2 += (double)q.s2_hi + (double)q.s2_lo;
+      // Float-float sums (fp64 issue is scarce on this GPU): lane-strided, then a butterfly.
+      // The float-float add is commutative bit for bit (TwoSum's error term is unique), so every
+      // lane ends with the same bits.
+      float h1 = 0.f, l1 = 0.f, h2 = 0.f, l2 = 0.f;
+      for (int sp = lane; sp < a.spans; sp += 32) {
+        const GnPartial q = a.part[((size_t)f * a.spans + sp) * a.G + g];
+        ff_add(h1, l1, q.s1_hi, q.s1_lo);
+        ff_add(h2, l2, q.s2_hi, q.s2_lo);
       }
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {  // fixed butterfly; addition commutes, so every
-        s1 += __shfl_xor_sync(0xffffffffu, s1, off);  // lane ends with the same bits
-        s2 += __shfl_xor_sync(0xffffffffu, s2, off);
+      for (int off = 1; off < 32; off <<= 1) {
+        const float oh1 = __shfl_xor_sync(0xffffffffu, h1, off), ol1 = __shfl_xor_sync(0xffffffffu, l1, off);
+        const float oh2 = __shfl_xor_sync(0xffffffffu, h2, off), ol2 = __shfl_xor_sync(0xffffffffu, l2, off);
+        ff_add(h1, l1, oh1, ol1);
+        ff_add(h2, l2, oh2, ol2);
       }
+      const double s1 = (double)h1 + (double)l1, s2 = (double)h2 + (double)l2;
       // fp64 division and square root are slow on this GPU: 1/L comes from the host and
       // 1/sqrt(v) is an fp32 estimate refined by two Newton steps r <- r (3 - v r^2) / 2 in fp64
       // (relative error 2^-22 -> 2^-44 -> below fp64 rounding).
@@ -284,8 +344,8 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
       } else {
         rstd = 1.0 / sqrt(v);
       }
-      for (int k = lane; k < cg; k += 32) {
-        const int c = g * cg + k;
+      for (int kk = lane; kk < cg; kk += 32) {
+        const int c = g * cg + kk;
         const double S = (double)a.gamma[c] * rstd;
         const double B = (double)a.beta[c] - mean * S;
         const float shi = (float)S, bhi = (float)B;
@@ -296,47 +356,60 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
   if (!grid_barrier(a.bar, 2 * gridDim.x, a.err, &s_flag)) return;
 
   // ---------------------------------------------------------------- C: apply, newest spans first
-  if (!active) return;
-  for (int k = blockIdx.x; k < items; k += gridDim.x) {
-    const int item = items - 1 - k;
-    const int f = item / a.spans, span = item - f * a.spans;
-    const int p0 = span * a.span_px, p1 = min(a.P, p0 + a.span_px);
+  for (int k = 0; k < cnt; ++k) {
+    const int item = a.items - 1 - (int)(blockIdx.x + k * gridDim.x);
+    const int f = item / a.spans;
     float2 shi[4], slo[4], bhi[4], blo[4];
-    const float4* cf = a.coef + (size_t)f * a.C + 8 * j;
+    if (active) {
+      const float4* cf = a.coef + (size_t)f * a.C + 8 * j;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float4 u = cf[2 * w], v = cf[2 * w + 1];
-      shi[w] = make_float2(u.x, v.x);
-      slo[w] = make_float2(u.y, v.y);
-      bhi[w] = make_float2(u.z, v.z);
-      blo[w] = make_float2(u.w, v.w);
-    }
-    const size_t frame_off = (size_t)f * a.P * a.C;
-    const char* xb = reinterpret_cast<const char*>(a.x + frame_off) + (size_t)j * 16;
-    char* yb = reinterpret_cast<char*>(a.y + frame_off) + (size_t)j * 16;
-    for (int p = p0 + lp; p < p1; p += U * ppi) {
-      uint4 v[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (p + u * ppi < p1) v[u] = ldg_nc_v4(xb + (size_t)(p + u * ppi) * pstride);
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (p + u * ppi >= p1) break;
-        uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          const float2 xv = unpack2(wv[w]);
-          const float2 z = __fadd2_rn(__ffma2_rn(xv, shi[w], bhi[w]), __ffma2_rn(xv, slo[w], blo[w]));
-          wv[w] = pack_bf16x2(silu_f32(z.x), silu_f32(z.y));
-        }
-        stg_v4(yb + (size_t)(p + u * ppi) * pstride, make_uint4(wv[0], wv[1], wv[2], wv[3]));
+      for (int w = 0; w < 4; ++w) {
+        const float4 u = cf[2 * w], v = cf[2 * w + 1];
+        shi[w] = make_float2(u.x, v.x);
+        slo[w] = make_float2(u.y, v.y);
+        bhi[w] = make_float2(u.z, v.z);
+        blo[w] = make_float2(u.w, v.w);
       }
+    }
+    for (int pj = 0; pj < kPiecesPerSpan; ++pj, ++n) {
+      bool ok = wait_piece(n);
+      int f2, q0, q1;
+      piece_of(a, n, cnt, f2, q0, q1);
+      if (ok && active) {
+        const uint8_t* src = slots + (n % kSlots) * piece_bytes + (size_t)j * 16;
+        char* dst = reinterpret_cast<char*>(a.y + ((size_t)f * a.P + q0) * a.C) + (size_t)j * 16;
+#pragma unroll
+        for (int i = 0; i < kVecPerThread; ++i) {
+          const int pl = lp + i * ppi;
+          if (q0 + pl >= q1) break;
+          const uint4 v = *reinterpret_cast<const uint4*>(src + (size_t)pl * vpp * 16);
+          uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+          float2 z[4];
+          float zmin = 0.f;
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            const float2 xv = unpack2(wv[w]);
+            z[w] = __fadd2_rn(__ffma2_rn(xv, shi[w], bhi[w]), __ffma2_rn(xv, slo[w], blo[w]));
+            zmin = fminf(zmin, fminf(z[w].x, z[w].y));
+          }
+          if (zmin >= -80.f) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) wv[w] = pack_bf16x2(silu_fast(z[w].x), silu_fast(z[w].y));
+          } else {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) wv[w] = pack_bf16x2(silu_exact_range(z[w].x), silu_exact_range(z[w].y));
+          }
+          stg_v4(dst + (size_t)pl * vpp * 16, make_uint4(wv[0], wv[1], wv[2], wv[3]));
+        }
+      }
+      if (__syncthreads_or(!ok)) return;
+      if (tid == 0) issue(n + kSlots);
     }
   }
 }
 
 struct GnPlan {
-  int P, F, threads, ppi, span_px, spans, slots;
+  int P, F, threads, ppi, piece_px, spans, items, slots;
   size_t part_bytes, coef_bytes, smem;
 };
 
@@ -347,19 +420,17 @@ GnPlan plan(int N, int T, int H, int W, int C, int G) {
   const int vpp = C / 8;
   pl.threads = (kThreads / vpp) * vpp;  // C <= 2048: vpp <= 256
   pl.ppi = pl.threads / vpp;
-  // Spans depend on the frame's geometry only (about 64 KB of x each), never on the number of
-  // frames in the call: a frame's statistics are summed in the same order in any chunking.
-  int span_px = (65536 / (C * 2)) / pl.ppi * pl.ppi;
-  if (span_px < pl.ppi) span_px = pl.ppi;
-  const int whole = cdiv(pl.P, pl.ppi) * pl.ppi;
-  if (span_px > whole) span_px = whole;
-  pl.span_px = span_px;
-  pl.spans = cdiv(pl.P, span_px);
+  // Pieces and spans depend on the frame's geometry only, never on the number of frames in the
+  // call: a frame's statistics are summed in the same order in any chunking of the video.
+  pl.piece_px = kVecPerThread * pl.ppi;
+  const int pieces = cdiv(pl.P, pl.piece_px);
+  pl.spans = cdiv(pieces, kPiecesPerSpan);
+  pl.items = pl.F * pl.spans;
   const int cg = C / G;
   pl.slots = cg >= 8 ? 1 : 8 / cg;
   pl.part_bytes = (size_t)pl.F * pl.spans * G * sizeof(GnPartial);
   pl.coef_bytes = (size_t)pl.F * C * sizeof(float4);
-  pl.smem = (size_t)pl.threads * pl.slots * 4 * sizeof(float);
+  pl.smem = (size_t)kSlots * pl.piece_px * C * 2 + (size_t)pl.threads * pl.slots * 4 * sizeof(float);
   return pl;
 }
 
@@ -399,18 +470,25 @@ cudaError_t gn_silu_launch(const wan_bf16* x, wan_bf16* y, const float* gamma, c
   a.C = C;
   a.G = G;
   a.F = pl.F;
-  a.span_px = pl.span_px;
+  a.piece_px = pl.piece_px;
   a.spans = pl.spans;
+  a.items = pl.items;
   a.eps = eps;
   a.inv_len = 1.0 / ((double)pl.P * (C / G));
   // Persistent grid: every CTA resident at once (the cooperative launch checks it).
+  cudaError_t e = cudaFuncSetAttribute(gn_silu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
+  if (e != cudaSuccess) return e;
   int per_sm = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gn_silu_kernel, pl.threads, pl.smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gn_silu_kernel, pl.threads, pl.smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  // As many CTAs as fit, then evened out so every CTA gets the same number of items (a CTA with
+  // fewer items would only wait at the grid barriers).
+  const int items = pl.items;
   int grid = per_sm * sms;
-  const int items = pl.F * pl.spans;
   if (grid > items) grid = items;
+  const int rounds = cdiv(items, grid);
+  grid = cdiv(items, rounds);
   // The barrier counter is the one scratch word that must start at zero.
   e = cudaMemsetAsync(a.bar, 0, sizeof(unsigned), stream);
   if (e != cudaSuccess) return e;
