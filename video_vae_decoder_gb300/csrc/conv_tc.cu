@@ -55,18 +55,21 @@ struct Tile {
   int n, t0, h0, w0, ph, nb;
 };
 
+// Tile order: N block fastest, then phase, then the frame block, then the pixel block. Tiles of
+// the same pixels in neighbouring frames run side by side, so the input frames they share (an
+// output frame reads frames t-2..t) are fetched from HBM about once and then hit in L2.
 __device__ __forceinline__ Tile decode_tile(const ConvArgs& a, int idx) {
   Tile t;
   t.nb = idx % a.n_blks;
   idx /= a.n_blks;
   t.ph = idx % a.phases;
   idx /= a.phases;
+  t.t0 = (idx % a.tiles_t) * a.TT;
+  idx /= a.tiles_t;
   t.w0 = (idx % a.tiles_w) * a.TW;
   idx /= a.tiles_w;
   t.h0 = (idx % a.tiles_h) * a.TH;
-  idx /= a.tiles_h;
-  t.t0 = (idx % a.tiles_t) * a.TT;
-  t.n = idx / a.tiles_t;
+  t.n = idx / a.tiles_h;
   return t;
 }
 
@@ -408,6 +411,12 @@ size_t conv_workspace() { return 0; }
 cudaError_t conv_launch(int mode, const wan_bf16* a, const wan_bf16* cache_in, const wan_bf16* w,
                         const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H,
                         int W, int Cin, int Cout, int sms, unsigned* err, cudaStream_t stream) {
+  if (conv_pair_supported(Cout)) {
+    int TT = 1, TH = 16, TW = 8;
+    choose_tile(T, H, W, TT, TH, TW);
+    return conv_pair_launch(mode, a, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, TT, TH, TW, sms, err,
+                            stream);
+  }
   ConvArgs args{};
   args.N = N;
   args.T = T;
