@@ -322,7 +322,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // This warp is done with the accumulator: one arrival per warp on the even CTA's barrier.
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc == 0 ? leader_empty0 : leader_empty1);
+      if (lane == 0) mbar_arrive_cluster_relaxed(acc == 0 ? leader_empty0 : leader_empty1);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;

@@ -8,19 +8,17 @@
 //
 // GB300 design (one kernel, no intermediate tensor):
 //   * GEMM per (image row r, output frame t): G[p, n] = sum_{kt, ci} W'[n, kt*Cin + ci]
-//     * x[t + kt - 2, r, p, ci] for the 128 pixels p of a column strip. W' (112 x 3*Cin bf16,
-//     168 KB at Cin = 256) is built once per CTA straight into shared memory in the 128-byte
-//     swizzled K-major layout and stays resident; only x streams through a 3-stage TMA ring.
-//   * Each CTA owns (batch item, pair of output frames t and t+1, 128-pixel column strip, band
-//     of image rows) and walks the rows of its band. A pair shares the input frames t-1 and t,
-//     so 4 input rows feed 2 output rows; the two accumulators (2 x 112 TMEM columns) are
-//     double-buffered so the epilogue of row r overlaps the MMAs of row r+1.
-//   * The epilogue applies the 3x3 stencil: out[h, w, c] = sum_{i,j} G[h+i-1, w+j-1, (i,j,c)].
-//     The column shift j is a warp shuffle (with the lanes at warp edges exchanged through
-//     shared memory); the row shift i is carried in registers: G of row r adds its i=2 part to
-//     output row r-1 (then complete and stored), its i=1 part to row r, its i=0 part to row r+1.
-//   * Strips overlap by two pixels (each strip's first and last pixel lack a neighbour), bands
-//     by one image row on each side (the rows just outside a band feed its edge outputs).
+//     * x[t + kt - 2, r, p, ci] for the 128 pixels p of a column strip. The kernel runs on CTA
+//     pairs (clusters of 2, tcgen05 .cta_group::2): each CTA owns one strip (M = 256 over the
+//     pair) and keeps HALF of W' (56 of its 112 rows, 84 KB at Cin = 256) resident in shared
+//     memory in the 128-byte swizzled K-major layout, built once straight from the weights. That
+//     leaves room for an 8-deep TMA ring of input strips (one resident copy of all of W' would
+//     leave room for 3, and the MMAs would wait on load latency). One thread of the even CTA
+//     issues the M256 x N112 MMAs; the odd CTA's loads complete on the even CTA's barriers.
+//   * Each pair owns (batch item, pair of output frames t and t+1, two neighbouring 128-pixel
+//     strips, band of image rows) and walks the rows of its band. A frame pair shares the input
+//     frames t-1 and t, so 4 input rows feed 2 output rows; the two accumulators (2 x 112 TMEM
+//     columns) are double-buffered so the epilogue of row r overlaps the MMAs of row r+1.
 // Reduction order per output is fixed (taps, then the 9 stencil terms), independent of the
 // band/strip/pair placement and of chunking along T.
 #include <cuda.h>
@@ -39,22 +37,25 @@ constexpr int kCout = 12;
 constexpr int kNP = 112;                 // 9 * 12 = 108 columns, padded to a multiple of 16
 constexpr int kStripW = 128;             // pixels per strip (the MMA's M)
 constexpr int kStripOut = kStripW - 2;   // outputs per strip
-constexpr int kStages = 3;
-constexpr int kThreads = 192;
+constexpr int kStages = 8;
+constexpr int kThreads = 320;            // producer, MMA issuer, 2 epilogue warpgroups
 constexpr int kABytes = kStripW * 128;   // one 64-channel slice of one image row strip
-constexpr int kBBlockBytes = kNP * 128;  // one 64-wide K block of W'
+constexpr int kBRows = kNP / 2;            // W' rows held by each CTA of a pair
+constexpr int kBBlockBytes = kBRows * 128;  // this CTA's rows of one 64-wide K block of W'
 constexpr int kMaxKB = 12;               // 3 frames x (Cin <= 256) / 64
 constexpr int kBOffset = kStages * kABytes;
 constexpr int kBarOffset = kBOffset + kMaxKB * kBBlockBytes;
 constexpr int kXchgOffset = kBarOffset + 256;
-constexpr int kXchgBytes = 2 * 4 * 2 * 2 * 3 * kCout * 4;  // [parity][quarter][frame][side][i][c]
+constexpr int kFrames = 4;               // output frames per item (4 x 112 of 512 TMEM columns)
+constexpr int kFramesPerGroup = kFrames / 2;  // frames of an item per epilogue warpgroup
+constexpr int kXchgBytes = 2 * 2 * 4 * 2 * 3 * kCout * 4;  // [group][parity][quarter][side][i][c]
 constexpr int kSmemTotal = kXchgOffset + kXchgBytes + 1024;
-constexpr int kTmemCols = 512;           // 2 buffers x 2 frames x 112 columns = 448
+constexpr int kTmemCols = 512;           // 4 frames x 112 columns = 448
 
 struct HeadArgs {
   int N, T, H, W, Cin;
   int kb_per_frame;          // Cin / 64
-  int pairs, strips, bands, band_rows, items;
+  int quads, strips, strip_pairs, bands, band_rows, items;
   int has_cache;
   const wan_bf16* w;         // [12, 3, 3, 3, Cin]
   const wan_bf16* bias;      // [12] or null
@@ -65,17 +66,22 @@ struct HeadArgs {
 
 struct Item {
   int n, t, w0, h0, h1;
+  bool valid;  // false for the odd CTA of a pair when the strip count is odd
 };
 
-__device__ __forceinline__ Item decode_item(const HeadArgs& a, int idx) {
+// item -> frame pair (fastest), band, pair of strips, batch item; `which` picks the strip of the
+// pair (the even CTA takes the first).
+__device__ __forceinline__ Item decode_item(const HeadArgs& a, int idx, int which) {
   Item it;
-  const int pair = idx % a.pairs;
-  idx /= a.pairs;
+  const int quad = idx % a.quads;
+  idx /= a.quads;
   const int band = idx % a.bands;
   idx /= a.bands;
-  const int strip = idx % a.strips;
-  it.n = idx / a.strips;
-  it.t = 2 * pair;
+  int strip = 2 * (idx % a.strip_pairs) + which;
+  it.n = idx / a.strip_pairs;
+  it.valid = strip < a.strips;
+  if (!it.valid) strip = a.strips + 1;  // entirely right of the frame: its loads read zeros
+  it.t = kFrames * quad;
   it.w0 = strip * kStripOut - 1;
   it.h0 = band * a.band_rows;
   it.h1 = min(a.H, it.h0 + a.band_rows);
@@ -86,66 +92,88 @@ __device__ __forceinline__ Item decode_item(const HeadArgs& a, int idx) {
 __device__ __forceinline__ int row_first(const Item& it) { return max(it.h0 - 1, 0); }
 __device__ __forceinline__ int row_last(const HeadArgs& a, const Item& it) { return min(it.h1, a.H - 1); }
 
-// Input frames of one row step: tau in [t-2, t+1] (t+1 only when frame t+1 exists); frames
-// before the chunk without a cache read zeros and are skipped.
+// Input frames of one row step: tau in [t-2, t+3] (up to the chunk's last frame); frames before
+// the chunk without a cache read zeros and are skipped.
 __device__ __forceinline__ int tau_first(const HeadArgs& a, const Item& it) {
   return a.has_cache ? it.t - 2 : max(it.t - 2, 0);
 }
 __device__ __forceinline__ int tau_last(const HeadArgs& a, const Item& it) {
-  return it.t + 1 < a.T ? it.t + 1 : it.t;
-}
-
-// 32 lanes x 4 columns
-__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
-  uint32_t r[4];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+  return min(it.t + kFrames - 1, a.T - 1);
 }
 
 // G columns of tap row i for this lane's pixel: g[j*12 + c] = G[p, (i*3 + j)*12 + c].
 __device__ __forceinline__ void load_tap_row(uint32_t taddr, int i, float (&g)[36]) {
-  float a[16], b[16], c[4];
-  tmem_ld16(taddr + i * 36, a);
-  tmem_ld16(taddr + i * 36 + 16, b);
-  tmem_ld4(taddr + i * 36 + 32, c);
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    g[k] = a[k];
-    g[16 + k] = b[k];
-  }
-#pragma unroll
-  for (int k = 0; k < 4; ++k) g[32 + k] = c[k];
+  uint32_t* r = reinterpret_cast<uint32_t*>(g);
+  const uint32_t a = taddr + i * 36;
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(a));
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(a + 16));
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35])
+               : "r"(a + 32));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// One output pixel: 12 channels + bias (+ residual), rounded once to bf16, 24 bytes stored.
+__device__ __forceinline__ void store_row(const HeadArgs& args, const float (&acc)[kCout], size_t pix) {
+  float o[kCout];
+#pragma unroll
+  for (int c = 0; c < kCout; ++c) o[c] = acc[c] + (args.bias ? __uint_as_float(((uint32_t)args.bias[c]) << 16) : 0.f);
+  if (args.residual) {
+    const uint2* rp = reinterpret_cast<const uint2*>(args.residual + pix * kCout);
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const uint2 rv = rp[k];
+      o[4 * k] += bf16lo_to_f32(rv.x);
+      o[4 * k + 1] += bf16hi_to_f32(rv.x);
+      o[4 * k + 2] += bf16lo_to_f32(rv.y);
+      o[4 * k + 3] += bf16hi_to_f32(rv.y);
+    }
+  }
+  uint2* yp = reinterpret_cast<uint2*>(args.y + pix * kCout);
+#pragma unroll
+  for (int k = 0; k < 3; ++k)
+    yp[k] = make_uint2(pack_bf16x2(o[4 * k], o[4 * k + 1]), pack_bf16x2(o[4 * k + 2], o[4 * k + 3]));
+}
+
+template <int KBPF>  // Cin / 64
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     head_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_cache,
                    const HeadArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBarOffset);
   uint64_t* empty = full + kStages;
-  uint64_t* tmem_full = empty + kStages;
-  uint64_t* tmem_empty = tmem_full + 2;
-  uint64_t* mma_done = tmem_empty + 2;
-  uint64_t* xbar = mma_done + 1;  // edge-exchange barrier of the 128 epilogue threads
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 1);
+  uint64_t* tmem_full = empty + kStages;       // per output frame of the item
+  uint64_t* tmem_empty = tmem_full + kFrames;  // per output frame, in the even CTA
+  uint64_t* mma_done = tmem_empty + kFrames;
+  uint64_t* xbar = mma_done + 1;  // edge-exchange barriers, one per epilogue warpgroup (128 threads)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xbar + 2);
   float* xchg = reinterpret_cast<float*>(smem + kXchgOffset);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int KB = 3 * args.kb_per_frame;
+  const int KB = 3 * KBPF;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int cluster = blockIdx.x >> 1;
+  const int nclusters = gridDim.x >> 1;
 
   // W' -> shared memory, 128-byte swizzle (16-byte chunk j of row n stored at chunk j ^ (n & 7)).
   {
-    const int chunks = KB * kNP * 8;
+    const int chunks = KB * kBRows * 8;
     for (int q = threadIdx.x; q < chunks; q += blockDim.x) {
       const int jc = q & 7;
-      const int n = (q >> 3) % kNP;
-      const int kb = (q >> 3) / kNP;
+      const int nl = (q >> 3) % kBRows;  // row within this CTA's half
+      const int kb = (q >> 3) / kBRows;
+      const int n = (int)rank * kBRows + nl;
       uint4 v = make_uint4(0, 0, 0, 0);
       if (n < 9 * kCout) {
         const int c = n % kCout, ij = n / kCout, i = ij / 3, j = ij % 3;
@@ -153,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kt = k / args.Cin, ci = k % args.Cin;
         v = *reinterpret_cast<const uint4*>(args.w + ((((size_t)c * 3 + kt) * 3 + i) * 3 + j) * args.Cin + ci);
       }
-      *reinterpret_cast<uint4*>(smem + kBOffset + kb * kBBlockBytes + n * 128 + ((jc ^ (n & 7)) << 4)) = v;
+      *reinterpret_cast<uint4*>(smem + kBOffset + kb * kBBlockBytes + nl * 128 + ((jc ^ (nl & 7)) << 4)) = v;
     }
     fence_proxy_async_smem();
   }
@@ -162,22 +190,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kFrames; ++s) {
       mbar_init(&tmem_full[s], 1);
-      mbar_init(&tmem_empty[s], 128);
+      mbar_init(&tmem_empty[s], 8);  // one arrival per epilogue warp of both CTAs
     }
     mbar_init(mma_done, 1);
-    mbar_init(xbar, 128);
+    mbar_init(&xbar[0], 128);
+    mbar_init(&xbar[1], 128);
     fence_mbarrier_init();
     prefetch_tensormap(&tm_a);
     prefetch_tensormap(&tm_cache);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, kTmemCols);  // one warp in each CTA of the pair, collectively
+    tmem_relinquish_pair();
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // the peer's barriers exist before anyone arrives on them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -186,24 +216,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0, armed = 0, armed_parity = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < args.items; item += gridDim.x) {
-      const Item it = decode_item(args, item);
+    for (int item = cluster; ok && item < args.items; item += nclusters) {
+      const Item it = decode_item(args, item, (int)rank);
       const int r1 = row_last(args, it);
       for (int r = row_first(it); ok && r <= r1; ++r) {
         for (int tau = tau_first(args, it); tau <= tau_last(args, it); ++tau) {
-          for (int kb = 0; kb < args.kb_per_frame; ++kb) {
-            if (!mbar_wait(&empty[stage], phase ^ 1, args.err, kDevErrTimeoutProducer)) {
+          for (int kb = 0; kb < KBPF; ++kb) {
+            if (!mbar_wait_cluster(&empty[stage], phase ^ 1, args.err, kDevErrTimeoutProducer)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full[stage], kABytes);
-            armed |= 1u << stage;
-            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            if (leader) {
+              mbar_arrive_expect_tx(&full[stage], 2 * kABytes);
+              armed |= 1u << stage;
+              armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+            }
             uint8_t* dst = smem + stage * kABytes;
+            const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);  // the even CTA's barrier
             if (tau < 0)
-              tma_load_5d(dst, &tm_cache, &full[stage], kb * 64, it.w0, r, tau + 2, it.n);
+              tma_load_5d_pair(dst, &tm_cache, bar, kb * 64, it.w0, r, tau + 2, it.n);
             else
-              tma_load_5d(dst, &tm_a, &full[stage], kb * 64, it.w0, r, tau, it.n);
+              tma_load_5d_pair(dst, &tm_a, bar, kb * 64, it.w0, r, tau, it.n);
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1;
@@ -215,235 +248,196 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < kStages; ++s)
       if (armed & (1u << s)) mbar_wait(&full[s], (armed_parity >> s) & 1, args.err, kDevErrTimeoutDrain);
-  } else if (warp == 1 && lane == 0) {
-    // ---------------------------------------------------------------- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(128, kNP);
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ---------------------------------------------------------------- MMA issuer (even CTA)
+    // Per row: input frames tau ascending. The KBPF tiles of one input frame are waited for
+    // together; then, for each output frame o the input frame is a tap of (kt = tau - (t+o) + 2
+    // in 0..2), the 4 * KBPF MMAs into o's accumulator go out back to back with all descriptors
+    // known in advance: the tensor pipe stays full only while MMAs follow each other directly,
+    // so no address arithmetic or branch sits between two of them. Per accumulator the order
+    // is tau, then K block, then K step. Frame o is complete after tau = t+o, and is first
+    // written in a row only after the epilogue released it for that row.
+    constexpr uint32_t idesc = idesc_bf16_f32(256, kNP);
+    constexpr uint32_t kBStep = kBBlockBytes >> 4;  // descriptor units between K blocks of W'
     const uint32_t b_base = smem_u32(smem + kBOffset);
     int stage = 0;
     uint32_t phase = 0;
-    int buf = 0;
-    uint32_t buf_phase = 0;
+    uint32_t rc = 0;  // rows processed so far (parity of the per-frame TMEM barriers)
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < args.items; item += gridDim.x) {
-      const Item it = decode_item(args, item);
-      const bool second = it.t + 1 < args.T;
+    for (int item = cluster; ok && item < args.items; item += nclusters) {
+      const Item it = decode_item(args, item, 0);
+      const int nfr = min(kFrames, args.T - it.t);
       const int r1 = row_last(args, it);
-      for (int r = row_first(it); ok && r <= r1; ++r) {
-        if (!mbar_wait(&tmem_empty[buf], buf_phase ^ 1, args.err, kDevErrTimeoutMma)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d0 = tmem_base + buf * 2 * kNP;  // frame t
-        const uint32_t d1 = d0 + kNP;                   // frame t + 1
-        bool first0 = true, first1 = true;
+      for (int r = row_first(it); ok && r <= r1; ++r, ++rc) {
+        uint32_t fresh = (1u << nfr) - 1;  // frames not yet written in this row
         for (int tau = tau_first(args, it); ok && tau <= tau_last(args, it); ++tau) {
-          const int kt0 = tau - it.t + 2;  // tap of this input frame for output frame t
-          const int kt1 = tau - it.t + 1;  // ... and for output frame t + 1
-          for (int kb = 0; kb < args.kb_per_frame; ++kb) {
-            if (!mbar_wait(&full[stage], phase, args.err, kDevErrTimeoutMma)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint64_t a_desc = smem_desc_sw128(smem_u32(smem + stage * kABytes));
-            if (kt0 >= 0 && kt0 <= 2) {
-              const uint64_t b_desc = smem_desc_sw128(b_base + (kt0 * args.kb_per_frame + kb) * kBBlockBytes);
+          uint64_t a_desc[KBPF];
+          int st[KBPF];
 #pragma unroll
-              for (int k = 0; k < 4; ++k) mma_bf16(d0, a_desc + 2 * k, b_desc + 2 * k, idesc, (first0 && k == 0) ? 0u : 1u);
-              first0 = false;
-            }
-            if (second && kt1 >= 0 && kt1 <= 2) {
-              const uint64_t b_desc = smem_desc_sw128(b_base + (kt1 * args.kb_per_frame + kb) * kBBlockBytes);
-#pragma unroll
-              for (int k = 0; k < 4; ++k) mma_bf16(d1, a_desc + 2 * k, b_desc + 2 * k, idesc, (first1 && k == 0) ? 0u : 1u);
-              first1 = false;
-            }
-            mma_commit(&empty[stage]);
+          for (int kb = 0; kb < KBPF; ++kb) {
+            if (ok && !mbar_wait_cluster(&full[stage], phase, args.err, kDevErrTimeoutMma)) ok = false;
+            st[kb] = stage;
+            a_desc[kb] = smem_desc_sw128(smem_u32(smem + stage * kABytes));
             if (++stage == kStages) {
               stage = 0;
               phase ^= 1;
             }
           }
-        }
-        if (!ok) break;
-        mma_commit(&tmem_full[buf]);
-        if (++buf == 2) {
-          buf = 0;
-          buf_phase ^= 1;
+          if (!ok) break;
+          tc_fence_after();
+          const int o_lo = max(tau - it.t, 0), o_hi = min(tau - it.t + 2, nfr - 1);
+          for (int o = o_lo; o <= o_hi; ++o) {
+            const bool first = (fresh >> o) & 1u;
+            if (first) {
+              if (!mbar_wait_cluster(&tmem_empty[o], (rc & 1) ^ 1, args.err, kDevErrTimeoutMma)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              fresh &= ~(1u << o);
+            }
+            const uint32_t d = tmem_base + o * kNP;
+            const int kt = tau - it.t - o + 2;
+            const uint64_t b_desc = smem_desc_sw128(b_base + kt * KBPF * kBBlockBytes);
+#pragma unroll
+            for (int kb = 0; kb < KBPF; ++kb)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_bf16_pair(d, a_desc[kb] + 2 * k, b_desc + kb * kBStep + 2 * k, idesc,
+                              (first && kb == 0 && k == 0) ? 0u : 1u);
+          }
+          if (!ok) break;
+#pragma unroll
+          for (int kb = 0; kb < KBPF; ++kb) mma_commit_pair(&empty[st[kb]], 0x3);
+          const int done = tau - it.t;  // frame t+done has seen its last input (kt = 2)
+          if (done >= 0 && done < nfr) mma_commit_pair(&tmem_full[done], 0x3);
         }
       }
     }
-    mma_commit(mma_done);
+    mma_commit_pair(mma_done, 0x1);
     mbar_wait(mma_done, 0, args.err, kDevErrTimeoutDrain);
   } else if (warp >= 2) {
     // ---------------------------------------------------------------- stencil epilogue
+    // Two warpgroups; group g owns frames 2g and 2g+1 of every item. A warp may read only its
+    // TMEM lane quarter (warp index mod 4), so each group covers the 128 pixels once.
+    const int group = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int q = quarter * 32 + lane;  // pixel index within the strip
-    float bias[kCout];
-#pragma unroll
-    for (int c = 0; c < kCout; ++c) bias[c] = args.bias ? __uint_as_float(((uint32_t)args.bias[c]) << 16) : 0.f;
-    int buf = 0;
-    uint32_t buf_phase = 0;
+    uint64_t* gbar = &xbar[group];
+    float* gx = xchg + group * (2 * 4 * 2 * 3 * kCout);
+    uint32_t rc = 0;
     int parity = 0;
     uint32_t xphase = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < args.items; item += gridDim.x) {
-      const Item it = decode_item(args, item);
-      const int nframes = it.t + 1 < args.T ? 2 : 1;
+    uint32_t leader_empty[kFramesPerGroup];
+#pragma unroll
+    for (int k = 0; k < kFramesPerGroup; ++k)
+      leader_empty[k] = mapa_shared(smem_u32(&tmem_empty[group * kFramesPerGroup + k]), 0);
+    for (int item = cluster; ok && item < args.items; item += nclusters) {
+      const Item it = decode_item(args, item, (int)rank);
+      const int nfr = min(kFrames, args.T - it.t);
       const int wcol = it.w0 + q;
-      const bool col_ok = q >= 1 && q <= kStripW - 2 && wcol >= 0 && wcol < args.W;
-      // Partial outputs carried across rows: prev = row r-1, cur = row r (per frame).
-      float prev[2][kCout], cur[2][kCout];
+      const bool col_ok = it.valid && q >= 1 && q <= kStripW - 2 && wcol >= 0 && wcol < args.W;
+      // Partial outputs carried across rows: prev = row r-1, cur = row r (per frame of the group).
+      float prev[kFramesPerGroup][kCout], cur[kFramesPerGroup][kCout];
 #pragma unroll
-      for (int f = 0; f < 2; ++f)
+      for (int k = 0; k < kFramesPerGroup; ++k)
 #pragma unroll
-        for (int c = 0; c < kCout; ++c) prev[f][c] = cur[f][c] = 0.f;
+        for (int c = 0; c < kCout; ++c) prev[k][c] = cur[k][c] = 0.f;
       const int r0 = row_first(it), r1 = row_last(args, it);
-      for (int r = r0; r <= r1; ++r) {
-        if (!mbar_wait(&tmem_full[buf], buf_phase, args.err, kDevErrTimeoutEpilogue)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        float next[2][kCout];
+      for (int r = r0; r <= r1; ++r, ++rc) {
+        const int ho = r - 1;  // output row completed by this row's G
 #pragma unroll
-        for (int f = 0; f < 2; ++f)
-#pragma unroll
-          for (int c = 0; c < kCout; ++c) next[f][c] = 0.f;
-        float* xw = xchg + ((parity * 4 + quarter) * 2) * 2 * 3 * kCout;  // [frame][side][i][c]
-#pragma unroll
-        for (int f = 0; f < 2; ++f) {
-          if (f >= nframes) break;
-          const uint32_t taddr = tmem_base + (uint32_t)(buf * 2 * kNP + f * kNP) + ((uint32_t)(quarter * 32) << 16);
+        for (int k = 0; k < kFramesPerGroup; ++k) {
+          const int f = group * kFramesPerGroup + k;
+          if (f >= nfr) break;
+          if (!mbar_wait_cluster(&tmem_full[f], rc & 1, args.err, kDevErrTimeoutEpilogue)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          float next[kCout];
+          float* xw = gx + (parity * 4 + quarter) * 2 * 3 * kCout;  // [side][i][c]
+          const uint32_t taddr = tmem_base + (uint32_t)(f * kNP) + ((uint32_t)(quarter * 32) << 16);
 #pragma unroll
           for (int i = 0; i < 3; ++i) {
             float g[36];
             __syncwarp();
             load_tap_row(taddr, i, g);
-            float s[kCout];
+            float sv[kCout];
 #pragma unroll
             for (int c = 0; c < kCout; ++c) {
               const float left = __shfl_up_sync(0xffffffffu, g[c], 1);        // G[p-1, (i,0,c)]
               const float right = __shfl_down_sync(0xffffffffu, g[24 + c], 1);  // G[p+1, (i,2,c)]
-              s[c] = ((lane > 0 ? left : 0.f) + g[12 + c]) + (lane < 31 ? right : 0.f);
+              sv[c] = ((lane > 0 ? left : 0.f) + g[12 + c]) + (lane < 31 ? right : 0.f);
             }
             // Warp-edge lanes publish what the neighbouring warp's edge lane is missing.
             if (lane == 31) {
 #pragma unroll
-              for (int c = 0; c < kCout; ++c) xw[((f * 2 + 0) * 3 + i) * kCout + c] = g[c];
+              for (int c = 0; c < kCout; ++c) xw[(0 * 3 + i) * kCout + c] = g[c];
             }
             if (lane == 0) {
 #pragma unroll
-              for (int c = 0; c < kCout; ++c) xw[((f * 2 + 1) * 3 + i) * kCout + c] = g[24 + c];
+              for (int c = 0; c < kCout; ++c) xw[(1 * 3 + i) * kCout + c] = g[24 + c];
             }
 #pragma unroll
             for (int c = 0; c < kCout; ++c) {
-              if (i == 2) prev[f][c] += s[c];
-              else if (i == 1) cur[f][c] += s[c];
-              else next[f][c] = s[c];
+              if (i == 2) prev[k][c] += sv[c];
+              else if (i == 1) cur[k][c] += sv[c];
+              else next[c] = sv[c];
             }
           }
-        }
-        // TMEM buffer free for the next row's MMAs.
-        tc_fence_before();
-        mbar_arrive(&tmem_empty[buf]);
-        if (++buf == 2) {
-          buf = 0;
-          buf_phase ^= 1;
-        }
-        mbar_arrive(xbar);  // publishes this thread's edge values (release) ...
-        if (!mbar_wait(xbar, xphase, args.err, kDevErrTimeoutEpilogue)) {  // ... and sees the others'
-          ok = false;
-          break;
-        }
-        xphase ^= 1;
-        // Edge fix-ups: lane 0 adds G[p-1, (i,0,c)] from the previous quarter's lane 31,
-        // lane 31 adds G[p+1, (i,2,c)] from the next quarter's lane 0.
-        if ((lane == 0 && quarter > 0) || (lane == 31 && quarter < 3)) {
-          const int nq = lane == 0 ? quarter - 1 : quarter + 1;
-          const int side = lane == 0 ? 0 : 1;
-          const float* xn = xchg + ((parity * 4 + nq) * 2) * 2 * 3 * kCout;
-#pragma unroll
-          for (int f = 0; f < 2; ++f) {
-            if (f >= nframes) break;
+          // Frame f's accumulator is free for the next row: one arrival per warp, even CTA.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster_relaxed(leader_empty[k]);
+          mbar_arrive(gbar);  // publishes this thread's edge values (release) ...
+          if (!mbar_wait(gbar, xphase, args.err, kDevErrTimeoutEpilogue)) {  // ... and sees the others'
+            ok = false;
+            break;
+          }
+          xphase ^= 1;
+          // Edge fix-ups: lane 0 adds G[p-1, (i,0,c)] from the previous quarter's lane 31,
+          // lane 31 adds G[p+1, (i,2,c)] from the next quarter's lane 0.
+          if ((lane == 0 && quarter > 0) || (lane == 31 && quarter < 3)) {
+            const int nq = lane == 0 ? quarter - 1 : quarter + 1;
+            const int side = lane == 0 ? 0 : 1;
+            const float* xn = gx + (parity * 4 + nq) * 2 * 3 * kCout;
 #pragma unroll
             for (int c = 0; c < kCout; ++c) {
-              prev[f][c] += xn[((f * 2 + side) * 3 + 2) * kCout + c];
-              cur[f][c] += xn[((f * 2 + side) * 3 + 1) * kCout + c];
-              next[f][c] += xn[((f * 2 + side) * 3 + 0) * kCout + c];
+              prev[k][c] += xn[(side * 3 + 2) * kCout + c];
+              cur[k][c] += xn[(side * 3 + 1) * kCout + c];
+              next[c] += xn[(side * 3 + 0) * kCout + c];
             }
           }
-        }
-        parity ^= 1;
-        // Output row r-1 is complete.
-        const int ho = r - 1;
-        if (col_ok && ho >= it.h0 && ho < it.h1) {
-#pragma unroll
-          for (int f = 0; f < 2; ++f) {
-            if (f >= nframes) break;
-            const size_t pix = (((size_t)it.n * args.T + it.t + f) * args.H + ho) * args.W + wcol;
-            float o[kCout];
-#pragma unroll
-            for (int c = 0; c < kCout; ++c) o[c] = prev[f][c] + bias[c];
-            if (args.residual) {
-              const uint2* rp = reinterpret_cast<const uint2*>(args.residual + pix * kCout);
-#pragma unroll
-              for (int k = 0; k < 3; ++k) {
-                const uint2 rv = rp[k];
-                o[4 * k] += bf16lo_to_f32(rv.x);
-                o[4 * k + 1] += bf16hi_to_f32(rv.x);
-                o[4 * k + 2] += bf16lo_to_f32(rv.y);
-                o[4 * k + 3] += bf16hi_to_f32(rv.y);
-              }
-            }
-            uint2* yp = reinterpret_cast<uint2*>(args.y + pix * kCout);
-#pragma unroll
-            for (int k = 0; k < 3; ++k)
-              yp[k] = make_uint2(pack_bf16x2(o[4 * k], o[4 * k + 1]), pack_bf16x2(o[4 * k + 2], o[4 * k + 3]));
-          }
-        }
-#pragma unroll
-        for (int f = 0; f < 2; ++f)
+          parity ^= 1;
+          if (col_ok && ho >= it.h0 && ho < it.h1)
+            store_row(args, prev[k], (((size_t)it.n * args.T + it.t + f) * args.H + ho) * args.W + wcol);
 #pragma unroll
           for (int c = 0; c < kCout; ++c) {
-            prev[f][c] = cur[f][c];
-            cur[f][c] = next[f][c];
+            prev[k][c] = cur[k][c];
+            cur[k][c] = next[c];
           }
+        }
+        if (!ok) break;
       }
       if (!ok) break;
       // The last computed row was the frame's last row: its output row (r1) has no row below.
       if (r1 == args.H - 1 && col_ok && r1 >= it.h0 && r1 < it.h1) {
 #pragma unroll
-        for (int f = 0; f < 2; ++f) {
-          if (f >= nframes) break;
-          const size_t pix = (((size_t)it.n * args.T + it.t + f) * args.H + r1) * args.W + wcol;
-          float o[kCout];
-#pragma unroll
-          for (int c = 0; c < kCout; ++c) o[c] = prev[f][c] + bias[c];
-          if (args.residual) {
-            const uint2* rp = reinterpret_cast<const uint2*>(args.residual + pix * kCout);
-#pragma unroll
-            for (int k = 0; k < 3; ++k) {
-              const uint2 rv = rp[k];
-              o[4 * k] += bf16lo_to_f32(rv.x);
-              o[4 * k + 1] += bf16hi_to_f32(rv.x);
-              o[4 * k + 2] += bf16lo_to_f32(rv.y);
-              o[4 * k + 3] += bf16hi_to_f32(rv.y);
-            }
-          }
-          uint2* yp = reinterpret_cast<uint2*>(args.y + pix * kCout);
-#pragma unroll
-          for (int k = 0; k < 3; ++k)
-            yp[k] = make_uint2(pack_bf16x2(o[4 * k], o[4 * k + 1]), pack_bf16x2(o[4 * k + 2], o[4 * k + 3]));
+        for (int k = 0; k < kFramesPerGroup; ++k) {
+          const int f = group * kFramesPerGroup + k;
+          if (f >= nfr) break;
+          store_row(args, prev[k], (((size_t)it.n * args.T + it.t + f) * args.H + r1) * args.W + wcol);
         }
       }
     }
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // neither CTA leaves while the pair's MMAs or arrivals may still touch it
   tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn_head() {
@@ -487,23 +481,54 @@ cudaError_t head_launch(const wan_bf16* a, const wan_bf16* cache_in, const wan_b
   args.W = W;
   args.Cin = Cin;
   args.kb_per_frame = Cin / 64;
-  args.pairs = cdiv(T, 2);
+  args.quads = cdiv(T, kFrames);
   args.strips = cdiv(W, kStripOut);
+  args.strip_pairs = cdiv(args.strips, 2);
   args.has_cache = cache_in != nullptr;
   args.w = w;
   args.bias = bias;
   args.residual = residual;
   args.y = y;
   args.err = err;
-  // Rows per band: the fewest rounds over the SMs, counting the two halo rows of every band.
-  const long long base = (long long)N * args.pairs * args.strips;
+  void (*kern)(const CUtensorMap, const CUtensorMap, const HeadArgs) = nullptr;
+  switch (args.kb_per_frame) {
+    case 1: kern = head_tc_kernel<1>; break;
+    case 2: kern = head_tc_kernel<2>; break;
+    case 3: kern = head_tc_kernel<3>; break;
+    case 4: kern = head_tc_kernel<4>; break;
+    default: return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
+  if (e != cudaSuccess) return e;
+  // CTA pairs the GPU can hold at once (a pair lives in one GPC).
+  static int max_clusters[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int slots = sms / 2;
+  if (dev >= 0 && dev < 64) {
+    if (max_clusters[dev] == 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+      cfg.blockDim = dim3(kThreads, 1, 1);
+      cfg.dynamicSmemBytes = kSmemTotal;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = sms / 2;
+      }
+      max_clusters[dev] = n;
+    }
+    slots = max_clusters[dev];
+  }
+  // Rows per band: the fewest rounds over the CTA pairs, counting the two halo rows of a band.
+  const long long base = (long long)N * args.quads * args.strip_pairs;
   long long best_cost = -1;
   int best_bands = 1;
   for (int bands = 1; bands <= H && bands <= 256; ++bands) {
     const int rows = cdiv(H, bands);
     const int nb = cdiv(H, rows);
     const long long items = base * nb;
-    const long long rounds = (items + sms - 1) / sms;
+    const long long rounds = (items + slots - 1) / slots;
     const long long cost = rounds * (rows + 2);
     if (best_cost < 0 || cost < best_cost) {
       best_cost = cost;
@@ -521,10 +546,8 @@ cudaError_t head_launch(const wan_bf16* a, const wan_bf16* cache_in, const wan_b
   } else {
     tc = ta;
   }
-  cudaError_t e = cudaFuncSetAttribute(head_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
-  if (e != cudaSuccess) return e;
-  const int grid = args.items < sms ? args.items : sms;
-  head_tc_kernel<<<grid, kThreads, kSmemTotal, stream>>>(ta, tc, args);
+  const int clusters = args.items < slots ? args.items : slots;
+  kern<<<2 * clusters, kThreads, kSmemTotal, stream>>>(ta, tc, args);
   return cudaGetLastError();
 }
 
