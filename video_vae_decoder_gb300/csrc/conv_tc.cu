@@ -411,12 +411,8 @@ size_t conv_workspace() { return 0; }
 cudaError_t conv_launch(int mode, const wan_bf16* a, const wan_bf16* cache_in, const wan_bf16* w,
                         const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H,
                         int W, int Cin, int Cout, int sms, unsigned* err, cudaStream_t stream) {
-  if (conv_pair_supported(Cout)) {
-    int TT = 1, TH = 16, TW = 8;
-    choose_tile(T, H, W, TT, TH, TW);
-    return conv_pair_launch(mode, a, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, TT, TH, TW, sms, err,
-                            stream);
-  }
+  if (conv_pair_supported(Cout))
+    return conv_pair_launch(mode, a, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, sms, err, stream);
   ConvArgs args{};
   args.N = N;
   args.T = T;

@@ -13,7 +13,7 @@ cudaError_t conv_launch(int mode, const wan_bf16* a, const wan_bf16* cache_in, c
 bool conv_pair_supported(int Cout);
 cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_in, const wan_bf16* w,
                              const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W,
-                             int Cin, int Cout, int TT, int TH, int TW, int sms, unsigned* err, cudaStream_t stream);
+                             int Cin, int Cout, int sms, unsigned* err, cudaStream_t stream);
 // cache_out[n, j] = ([cache_in or zeros; a])[n, T + j], j = 0, 1.
 cudaError_t cache_update_launch(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out,
                                 int N, int T, int H, int W, int C, int sms, cudaStream_t stream);
