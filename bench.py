@@ -125,7 +125,7 @@ CASES = ("all", "gn", "c256", "up", "c1024", "head")
 
 
 class Workload:
-    def __init__(self, dev, case="all", seed=0):
+    def __init__(self, dev, case="all", seed=0, head_frames=16):
         import numpy as np
         import torch
         from video_vae_decoder_gb300 import synth
@@ -165,7 +165,7 @@ class Workload:
         self.x5 = n((1, 4, 44, 78, 1024) if want("c1024") else small + (1024,), "bench/c1024/x")
         self.blocks5 = [block(1024, f"bench/c1024/block{i}") for i in range(2 if want("c1024") else 0)]
         # head
-        hshape = (1, 16, 704, 1248, 256) if want("head") else (1, 1, 8, 8, 256)
+        hshape = (1, head_frames, 704, 1248, 256) if want("head") else (1, 1, 8, 8, 256)
         self.xh = n(hshape, "bench/head/x")
         self.wh = n((12, 3, 3, 3, 256), "bench/head/w", 0.0, float(np.sqrt(1.0 / (27 * 256))))
         self.yh = torch.empty(hshape[:-1] + (12,), dtype=bf, device=dev)
@@ -195,7 +195,7 @@ class Workload:
         if want("up"):
             self.flops["up"] = phase_flops(1, 4, 44, 78, 512, 512)
         if want("head"):
-            self.flops["head"] = conv_flops(1, 16, 704, 1248, 256, 12)
+            self.flops["head"] = conv_flops(1, head_frames, 704, 1248, 256, 12)
         self.gn_bytes = 4.0 * self.gn_x.numel()
 
     # ---- one step as the sequence of C-ABI calls, each bracketed by events -----------------
@@ -266,7 +266,7 @@ def run_ours(args, rank, world, dev):
     import torch
     from video_vae_decoder_gb300 import binding as wan
     torch.cuda.set_device(dev)
-    wl = Workload(dev, args.case)
+    wl = Workload(dev, args.case, head_frames=args.head_frames)
     calls = wl.step_calls()
     stream = torch.cuda.current_stream()
     # warm-up (also fills the caches: the timed steps are steady-state chunks with history)
@@ -368,7 +368,10 @@ def run_ours(args, rank, world, dev):
                 "unit": "TFLOP/s", "frac": kernels[dom]["tflops"] / pk_tf,
                 "frac_of_sustained": kernels[dom]["tflops"] / pk["bf16_tflops_sustained"],
                 "peak_source": f"{pk['source']} {pk_tf_note}"}
-    roof["traffic"] = None
+    # DRAM bytes (read + write) per launch from one ncu capture of the current kernel build
+    # (profiles/conv_tc2_c256_chunk.md); None for kernels without a capture of their current build.
+    traffic = {"conv_c256": 172.297472e6 + 75.833856e6}
+    roof["traffic"] = traffic.get(roof["kernel"])
     roof["share_of_step"] = shares[dom] / ms
     launches = sum(k for _, k, _ in calls) * args.steps
 
@@ -492,6 +495,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--head-frames", type=int, default=16,
+                    help="frames of the head's input (smaller values make a case small enough for ncu --set full)")
     ap.add_argument("--case", default="all", choices=CASES,
                     help="time one part of the step only (profiling captures); the default is the whole step")
     args = ap.parse_args()
