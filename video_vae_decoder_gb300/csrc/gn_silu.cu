@@ -8,10 +8,9 @@
 // GB300 layout of the work: ONE cooperative, persistent kernel in three phases separated by
 // two grid barriers (bounded waits; a barrier that times out records an error and the kernel
 // winds down):
-//   x streams through shared memory: each CTA keeps four 16 KB pieces of its work in flight with
-//   bulk async copies (cp.async.bulk, completion on an mbarrier), from the statistics items
-//   straight on into the apply items, so the apply pass's first pieces load during the barriers.
-//   A  statistics: work items are (frame, pixel span of ~64 KB). Every thread owns one 16-byte
+//   A  statistics: work items are (frame, pixel span of ~64 KB), dealt round-robin to the CTAs.
+//      x streams through shared memory: each CTA keeps six 16 KB pieces in flight with bulk async
+//      copies (cp.async.bulk, completion on an mbarrier). Every thread owns one 16-byte
 //      vector of 8 channels (so its groups are fixed) and accumulates, per channel, sum(d) and
 //      sum(d^2) of d = x - s, where s is one value of the channel's group in the frame (its
 //      first pixel). Both sums are fp32 pairs (hi, lo): sum(d) with Knuth's TwoSum, sum(d^2)
@@ -22,10 +21,12 @@
 //      fixed order (lane-strided, then a butterfly), gets in fp64 mean = s + S1/L and the variance
 //      S2/L - (S1/L)^2, and writes per channel the scale S = gamma/sqrt(var + eps) and shift
 //      B = beta - mean*S, each as an fp32 (hi, lo) pair.
-//   C  apply: z = (x*S_hi + B_hi) + (x*S_lo + B_lo) (two FMAs: z is accurate to fp32 rounding
-//      even where x*S and B nearly cancel), then z * sigmoid(z) with sigmoid = 1/(1+e^-z) for
-//      z >= 0 and e^z/(1+e^z) for z < 0, rounded once to bf16. Items run in the reverse order
-//      of phase A, so the most recently read spans (still in L2) are read again first.
+//   C  apply, newest items first (their x is still in L2), read with plain 16-byte loads
+//      (eight in flight per thread); the frame's coefficients reach shared memory with one bulk
+//      copy per CTA. z = (x*S_hi + B_hi) + (x*S_lo + B_lo) (two FMAs: z is accurate to fp32
+//      rounding even where x*S and B nearly cancel), then z * sigmoid(z) = z / (1 + e^-z)
+//      (z e^z / (1 + e^z) for vectors holding a z < -80, whose result may be subnormal), rounded
+//      once to bf16.
 // x is read from HBM once (phase A); phase C re-reads it mostly from L2 and writes y. The
 // pages' second, centred pass over x is replaced by the shifted one-pass sums: the shift is a
 // value of the group itself, so the subtraction in the variance loses only the few bits of
@@ -102,20 +103,24 @@ __device__ __forceinline__ float ex2_approx_ftz(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-__device__ __forceinline__ float rcp_approx_ftz(float x) {  // used on [1, 2] only
+__device__ __forceinline__ float rcp_approx_ftz(float x) {  // used on [1, 5.6e34]
   float y;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
-// z * sigmoid(z): t = e^-|z| (never overflows), sigmoid = 1/(1+t) or t/(1+t). The fast form
-// flushes t to zero once it is subnormal (|z| > 87); vectors holding a z < -80 take the exact
-// form, whose result there is still a representable bf16.
-__device__ __forceinline__ float silu_fast(float z) {
-  const float t = ex2_approx_ftz(fminf(z, -z) * 1.4426950408889634f);
-  const float r = rcp_approx_ftz(1.0f + t);
-  return z < 0.f ? (z * t) * r : z * r;
+// SiLU of two values for z >= -80: z / (1 + e^-z), with e^-z = 2^(-z log2 e) <= 2^116 (no overflow;
+// it underflows to 0 for large z, where the result is z) and 1 + e^-z <= 5.6e34, whose reciprocal
+// is a normal fp32 number (no flush). For z << 0, 1 + e^-z rounds to e^-z and the quotient to
+// z e^z with fp32 relative precision.
+__device__ __forceinline__ float2 silu2_fast(float2 z) {
+  const float2 m = __fmul2_rn(z, make_float2(-1.4426950408889634f, -1.4426950408889634f));
+  const float2 u = __fadd2_rn(make_float2(ex2_approx_ftz(m.x), ex2_approx_ftz(m.y)), make_float2(1.f, 1.f));
+  return __fmul2_rn(z, make_float2(rcp_approx_ftz(u.x), rcp_approx_ftz(u.y)));
 }
+
+// z * sigmoid(z): t = e^-|z| (never overflows), sigmoid = 1/(1+t) or t/(1+t). Used for vectors
+// holding a z < -80, whose result may be subnormal.
 __device__ __forceinline__ float silu_exact_range(float z) {
   const float t = ex2_approx(fminf(z, -z) * 1.4426950408889634f);
   const float r = rcp_approx_ftz(1.0f + t);
@@ -153,13 +158,15 @@ __device__ bool grid_barrier(unsigned* ctr, unsigned target, unsigned* err, int*
 constexpr int kSlots = 6;          // 16 KB pieces of x in flight per CTA
 constexpr int kVecPerThread = 4;   // 16-byte vectors per thread per piece
 constexpr int kPiecesPerSpan = 4;  // a statistics partial covers 4 pieces (about 64 KB)
+constexpr int kApplyUnroll = 8;    // 16-byte loads in flight per thread in the apply phase
+constexpr int kFinBatch = 8;       // partials in flight per lane in the finalize
 
 struct GnArgs {
   const wan_bf16* x;
   wan_bf16* y;
   const float* gamma;
   const float* beta;
-  GnPartial* part;  // [F][spans][G]
+  GnPartial* part;  // [F][G][spans]
   float4* coef;     // [F][C]: (S_hi, S_lo, B_hi, B_lo)
   unsigned* bar;    // grid-barrier arrival counter, zero at launch
   unsigned* err;
@@ -168,22 +175,12 @@ struct GnArgs {
   double inv_len;   // 1 / (H * W * C / G)
 };
 
-// The CTA's stream of pieces: first its statistics items (item = blockIdx + k * grid), then its
-// apply items in the reverse global order, kPiecesPerSpan pieces each. Piece n -> frame f and
-// pixel range [q0, q1) (empty past the end of a frame). False past the end of the stream.
-__device__ __forceinline__ bool piece_of(const GnArgs& a, int n, int cnt, int& f, int& q0, int& q1) {
-  const int per = cnt * kPiecesPerSpan;
-  if (n >= 2 * per) return false;
-  const bool apply = n >= per;
-  const int m = apply ? n - per : n;
-  const int k = m / kPiecesPerSpan, j = m - k * kPiecesPerSpan;
-  int item = blockIdx.x + k * gridDim.x;
-  if (apply) item = a.items - 1 - item;
+// Pixel range [q0, q1) of piece j of statistics item `item` (empty past the end of a frame).
+__device__ __forceinline__ void piece_range(const GnArgs& a, int item, int j, int& f, int& q0, int& q1) {
   f = item / a.spans;
   const int piece = (item - f * a.spans) * kPiecesPerSpan + j;
   q0 = min(a.P, piece * a.piece_px);
   q1 = min(a.P, q0 + a.piece_px);
-  return true;
 }
 
 __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
@@ -193,7 +190,10 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
   const int ppi = blockDim.x / vpp;
   const int piece_bytes = a.piece_px * a.C * 2;
   float* red = reinterpret_cast<float*>(gsm + kSlots * piece_bytes);   // [blockDim][slots][4]
+  float* s_shift = red + (size_t)blockDim.x * (a.C / a.G >= 8 ? 1 : 8 / (a.C / a.G)) * 4;  // [G]
+  float4* s_coef = reinterpret_cast<float4*>(slots);  // [C], phase C only (the slots are idle then)
   __shared__ uint64_t full[kSlots];
+  __shared__ uint64_t cbar;
   __shared__ int s_flag;
   const int tid = threadIdx.x;
   const int j = tid % vpp;
@@ -203,10 +203,14 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
   const int nslot = cg >= 8 ? 1 : 8 / cg;
   const int cnt = (a.items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;  // items of this CTA
 
+  // The CTA's stream of pieces: its statistics items (item = blockIdx + k * grid), kPiecesPerSpan
+  // pieces each; piece n is piece n % kPiecesPerSpan of the (n / kPiecesPerSpan)-th item.
   auto issue = [&](int n) {  // thread 0: start loading piece n of the stream
-    int f, q0, q1;
-    if (!piece_of(a, n, cnt, f, q0, q1)) return;
+    if (n >= cnt * kPiecesPerSpan) return;
+    const int k = n / kPiecesPerSpan, jj = n - k * kPiecesPerSpan;
     uint64_t* bar = &full[n % kSlots];
+    int f, q0, q1;
+    piece_range(a, blockIdx.x + k * gridDim.x, jj, f, q0, q1);
     const uint32_t bytes = (uint32_t)(q1 - q0) * a.C * 2;
     if (bytes) {
       mbar_arrive_expect_tx(bar, bytes);
@@ -232,19 +236,22 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
   for (int k = 0; k < cnt; ++k) {
     const int item = blockIdx.x + k * gridDim.x;
     const int f = item / a.spans, span = item - f * a.spans;
+    // The group shifts (each group's first value in the frame), loaded once per CTA: a
+    // per-thread load would send every thread of the grid to the same few L2 lines.
     const wan_bf16* xf = a.x + (size_t)f * a.P * a.C;
+    for (int g = tid; g < a.G; g += blockDim.x) s_shift[g] = bf16_at(xf + (size_t)g * cg);
+    __syncthreads();
     float2 s1h[4], s1l[4], s2h[4], s2l[4], sh[4];
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       s1h[w] = s1l[w] = s2h[w] = s2l[w] = make_float2(0.f, 0.f);
       const int c0 = 8 * j + 2 * w;
-      sh[w] = active ? make_float2(bf16_at(xf + (c0 / cg) * cg), bf16_at(xf + ((c0 + 1) / cg) * cg))
-                     : make_float2(0.f, 0.f);
+      sh[w] = active ? make_float2(s_shift[c0 / cg], s_shift[(c0 + 1) / cg]) : make_float2(0.f, 0.f);
     }
     for (int pj = 0; pj < kPiecesPerSpan; ++pj, ++n) {
-      bool ok = wait_piece(n);
+      const bool ok = wait_piece(n);
       int f2, q0, q1;
-      piece_of(a, n, cnt, f2, q0, q1);
+      piece_range(a, item, pj, f2, q0, q1);
       if (ok && active) {
         const uint8_t* src = slots + (n % kSlots) * piece_bytes + (size_t)j * 16;
 #pragma unroll
@@ -301,7 +308,7 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
       out.s1_lo = al;
       out.s2_hi = bh;
       out.s2_lo = bl;
-      a.part[((size_t)f * a.spans + span) * a.G + g] = out;
+      a.part[((size_t)f * a.G + g) * a.spans + span] = out;
     }
     __syncthreads();  // red is reused by the next item
   }
@@ -316,11 +323,21 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
       // Float-float sums (fp64 issue is scarce on this GPU): lane-strided, then a butterfly.
       // The float-float add is commutative bit for bit (TwoSum's error term is unique), so every
       // lane ends with the same bits.
+      // A lane adds spans lane, lane + 32, ... in order, loading kFinBatch of them at a time.
       float h1 = 0.f, l1 = 0.f, h2 = 0.f, l2 = 0.f;
-      for (int sp = lane; sp < a.spans; sp += 32) {
-        const GnPartial q = a.part[((size_t)f * a.spans + sp) * a.G + g];
-        ff_add(h1, l1, q.s1_hi, q.s1_lo);
-        ff_add(h2, l2, q.s2_hi, q.s2_lo);
+      const float4* src = reinterpret_cast<const float4*>(a.part) + ((size_t)f * a.G + g) * a.spans;
+      for (int sp0 = 0; sp0 < a.spans; sp0 += 32 * kFinBatch) {
+        float4 q[kFinBatch];
+#pragma unroll
+        for (int i = 0; i < kFinBatch; ++i) {
+          const int sp = sp0 + lane + 32 * i;
+          q[i] = sp < a.spans ? __ldcg(src + sp) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < kFinBatch; ++i) {  // adding (0, 0) to a normalised pair changes nothing
+          ff_add(h1, l1, q[i].x, q[i].y);
+          ff_add(h2, l2, q[i].z, q[i].w);
+        }
       }
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -356,12 +373,33 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
   if (!grid_barrier(a.bar, 2 * gridDim.x, a.err, &s_flag)) return;
 
   // ---------------------------------------------------------------- C: apply, newest spans first
+  // The frame's coefficients reach shared memory with one bulk copy per CTA (a per-thread load
+  // would send every thread of the grid to the same few L2 lines).
+  if (tid == 0) {
+    mbar_init(&cbar, 1);
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  int fcur = -1;
+  uint32_t cphase = 0;
+  float2 shi[4], slo[4], bhi[4], blo[4];
   for (int k = 0; k < cnt; ++k) {
-    const int item = a.items - 1 - (int)(blockIdx.x + k * gridDim.x);
+    const int item = a.items - 1 - (int)(blockIdx.x + k * gridDim.x);  // newest spans first
     const int f = item / a.spans;
-    float2 shi[4], slo[4], bhi[4], blo[4];
-    if (active) {
-      const float4* cf = a.coef + (size_t)f * a.C + 8 * j;
+    if (f != fcur) {
+      __syncthreads();  // the previous frame's coefficients have been read
+      if (tid == 0) {
+        // Written by other CTAs with ordinary stores (ordered before the grid barrier); the copy
+        // reads them through the async proxy.
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        mbar_arrive_expect_tx(&cbar, (uint32_t)a.C * 16u);
+        bulk_load(s_coef, a.coef + (size_t)f * a.C, (uint32_t)a.C * 16u, &cbar);
+      }
+      const bool okc = mbar_wait(&cbar, cphase, a.err, kDevErrTimeoutGrid);
+      cphase ^= 1;
+      if (__syncthreads_or(!okc)) return;
+      fcur = f;
+      const float4* cf = s_coef + 8 * j;
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         const float4 u = cf[2 * w], v = cf[2 * w + 1];
@@ -371,19 +409,26 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
         blo[w] = make_float2(u.w, v.w);
       }
     }
-    for (int pj = 0; pj < kPiecesPerSpan; ++pj, ++n) {
-      bool ok = wait_piece(n);
-      int f2, q0, q1;
-      piece_of(a, n, cnt, f2, q0, q1);
-      if (ok && active) {
-        const uint8_t* src = slots + (n % kSlots) * piece_bytes + (size_t)j * 16;
-        char* dst = reinterpret_cast<char*>(a.y + ((size_t)f * a.P + q0) * a.C) + (size_t)j * 16;
+    // x comes back from L2 (phase A read it from HBM moments ago) with plain 16-byte loads,
+    // kApplyUnroll in flight per thread, and no CTA-wide synchronisation.
+    const int span = item - f * a.spans;
+    const int q0 = min(a.P, span * kPiecesPerSpan * a.piece_px);
+    const int q1 = min(a.P, q0 + kPiecesPerSpan * a.piece_px);
+    if (active) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.x + (size_t)f * a.P * a.C) + j;
+      char* dst = reinterpret_cast<char*>(a.y + (size_t)f * a.P * a.C) + (size_t)j * 16;
+      for (int p = q0 + lp; p < q1; p += ppi * kApplyUnroll) {
+        uint4 v[kApplyUnroll];
 #pragma unroll
-        for (int i = 0; i < kVecPerThread; ++i) {
-          const int pl = lp + i * ppi;
-          if (q0 + pl >= q1) break;
-          const uint4 v = *reinterpret_cast<const uint4*>(src + (size_t)pl * vpp * 16);
-          uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        for (int u = 0; u < kApplyUnroll; ++u) {
+          const int pp = p + u * ppi;
+          v[u] = pp < q1 ? __ldg(src + (size_t)pp * vpp) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < kApplyUnroll; ++u) {
+          const int pp = p + u * ppi;
+          if (pp >= q1) break;
+          uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
           float2 z[4];
           float zmin = 0.f;
 #pragma unroll
@@ -394,16 +439,17 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
           }
           if (zmin >= -80.f) {
 #pragma unroll
-            for (int w = 0; w < 4; ++w) wv[w] = pack_bf16x2(silu_fast(z[w].x), silu_fast(z[w].y));
+            for (int w = 0; w < 4; ++w) {
+              const float2 o = silu2_fast(z[w]);
+              wv[w] = pack_bf16x2(o.x, o.y);
+            }
           } else {
 #pragma unroll
             for (int w = 0; w < 4; ++w) wv[w] = pack_bf16x2(silu_exact_range(z[w].x), silu_exact_range(z[w].y));
           }
-          stg_v4(dst + (size_t)pl * vpp * 16, make_uint4(wv[0], wv[1], wv[2], wv[3]));
+          stg_v4(dst + (size_t)pp * vpp * 16, make_uint4(wv[0], wv[1], wv[2], wv[3]));
         }
       }
-      if (__syncthreads_or(!ok)) return;
-      if (tid == 0) issue(n + kSlots);
     }
   }
 }
@@ -430,7 +476,8 @@ GnPlan plan(int N, int T, int H, int W, int C, int G) {
   pl.slots = cg >= 8 ? 1 : 8 / cg;
   pl.part_bytes = (size_t)pl.F * pl.spans * G * sizeof(GnPartial);
   pl.coef_bytes = (size_t)pl.F * C * sizeof(float4);
-  pl.smem = (size_t)kSlots * pl.piece_px * C * 2 + (size_t)pl.threads * pl.slots * 4 * sizeof(float);
+  pl.smem = (size_t)kSlots * pl.piece_px * C * 2 + (size_t)pl.threads * pl.slots * 4 * sizeof(float) +
+            (size_t)G * sizeof(float);
   return pl;
 }
 
