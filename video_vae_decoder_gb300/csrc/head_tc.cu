@@ -88,6 +88,18 @@ __device__ __forceinline__ Item decode_item(const HeadArgs& a, int idx, int whic
   return it;
 }
 
+// Items go to the CTA pairs in snake order (round r: pair c takes item r * P + c, or r * P + P - 1 - c
+// on odd rounds). The frame quad is the fastest index of an item and the pair count is often a
+// multiple of the quad count, so plain round-robin would hand one pair the same quad every round
+// (the first quad of a chunk without history is the cheapest). -1: no item left; -2: none in this
+// last round.
+__device__ __forceinline__ int item_of(const HeadArgs& a, int r, int cluster, int nclusters) {
+  const int base = r * nclusters;
+  if (base >= a.items) return -1;
+  const int item = base + ((r & 1) ? nclusters - 1 - cluster : cluster);
+  return item < a.items ? item : -2;
+}
+
 // Rows of G this item computes: the band plus one row on each side (inside the frame).
 __device__ __forceinline__ int row_first(const Item& it) { return max(it.h0 - 1, 0); }
 __device__ __forceinline__ int row_last(const HeadArgs& a, const Item& it) { return min(it.h1, a.H - 1); }
@@ -216,7 +228,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0, armed = 0, armed_parity = 0;
     bool ok = true;
-    for (int item = cluster; ok && item < args.items; item += nclusters) {
+    for (int round = 0; ok; ++round) {
+      const int item = item_of(args, round, cluster, nclusters);
+      if (item == -1) break;
+      if (item < 0) continue;
       const Item it = decode_item(args, item, (int)rank);
       const int r1 = row_last(args, it);
       for (int r = row_first(it); ok && r <= r1; ++r) {
@@ -264,7 +279,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t phase = 0;
     uint32_t rc = 0;  // rows processed so far (parity of the per-frame TMEM barriers)
     bool ok = true;
-    for (int item = cluster; ok && item < args.items; item += nclusters) {
+    for (int round = 0; ok; ++round) {
+      const int item = item_of(args, round, cluster, nclusters);
+      if (item == -1) break;
+      if (item < 0) continue;
       const Item it = decode_item(args, item, 0);
       const int nfr = min(kFrames, args.T - it.t);
       const int r1 = row_last(args, it);
@@ -333,7 +351,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int k = 0; k < kFramesPerGroup; ++k)
       leader_empty[k] = mapa_shared(smem_u32(&tmem_empty[group * kFramesPerGroup + k]), 0);
-    for (int item = cluster; ok && item < args.items; item += nclusters) {
+    for (int round = 0; ok; ++round) {
+      const int item = item_of(args, round, cluster, nclusters);
+      if (item == -1) break;
+      if (item < 0) continue;
       const Item it = decode_item(args, item, (int)rank);
       const int nfr = min(kFrames, args.T - it.t);
       const int wcol = it.w0 + q;
