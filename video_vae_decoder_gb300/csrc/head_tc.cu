@@ -223,9 +223,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
+  // The ring holds kGroups groups of KBPF stages, one group per input frame tau: the KBPF tiles of
+  // a tau are produced, waited for and released together (one barrier, one wait, one commit).
+  constexpr int kGroups = kStages / KBPF;
   if (warp == 0 && lane == 0) {
     // ---------------------------------------------------------------- TMA producer
-    int stage = 0;
+    int grp = 0;
     uint32_t phase = 0, armed = 0, armed_parity = 0;
     bool ok = true;
     for (int round = 0; ok; ++round) {
@@ -236,28 +239,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int r1 = row_last(args, it);
       for (int r = row_first(it); ok && r <= r1; ++r) {
         for (int tau = tau_first(args, it); tau <= tau_last(args, it); ++tau) {
+          if (!mbar_wait_cluster(&empty[grp], phase ^ 1, args.err, kDevErrTimeoutProducer)) {
+            ok = false;
+            break;
+          }
+          if (leader) {
+            mbar_arrive_expect_tx(&full[grp], 2 * KBPF * kABytes);  // both CTAs' tiles of this tau
+            armed |= 1u << grp;
+            armed_parity = (armed_parity & ~(1u << grp)) | (phase << grp);
+          }
+          const uint32_t bar = mapa_shared(smem_u32(&full[grp]), 0);  // the even CTA's barrier
+#pragma unroll
           for (int kb = 0; kb < KBPF; ++kb) {
-            if (!mbar_wait_cluster(&empty[stage], phase ^ 1, args.err, kDevErrTimeoutProducer)) {
-              ok = false;
-              break;
-            }
-            if (leader) {
-              mbar_arrive_expect_tx(&full[stage], 2 * kABytes);
-              armed |= 1u << stage;
-              armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
-            }
-            uint8_t* dst = smem + stage * kABytes;
-            const uint32_t bar = mapa_shared(smem_u32(&full[stage]), 0);  // the even CTA's barrier
+            uint8_t* dst = smem + (grp * KBPF + kb) * kABytes;
             if (tau < 0)
               tma_load_5d_pair(dst, &tm_cache, bar, kb * 64, it.w0, r, tau + 2, it.n);
             else
               tma_load_5d_pair(dst, &tm_a, bar, kb * 64, it.w0, r, tau, it.n);
-            if (++stage == kStages) {
-              stage = 0;
-              phase ^= 1;
-            }
           }
-          if (!ok) break;
+          if (++grp == kGroups) {
+            grp = 0;
+            phase ^= 1;
+          }
         }
       }
     }
@@ -275,7 +278,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc = idesc_bf16_f32(256, kNP);
     constexpr uint32_t kBStep = kBBlockBytes >> 4;  // descriptor units between K blocks of W'
     const uint32_t b_base = smem_u32(smem + kBOffset);
-    int stage = 0;
+    int grp = 0;
     uint32_t phase = 0;
     uint32_t rc = 0;  // rows processed so far (parity of the per-frame TMEM barriers)
     bool ok = true;
@@ -289,20 +292,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int r = row_first(it); ok && r <= r1; ++r, ++rc) {
         uint32_t fresh = (1u << nfr) - 1;  // frames not yet written in this row
         for (int tau = tau_first(args, it); ok && tau <= tau_last(args, it); ++tau) {
-          uint64_t a_desc[KBPF];
-          int st[KBPF];
-#pragma unroll
-          for (int kb = 0; kb < KBPF; ++kb) {
-            if (ok && !mbar_wait_cluster(&full[stage], phase, args.err, kDevErrTimeoutMma)) ok = false;
-            st[kb] = stage;
-            a_desc[kb] = smem_desc_sw128(smem_u32(smem + stage * kABytes));
-            if (++stage == kStages) {
-              stage = 0;
-              phase ^= 1;
-            }
+          if (!mbar_wait_cluster(&full[grp], phase, args.err, kDevErrTimeoutMma)) {
+            ok = false;
+            break;
           }
-          if (!ok) break;
           tc_fence_after();
+          uint64_t a_desc[KBPF];
+#pragma unroll
+          for (int kb = 0; kb < KBPF; ++kb) a_desc[kb] = smem_desc_sw128(smem_u32(smem + (grp * KBPF + kb) * kABytes));
           const int o_lo = max(tau - it.t, 0), o_hi = min(tau - it.t + 2, nfr - 1);
           for (int o = o_lo; o <= o_hi; ++o) {
             const bool first = (fresh >> o) & 1u;
@@ -325,8 +322,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                               (first && kb == 0 && k == 0) ? 0u : 1u);
           }
           if (!ok) break;
-#pragma unroll
-          for (int kb = 0; kb < KBPF; ++kb) mma_commit_pair(&empty[st[kb]], 0x3);
+          mma_commit_pair(&empty[grp], 0x3);
+          if (++grp == kGroups) {
+            grp = 0;
+            phase ^= 1;
+          }
           const int done = tau - it.t;  // frame t+done has seen its last input (kt = 2)
           if (done >= 0 && done < nfr) mma_commit_pair(&tmem_full[done], 0x3);
         }
