@@ -257,6 +257,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             else
               tma_load_5d_pair(dst, &tm_a, bar, kb * 64, it.w0, r, tau, it.n);
           }
+          // The ring holds only the next input frame; the one after it is pulled into L2 now so
+          // that its loads, issued once a group frees up, do not wait for HBM.
+          {
+            int pr = r, pt = tau + 2;
+            if (pt > tau_last(args, it)) {
+              pt = tau_first(args, it) + (pt - tau_last(args, it) - 1);
+              ++pr;
+            }
+            if (pr <= r1 && pt >= 0)
+#pragma unroll
+              for (int kb = 0; kb < KBPF; ++kb) tma_prefetch_5d(&tm_a, kb * 64, it.w0, pr, pt, it.n);
+          }
           if (++grp == kGroups) {
             grp = 0;
             phase ^= 1;
