@@ -313,25 +313,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int kb = 0; kb < KBPF; ++kb) a_desc[kb] = smem_desc_sw128(smem_u32(smem + (grp * KBPF + kb) * kABytes));
           const int o_lo = max(tau - it.t, 0), o_hi = min(tau - it.t + 2, nfr - 1);
-          for (int o = o_lo; o <= o_hi; ++o) {
-            const bool first = (fresh >> o) & 1u;
-            if (first) {
-              if (!mbar_wait_cluster(&tmem_empty[o], (rc & 1) ^ 1, args.err, kDevErrTimeoutMma)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              fresh &= ~(1u << o);
-            }
-            const uint32_t d = tmem_base + o * kNP;
-            const int kt = tau - it.t - o + 2;
-            const uint64_t b_desc = smem_desc_sw128(b_base + kt * KBPF * kBBlockBytes);
+          // Frames written for the first time in this row wait until the epilogue released their
+          // accumulator; then every MMA of this input frame goes out in one straight-line burst.
+          uint32_t acc0[3];  // accumulate flag of each frame's first MMA (0: first write in the row)
+#pragma unroll
+          for (int i = 0; i < 3; ++i) {
+            const int o = o_lo + i;
+            acc0[i] = 1u;
+            if (o > o_hi || !((fresh >> o) & 1u)) continue;
+            if (!mbar_wait_cluster(&tmem_empty[o], (rc & 1) ^ 1, args.err, kDevErrTimeoutMma)) ok = false;
+            fresh &= ~(1u << o);
+            acc0[i] = 0u;
+          }
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d0 = tmem_base + o_lo * kNP;
+          // W' block of kernel tap kt = tau - (t + o) + 2: one frame further is one tap lower.
+          const uint64_t b0 = smem_desc_sw128(b_base + (tau - it.t - o_lo + 2) * KBPF * kBBlockBytes);
+          constexpr uint64_t kTapDesc = (uint64_t)(KBPF * kBBlockBytes) >> 4;
+          auto burst = [&](int i) {
 #pragma unroll
             for (int kb = 0; kb < KBPF; ++kb)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
-                mma_bf16_pair(d, a_desc[kb] + 2 * k, b_desc + kb * kBStep + 2 * k, idesc,
-                              (first && kb == 0 && k == 0) ? 0u : 1u);
+                mma_bf16_pair(d0 + i * kNP, a_desc[kb] + 2 * k, b0 - i * kTapDesc + kb * kBStep + 2 * k, idesc,
+                              (kb == 0 && k == 0) ? acc0[i] : 1u);
+          };
+          switch (o_hi - o_lo) {
+            case 0:
+              burst(0);
+              break;
+            case 1:
+              burst(0);
+              burst(1);
+              break;
+            default:
+              burst(0);
+              burst(1);
+              burst(2);
+              break;
           }
           if (!ok) break;
           mma_commit_pair(&empty[grp], 0x3);
