@@ -26,6 +26,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+#include <vector>
+
 #include "common.cuh"
 #include "conv_tc.h"
 
@@ -56,6 +59,7 @@ struct HeadArgs {
   int N, T, H, W, Cin;
   int kb_per_frame;          // Cin / 64
   int quads, strips, strip_pairs, bands, band_rows, items;
+  int order;                 // item order over the CTA pairs: 0 snake, 1 rotating (see item_of)
   int has_cache;
   const wan_bf16* w;         // [12, 3, 3, 3, Cin]
   const wan_bf16* bias;      // [12] or null
@@ -88,15 +92,17 @@ __device__ __forceinline__ Item decode_item(const HeadArgs& a, int idx, int whic
   return it;
 }
 
-// Items go to the CTA pairs in snake order (round r: pair c takes item r * P + c, or r * P + P - 1 - c
-// on odd rounds). The frame quad is the fastest index of an item and the pair count is often a
-// multiple of the quad count, so plain round-robin would hand one pair the same quad every round
-// (the first quad of a chunk without history is the cheapest). -1: no item left; -2: none in this
-// last round.
+// Items of round r go to the P CTA pairs as a permutation of items r * P .. r * P + P - 1 (so the
+// items running together share input frames in L2): snake order (pair c takes r * P + c, or
+// r * P + P - 1 - c on odd rounds) or rotating order (r * P + (c + r) % P). The frame quad is the
+// fastest index of an item and the quads differ in cost (the first quad of a chunk without
+// history has fewer taps), so which order spreads them evenly depends on P; the launcher picks
+// the better one. -1: no item left; -2: none in this last round.
 __device__ __forceinline__ int item_of(const HeadArgs& a, int r, int cluster, int nclusters) {
   const int base = r * nclusters;
   if (base >= a.items) return -1;
-  const int item = base + ((r & 1) ? nclusters - 1 - cluster : cluster);
+  const int off = a.order ? (cluster + r) % nclusters : ((r & 1) ? nclusters - 1 - cluster : cluster);
+  const int item = base + off;
   return item < a.items ? item : -2;
 }
 
@@ -573,24 +579,59 @@ cudaError_t head_launch(const wan_bf16* a, const wan_bf16* cache_in, const wan_b
     }
     slots = max_clusters[dev];
   }
-  // Rows per band: the fewest rounds over the CTA pairs, counting the two halo rows of a band.
+  // Rows per band and item order. First the fewest rounds over the CTA pairs, counting the two halo
+  // rows of a band; then, among band counts within 10% of that, the schedule whose busiest pair
+  // has the least work, counting a quad's real taps (frames before a chunk without history have
+  // none) and a band's real rows.
   const long long base = (long long)N * args.quads * args.strip_pairs;
-  long long best_cost = -1;
-  int best_bands = 1;
+  auto rounds_cost = [&](int bands) {
+    const int rows = cdiv(H, bands);
+    const long long items = base * cdiv(H, rows);
+    return ((items + slots - 1) / slots) * (rows + 2);
+  };
+  long long min_cost = -1;
   for (int bands = 1; bands <= H && bands <= 256; ++bands) {
+    const long long c = rounds_cost(bands);
+    if (min_cost < 0 || c < min_cost) min_cost = c;
+  }
+  int quad_taps[64];
+  for (int q = 0; q < args.quads && q < 64; ++q) {
+    quad_taps[q] = 0;
+    for (int o = 0; o < kFrames && kFrames * q + o < T; ++o)
+      quad_taps[q] += args.has_cache ? 3 : std::min(3, kFrames * q + o + 1);
+  }
+  long long best_max = -1;
+  int best_bands = 1, best_order = 0;
+  std::vector<long long> load(slots);
+  for (int bands = 1; bands <= H && bands <= 256; ++bands) {
+    if (rounds_cost(bands) * 10 > min_cost * 11) continue;
     const int rows = cdiv(H, bands);
     const int nb = cdiv(H, rows);
     const long long items = base * nb;
-    const long long rounds = (items + slots - 1) / slots;
-    const long long cost = rounds * (rows + 2);
-    if (best_cost < 0 || cost < best_cost) {
-      best_cost = cost;
-      best_bands = nb;
+    for (int order = 0; order < 2; ++order) {
+      std::fill(load.begin(), load.end(), 0);
+      for (long long r = 0; r * slots < items; ++r)
+        for (int c = 0; c < slots; ++c) {
+          const long long off = order ? (c + r) % slots : ((r & 1) ? slots - 1 - c : c);
+          const long long it = r * slots + off;
+          if (it >= items) continue;
+          const int q = (int)(it % args.quads), band = (int)((it / args.quads) % nb);
+          const int h0 = band * rows, h1 = std::min(H, h0 + rows);
+          const int nrows = std::min(h1, H - 1) - std::max(h0 - 1, 0) + 1;
+          load[c] += (long long)nrows * (q < 64 ? quad_taps[q] : 3 * kFrames);
+        }
+      const long long mx = *std::max_element(load.begin(), load.end());
+      if (best_max < 0 || mx < best_max) {
+        best_max = mx;
+        best_bands = nb;
+        best_order = order;
+      }
     }
   }
   args.band_rows = cdiv(H, best_bands);
   args.bands = cdiv(H, args.band_rows);
   args.items = (int)(base * args.bands);
+  args.order = best_order;
 
   CUtensorMap ta, tc;
   if (!make_row_map(&ta, a, Cin, W, H, T, N)) return cudaErrorInvalidValue;
