@@ -38,6 +38,11 @@ def run(wan, a, w, b, r, c, with_cache_out=True):
     ((1, 4, 10, 24, 64), 12, False, False, False),    # head-like: 12 output channels
     ((1, 1, 8, 8, 64), 64, True, False, True),        # a single frame: both history frames from the cache
     ((1, 2, 5, 5, 192), 256, True, True, False),
+    # CTA-pair path (Cout >= 256, 8 x 16-pixel tiles with their halo boxes):
+    ((1, 3, 19, 37, 128), 256, True, True, False),    # ragged rows and columns, odd tile count, no history
+    ((1, 4, 8, 16, 64), 512, False, False, True),     # exactly one tile per frame, two N blocks
+    ((1, 1, 3, 50, 64), 256, True, False, False),     # one frame, fewer rows than a tile, 4 tiles wide
+    ((2, 2, 12, 33, 64), 256, True, True, True),      # batch 2: tile pairs that cross batch items
 ])
 def test_conv_small(wan, shape, Cout, bias, residual, cache):
     a, w, b, r, c = make(shape, Cout, f"conv/{shape}/{Cout}", bias, residual, cache)
@@ -56,6 +61,19 @@ def test_conv_chunked_equals_unchunked(wan):
     full, full_cache = run(wan, a, w, b, None, None)
     parts, cache = [], None
     for s in range(0, 12, 4):
+        y, cache = run(wan, a[:, s:s + 4], w, b, None, cache)
+        parts.append(y)
+    assert np.array_equal(np.concatenate(parts, 1), full)
+    assert np.array_equal(cache, full_cache)
+
+
+def test_conv_pair_chunked_equals_unchunked(wan):
+    # The CTA-pair path: chunks of 4 frames give the same bits as one 8-frame call.
+    shape = (1, 8, 10, 30, 64)
+    a, w, b, _, _ = make(shape, 256, "conv/pair-chunks")
+    full, full_cache = run(wan, a, w, b, None, None)
+    parts, cache = [], None
+    for s in range(0, 8, 4):
         y, cache = run(wan, a[:, s:s + 4], w, b, None, cache)
         parts.append(y)
     assert np.array_equal(np.concatenate(parts, 1), full)
