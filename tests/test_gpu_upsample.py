@@ -20,6 +20,8 @@ def test_phase_weights_bit_exact(wan):
     ((1, 1, 6, 10, 64), 64, False),
     ((1, 3, 9, 13, 128), 96, True),     # ragged tiles, odd sizes
     ((2, 2, 5, 7, 64), 320, True),
+    ((1, 2, 19, 40, 64), 256, True),    # CTA-pair path: ragged 8 x 16 tiles, 3 tiles wide
+    ((1, 1, 9, 17, 128), 512, False),   # CTA-pair path: two N blocks
 ])
 def test_upsample_small(wan, shape, Cout, bias):
     Cin = shape[-1]
