@@ -270,6 +270,22 @@ class Workload:
         return (self.gn_y, self.o4[-1], self.y3, self.o5[-1], self.yh)
 
 
+def max_over_ranks(x, world, device):
+    """The largest of the ranks' values of x: the job takes as long as its slowest rank."""
+    if world <= 1:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank_step, world, ms_per_step):
+    """Whole-job throughput of `world` replicas that each run one step of the given FLOPs in
+    ms_per_step (the slowest rank's time): every rank's work counts."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def run_ours(args, rank, world, dev):
     import torch
     from video_vae_decoder_gb300 import binding as wan
@@ -315,11 +331,7 @@ def run_ours(args, rank, world, dev):
         step_ms.append(ev[s][0].elapsed_time(ev[s][-1]))
         for i, (tag, _, _) in enumerate(calls):
             per_tag.setdefault(tag, []).append(ev[s][i].elapsed_time(ev[s][i + 1]))
-    ms = statistics.mean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(statistics.mean(step_ms), world, dev)
     flops = sum(wl.flops.values())
     pk = peaks()
 
@@ -385,7 +397,7 @@ def run_ours(args, rank, world, dev):
     launches = sum(k for _, k, _ in calls) * args.steps
 
     out = {
-        "metric": METRIC, "value": world * flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "metric": METRIC, "value": job_tflops(flops, world, ms), "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded counter-based normals; random-init weights of the decoder shapes)",

@@ -1,0 +1,56 @@
+"""bench.py's N > 1 host logic, run as 2 gloo ranks on the CPU: each rank is an independent replica,
+the job's step time is the slowest rank's, whole-job throughput counts every rank's work, and only
+rank 0 prints (the reference arm's other ranks exit 0 without work)."""
+import os
+import socket
+import subprocess
+import sys
+
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out_dir):
+    import torch.distributed as dist
+    sys.path.insert(0, ROOT)
+    import bench as b
+    dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    try:
+        ms = b.max_over_ranks(3.0 + 2.0 * rank, world, "cpu")  # rank 1 is the slow one
+        with open(os.path.join(out_dir, f"rank{rank}.txt"), "w") as f:
+            f.write(repr(ms))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_max_over_ranks_two_gloo_ranks(tmp_path):
+    mp.spawn(_rank_main, args=(2, _free_port(), str(tmp_path)), nprocs=2, join=True)
+    got = [float(open(tmp_path / f"rank{r}.txt").read()) for r in range(2)]
+    assert got == [5.0, 5.0]
+
+
+def test_single_rank_needs_no_process_group():
+    assert bench.max_over_ranks(7.25, 1, "cpu") == 7.25
+
+
+def test_job_throughput_counts_every_replica():
+    one = bench.job_tflops(4.0e12, 1, 2.0)
+    assert abs(one - 2000.0) < 1e-9
+    assert abs(bench.job_tflops(4.0e12, 2, 2.0) - 2 * one) < 1e-9
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == ""
