@@ -155,9 +155,9 @@ __device__ bool grid_barrier(unsigned* ctr, unsigned target, unsigned* err, int*
   return *s_flag != 0;
 }
 
-constexpr int kSlots = 6;          // 16 KB pieces of x in flight per CTA
-constexpr int kVecPerThread = 4;   // 16-byte vectors per thread per piece
-constexpr int kPiecesPerSpan = 4;  // a statistics partial covers 4 pieces (about 64 KB)
+constexpr int kSlots = 3;          // 32 KB pieces of x in flight per CTA
+constexpr int kVecPerThread = 8;   // 16-byte vectors per thread per piece
+constexpr int kPiecesPerSpan = 2;  // a statistics partial covers 2 pieces (about 64 KB)
 constexpr int kApplyUnroll = 8;    // 16-byte loads in flight per thread in the apply phase
 constexpr int kFinBatch = 8;       // partials in flight per lane in the finalize
 
