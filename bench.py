@@ -175,9 +175,10 @@ class Workload:
             caches = [(torch.zeros((N, 2, H, W, C), dtype=bf, device=dev),
                        torch.zeros((N, 2, H, W, C), dtype=bf, device=dev)) for _ in range(nblk)]
             outs = [torch.empty_like(x) for _ in range(nblk)]
-            return caches, outs, torch.empty_like(x), torch.empty_like(x)
-        self.c4, self.o4, self.a4, self.h4 = stage_bufs(self.x4, 3)
-        self.c5, self.o5, self.a5, self.h5 = stage_bufs(self.x5, 2)
+            coef = torch.empty(N * T * C * 16, dtype=torch.uint8, device=dev)  # GroupNorm coefficients
+            return caches, outs, coef, torch.empty_like(x)
+        self.c4, self.o4, self.k4, self.h4 = stage_bufs(self.x4, 3)
+        self.c5, self.o5, self.k5, self.h5 = stage_bufs(self.x5, 2)
         from video_vae_decoder_gb300 import binding as wan
         need = max(wan.wan_workspace_size(wan.WAN_OP_GN_SILU, *t.shape, 0, GROUPS)
                    for t in (self.gn_x, self.x4, self.x5))
@@ -205,40 +206,43 @@ class Workload:
         want = (lambda part: self.case in ("all", part))
         calls = []
         if want("gn"):
-            calls.append(("gn", 3, lambda: wan.wan_gn_silu(self.gn_x, self.gn_g, self.gn_b, GROUPS, EPS, self.gn_y,
+            calls.append(("gn", 1, lambda: wan.wan_gn_silu(self.gn_x, self.gn_g, self.gn_b, GROUPS, EPS, self.gn_y,
                                                            self.gn_ws)))
 
-        def stage(tag, x, blocks, caches, outs, act, h):
+        def stage(tag, x, blocks, caches, outs, coef, h):
+            # Each ResBlock as the calls wan_resblock makes, twice (GroupNorm + SiLU into each conv):
+            # the norm's coefficients (one pass over its input), the conv normalising its operand
+            # tiles as they arrive, then the last two normalised frames into the conv's cache.
             cur = x
             for i, (p, (c1, c2), out) in enumerate(zip(blocks, caches, outs)):
-                def g1(cur=cur, p=p):
-                    wan.wan_gn_silu(cur, p["gamma1"], p["beta1"], GROUPS, EPS, act, self.gn_ws)
+                def n1(cur=cur, p=p):
+                    wan.wan_gn_silu_coefficients(cur, p["gamma1"], p["beta1"], GROUPS, EPS, coef, self.gn_ws)
 
-                def k1(p=p, c1=c1):
-                    wan.wan_causal_conv3d(act, p["w1"], p["b1"], None, c1, None, h)
+                def k1(cur=cur, p=p, c1=c1):
+                    wan.wan_causal_conv3d_gn_input(cur, coef, p["w1"], p["b1"], None, c1, h)
 
-                def u1(c1=c1):
-                    wan.wan_cache_update(act, c1, c1)
+                def u1(cur=cur, c1=c1):
+                    wan.wan_gn_silu_cache_update(cur, coef, c1, c1)
 
-                def g2(p=p):
-                    wan.wan_gn_silu(h, p["gamma2"], p["beta2"], GROUPS, EPS, act, self.gn_ws)
+                def n2(p=p):
+                    wan.wan_gn_silu_coefficients(h, p["gamma2"], p["beta2"], GROUPS, EPS, coef, self.gn_ws)
 
                 def k2(cur=cur, p=p, c2=c2, out=out):
-                    wan.wan_causal_conv3d(act, p["w2"], p["b2"], cur, c2, None, out)
+                    wan.wan_causal_conv3d_gn_input(h, coef, p["w2"], p["b2"], cur, c2, out)
 
                 def u2(c2=c2):
-                    wan.wan_cache_update(act, c2, c2)
-                calls.extend([(f"{tag}.gn", 3, g1), (f"{tag}.conv", 1, k1), (f"{tag}.cache", 2, u1),
-                              (f"{tag}.gn", 3, g2), (f"{tag}.conv", 1, k2), (f"{tag}.cache", 2, u2)])
+                    wan.wan_gn_silu_cache_update(h, coef, c2, c2)
+                calls.extend([(f"{tag}.coef", 1, n1), (f"{tag}.conv", 1, k1), (f"{tag}.cache", 1, u1),
+                              (f"{tag}.coef", 1, n2), (f"{tag}.conv", 1, k2), (f"{tag}.cache", 1, u2)])
                 cur = out
 
         if want("c256"):
-            stage("c256", self.x4, self.blocks4, self.c4, self.o4, self.a4, self.h4)
+            stage("c256", self.x4, self.blocks4, self.c4, self.o4, self.k4, self.h4)
         if want("up"):
             calls.append(("up.weights", 1, lambda: wan.wan_upsample_phase_weights(self.w3, self.wp)))
             calls.append(("up.conv", 1, lambda: wan.wan_upsample_phase_conv(self.x3, self.wp, None, self.y3)))
         if want("c1024"):
-            stage("c1024", self.x5, self.blocks5, self.c5, self.o5, self.a5, self.h5)
+            stage("c1024", self.x5, self.blocks5, self.c5, self.o5, self.k5, self.h5)
         if want("head"):
             calls.append(("head.conv", 1, lambda: wan.wan_causal_conv3d(self.xh, self.wh, None, None, None, None,
                                                                         self.yh)))
@@ -353,14 +357,19 @@ def run_ours(args, rank, world, dev):
         f4 = conv_flops(1, 4, 176, 312, 256, 256)
         kernels["conv_c256"] = {"ms": per_launch("c256.conv"), "tflops": f4 / per_launch("c256.conv") / 1e9,
                                 "total_ms": tot("c256.conv")}
-        kernels["gn_silu_c256"] = {"ms": per_launch("c256.gn"), "gbs": 4.0 * wl.x4.numel() / per_launch("c256.gn") / 1e6}
-        kernels["resblock_c256_ms"] = (tot("c256.gn") + tot("c256.conv") + tot("c256.cache")) / 3.0
+        # the norm's coefficients: one read of its input (2 bytes per element); the cache frames:
+        # 2 of the 4 frames read and written
+        kernels["gn_coef_c256"] = {"ms": per_launch("c256.coef"),
+                                   "gbs": 2.0 * wl.x4.numel() / per_launch("c256.coef") / 1e6}
+        kernels["gn_cache_frames_c256"] = {"ms": per_launch("c256.cache"),
+                                           "gbs": 2.0 * wl.x4.numel() / per_launch("c256.cache") / 1e6}
+        kernels["resblock_c256_ms"] = (tot("c256.coef") + tot("c256.conv") + tot("c256.cache")) / 3.0
         shares["conv_c256"] = tot("c256.conv")
     if "c1024.conv" in per_tag:
         f5 = conv_flops(1, 4, 44, 78, 1024, 1024)
         kernels["conv_c1024"] = {"ms": per_launch("c1024.conv"), "tflops": f5 / per_launch("c1024.conv") / 1e9,
                                  "total_ms": tot("c1024.conv")}
-        kernels["resblock_c1024_ms"] = (tot("c1024.gn") + tot("c1024.conv") + tot("c1024.cache")) / 2.0
+        kernels["resblock_c1024_ms"] = (tot("c1024.coef") + tot("c1024.conv") + tot("c1024.cache")) / 2.0
         shares["conv_c1024"] = tot("c1024.conv")
     if "head.conv" in per_tag:
         hm = per_launch("head.conv")
@@ -375,12 +384,12 @@ def run_ours(args, rank, world, dev):
         gm = per_launch("gn")
         kernels["gn_silu_decode_mid"] = {"ms": gm, "gbs": wl.gn_bytes / gm / 1e6,
                                          "frac_hbm": wl.gn_bytes / gm / 1e6 / pk["hbm_gbs"]}
-    gn_total = tot("gn") + tot("c256.gn") + tot("c1024.gn")
+    gn_total = tot("gn") + tot("c256.coef") + tot("c1024.coef") + tot("c256.cache") + tot("c1024.cache")
     if gn_total:
         shares["gn_silu"] = gn_total
     dom = max(shares, key=shares.get)
     if dom == "gn_silu":
-        k = kernels.get("gn_silu_c256") or kernels["gn_silu_decode_mid"]
+        k = kernels["gn_silu_decode_mid"]
         roof = {"kernel": "gn_silu", "bound": "hbm", "achieved": k["gbs"], "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": k["gbs"] / pk["hbm_gbs"], "peak_source": f"{pk['source']} HBM copy"}
     else:
@@ -389,9 +398,8 @@ def run_ours(args, rank, world, dev):
                 "frac_of_sustained": kernels[dom]["tflops"] / pk["bf16_tflops_sustained"],
                 "peak_source": f"{pk['source']} {pk_tf_note}"}
     # DRAM bytes (read + write) per launch from one `ncu --set full` capture of the current kernel
-    # build (the first conv of a C=256 step: 172.3 MB read, 75.8 MB written); None for kernels
-    # without a capture of their current build.
-    traffic = {"conv_c256": 172.297472e6 + 75.833856e6}
+    # build; None for kernels without a capture of their current build.
+    traffic = {}
     roof["traffic"] = traffic.get(roof["kernel"])
     roof["share_of_step"] = shares[dom] / ms
     launches = sum(k for _, k, _ in calls) * args.steps

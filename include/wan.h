@@ -54,7 +54,9 @@ typedef enum wan_op {
   WAN_OP_GN_SILU = 0,
   WAN_OP_CAUSAL_CONV3D = 1,
   WAN_OP_RESBLOCK = 2,
-  WAN_OP_UPSAMPLE_PHASE_CONV = 3
+  WAN_OP_UPSAMPLE_PHASE_CONV = 3,
+  WAN_OP_GN_STATS = 4,           /* statistics buffer of wan_causal_conv3d_gn_stats (Cout, groups) */
+  WAN_OP_GN_SILU_CONV3D = 5      /* wan_gn_silu_causal_conv3d (Cin, Cout, groups) */
 } wan_op;
 
 /* Human-readable name of a status (static storage, never NULL). */
@@ -141,6 +143,105 @@ wan_status wan_causal_conv3d(const wan_bf16* a, const wan_bf16* cache_in, wan_bf
                              const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual,
                              wan_bf16* y, int N, int T, int H, int W, int Cin, int Cout,
                              void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * wan_causal_conv3d that also emits the GroupNorm statistics of its output y, so that the
+ * GroupNorm + SiLU which follows it (wan_gn_silu_from_stats) needs no pass over y of its own.
+ * The pages have no such call: their decoder reads the conv output again for its norm
+ * (binding.cpp, `Decoder::resnet`); fusing the statistics into the producing conv is the
+ * cross-op fusion the scope lists after the hot path itself.
+ *
+ * y and the cache are exactly those of wan_causal_conv3d with the same arguments. stats receives,
+ * per (frame, group, 32-pixel quarter of an 8 x 16-pixel tile of the frame), the fp32 sums of d
+ * and d^2 of d = y - s over the quarter's pixels and the group's channels, s being one value of
+ * the group there, with s and the count; its exact layout is private to this library: pass it
+ * unchanged to wan_gn_silu_from_stats with the same N, T, H, W, C = Cout and groups.
+ *
+ *   groups     GroupNorm groups of the following norm; Cout % 256 == 0, groups divides Cout and
+ *              the channels per group are a power of two from 4 to 64 (else
+ *              WAN_ERR_UNSUPPORTED_SHAPE).
+ *   stats      device buffer of >= wan_workspace_size(WAN_OP_GN_STATS, N, T, H, W, Cin, Cout,
+ *              groups) bytes, 16-byte aligned, owned by the caller; must not overlap the tensors.
+ *   Other arguments as wan_causal_conv3d (its 12-channel head path does not emit statistics).
+ */
+wan_status wan_causal_conv3d_gn_stats(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out,
+                                      const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual,
+                                      wan_bf16* y, int N, int T, int H, int W, int Cin, int Cout,
+                                      int groups, void* stats, size_t stats_bytes, void* stream);
+
+/*
+ * GroupNorm + SiLU of x (the definition of wan_gn_silu, per (n, t, group)) using the statistics
+ * that wan_causal_conv3d_gn_stats emitted when it wrote x: the per-part sums are moved to one
+ * shift and added as float-float pairs in a fixed part order, so the result depends only on x's
+ * frames (the same bits in any chunking of the video). y is within one bf16 ulp of the exact
+ * (fp64, rounded once) GroupNorm + SiLU, like wan_gn_silu's.
+ *
+ *   x, y, gamma, beta, groups, eps, ws  as wan_gn_silu (ws >= wan_workspace_size(WAN_OP_GN_SILU,
+ *              N, T, H, W, C, 0, groups)).
+ *   stats      the buffer filled by wan_causal_conv3d_gn_stats for this x (Cout = C, same groups);
+ *              stats_bytes >= wan_workspace_size(WAN_OP_GN_STATS, ...) (else WAN_ERR_INVALID_ARG).
+ */
+wan_status wan_gn_silu_from_stats(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta,
+                                  int N, int T, int H, int W, int C, int groups, float eps,
+                                  const void* stats, size_t stats_bytes, void* ws, size_t ws_bytes,
+                                  void* stream);
+
+/*
+ * GroupNorm + SiLU feeding a causal conv, the pair that every ResBlock of the decoder runs twice:
+ *     a = silu(group_norm(x));  y = conv(a; cache_in) + bias + residual;
+ *     cache_out = the last two frames of [cache_in or zeros; a]
+ * Source: binding.cpp, `Decoder::conv` (its input is either the producer's "prepared" edge or
+ * `norm_pad`: norm + SiLU + causal padding from the cache, which then keeps the last frames of
+ * that padded input) and `Decoder::resnet`. The definitions are wan_gn_silu's,
+ * wan_causal_conv3d's and wan_cache_update's; y and cache_out are bit for bit what those three
+ * calls return.
+ * For Cout >= 256 a is never stored: the norm's pass over x writes per-(frame, channel)
+ * coefficients only, the conv normalises each operand tile of x in shared memory as it arrives,
+ * and the last two frames of a are written once, straight into cache_out.
+ *
+ *   x          [N, T, H, W, Cin] bf16 (the norm's input); gamma, beta, groups, eps as wan_gn_silu.
+ *   cache_in   NULL (zero history) or [N, 2, H, W, Cin] bf16, already activated (a previous
+ *              chunk's cache_out).
+ *   cache_out  NULL or [N, 2, H, W, Cin] bf16 receiving the new history; may equal cache_in.
+ *   w, bias, residual, y, Cout  as wan_causal_conv3d.
+ *   ws         >= wan_workspace_size(WAN_OP_GN_SILU_CONV3D, N, T, H, W, Cin, Cout, groups)
+ *              bytes, 16-byte aligned.
+ * Errors as wan_gn_silu and wan_causal_conv3d; x, y and the caches may not overlap (except
+ * cache_in == cache_out).
+ */
+wan_status wan_gn_silu_causal_conv3d(const wan_bf16* x, const float* gamma, const float* beta, int groups,
+                                     float eps, const wan_bf16* cache_in, wan_bf16* cache_out,
+                                     const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual,
+                                     wan_bf16* y, int N, int T, int H, int W, int Cin, int Cout, void* ws,
+                                     size_t ws_bytes, void* stream);
+
+/*
+ * The three steps of wan_gn_silu_causal_conv3d for Cout >= 256, as separate calls (a norm whose
+ * output feeds more than one consumer computes its coefficients once):
+ *   1. wan_gn_silu_coefficients: the per-(frame, channel) scale S and shift B of x's GroupNorm
+ *      (gamma, beta, groups and eps folded in), so that silu(x S + B) is wan_gn_silu's output.
+ *   2. wan_causal_conv3d_gn_input: y = conv(silu(x S + B); cache_in) + bias + residual, the
+ *      normalisation applied to the conv's operand tiles as they arrive.
+ *   3. wan_gn_silu_cache_update: cache_out = the last two frames of [cache_in or zeros;
+ *      silu(x S + B)].
+ * coef holds N*T*C*16 bytes (16-byte aligned, caller-owned) in a layout private to the library:
+ * pass it unchanged between the calls with the same x, N, T, H, W and C. Each result is bit for
+ * bit what the corresponding step of wan_gn_silu_causal_conv3d writes. C (Cin) % 64 == 0.
+ *
+ *   wan_gn_silu_coefficients  x, gamma, beta, groups, eps, ws as wan_gn_silu (ws >=
+ *                             wan_workspace_size(WAN_OP_GN_SILU, ...)).
+ *   wan_causal_conv3d_gn_input  cache_in (activated history, or NULL), w, bias, residual, y as
+ *                             wan_causal_conv3d; Cout < 256 gives WAN_ERR_UNSUPPORTED_SHAPE.
+ *   wan_gn_silu_cache_update  cache_out may equal cache_in; must not overlap x or coef.
+ */
+wan_status wan_gn_silu_coefficients(const wan_bf16* x, const float* gamma, const float* beta, int N, int T,
+                                    int H, int W, int C, int groups, float eps, void* coef, void* ws,
+                                    size_t ws_bytes, void* stream);
+wan_status wan_causal_conv3d_gn_input(const wan_bf16* x, const void* coef, const wan_bf16* cache_in,
+                                      const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual,
+                                      wan_bf16* y, int N, int T, int H, int W, int Cin, int Cout, void* stream);
+wan_status wan_gn_silu_cache_update(const wan_bf16* x, const void* coef, const wan_bf16* cache_in,
+                                    wan_bf16* cache_out, int N, int T, int H, int W, int C, void* stream);
 
 /*
  * Temporal-cache update (the cache manager of the causal convolutions), on its own.

@@ -47,6 +47,27 @@ def test_workspace_sizes(L):
     rb = b.wan_workspace_size(b.WAN_OP_RESBLOCK, 1, 4, 16, 16, 64, 64, 32)
     assert rb >= 2 * 4 * 16 * 16 * 64 * 2
     assert b.wan_workspace_size(b.WAN_OP_GN_SILU, 1, 4, 8, 8, 60, 0, 32) == 0   # groups do not divide C
+    # statistics of a conv output: one (fp64 pair + float pair) per (frame, group, 8x16 tile)
+    st = b.wan_workspace_size(b.WAN_OP_GN_STATS, 1, 4, 176, 312, 256, 256, 32)
+    assert st == 4 * 32 * (22 * 20 * 4) * 24  # float4 + float2 per (frame, group, tile, warp)
+    assert b.wan_workspace_size(b.WAN_OP_GN_STATS, 1, 4, 16, 16, 64, 320, 32) == 0   # Cout % 256 != 0
+    assert b.wan_workspace_size(b.WAN_OP_GN_STATS, 1, 4, 16, 16, 64, 256, 128) == 0  # 2 channels per group
+    assert b.wan_workspace_size(b.WAN_OP_GN_STATS, 1, 4, 16, 16, 64, 768, 64) == 0   # 12 channels per group
+    assert b.wan_workspace_size(b.WAN_OP_GN_STATS, 1, 4, 16, 16, 64, 512, 4) == 0    # 128 channels per group
+    # GroupNorm + SiLU into a causal conv: Cout >= 256 never stores the activation (only the norm's
+    # workspace); smaller convs read it from the workspace.
+    def a256(n):
+        return (n + 255) // 256 * 256
+    gnws = b.wan_workspace_size(b.WAN_OP_GN_SILU, 1, 4, 16, 16, 256, 0, 32)
+    assert b.wan_workspace_size(b.WAN_OP_GN_SILU_CONV3D, 1, 4, 16, 16, 256, 256, 32) == a256(gnws)
+    gn1 = b.wan_workspace_size(b.WAN_OP_GN_SILU, 1, 1, 16, 16, 256, 0, 32)
+    assert b.wan_workspace_size(b.WAN_OP_GN_SILU_CONV3D, 1, 1, 16, 16, 256, 256, 32) == a256(gn1)
+    gn64 = b.wan_workspace_size(b.WAN_OP_GN_SILU, 1, 4, 16, 16, 64, 0, 32)
+    assert b.wan_workspace_size(b.WAN_OP_GN_SILU_CONV3D, 1, 4, 16, 16, 64, 64, 32) == a256(gn64) + 4 * 16 * 16 * 64 * 2
+    assert b.wan_workspace_size(b.WAN_OP_GN_SILU_CONV3D, 1, 4, 16, 16, 60, 64, 32) == 0  # groups do not divide Cin
+    # the ResBlock: h, then the norm-into-conv workspace shared by its two convs
+    assert b.wan_workspace_size(b.WAN_OP_RESBLOCK, 1, 4, 16, 16, 256, 256, 32) == \
+        4 * 16 * 16 * 256 * 2 + b.wan_workspace_size(b.WAN_OP_GN_SILU_CONV3D, 1, 4, 16, 16, 256, 256, 32)
 
 
 # Fake, never-dereferenced device addresses: every call below must be rejected on the host.
@@ -86,6 +107,62 @@ def test_conv_rejects_invalid(L):
     assert f(A, None, None, A * 5, None, None, A + 64, 1, 2, 4, 4, 64, 64, None, 0, None) == 1
     # cache_out overlapping a
     assert f(A, None, A + 128, A * 5, None, None, A * 9, 1, 2, 4, 4, 64, 64, None, 0, None) == 1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers are only passed where no GPU exists")
+def test_fused_gn_statistics_calls_reject_invalid(L):
+    f = L.wan_causal_conv3d_gn_stats
+    ok = (A, None, None, A * 5, None, None, A * 9)
+    big = 1 << 30
+    assert f(*ok, 1, 2, 16, 16, 64, 320, 32, A * 13, big, None) == 2    # Cout % 256 != 0
+    assert f(*ok, 1, 2, 16, 16, 64, 256, 128, A * 13, big, None) == 2   # 2 channels per group
+    assert f(*ok, 1, 2, 16, 16, 64, 256, 32, None, big, None) == 1      # no statistics buffer
+    assert f(*ok, 1, 2, 16, 16, 64, 256, 32, MIS, big, None) == 3       # misaligned statistics buffer
+    assert f(*ok, 1, 2, 16, 16, 64, 256, 32, A * 13, 64, None) == 1     # buffer too small
+    g = L.wan_gn_silu_from_stats
+    gn = (A, A * 3, A * 5, A * 7)
+    assert g(*gn, 1, 2, 16, 16, 256, 32, 1e-6, None, big, A * 11, big, None) == 1      # no statistics
+    assert g(*gn, 1, 2, 16, 16, 64, 32, 1e-6, A * 13, big, A * 11, big, None) == 2     # C % 256 != 0
+    assert g(*gn, 1, 2, 16, 16, 256, 32, 1e-6, A * 13, 64, A * 11, big, None) == 1     # buffer too small
+    assert g(*gn, 1, 2, 16, 16, 256, 32, 1e-6, A * 13, big, None, 0, None) == 4        # no workspace
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers are only passed where no GPU exists")
+def test_gn_silu_causal_conv3d_rejects_invalid(L):
+    f = L.wan_gn_silu_causal_conv3d
+    big = 1 << 30
+
+    def call(x=A, groups=32, eps=1e-6, cache_in=None, cache_out=A * 20, y=A * 9, Cin=256, ws=A * 30, ws_bytes=big):
+        return f(x, A * 2, A * 3, groups, eps, cache_in, cache_out, A * 5, None, None, y, 1, 2, 16, 16, Cin, 256,
+                 ws, ws_bytes, None)
+    assert call(x=None) == 1                        # no input
+    assert call(groups=48) == 1                     # groups do not divide Cin
+    assert call(eps=0.0) == 1                       # eps must be positive
+    assert call(Cin=96) == 2                        # the conv wants Cin % 64 == 0
+    assert call(y=A) == 1                           # y overlaps x
+    assert call(cache_out=A + 4096) == 1            # the cache overlaps x
+    assert call(cache_in=MIS) == 3                  # misaligned history
+    assert call(ws=None) == 4                       # no workspace
+    assert call(ws_bytes=64) == 4                   # workspace too small
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers are only passed where no GPU exists")
+def test_gn_silu_steps_reject_invalid(L):
+    big = 1 << 30
+    co = L.wan_gn_silu_coefficients
+    assert co(A, A * 2, A * 3, 1, 2, 16, 16, 96, 32, 1e-6, A * 4, A * 5, big, None) == 2   # C % 64 != 0
+    assert co(A, A * 2, A * 3, 1, 2, 16, 16, 256, 32, 1e-6, None, A * 5, big, None) == 1  # no coefficient buffer
+    assert co(A, A * 2, A * 3, 1, 2, 16, 16, 256, 32, 1e-6, A * 4, None, 0, None) == 4    # no workspace
+    cv = L.wan_causal_conv3d_gn_input
+    assert cv(A, None, None, A * 5, None, None, A * 9, 1, 2, 16, 16, 256, 256, None) == 1  # no coefficients
+    assert cv(A, A * 4, None, A * 5, None, None, A * 9, 1, 2, 16, 16, 256, 128, None) == 2  # Cout < 256
+    assert cv(A, MIS, None, A * 5, None, None, A * 9, 1, 2, 16, 16, 256, 256, None) == 3    # misaligned coefficients
+    assert cv(A, A * 4, None, A * 5, None, None, A, 1, 2, 16, 16, 256, 256, None) == 1      # y overlaps x
+    cu = L.wan_gn_silu_cache_update
+    assert cu(A, A * 4, None, None, 1, 2, 16, 16, 256, None) == 1        # no cache_out
+    assert cu(A, A * 4, None, A * 20, 1, 2, 16, 16, 96, None) == 2       # C % 64 != 0
+    assert cu(A, A * 4, MIS, A * 20, 1, 2, 16, 16, 256, None) == 3       # misaligned history
+    assert cu(A, A * 4, None, A + 4096, 1, 2, 16, 16, 256, None) == 1    # cache overlaps x
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers are only passed where no GPU exists")

@@ -18,12 +18,15 @@ WAN_OP_GN_SILU = 0
 WAN_OP_CAUSAL_CONV3D = 1
 WAN_OP_RESBLOCK = 2
 WAN_OP_UPSAMPLE_PHASE_CONV = 3
+WAN_OP_GN_STATS = 4
+WAN_OP_GN_SILU_CONV3D = 5
 
 STATUS = {0: "WAN_OK", 1: "WAN_ERR_INVALID_ARG", 2: "WAN_ERR_UNSUPPORTED_SHAPE", 3: "WAN_ERR_MISALIGNED",
           4: "WAN_ERR_WORKSPACE", 5: "WAN_ERR_CUDA", 6: "WAN_ERR_TIMEOUT"}
 
 EXPORTS = ("wan_status_string", "wan_workspace_size", "wan_gn_silu", "wan_gn_silu_noalloc", "wan_causal_conv3d",
-           "wan_cache_update",
+           "wan_causal_conv3d_gn_stats", "wan_gn_silu_from_stats", "wan_gn_silu_causal_conv3d", "wan_gn_silu_coefficients",
+           "wan_causal_conv3d_gn_input", "wan_gn_silu_cache_update", "wan_cache_update",
            "wan_upsample_phase_weights", "wan_upsample_phase_conv", "wan_resblock", "wan_device_status")
 
 
@@ -63,6 +66,18 @@ def lib() -> ctypes.CDLL:
     L.wan_gn_silu_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P]
     L.wan_causal_conv3d.restype = I
     L.wan_causal_conv3d.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P, S, P]
+    L.wan_causal_conv3d_gn_stats.restype = I
+    L.wan_causal_conv3d_gn_stats.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, S, P]
+    L.wan_gn_silu_from_stats.restype = I
+    L.wan_gn_silu_from_stats.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, S, P, S, P]
+    L.wan_gn_silu_causal_conv3d.restype = I
+    L.wan_gn_silu_causal_conv3d.argtypes = [P, P, P, I, F, P, P, P, P, P, P, I, I, I, I, I, I, P, S, P]
+    L.wan_gn_silu_coefficients.restype = I
+    L.wan_gn_silu_coefficients.argtypes = [P, P, P, I, I, I, I, I, I, F, P, P, S, P]
+    L.wan_causal_conv3d_gn_input.restype = I
+    L.wan_causal_conv3d_gn_input.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P]
+    L.wan_gn_silu_cache_update.restype = I
+    L.wan_gn_silu_cache_update.argtypes = [P, P, P, P, I, I, I, I, I, P]
     L.wan_cache_update.restype = I
     L.wan_cache_update.argtypes = [P, P, P, I, I, I, I, I, P]
     L.wan_upsample_phase_weights.restype = I
@@ -156,6 +171,106 @@ def wan_causal_conv3d(a, w, bias=None, residual=None, cache_in=None, cache_out=N
     _check(lib().wan_causal_conv3d(_ptr(a), _ptr(cache_in), _ptr(cache_out), _ptr(w), _ptr(bias), _ptr(residual),
                                    _ptr(y), N, T, H, W, Cin, Cout, None, 0, _stream(stream)), "wan_causal_conv3d")
     return y
+
+
+def wan_causal_conv3d_gn_stats(a, w, groups: int, bias=None, residual=None, cache_in=None, cache_out=None, y=None,
+                               stats=None, stream=None):
+    """wan_causal_conv3d that also emits the GroupNorm statistics of y for wan_gn_silu_from_stats.
+    Returns (y, stats); stats is a uint8 device buffer private to the library."""
+    for t, n in ((a, "a"), (w, "w"), (bias, "bias"), (residual, "residual"), (cache_in, "cache_in"),
+                 (cache_out, "cache_out")):
+        _need(t, torch.bfloat16, n)
+    N, T, H, W, Cin = a.shape
+    Cout = w.shape[0]
+    y = torch.empty((N, T, H, W, Cout), dtype=torch.bfloat16, device=a.device) if y is None else y
+    _need(y, torch.bfloat16, "y")
+    need = wan_workspace_size(WAN_OP_GN_STATS, N, T, H, W, Cin, Cout, groups)
+    if need == 0:
+        raise WanError(2, "wan_causal_conv3d_gn_stats")
+    stats = _workspace(need, a.device, stats)
+    _check(lib().wan_causal_conv3d_gn_stats(_ptr(a), _ptr(cache_in), _ptr(cache_out), _ptr(w), _ptr(bias),
+                                            _ptr(residual), _ptr(y), N, T, H, W, Cin, Cout, groups, _ptr(stats),
+                                            stats.numel() * stats.element_size(), _stream(stream)), "wan_causal_conv3d_gn_stats")
+    return y, stats
+
+
+def wan_gn_silu_from_stats(x, gamma, beta, groups: int, eps: float, stats, y=None, ws=None, stream=None):
+    """silu(group_norm(x)) using the statistics wan_causal_conv3d_gn_stats emitted with x."""
+    _need(x, torch.bfloat16, "x")
+    _need(gamma, torch.float32, "gamma")
+    _need(beta, torch.float32, "beta")
+    N, T, H, W, C = x.shape
+    y = torch.empty_like(x) if y is None else y
+    _need(y, torch.bfloat16, "y")
+    need = wan_workspace_size(WAN_OP_GN_SILU, N, T, H, W, C, 0, groups)
+    ws = _workspace(need, x.device, ws)
+    _check(lib().wan_gn_silu_from_stats(_ptr(x), _ptr(y), _ptr(gamma), _ptr(beta), N, T, H, W, C, groups, eps,
+                                        _ptr(stats), stats.numel() * stats.element_size(), _ptr(ws), need if ws is not None else 0,
+                                        _stream(stream)), "wan_gn_silu_from_stats")
+    return y
+
+
+def wan_gn_silu_causal_conv3d(x, gamma, beta, groups: int, eps: float, w, bias=None, residual=None, cache_in=None,
+                              cache_out=None, y=None, ws=None, stream=None):
+    """y = causal_conv3d(silu(group_norm(x)); cache_in) + bias + residual, and cache_out = the last two
+    frames of [cache_in (or zeros); silu(group_norm(x))]; x [N, T, H, W, Cin], w [Cout, 3, 3, 3, Cin]."""
+    for t, n in ((x, "x"), (w, "w"), (bias, "bias"), (residual, "residual"), (cache_in, "cache_in"),
+                 (cache_out, "cache_out")):
+        _need(t, torch.bfloat16, n)
+    _need(gamma, torch.float32, "gamma")
+    _need(beta, torch.float32, "beta")
+    N, T, H, W, Cin = x.shape
+    Cout = w.shape[0]
+    y = torch.empty((N, T, H, W, Cout), dtype=torch.bfloat16, device=x.device) if y is None else y
+    _need(y, torch.bfloat16, "y")
+    need = wan_workspace_size(WAN_OP_GN_SILU_CONV3D, N, T, H, W, Cin, Cout, groups)
+    ws = _workspace(need, x.device, ws)
+    _check(lib().wan_gn_silu_causal_conv3d(_ptr(x), _ptr(gamma), _ptr(beta), groups, eps, _ptr(cache_in),
+                                           _ptr(cache_out), _ptr(w), _ptr(bias), _ptr(residual), _ptr(y), N, T, H, W,
+                                           Cin, Cout, _ptr(ws), need if ws is not None else 0, _stream(stream)),
+           "wan_gn_silu_causal_conv3d")
+    return y
+
+
+def wan_gn_silu_coefficients(x, gamma, beta, groups: int, eps: float, coef=None, ws=None, stream=None):
+    """Per-(frame, channel) GroupNorm + SiLU coefficients of x [N, T, H, W, C]: a uint8 device buffer of
+    N*T*C*16 bytes, private layout, for wan_causal_conv3d_gn_input and wan_gn_silu_cache_update."""
+    _need(x, torch.bfloat16, "x")
+    _need(gamma, torch.float32, "gamma")
+    _need(beta, torch.float32, "beta")
+    N, T, H, W, C = x.shape
+    coef = torch.empty(N * T * C * 16, dtype=torch.uint8, device=x.device) if coef is None else coef
+    need = wan_workspace_size(WAN_OP_GN_SILU, N, T, H, W, C, 0, groups)
+    ws = _workspace(need, x.device, ws)
+    _check(lib().wan_gn_silu_coefficients(_ptr(x), _ptr(gamma), _ptr(beta), N, T, H, W, C, groups, eps, _ptr(coef),
+                                          _ptr(ws), need if ws is not None else 0, _stream(stream)),
+           "wan_gn_silu_coefficients")
+    return coef
+
+
+def wan_causal_conv3d_gn_input(x, coef, w, bias=None, residual=None, cache_in=None, y=None, stream=None):
+    """y = causal_conv3d(silu(x S + B); cache_in) + bias + residual with coefficients from
+    wan_gn_silu_coefficients(x, ...); Cout >= 256."""
+    for t, n in ((x, "x"), (w, "w"), (bias, "bias"), (residual, "residual"), (cache_in, "cache_in")):
+        _need(t, torch.bfloat16, n)
+    N, T, H, W, Cin = x.shape
+    Cout = w.shape[0]
+    y = torch.empty((N, T, H, W, Cout), dtype=torch.bfloat16, device=x.device) if y is None else y
+    _need(y, torch.bfloat16, "y")
+    _check(lib().wan_causal_conv3d_gn_input(_ptr(x), _ptr(coef), _ptr(cache_in), _ptr(w), _ptr(bias), _ptr(residual),
+                                            _ptr(y), N, T, H, W, Cin, Cout, _stream(stream)),
+           "wan_causal_conv3d_gn_input")
+    return y
+
+
+def wan_gn_silu_cache_update(x, coef, cache_out, cache_in=None, stream=None):
+    """cache_out = last two frames of [cache_in (or zeros); silu(x S + B)]; cache_out may be cache_in."""
+    for t, n in ((x, "x"), (cache_in, "cache_in"), (cache_out, "cache_out")):
+        _need(t, torch.bfloat16, n)
+    N, T, H, W, C = x.shape
+    _check(lib().wan_gn_silu_cache_update(_ptr(x), _ptr(coef), _ptr(cache_in), _ptr(cache_out), N, T, H, W, C,
+                                          _stream(stream)), "wan_gn_silu_cache_update")
+    return cache_out
 
 
 def wan_cache_update(a, cache_out, cache_in=None, stream=None):

@@ -76,6 +76,33 @@ wan_status check_conv(const void* a, const void* w, const void* y, int N, int T,
   return WAN_OK;
 }
 
+// GroupNorm + SiLU feeding a causal conv. The CTA-pair conv (Cout >= 256) normalises its operand
+// tiles as they arrive: the norm's statistics pass writes coefficients only and the activation
+// a = silu(gn(x)) is never stored, except its last two frames, which go to the cache. Otherwise a
+// is materialised in the workspace and the conv reads it.
+bool gn_conv_fused(int Cout) { return conv_pair_supported(Cout); }
+
+size_t gn_conv_workspace(int N, int T, int H, int W, int Cin, int Cout, int groups) {
+  const size_t gnws = align256(gn_silu_workspace(N, T, H, W, Cin, groups, sm_count()));
+  if (gn_conv_fused(Cout)) return gnws;
+  return gnws + align256((size_t)N * T * H * W * Cin * sizeof(wan_bf16));
+}
+
+// cache_out = the last two frames of [cache_in or zeros; silu(x S + B)] with the blocked
+// coefficients of x. T >= 2: the normalised last two frames of x, written once. T = 1: the old
+// frame 1 (or zeros) moves to frame 0 first (one strided copy; in place it reads frame 1 before
+// anything writes it), then frame 0 of x goes to frame 1.
+cudaError_t gn_cache_update(const wan_bf16* x, const float4* coef, const wan_bf16* cache_in, wan_bf16* cache_out,
+                            int N, int T, int H, int W, int C, int sms, cudaStream_t s) {
+  if (T >= 2) return gn_apply_frames_launch(x, coef, cache_out, N, T, H, W, C, T - 2, 2, 0, sms, s);
+  const size_t fb = (size_t)H * W * C * sizeof(wan_bf16);
+  cudaError_t e = cache_in ? cudaMemcpy2DAsync(cache_out, 2 * fb, cache_in + fb / sizeof(wan_bf16), 2 * fb, fb, N,
+                                               cudaMemcpyDeviceToDevice, s)
+                           : cudaMemset2DAsync(cache_out, 2 * fb, 0, fb, N, s);
+  if (e != cudaSuccess) return e;
+  return gn_apply_frames_launch(x, coef, cache_out, N, 1, H, W, C, 0, 2, 1, sms, s);
+}
+
 }  // namespace
 
 unsigned* device_error_word() {
@@ -118,11 +145,17 @@ size_t wan_workspace_size(wan_op op, int N, int T, int H, int W, int Cin, int Co
     case WAN_OP_CAUSAL_CONV3D:
     case WAN_OP_UPSAMPLE_PHASE_CONV:
       return 0;
-    case WAN_OP_RESBLOCK: {
+    case WAN_OP_RESBLOCK: {  // h, then the norm-into-conv workspace
       if (groups <= 0 || Cin % groups || !gn_silu_supported(Cin, groups)) return 0;
-      const size_t act = (size_t)N * T * H * W * Cin * sizeof(wan_bf16);
-      return 2 * align256(act) + align256(gn_silu_workspace(N, T, H, W, Cin, groups, sm_count()));
+      const size_t h = (size_t)N * T * H * W * Cin * sizeof(wan_bf16);
+      return align256(h) + gn_conv_workspace(N, T, H, W, Cin, Cin, groups);
     }
+    case WAN_OP_GN_STATS:
+      if (!positive(Cout, groups, 1, 1, 1) || !conv_gn_stats_supported(Cout, groups)) return 0;
+      return conv_gn_stats_bytes(N, T, H, W, Cout, groups);
+    case WAN_OP_GN_SILU_CONV3D:
+      if (Cout <= 0 || groups <= 0 || Cin % groups || !gn_silu_supported(Cin, groups)) return 0;
+      return gn_conv_workspace(N, T, H, W, Cin, Cout, groups);
   }
   return 0;
 }
@@ -140,12 +173,43 @@ wan_status wan_gn_silu(const wan_bf16* x, wan_bf16* y, const float* gamma, const
                                     static_cast<cudaStream_t>(stream)));
 }
 
-wan_status wan_causal_conv3d(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out,
-                             const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y,
-                             int N, int T, int H, int W, int Cin, int Cout, void* ws, size_t ws_bytes,
-                             void* stream) {
-  (void)ws;
-  (void)ws_bytes;
+wan_status wan_gn_silu_from_stats(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta, int N,
+                                  int T, int H, int W, int C, int groups, float eps, const void* stats,
+                                  size_t stats_bytes, void* ws, size_t ws_bytes, void* stream) {
+  wan_status st = check_gn(x, y, gamma, beta, N, T, H, W, C, groups, eps);
+  if (st != WAN_OK) return st;
+  if (!stats) return WAN_ERR_INVALID_ARG;
+  if (!conv_gn_stats_supported(C, groups)) return WAN_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(stats)) return WAN_ERR_MISALIGNED;
+  if (stats_bytes < conv_gn_stats_bytes(N, T, H, W, C, groups)) return WAN_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)N * T * H * W * C * sizeof(wan_bf16);
+  if (overlap(x, bytes, y, bytes)) return WAN_ERR_INVALID_ARG;
+  const size_t need = wan_workspace_size(WAN_OP_GN_SILU, N, T, H, W, C, 0, groups);
+  if (!ws || ws_bytes < need) return WAN_ERR_WORKSPACE;
+  if (!aligned16(ws)) return WAN_ERR_MISALIGNED;
+  return cuda_status(gn_silu_launch(x, y, gamma, beta, N, T, H, W, C, groups, eps, ws, sm_count(),
+                                    static_cast<cudaStream_t>(stream), stats, conv_gn_stats_parts(H, W)));
+}
+
+}  // extern "C"
+
+namespace {
+
+// The conv kernel for these sizes: the 12-channel output head, else the general causal conv
+// (stats: null or the checked statistics buffer of y).
+cudaError_t launch_causal_conv(const wan_bf16* a, const wan_bf16* cache_in, const wan_bf16* w, const wan_bf16* bias,
+                               const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W, int Cin, int Cout,
+                               void* stats, int groups, unsigned* err, cudaStream_t s) {
+  if (head_supported(Cin, Cout) && !stats)
+    return head_launch(a, cache_in, w, bias, residual, y, N, T, H, W, Cin, sm_count(), err, s);
+  return conv_launch(0, a, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, sm_count(), err, s, stats, groups);
+}
+
+// The causal conv behind wan_causal_conv3d and wan_causal_conv3d_gn_stats (stats: null or the
+// checked statistics buffer of y).
+wan_status causal_conv(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out, const wan_bf16* w,
+                       const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W,
+                       int Cin, int Cout, void* stats, int groups, void* stream) {
   wan_status st = check_conv(a, w, y, N, T, H, W, Cin, Cout);
   if (st != WAN_OK) return st;
   if (!aligned16(cache_in) && cache_in) return WAN_ERR_MISALIGNED;
@@ -160,12 +224,137 @@ wan_status wan_causal_conv3d(const wan_bf16* a, const wan_bf16* cache_in, wan_bf
   unsigned* err = device_error_word();
   if (!err) return WAN_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (head_supported(Cin, Cout))
-    st = cuda_status(head_launch(a, cache_in, w, bias, residual, y, N, T, H, W, Cin, sm_count(), err, s));
-  else
-    st = cuda_status(conv_launch(0, a, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, sm_count(), err, s));
+  st = cuda_status(launch_causal_conv(a, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, stats, groups, err, s));
   if (st != WAN_OK || !cache_out) return st;
   return cuda_status(cache_update_launch(a, cache_in, cache_out, N, T, H, W, Cin, sm_count(), s));
+}
+
+// silu(gn(x)) into the causal conv, and the cache update, on checked arguments (gn_conv_fused
+// above says how). cache_out may be cache_in: every conv read of it precedes the cache writes.
+cudaError_t gn_conv(const wan_bf16* x, const float* gamma, const float* beta, int groups, float eps,
+                    const wan_bf16* cache_in, wan_bf16* cache_out, const wan_bf16* w, const wan_bf16* bias,
+                    const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W, int Cin, int Cout, void* ws,
+                    unsigned* err, cudaStream_t s) {
+  const int sms = sm_count();
+  char* base = static_cast<char*>(ws);
+  wan_bf16* act = reinterpret_cast<wan_bf16*>(base + align256(gn_silu_workspace(N, T, H, W, Cin, groups, sms)));
+  cudaError_t e;
+  if (!gn_conv_fused(Cout)) {
+    e = gn_silu_launch(x, act, gamma, beta, N, T, H, W, Cin, groups, eps, ws, sms, s);
+    if (e == cudaSuccess) e = launch_causal_conv(act, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout,
+                                                 nullptr, 0, err, s);
+    if (e == cudaSuccess && cache_out) e = cache_update_launch(act, cache_in, cache_out, N, T, H, W, Cin, sms, s);
+    return e;
+  }
+  e = gn_silu_launch(x, nullptr, gamma, beta, N, T, H, W, Cin, groups, eps, ws, sms, s, nullptr, 0, false);
+  const float4* coef = gn_silu_coef(ws, N, T, H, W, Cin, groups);
+  if (e == cudaSuccess)
+    e = conv_pair_launch(0, x, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, sms, err, s, nullptr, 0, coef);
+  if (e != cudaSuccess || !cache_out) return e;
+  return gn_cache_update(x, coef, cache_in, cache_out, N, T, H, W, Cin, sms, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+wan_status wan_causal_conv3d(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out,
+                             const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y,
+                             int N, int T, int H, int W, int Cin, int Cout, void* ws, size_t ws_bytes,
+                             void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  return causal_conv(a, cache_in, cache_out, w, bias, residual, y, N, T, H, W, Cin, Cout, nullptr, 0, stream);
+}
+
+wan_status wan_causal_conv3d_gn_stats(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out,
+                                      const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y,
+                                      int N, int T, int H, int W, int Cin, int Cout, int groups, void* stats,
+                                      size_t stats_bytes, void* stream) {
+  if (!stats || groups <= 0) return WAN_ERR_INVALID_ARG;
+  if (!positive(N, T, H, W, Cin) || Cout <= 0) return WAN_ERR_INVALID_ARG;
+  if (!conv_gn_stats_supported(Cout, groups)) return WAN_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(stats)) return WAN_ERR_MISALIGNED;
+  if (stats_bytes < conv_gn_stats_bytes(N, T, H, W, Cout, groups)) return WAN_ERR_INVALID_ARG;
+  return causal_conv(a, cache_in, cache_out, w, bias, residual, y, N, T, H, W, Cin, Cout, stats, groups, stream);
+}
+
+wan_status wan_gn_silu_causal_conv3d(const wan_bf16* x, const float* gamma, const float* beta, int groups,
+                                     float eps, const wan_bf16* cache_in, wan_bf16* cache_out, const wan_bf16* w,
+                                     const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H,
+                                     int W, int Cin, int Cout, void* ws, size_t ws_bytes, void* stream) {
+  wan_status st = check_gn(x, y, gamma, beta, N, T, H, W, Cin, groups, eps);
+  if (st != WAN_OK) return st;
+  st = check_conv(x, w, y, N, T, H, W, Cin, Cout);
+  if (st != WAN_OK) return st;
+  if ((cache_in && !aligned16(cache_in)) || (cache_out && !aligned16(cache_out)) || (bias && !aligned16(bias)) ||
+      (residual && !aligned16(residual)))
+    return WAN_ERR_MISALIGNED;
+  const size_t xbytes = (size_t)N * T * H * W * Cin * 2, ybytes = (size_t)N * T * H * W * Cout * 2;
+  const size_t cbytes = (size_t)N * 2 * H * W * Cin * 2;
+  if (overlap(x, xbytes, y, ybytes) || overlap(residual, ybytes, y, ybytes) || overlap(cache_in, cbytes, y, ybytes) ||
+      overlap(cache_out, cbytes, y, ybytes) || overlap(cache_out, cbytes, x, xbytes) ||
+      (cache_in && cache_in != cache_out && overlap(cache_in, cbytes, cache_out, cbytes)))
+    return WAN_ERR_INVALID_ARG;
+  const size_t need = gn_conv_workspace(N, T, H, W, Cin, Cout, groups);
+  if (!ws || ws_bytes < need) return WAN_ERR_WORKSPACE;
+  if (!aligned16(ws)) return WAN_ERR_MISALIGNED;
+  unsigned* err = device_error_word();
+  if (!err) return WAN_ERR_CUDA;
+  return cuda_status(gn_conv(x, gamma, beta, groups, eps, cache_in, cache_out, w, bias, residual, y, N, T, H, W, Cin,
+                             Cout, ws, err, static_cast<cudaStream_t>(stream)));
+}
+
+wan_status wan_gn_silu_coefficients(const wan_bf16* x, const float* gamma, const float* beta, int N, int T, int H,
+                                    int W, int C, int groups, float eps, void* coef, void* ws, size_t ws_bytes,
+                                    void* stream) {
+  wan_status st = check_gn(x, coef, gamma, beta, N, T, H, W, C, groups, eps);
+  if (st != WAN_OK) return st;
+  if (C % 64 != 0) return WAN_ERR_UNSUPPORTED_SHAPE;
+  const size_t xbytes = (size_t)N * T * H * W * C * 2, cbytes = (size_t)N * T * C * 16;
+  if (overlap(x, xbytes, coef, cbytes)) return WAN_ERR_INVALID_ARG;
+  const size_t need = wan_workspace_size(WAN_OP_GN_SILU, N, T, H, W, C, 0, groups);
+  if (!ws || ws_bytes < need) return WAN_ERR_WORKSPACE;
+  if (!aligned16(ws)) return WAN_ERR_MISALIGNED;
+  return cuda_status(gn_silu_launch(x, nullptr, gamma, beta, N, T, H, W, C, groups, eps, ws, sm_count(),
+                                    static_cast<cudaStream_t>(stream), nullptr, 0, false,
+                                    static_cast<float4*>(coef)));
+}
+
+wan_status wan_causal_conv3d_gn_input(const wan_bf16* x, const void* coef, const wan_bf16* cache_in, const wan_bf16* w,
+                                      const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H,
+                                      int W, int Cin, int Cout, void* stream) {
+  if (!coef) return WAN_ERR_INVALID_ARG;
+  wan_status st = check_conv(x, w, y, N, T, H, W, Cin, Cout);
+  if (st != WAN_OK) return st;
+  if (!gn_conv_fused(Cout)) return WAN_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(coef) || (cache_in && !aligned16(cache_in)) || (bias && !aligned16(bias)) ||
+      (residual && !aligned16(residual)))
+    return WAN_ERR_MISALIGNED;
+  const size_t xbytes = (size_t)N * T * H * W * Cin * 2, ybytes = (size_t)N * T * H * W * Cout * 2;
+  if (overlap(x, xbytes, y, ybytes) || overlap(residual, ybytes, y, ybytes) ||
+      overlap(cache_in, (size_t)N * 2 * H * W * Cin * 2, y, ybytes) || overlap(coef, (size_t)N * T * Cin * 16, y, ybytes))
+    return WAN_ERR_INVALID_ARG;
+  unsigned* err = device_error_word();
+  if (!err) return WAN_ERR_CUDA;
+  return cuda_status(conv_pair_launch(0, x, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, sm_count(), err,
+                                      static_cast<cudaStream_t>(stream), nullptr, 0,
+                                      static_cast<const float4*>(coef)));
+}
+
+wan_status wan_gn_silu_cache_update(const wan_bf16* x, const void* coef, const wan_bf16* cache_in, wan_bf16* cache_out,
+                                    int N, int T, int H, int W, int C, void* stream) {
+  if (!x || !coef || !cache_out) return WAN_ERR_INVALID_ARG;
+  if (!positive(N, T, H, W, C)) return WAN_ERR_INVALID_ARG;
+  if (C % 64 != 0 || C > 2048 || !fits(N, T, H, W, C)) return WAN_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(coef) || !aligned16(cache_out) || (cache_in && !aligned16(cache_in)))
+    return WAN_ERR_MISALIGNED;
+  const size_t xbytes = (size_t)N * T * H * W * C * 2, cbytes = (size_t)N * 2 * H * W * C * 2;
+  if (overlap(cache_out, cbytes, x, xbytes) || overlap(cache_out, cbytes, coef, (size_t)N * T * C * 16) ||
+      (cache_in && cache_in != cache_out && overlap(cache_in, cbytes, cache_out, cbytes)))
+    return WAN_ERR_INVALID_ARG;
+  return cuda_status(gn_cache_update(x, static_cast<const float4*>(coef), cache_in, cache_out, N, T, H, W, C,
+                                     sm_count(), static_cast<cudaStream_t>(stream)));
 }
 
 wan_status wan_cache_update(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out, int N, int T, int H,
@@ -225,21 +414,18 @@ wan_status wan_resblock(const wan_bf16* x, wan_bf16* out, const wan_resblock_par
   if (!aligned16(ws)) return WAN_ERR_MISALIGNED;
   unsigned* err = device_error_word();
   if (!err) return WAN_ERR_CUDA;
-  const int sms = sm_count();
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* base = static_cast<char*>(ws);
-  wan_bf16* act = reinterpret_cast<wan_bf16*>(base);
-  wan_bf16* h = reinterpret_cast<wan_bf16*>(base + align256(bytes));
-  void* gn_ws = base + 2 * align256(bytes);
+  wan_bf16* h = reinterpret_cast<wan_bf16*>(base);
+  void* gws = base + align256(bytes);
   const wan_bf16* c1_in = cache_valid ? cache1 : nullptr;
   const wan_bf16* c2_in = cache_valid ? cache2 : nullptr;
-
-  cudaError_t e = gn_silu_launch(x, act, p->gamma1, p->beta1, N, T, H, W, C, p->groups, p->eps, gn_ws, sms, s);
-  if (e == cudaSuccess) e = conv_launch(0, act, c1_in, p->w1, p->b1, nullptr, h, N, T, H, W, C, C, sms, err, s);
-  if (e == cudaSuccess) e = cache_update_launch(act, c1_in, cache1, N, T, H, W, C, sms, s);
-  if (e == cudaSuccess) e = gn_silu_launch(h, act, p->gamma2, p->beta2, N, T, H, W, C, p->groups, p->eps, gn_ws, sms, s);
-  if (e == cudaSuccess) e = conv_launch(0, act, c2_in, p->w2, p->b2, x, out, N, T, H, W, C, C, sms, err, s);
-  if (e == cudaSuccess) e = cache_update_launch(act, c2_in, cache2, N, T, H, W, C, sms, s);
+  // Each norm feeds its conv directly (the cache update of that conv's input included).
+  cudaError_t e = gn_conv(x, p->gamma1, p->beta1, p->groups, p->eps, c1_in, cache1, p->w1, p->b1, nullptr, h, N, T,
+                          H, W, C, C, gws, err, s);
+  if (e == cudaSuccess)
+    e = gn_conv(h, p->gamma2, p->beta2, p->groups, p->eps, c2_in, cache2, p->w2, p->b2, x, out, N, T, H, W, C, C, gws,
+                err, s);
   return cuda_status(e);
 }
 

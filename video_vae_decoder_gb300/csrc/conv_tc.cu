@@ -410,9 +410,12 @@ size_t conv_workspace() { return 0; }
 
 cudaError_t conv_launch(int mode, const wan_bf16* a, const wan_bf16* cache_in, const wan_bf16* w,
                         const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H,
-                        int W, int Cin, int Cout, int sms, unsigned* err, cudaStream_t stream) {
+                        int W, int Cin, int Cout, int sms, unsigned* err, cudaStream_t stream, void* st_buf,
+                        int st_groups) {
   if (conv_pair_supported(Cout))
-    return conv_pair_launch(mode, a, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, sms, err, stream);
+    return conv_pair_launch(mode, a, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, sms, err, stream, st_buf,
+                            st_groups);
+  if (st_buf) return cudaErrorInvalidValue;  // output statistics come from the CTA-pair kernel only
   ConvArgs args{};
   args.N = N;
   args.T = T;

@@ -8,12 +8,24 @@ namespace wan {
 // mode 0: causal 3x3x3 conv (w [Cout, 27, Cin]); mode 1: 2x2 phase convs (w [4, Cout, 4, Cin]).
 cudaError_t conv_launch(int mode, const wan_bf16* a, const wan_bf16* cache_in, const wan_bf16* w,
                         const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T,
-                        int H, int W, int Cin, int Cout, int sms, unsigned* err, cudaStream_t stream);
+                        int H, int W, int Cin, int Cout, int sms, unsigned* err, cudaStream_t stream,
+                        void* st_buf = nullptr, int st_groups = 0);
 // The same convolutions on CTA pairs (tcgen05 .cta_group::2), for Cout >= 256 (conv_tc2.cu).
 bool conv_pair_supported(int Cout);
 cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_in, const wan_bf16* w,
                              const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W,
-                             int Cin, int Cout, int sms, unsigned* err, cudaStream_t stream);
+                             int Cin, int Cout, int sms, unsigned* err, cudaStream_t stream,
+                             void* st_buf = nullptr, int st_groups = 0, const float4* coef = nullptr);
+// coef (optional, mode 0): GroupNorm + SiLU of `a` applied to the conv's operand tiles as they
+// arrive (per (frame n*T + t, Cin channel) float4 coefficients as the norm's coefficients-only
+// pass leaves them, blocked layout); the cache frames are used as they are.
+// GroupNorm statistics of the causal conv's output, emitted by the CTA-pair kernel's epilogue
+// (Cout a multiple of 256, channels per group a power of two from 4 to 64): per (frame, group,
+// 8 x 16-pixel tile, epilogue warp) the float-float sums of d and d^2 of d = y - s as a float4,
+// followed by the (s, count) pairs as float2.
+bool conv_gn_stats_supported(int Cout, int groups);
+size_t conv_gn_stats_bytes(int N, int T, int H, int W, int Cout, int groups);
+int conv_gn_stats_parts(int H, int W);  // parts (pixel tiles x 4 warps) per (frame, group)
 // cache_out[n, j] = ([cache_in or zeros; a])[n, T + j], j = 0, 1.
 cudaError_t cache_update_launch(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out,
                                 int N, int T, int H, int W, int C, int sms, cudaStream_t stream);

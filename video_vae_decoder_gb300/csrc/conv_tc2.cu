@@ -41,23 +41,38 @@ namespace wan {
 
 namespace {
 
-constexpr int kThreads = 192;           // producer, MMA issuer, 4 epilogue warps
 constexpr int kBlockK = 64;
 constexpr int kTileH = 8, kTileW = 16;  // output pixels of one CTA: 8 rows x 16 columns
 constexpr int kBoxW = kTileW + 2;       // input columns of one A box (one halo column per side)
 constexpr int kABytes = kTileH * kBoxW * 128;  // 144 rows x 64 bf16 = 18 KB
 constexpr int kBBytes = 128 * 128;             // this CTA's 128 weight rows x 64 bf16
-constexpr int kAStages = 4;
-constexpr int kBStages = 9;
-constexpr int kBOffset = kAStages * kABytes;
-constexpr int kBarOffset = kBOffset + kBStages * kBBytes;
-constexpr int kSmemTotal = kBarOffset + 512 + 1024;
 constexpr int kN = 256;                 // output channels per item (both halves)
 constexpr int kTmemCols = 512;          // 2 accumulators x 256 columns
 constexpr uint32_t kShiftDesc = (kTileH * 128) >> 4;  // one column of the box, in descriptor units
+constexpr int kCoefBytes = kBlockK * 16;                // GroupNorm coefficients of one A stage
+constexpr int kTallRows = kTileH + 2;                   // rows of a tall A box (one halo row per side)
 
 static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
-static_assert(kSmemTotal <= 232448, "shared memory per CTA");
+// Stage rings and shared memory. The plain kernel: producer, MMA issuer, 4 epilogue warps. With
+// the GroupNorm + SiLU operand prologue: 8 more warps that normalise each A box in place between
+// its arrival and the MMAs.
+template <bool kNorm>
+struct Cfg {
+  static constexpr int kThreads = kNorm ? 448 : 192;  // + 8 prologue warps
+  // kNorm: one tall A box per (kernel frame, 64 channels), 10 x 18 pixels, serves all 9 taps of
+  // that frame (the plain kernel loads one 8 x 18 box per kernel row, for its 3 taps), so every
+  // pixel is normalised once per box instead of three times.
+  static constexpr int kABox = kNorm ? kTallRows * kBoxW * 128 : kABytes;
+  static constexpr int kAStride = (kABox + 1023) / 1024 * 1024;
+  static constexpr int kAStages = kNorm ? 3 : 4;
+  static constexpr int kBStages = 9;
+  static constexpr int kBOffset = kAStages * kAStride;
+  // kNorm: each A stage's 64 channels of coefficients (16 bytes each) arrive with the box.
+  static constexpr int kCoefOffset = kBOffset + kBStages * kBBytes;
+  static constexpr int kBarOffset = kCoefOffset + (kNorm ? kAStages * kCoefBytes : 0);
+  static constexpr int kSmemTotal = kBarOffset + 512 + 1024;
+};
+static_assert(Cfg<false>::kSmemTotal <= 232448 && Cfg<true>::kSmemTotal <= 232448, "shared memory per CTA");
 
 struct Conv2Args {
   int N, T, H, W, Cin, Cout;
@@ -69,6 +84,18 @@ struct Conv2Args {
   const wan_bf16* residual;
   wan_bf16* y;
   unsigned* err;
+  // GroupNorm statistics of y (null: none): one record per (frame, group, pixel tile, epilogue
+  // warp): st_rec = float-float (sum d, sum d^2) over the warp's valid pixels x the group's
+  // cg = 2^st_lg channels, d = y - s as stored (bf16); st_meta = (s, count), s the group's first
+  // channel at the warp's first valid pixel (all zero for a warp without valid pixels).
+  float4* st_rec;
+  float2* st_meta;
+  int st_cg, st_lg;
+  // Operand prologue (the kNorm kernel): per (frame n*T + t, input channel) the GroupNorm + SiLU
+  // coefficients (S_hi, S_lo, B_hi, B_lo), blocked layout (coef_blocked_index), applied to every
+  // A box read from `a` (not the cache).
+  const float4* coef;
+  const wan_bf16* a;  // the conv input itself (the prologue's rare exact path reads it again)
 };
 
 struct PTile {
@@ -128,19 +155,59 @@ __device__ __forceinline__ bool skip_pair(const Conv2Args& a, const PTile& p0, c
   return z0 && z1;
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// Float-float sums of 8 values over the 32 lanes of a warp as a reduce-scatter: three halving
+// exchanges (xor 4, 2, 1) leave lane l with value l & 7 summed over its 8-lane set, two butterfly
+// steps (xor 8, 16) add the 4 sets. 18 shuffles for 8 totals.
+__device__ __forceinline__ void st_reduce8(const float (&vh)[8], const float (&vl)[8], int lane, float& H, float& L) {
+  const bool b2 = lane & 4, b1 = lane & 2, b0 = lane & 1;
+  float hh[4], hl[4], eh[2], el[2];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    hh[j] = b2 ? vh[j + 4] : vh[j];
+    hl[j] = b2 ? vl[j + 4] : vl[j];
+    const float oh = __shfl_xor_sync(0xffffffffu, b2 ? vh[j] : vh[j + 4], 4);
+    const float ol = __shfl_xor_sync(0xffffffffu, b2 ? vl[j] : vl[j + 4], 4);
+    ff_add(hh[j], hl[j], oh, ol);
+  }
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    eh[j] = b1 ? hh[j + 2] : hh[j];
+    el[j] = b1 ? hl[j + 2] : hl[j];
+    const float oh = __shfl_xor_sync(0xffffffffu, b1 ? hh[j] : hh[j + 2], 2);
+    const float ol = __shfl_xor_sync(0xffffffffu, b1 ? hl[j] : hl[j + 2], 2);
+    ff_add(eh[j], el[j], oh, ol);
+  }
+  H = b0 ? eh[1] : eh[0];
+  L = b0 ? el[1] : el[0];
+  {
+    const float oh = __shfl_xor_sync(0xffffffffu, b0 ? eh[0] : eh[1], 1);
+    const float ol = __shfl_xor_sync(0xffffffffu, b0 ? el[0] : el[1], 1);
+    ff_add(H, L, oh, ol);
+  }
+#pragma unroll
+  for (int off = 8; off < 32; off <<= 1) {
+    const float oh = __shfl_xor_sync(0xffffffffu, H, off), ol = __shfl_xor_sync(0xffffffffu, L, off);
+    ff_add(H, L, oh, ol);
+  }
+}
+
+template <bool kNorm>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads, 1)
     conv_tc2_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_cache,
                     const __grid_constant__ CUtensorMap tm_w, const Conv2Args args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full_a = reinterpret_cast<uint64_t*>(smem + kBarOffset);
+  constexpr int kAStages = Cfg<kNorm>::kAStages, kBStages = Cfg<kNorm>::kBStages;
+  constexpr int kBOffset = Cfg<kNorm>::kBOffset, kAStride = Cfg<kNorm>::kAStride, kABox = Cfg<kNorm>::kABox;
+  uint64_t* full_a = reinterpret_cast<uint64_t*>(smem + Cfg<kNorm>::kBarOffset);
   uint64_t* empty_a = full_a + kAStages;
   uint64_t* full_b = empty_a + kAStages;
   uint64_t* empty_b = full_b + kBStages;
   uint64_t* tmem_full = empty_b + kBStages;
   uint64_t* tmem_empty = tmem_full + 2;
   uint64_t* mma_done = tmem_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* ready_a = mma_done + 1;  // kNorm: both CTAs' prologue warps are done with stage s (leader)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ready_a + kAStages);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -148,8 +215,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const bool leader = rank == 0;
   const int cluster = blockIdx.x >> 1;
   const int nclusters = gridDim.x >> 1;
-  const int rows = args.mode == 0 ? 9 : 2;     // kernel rows
-  const int taps_per_row = args.mode == 0 ? 3 : 2;
+  // A boxes per K slice of an item, and taps (B stages) per A box: kernel rows of 3 (mode 0) or 2
+  // (mode 1) taps; with the prologue, kernel frames of 9 taps. The boxes go in the order (group of
+  // rows_in rows, K slice, row in the group): mode 0 takes a kernel frame's 3 rows per K slice, so
+  // the taps are added in the order (dt, K slice, dh, dw), the prologue kernel's order too, and
+  // the two kernels give the same bits.
+  const int rows = kNorm ? 3 : (args.mode == 0 ? 9 : 2);
+  const int taps_per_row = kNorm ? 9 : (args.mode == 0 ? 3 : 2);
+  const int rows_in = (!kNorm && args.mode == 0) ? 3 : 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAStages; ++s) {
@@ -165,6 +238,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&tmem_empty[s], 8);  // 4 epilogue warps in each CTA of the pair
     }
     mbar_init(mma_done, 1);
+    if (kNorm)
+      for (int s = 0; s < kAStages; ++s) mbar_init(&ready_a[s], 16);  // 8 prologue warps per CTA
     fence_mbarrier_init();
     prefetch_tensormap(&tm_a);
     prefetch_tensormap(&tm_cache);
@@ -194,55 +269,80 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const PTile me = decode_pair(args, item, (int)rank);
       const PTile p0 = decode_pair(args, item, 0), p1 = decode_pair(args, item, 1);
       const int brow = me.nb * kN + (int)rank * 128;
-      for (int row = 0; ok && row < rows; ++row) {
-        int dt, dh, dw0;
-        row_offsets(args, row, me.ph, dt, dh, dw0);
-        if (skip_pair(args, p0, p1, dt)) continue;
-        const int hh = me.h0 + dh, ww = me.w0 + dw0;
-        int tau = me.t0 + dt;
-        if (!me.valid) tau = args.T + 8;  // out of range: the TMA unit fills zeros
+      for (int rg = 0; ok && rg < rows; rg += rows_in) {
         for (int kb = 0; ok && kb < args.kb_per_tap; ++kb) {
-          if (!mbar_wait_cluster(&empty_a[sa], pha ^ 1, args.err, kDevErrTimeoutProducer)) {
-            ok = false;
-            break;
-          }
-          if (leader) {
-            mbar_arrive_expect_tx(&full_a[sa], 2 * kABytes);  // both CTAs' bytes land on it
-            armed_a |= 1u << sa;
-            parity_a = (parity_a & ~(1u << sa)) | (pha << sa);
-          }
-          const uint32_t bar_a = mapa_shared(smem_u32(&full_a[sa]), 0);
-          uint8_t* a_dst = smem + sa * kABytes;
-          if (tau < 0 && args.has_cache)
-            tma_load_5d_pair(a_dst, &tm_cache, bar_a, kb * kBlockK, hh, ww, tau + 2, me.n);
-          else
-            tma_load_5d_pair(a_dst, &tm_a, bar_a, kb * kBlockK, hh, ww, tau, me.n);
-          if (++sa == kAStages) {
-            sa = 0;
-            pha ^= 1;
-          }
-          for (int j = 0; j < taps_per_row; ++j) {
-            if (!mbar_wait_cluster(&empty_b[sb], phb ^ 1, args.err, kDevErrTimeoutProducer)) {
+          for (int row = rg; ok && row < rg + rows_in; ++row) {
+            int dt, dh, dw0;
+            if (kNorm) {  // kernel frame row: the tall box starts one row above and left of the tile
+              dt = row - 2;
+              dh = -1;
+              dw0 = -1;
+            } else {
+              row_offsets(args, row, me.ph, dt, dh, dw0);
+            }
+            if (skip_pair(args, p0, p1, dt)) continue;
+            const int hh = me.h0 + dh, ww = me.w0 + dw0;
+            int tau = me.t0 + dt;
+            if (!me.valid) tau = args.T + 8;  // out of range: the TMA unit fills zeros
+            if (!mbar_wait_cluster(&empty_a[sa], pha ^ 1, args.err, kDevErrTimeoutProducer)) {
               ok = false;
               break;
             }
-            if (leader) {
-              mbar_arrive_expect_tx(&full_b[sb], 2 * kBBytes);
-              armed_b |= 1u << sb;
-              parity_b = (parity_b & ~(1u << sb)) | (phb << sb);
+            uint8_t* a_dst = smem + sa * kAStride;
+            if (kNorm) {
+              // Each CTA's box lands on its own barrier, with the 64 channels' coefficients of its
+              // frame (any in-range frame for boxes the prologue leaves alone): its prologue warps
+              // wait for both.
+              mbar_arrive_expect_tx(&full_a[sa], kABox + kCoefBytes);
+              const int fc = min(max(tau, 0), args.T - 1);
+              bulk_load(smem + Cfg<kNorm>::kCoefOffset + sa * kCoefBytes,
+                        args.coef + ((size_t)me.n * args.T + fc) * args.Cin + kb * kBlockK, kCoefBytes, &full_a[sa]);
+              armed_a |= 1u << sa;
+              parity_a = (parity_a & ~(1u << sa)) | (pha << sa);
+              if (tau < 0 && args.has_cache)
+                tma_load_5d(a_dst, &tm_cache, &full_a[sa], kb * kBlockK, hh, ww, tau + 2, me.n);
+              else
+                tma_load_5d(a_dst, &tm_a, &full_a[sa], kb * kBlockK, hh, ww, tau, me.n);
+            } else {
+              if (leader) {
+                mbar_arrive_expect_tx(&full_a[sa], 2 * kABytes);  // both CTAs' bytes land on it
+                armed_a |= 1u << sa;
+                parity_a = (parity_a & ~(1u << sa)) | (pha << sa);
+              }
+              const uint32_t bar_a = mapa_shared(smem_u32(&full_a[sa]), 0);
+              if (tau < 0 && args.has_cache)
+                tma_load_5d_pair(a_dst, &tm_cache, bar_a, kb * kBlockK, hh, ww, tau + 2, me.n);
+              else
+                tma_load_5d_pair(a_dst, &tm_a, bar_a, kb * kBlockK, hh, ww, tau, me.n);
             }
-            const int tap = row * taps_per_row + j;
-            tma_load_3d_pair(smem + kBOffset + sb * kBBytes, &tm_w, mapa_shared(smem_u32(&full_b[sb]), 0),
-                             tap * args.Cin + kb * kBlockK, brow, me.ph, w_policy);
-            if (++sb == kBStages) {
-              sb = 0;
-              phb ^= 1;
+            if (++sa == kAStages) {
+              sa = 0;
+              pha ^= 1;
+            }
+            for (int j = 0; j < taps_per_row; ++j) {
+              if (!mbar_wait_cluster(&empty_b[sb], phb ^ 1, args.err, kDevErrTimeoutProducer)) {
+                ok = false;
+                break;
+              }
+              if (leader) {
+                mbar_arrive_expect_tx(&full_b[sb], 2 * kBBytes);
+                armed_b |= 1u << sb;
+                parity_b = (parity_b & ~(1u << sb)) | (phb << sb);
+              }
+              const int tap = row * taps_per_row + j;
+              tma_load_3d_pair(smem + kBOffset + sb * kBBytes, &tm_w, mapa_shared(smem_u32(&full_b[sb]), 0),
+                               tap * args.Cin + kb * kBlockK, brow, me.ph, w_policy);
+              if (++sb == kBStages) {
+                sb = 0;
+                phb ^= 1;
+              }
             }
           }
         }
       }
     }
-    // Drain (even CTA): both CTAs' loads counted on its full barriers have landed.
+    // Drain: every load counted on this CTA's full barriers has landed (the even CTA's B barriers
+    // count both CTAs' weights; with the prologue each CTA's A barriers count its own boxes).
     for (int s = 0; s < kAStages; ++s)
       if (armed_a & (1u << s)) mbar_wait(&full_a[s], (parity_a >> s) & 1, args.err, kDevErrTimeoutDrain);
     for (int s = 0; s < kBStages; ++s)
@@ -265,41 +365,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * kN;
       bool first = true;
-      for (int row = 0; ok && row < rows; ++row) {
-        if (!args.has_cache) {  // without history some rows read only zeros for both tiles
-          int dt, dh, dw0;
-          row_offsets(args, row, p0.ph, dt, dh, dw0);
-          if (skip_pair(args, p0, p1, dt)) continue;
-        }
+      for (int rg = 0; ok && rg < rows; rg += rows_in) {
         for (int kb = 0; ok && kb < args.kb_per_tap; ++kb) {
-          if (!mbar_wait_cluster(&full_a[sa], pha, args.err, kDevErrTimeoutMma)) {
-            ok = false;
-            break;
-          }
-          const uint64_t a_desc = smem_desc_sw128(a_base + sa * kABytes);
-          for (int j = 0; j < taps_per_row; ++j) {
-            if (!mbar_wait_cluster(&full_b[sb], phb, args.err, kDevErrTimeoutMma)) {
+          for (int row = rg; ok && row < rg + rows_in; ++row) {
+            if (!args.has_cache) {  // without history some rows read only zeros for both tiles
+              int dt, dh, dw0;
+              if (kNorm)
+                dt = row - 2;
+              else
+                row_offsets(args, row, p0.ph, dt, dh, dw0);
+              if (skip_pair(args, p0, p1, dt)) continue;
+            }
+            if (!mbar_wait_cluster(kNorm ? &ready_a[sa] : &full_a[sa], pha, args.err, kDevErrTimeoutMma)) {
               ok = false;
               break;
             }
-            tc_fence_after();
-            const uint64_t aj = a_desc + j * kShiftDesc;
-            const uint64_t b_desc = smem_desc_sw128(b_base + sb * kBBytes);
-#pragma unroll
-            for (int k = 0; k < kBlockK / 16; ++k)
-              mma_bf16_pair(d_tmem, aj + 2 * k, b_desc + 2 * k, idesc, (first && k == 0) ? 0u : 1u);
-            first = false;
-            mma_commit_pair(&empty_b[sb], 0x3);
-            if (++sb == kBStages) {
-              sb = 0;
-              phb ^= 1;
+            const uint32_t a_box = a_base + sa * kAStride;
+            const uint64_t a_desc = smem_desc_sw128(a_box);
+            for (int j = 0; j < taps_per_row; ++j) {
+              if (!mbar_wait_cluster(&full_b[sb], phb, args.err, kDevErrTimeoutMma)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              // Tap j of the box: plain, the next column (1024 bytes on); tall box, rows
+              // dh + 10 dw of its 10-row columns (tap j = 3 dh + dw), columns 1280 bytes apart.
+              const uint64_t aj = kNorm ? smem_desc_sw128(a_box + ((j % 3) * kTallRows + j / 3) * 128, kTallRows * 128)
+                                        : a_desc + j * kShiftDesc;
+              const uint64_t b_desc = smem_desc_sw128(b_base + sb * kBBytes);
+  #pragma unroll
+              for (int k = 0; k < kBlockK / 16; ++k)
+                mma_bf16_pair(d_tmem, aj + 2 * k, b_desc + 2 * k, idesc, (first && k == 0) ? 0u : 1u);
+              first = false;
+              mma_commit_pair(&empty_b[sb], 0x3);
+              if (++sb == kBStages) {
+                sb = 0;
+                phb ^= 1;
+              }
             }
-          }
-          if (!ok) break;
-          mma_commit_pair(&empty_a[sa], 0x3);
-          if (++sa == kAStages) {
-            sa = 0;
-            pha ^= 1;
+            if (!ok) break;
+            mma_commit_pair(&empty_a[sa], 0x3);
+            if (++sa == kAStages) {
+              sa = 0;
+              pha ^= 1;
+            }
           }
         }
       }
@@ -312,7 +421,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mma_commit_pair(mma_done, 0x1);
     mbar_wait(mma_done, 0, args.err, kDevErrTimeoutDrain);
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------ epilogue (both CTAs, own 128 rows)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
@@ -341,9 +450,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       wan_bf16* yrow = args.y + pix * args.Cout;
       const wan_bf16* rrow = args.residual ? args.residual + pix * args.Cout : nullptr;
       const uint32_t taddr = tmem_base + (uint32_t)(acc * kN) + ((uint32_t)(quarter * 32) << 16);
+      // GroupNorm statistics of this tile's output (optional): per group, each lane adds d and d^2
+      // over the group's channels as float-float pairs (TwoSum, Fast2Sum; even and odd channels
+      // in the two halves of packed fp32x2), the warp totals 4 groups at once (float-float
+      // reduce-scatter) and writes one record per group.
+      const bool stats = args.st_rec != nullptr && t.valid;
+      const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+      const int src = vmask ? __ffs(vmask) - 1 : 0;
+      const int cg = args.st_cg, lg = args.st_lg;
+      const size_t rec_stride = (size_t)args.tiles_h * args.tiles_w * 4;  // between groups
+      const size_t rec0 = ((((size_t)t.n * args.T + tt) * (args.Cout >> lg) + (size_t)t.nb * (kN >> lg)) *
+                               (size_t)args.tiles_h * args.tiles_w +
+                           (size_t)(t.h0 / kTileH) * args.tiles_w + t.w0 / kTileW) * 4 + quarter;
+      float wh[8], wl[8], shw[4];  // the window's 4 groups: (sum d, sum d^2) as float-float, shifts
+#pragma unroll
+      for (int k = 0; k < 8; ++k) wh[k] = wl[k] = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) shw[k] = 0.f;
+      float sh = 0.f;
+      float2 h1 = make_float2(0.f, 0.f), l1 = h1, h2 = h1, l2 = h1;
 #pragma unroll 1
       for (int c0 = 0; c0 < kN; c0 += 16) {
         float v[16];
+        uint32_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // the chunk as stored (valid lanes)
         __syncwarp();
         tmem_ld16(taddr + c0, v);
         const int col = t.nb * kN + c0;
@@ -364,7 +493,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 v[2 * i + 1] += bf16hi_to_f32(rw[i]);
               }
             }
-            uint32_t o[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) o[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
             *reinterpret_cast<uint4*>(yrow + col) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -384,6 +512,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
         }
+        if (stats) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int ch = c0 + 4 * j;  // channel within the N block (the same for the whole warp)
+            if ((ch & (cg - 1)) == 0) sh = __shfl_sync(0xffffffffu, bf16lo_to_f32(o[2 * j]), src);
+            const float2 nsh = make_float2(-sh, -sh);
+            const float2 d01 = __fadd2_rn(make_float2(bf16lo_to_f32(o[2 * j]), bf16hi_to_f32(o[2 * j])), nsh);
+            const float2 d23 = __fadd2_rn(make_float2(bf16lo_to_f32(o[2 * j + 1]), bf16hi_to_f32(o[2 * j + 1])), nsh);
+            if (valid) {
+              two_sum2(h1, l1, d01);
+              two_sum2(h1, l1, d23);
+              fast_two_sum2(h2, l2, __fmul2_rn(d01, d01));
+              fast_two_sum2(h2, l2, __fmul2_rn(d23, d23));
+            }
+            if (((ch + 4) & (cg - 1)) == 0) {  // the group ends: even + odd halves into its slot
+              float a1h = h1.x, a1l = l1.x, a2h = h2.x, a2l = l2.x;
+              ff_add(a1h, a1l, h1.y, l1.y);
+              ff_add(a2h, a2l, h2.y, l2.y);
+              const int slot = (ch >> lg) & 3;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                if (slot == k) {
+                  wh[2 * k] = a1h;
+                  wl[2 * k] = a1l;
+                  wh[2 * k + 1] = a2h;
+                  wl[2 * k + 1] = a2l;
+                  shw[k] = sh;
+                }
+              }
+              h1 = l1 = h2 = l2 = make_float2(0.f, 0.f);
+            }
+          }
+          if (((c0 + 16) & (4 * cg - 1)) == 0) {  // 4 groups complete: lane 2k (k < 4) writes group k
+            float H, L;
+            st_reduce8(wh, wl, lane, H, L);
+            const float H2 = __shfl_down_sync(0xffffffffu, H, 1), L2 = __shfl_down_sync(0xffffffffu, L, 1);
+            const int k = lane >> 1;
+            const float sk = k == 0 ? shw[0] : k == 1 ? shw[1] : k == 2 ? shw[2] : shw[3];
+            if (lane < 8 && !(lane & 1)) {
+              const size_t idx = rec0 + (size_t)(((c0 + 16) >> lg) - 4 + k) * rec_stride;
+              __stcg(args.st_rec + idx, make_float4(H, L, H2, L2));
+              __stcg(args.st_meta + idx, make_float2(sk, (float)(__popc(vmask) << lg)));
+            }
+          }
+        }
       }
       // This warp is done with the accumulator: one arrival per warp on the even CTA's barrier.
       tc_fence_before();
@@ -392,6 +565,88 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;
+      }
+    }
+  } else if (kNorm && warp >= 6) {
+    // ------------------------------------------------------------ operand prologue (both CTAs)
+    // Each tall A box of x is replaced in place by silu(x S + B) with its frame's coefficients,
+    // the arithmetic of the norm's own apply pass (so the MMAs see exactly the bf16 values it
+    // would have written). Boxes of the cache (already normalised) and rows of zero padding are
+    // left as loaded. Thread t of the 256 owns the 16-byte chunk jl = t % 8 (channels 8 jl ..
+    // 8 jl + 7 of the box's 64) of rows r0 + 32 i, r0 = t / 8, of the box's 180 rows
+    // (row = h + 10 c, c the column); the swizzle puts the chunk at jl ^ (row % 8) = jl ^ (r0 % 8).
+    constexpr int kRows = kTallRows * kBoxW;
+    const int pt = (int)threadIdx.x - 192;
+    const int jl = pt & 7, r0 = pt >> 3;
+    const uint32_t chunk_off = (uint32_t)r0 * 128 + ((uint32_t)(jl ^ (r0 & 7)) << 4);
+    const uint32_t ready0 = mapa_shared(smem_u32(&ready_a[0]), 0);
+    const float4* coef_sm = reinterpret_cast<const float4*>(smem + Cfg<kNorm>::kCoefOffset) + jl;  // blocked
+    int sa = 0;
+    uint32_t pha = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int item = item_of(args, r, cluster, nclusters);
+      if (item == -1) break;
+      if (item < 0) continue;
+      const PTile me = decode_pair(args, item, (int)rank);
+      const PTile p0 = decode_pair(args, item, 0), p1 = decode_pair(args, item, 1);
+      for (int row = 0; ok && row < rows; ++row) {
+        const int dt = row - 2;
+        if (skip_pair(args, p0, p1, dt)) continue;
+        const int tau = me.t0 + dt;
+        const bool xf = me.valid && tau >= 0;  // this box holds x
+        for (int kb = 0; kb < args.kb_per_tap; ++kb) {
+          if (!mbar_wait(&full_a[sa], pha, args.err, kDevErrTimeoutPrologue)) {
+            ok = false;
+            break;
+          }
+          if (xf) {
+            const GnCoef8 k8 = gn_coef8_blocked(coef_sm + sa * (kCoefBytes / 16));
+            uint8_t* box = smem + sa * kAStride + chunk_off;
+            // Branch-free fast formula for all chunks (their exp/reciprocal chains interleave),
+            // then the rare chunk with a z < -80 again through gn_silu8: per chunk the same
+            // choice as the norm's own pass.
+            unsigned slow = 0;
+#pragma unroll
+            for (int i = 0; i < 6; ++i) {
+              const int rr = r0 + 32 * i;
+              const int hh = me.h0 - 1 + rr % kTallRows, ww = me.w0 - 1 + rr / kTallRows;
+              if (rr < kRows && hh >= 0 && hh < args.H && ww >= 0 && ww < args.W) {
+                bool sl;
+                uint4* q = reinterpret_cast<uint4*>(box + i * 4096);
+                *q = gn_silu8_fast(*q, k8, &sl);
+                slow |= (unsigned)sl << i;
+              }
+            }
+            if (slow) {  // x of those chunks again from global memory (the box now holds results)
+              const wan_bf16* src = args.a + (size_t)kb * kBlockK + 8 * jl;
+#pragma unroll 1
+              for (int i = 0; i < 6; ++i) {
+                if ((slow >> i) & 1) {
+                  const int rr = r0 + 32 * i;
+                  const int hh = me.h0 - 1 + rr % kTallRows, ww = me.w0 - 1 + rr / kTallRows;
+                  const size_t px = (((size_t)me.n * args.T + tau) * args.H + hh) * args.W + ww;
+                  const uint4 xv = *reinterpret_cast<const uint4*>(src + px * args.Cin);
+                  *reinterpret_cast<uint4*>(box + i * 4096) = gn_silu8(xv, k8);
+                }
+              }
+            }
+            fence_proxy_async_smem();  // the MMAs read the box through the async proxy
+          }
+          __syncwarp();
+          // Hand the box to the MMA issuer in the even CTA: what it hands over is this CTA's own
+          // shared memory, complete with a release at CTA scope.
+          if (lane == 0) {
+            if (leader)
+              mbar_arrive(&ready_a[sa]);
+            else
+              mbar_arrive_remote_cta(ready0 + 8u * (uint32_t)sa);
+          }
+          if (++sa == kAStages) {
+            sa = 0;
+            pha ^= 1;
+          }
+        }
       }
     }
   }
@@ -416,13 +671,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn2() {
 
 // Activations [N, T, H, W, C] addressed as (c, h, w, t, n): H is listed before W, so a box of
 // 8 rows x 18 columns lands in shared memory column by column (row m = h + 8 w).
-bool map_act_hw(CUtensorMap* m, const void* base, int C, int W, int H, int T, int N) {
+bool map_act_hw(CUtensorMap* m, const void* base, int C, int W, int H, int T, int N, int box_h = kTileH) {
   auto fn = encode_fn2();
   if (!fn) return false;
   const cuuint64_t dims[5] = {(cuuint64_t)C, (cuuint64_t)H, (cuuint64_t)W, (cuuint64_t)T, (cuuint64_t)N};
   const cuuint64_t e = 2;
   const cuuint64_t strides[4] = {(cuuint64_t)W * C * e, C * e, (cuuint64_t)H * W * C * e, (cuuint64_t)T * H * W * C * e};
-  const cuuint32_t box[5] = {(cuuint32_t)kBlockK, (cuuint32_t)kTileH, (cuuint32_t)kBoxW, 1, 1};
+  const cuuint32_t box[5] = {(cuuint32_t)kBlockK, (cuuint32_t)box_h, (cuuint32_t)kBoxW, 1, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -441,13 +696,57 @@ bool map_w_half(CUtensorMap* m, const void* base, int K, int Cout, int P) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Persistent grid: as many CTA pairs as the GPU can hold at once (not every SM can be paired:
+// a pair lives in one GPC), so no pair waits for a second wave.
+template <bool kNorm>
+cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tc, const CUtensorMap& tw, const Conv2Args& args,
+                        int sms, cudaStream_t stream) {
+  constexpr int kSmem = Cfg<kNorm>::kSmemTotal, kThr = Cfg<kNorm>::kThreads;
+  cudaError_t e = cudaFuncSetAttribute(conv_tc2_kernel<kNorm>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  static int max_clusters[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && max_clusters[dev] == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+    cfg.blockDim = dim3(kThr, 1, 1);
+    cfg.dynamicSmemBytes = kSmem;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, conv_tc2_kernel<kNorm>, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = sms / 2;
+    }
+    max_clusters[dev] = n;
+  }
+  int clusters = (dev >= 0 && dev < 64) ? max_clusters[dev] : sms / 2;
+  if (clusters > args.items) clusters = args.items;
+  if (clusters < 1) clusters = 1;
+  conv_tc2_kernel<kNorm><<<2 * clusters, kThr, kSmem, stream>>>(ta, tc, tw, args);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool conv_pair_supported(int Cout) { return Cout >= 256; }
 
+bool conv_gn_stats_supported(int Cout, int groups) {
+  if (groups <= 0 || Cout % 256 != 0 || Cout % groups != 0) return false;
+  const int cg = Cout / groups;  // a power of two from 4 to 64: 4 groups tile a 256-channel block
+  return cg >= 4 && cg <= 64 && (cg & (cg - 1)) == 0;
+}
+
+int conv_gn_stats_parts(int H, int W) { return cdiv(H, kTileH) * cdiv(W, kTileW) * 4; }
+
+size_t conv_gn_stats_bytes(int N, int T, int H, int W, int Cout, int groups) {
+  (void)Cout;
+  return (size_t)N * T * groups * conv_gn_stats_parts(H, W) * (sizeof(float4) + sizeof(float2));
+}
+
 cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_in, const wan_bf16* w,
                              const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W,
-                             int Cin, int Cout, int sms, unsigned* err, cudaStream_t stream) {
+                             int Cin, int Cout, int sms, unsigned* err, cudaStream_t stream, void* st_buf,
+                             int st_groups, const float4* coef) {
   Conv2Args args{};
   args.N = N;
   args.T = T;
@@ -469,38 +768,29 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
   args.residual = residual;
   args.y = y;
   args.err = err;
+  if (st_buf) {
+    if (mode != 0 || !conv_gn_stats_supported(Cout, st_groups)) return cudaErrorInvalidValue;
+    args.st_rec = reinterpret_cast<float4*>(st_buf);
+    args.st_meta = reinterpret_cast<float2*>(args.st_rec + (size_t)N * T * st_groups * conv_gn_stats_parts(H, W));
+    args.st_cg = Cout / st_groups;
+    while ((1 << args.st_lg) < args.st_cg) ++args.st_lg;
+  }
   CUtensorMap ta, tc, tw;
-  if (!map_act_hw(&ta, a, Cin, W, H, T, N)) return cudaErrorInvalidValue;
+  const int box_h = coef ? kTallRows : kTileH;  // the prologue kernel loads tall boxes
+  if (!map_act_hw(&ta, a, Cin, W, H, T, N, box_h)) return cudaErrorInvalidValue;
   if (cache_in) {
-    if (!map_act_hw(&tc, cache_in, Cin, W, H, 2, N)) return cudaErrorInvalidValue;
+    if (!map_act_hw(&tc, cache_in, Cin, W, H, 2, N, box_h)) return cudaErrorInvalidValue;
   } else {
     tc = ta;
   }
   if (!map_w_half(&tw, w, (mode == 0 ? 27 : 4) * Cin, Cout, args.phases)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(conv_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
-  if (e != cudaSuccess) return e;
-  // Persistent grid: as many CTA pairs as the GPU can hold at once (not every SM can be paired:
-  // a pair lives in one GPC), so no pair waits for a second wave.
-  static int max_clusters[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && max_clusters[dev] == 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemTotal;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, conv_tc2_kernel, &cfg) != cudaSuccess || n <= 0) {
-      cudaGetLastError();
-      n = sms / 2;
-    }
-    max_clusters[dev] = n;
+  if (coef) {
+    if (mode != 0) return cudaErrorInvalidValue;
+    args.coef = coef;
+    args.a = a;
+    return launch_pair<true>(ta, tc, tw, args, sms, stream);
   }
-  int clusters = (dev >= 0 && dev < 64) ? max_clusters[dev] : sms / 2;
-  if (clusters > args.items) clusters = args.items;
-  if (clusters < 1) clusters = 1;
-  conv_tc2_kernel<<<2 * clusters, kThreads, kSmemTotal, stream>>>(ta, tc, tw, args);
-  return cudaGetLastError();
+  return launch_pair<false>(ta, tc, tw, args, sms, stream);
 }
 
 }  // namespace wan

@@ -34,6 +34,8 @@
 // Statistics depend only on the frame (the span partition depends on H, W and C alone), so a
 // frame gets the same bits whether the video comes in one call or in chunks.
 #include <cuda_runtime.h>
+
+#include <algorithm>
 #include <math.h>
 #include <stdint.h>
 
@@ -50,82 +52,12 @@ struct GnPartial {  // one (frame, span, group): float-float sums of d and d^2
   float s1_hi, s1_lo, s2_hi, s2_lo;
 };
 
-// a - b on float2 in one packed instruction: b * (-1) + a with one rounding equals the rounded
-// difference (there is no packed subtract).
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) { return __ffma2_rn(b, make_float2(-1.f, -1.f), a); }
-
-// Knuth TwoSum: s + e == a + b exactly (round-to-nearest, no overflow). Packed on float2.
-__device__ __forceinline__ void two_sum2(float2& hi, float2& lo, float2 x) {
-  const float2 s = __fadd2_rn(hi, x);
-  const float2 bb = sub2(s, hi);
-  const float2 e1 = sub2(hi, sub2(s, bb));  // hi - (s - bb)
-  const float2 e2 = sub2(x, bb);            // x - bb
-  lo = __fadd2_rn(lo, __fadd2_rn(e1, e2));
-  hi = s;
-}
-
-// Dekker Fast2Sum for non-negative running sums: exact when hi >= x, and otherwise off by at
-// most the rounding of the smaller (earlier) partial sum.
-__device__ __forceinline__ void fast_two_sum2(float2& hi, float2& lo, float2 x) {
-  const float2 s = __fadd2_rn(hi, x);
-  lo = __fadd2_rn(lo, sub2(x, sub2(s, hi)));
-  hi = s;
-}
-
-// Float-float addition (hi, lo) += (bhi, blo), result renormalised.
-__device__ __forceinline__ void ff_add(float& hi, float& lo, float bhi, float blo) {
-  const float s = __fadd_rn(hi, bhi);
-  const float bb = __fsub_rn(s, hi);
-  const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(bhi, bb));
-  const float t = __fadd_rn(e, __fadd_rn(lo, blo));
-  hi = __fadd_rn(s, t);
-  lo = __fsub_rn(t, __fsub_rn(hi, s));
-}
-
 __device__ __forceinline__ void stg_v4(void* p, uint4 v) {
   asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                : "memory");
 }
 
-__device__ __forceinline__ float2 unpack2(uint32_t w) {
-  return make_float2(bf16lo_to_f32(w), bf16hi_to_f32(w));
-}
-
 __device__ __forceinline__ float bf16_at(const wan_bf16* p) { return __uint_as_float(((uint32_t)*p) << 16); }
-
-__device__ __forceinline__ float ex2_approx(float x) {  // subnormal results kept
-  float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float ex2_approx_ftz(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ float rcp_approx_ftz(float x) {  // used on [1, 5.6e34]
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// SiLU of two values for z >= -80: z / (1 + e^-z), with e^-z = 2^(-z log2 e) <= 2^116 (no overflow;
-// it underflows to 0 for large z, where the result is z) and 1 + e^-z <= 5.6e34, whose reciprocal
-// is a normal fp32 number (no flush). For z << 0, 1 + e^-z rounds to e^-z and the quotient to
-// z e^z with fp32 relative precision.
-__device__ __forceinline__ float2 silu2_fast(float2 z) {
-  const float2 m = __fmul2_rn(z, make_float2(-1.4426950408889634f, -1.4426950408889634f));
-  const float2 u = __fadd2_rn(make_float2(ex2_approx_ftz(m.x), ex2_approx_ftz(m.y)), make_float2(1.f, 1.f));
-  return __fmul2_rn(z, make_float2(rcp_approx_ftz(u.x), rcp_approx_ftz(u.y)));
-}
-
-// z * sigmoid(z): t = e^-|z| (never overflows), sigmoid = 1/(1+t) or t/(1+t). Used for vectors
-// holding a z < -80, whose result may be subnormal.
-__device__ __forceinline__ float silu_exact_range(float z) {
-  const float t = ex2_approx(fminf(z, -z) * 1.4426950408889634f);
-  const float r = rcp_approx_ftz(1.0f + t);
-  return z < 0.f ? (z * t) * r : z * r;
-}
 
 // Grid-wide barrier for a cooperative launch (all CTAs co-resident). `ctr` counts arrivals
 // over the whole call (cleared before the launch); barrier k waits for k * gridDim.x arrivals.
@@ -173,6 +105,16 @@ struct GnArgs {
   int P, C, G, F, piece_px, spans, items;
   float eps;
   double inv_len;   // 1 / (H * W * C / G)
+  // Statistics produced elsewhere (null: phase A computes them): per (frame, group, part q < ext_q)
+  // ext_rec = float-float (sum d, sum d^2) of d = x - s around the part's own shift s and
+  // ext_meta = (s, count); part 0 has count > 0.
+  const float4* ext_rec;
+  const float2* ext_meta;
+  int ext_q;
+  int apply;  // 0: stop after the coefficients (phase B), the caller applies them elsewhere
+  // 1: coefficients in the blocked layout (coef_blocked_index), for readers that take 8
+  // consecutive channels per thread with 8 threads side by side (apply == 0 only).
+  int coef_blocked;
 };
 
 // Pixel range [q0, q1) of piece j of statistics item `item` (empty past the end of a frame).
@@ -205,8 +147,9 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
 
   // The CTA's stream of pieces: its statistics items (item = blockIdx + k * grid), kPiecesPerSpan
   // pieces each; piece n is piece n % kPiecesPerSpan of the (n / kPiecesPerSpan)-th item.
+  const int cnt_a = a.ext_rec ? 0 : cnt;  // statistics items (none when they come with x)
   auto issue = [&](int n) {  // thread 0: start loading piece n of the stream
-    if (n >= cnt * kPiecesPerSpan) return;
+    if (n >= cnt_a * kPiecesPerSpan) return;
     const int k = n / kPiecesPerSpan, jj = n - k * kPiecesPerSpan;
     uint64_t* bar = &full[n % kSlots];
     int f, q0, q1;
@@ -233,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
   };
 
   // ---------------------------------------------------------------- A: statistics
-  for (int k = 0; k < cnt; ++k) {
+  for (int k = 0; k < cnt_a; ++k) {
     const int item = blockIdx.x + k * gridDim.x;
     const int f = item / a.spans, span = item - f * a.spans;
     // The group shifts (each group's first value in the frame), loaded once per CTA: a
@@ -323,21 +266,57 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
       // Float-float sums (fp64 issue is scarce on this GPU): lane-strided, then a butterfly.
       // The float-float add is commutative bit for bit (TwoSum's error term is unique), so every
       // lane ends with the same bits.
-      // A lane adds spans lane, lane + 32, ... in order, loading kFinBatch of them at a time.
+      // A lane adds items lane, lane + 32, ... in order, loading kFinBatch of them at a time.
       float h1 = 0.f, l1 = 0.f, h2 = 0.f, l2 = 0.f;
-      const float4* src = reinterpret_cast<const float4*>(a.part) + ((size_t)f * a.G + g) * a.spans;
-      for (int sp0 = 0; sp0 < a.spans; sp0 += 32 * kFinBatch) {
-        float4 q[kFinBatch];
+      double shift;
+      if (a.ext_rec) {
+        // Parts with their own shifts s_q, moved exactly to the first part's shift s, all in
+        // float-float (dl = s_q - s by TwoSum, n dl by an FMA product error):
+        //   sum (x - s) = S1_q + n dl,  sum (x - s)^2 = S2_q + dl (2 S1_q + n dl).
+        const float4* ep = a.ext_rec + ((size_t)f * a.G + g) * a.ext_q;
+        const float2* em = a.ext_meta + ((size_t)f * a.G + g) * a.ext_q;
+        const float s = __ldcg(em).x;
+        for (int q0 = 0; q0 < a.ext_q; q0 += 32 * kFinBatch) {
+          float4 r[kFinBatch];
+          float2 m[kFinBatch];
 #pragma unroll
-        for (int i = 0; i < kFinBatch; ++i) {
-          const int sp = sp0 + lane + 32 * i;
-          q[i] = sp < a.spans ? __ldcg(src + sp) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+          for (int i = 0; i < kFinBatch; ++i) {
+            const int q = q0 + lane + 32 * i;
+            r[i] = q < a.ext_q ? __ldcg(ep + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+            m[i] = q < a.ext_q ? __ldcg(em + q) : make_float2(s, 0.f);
+          }
 #pragma unroll
-        for (int i = 0; i < kFinBatch; ++i) {  // adding (0, 0) to a normalised pair changes nothing
-          ff_add(h1, l1, q[i].x, q[i].y);
-          ff_add(h2, l2, q[i].z, q[i].w);
+          for (int i = 0; i < kFinBatch; ++i) {
+            float dh = m[i].x, dlo = 0.f;
+            ff_add(dh, dlo, -s, 0.f);  // s_q - s exactly
+            const float n = m[i].y;
+            const float ph = n * dh, pl = fmaf(n, dh, -ph) + n * dlo;  // n dl (n < 2^24)
+            ff_add(h1, l1, r[i].x, r[i].y);
+            ff_add(h1, l1, ph, pl);
+            float uh = 2.f * r[i].x, ul = 2.f * r[i].y;  // 2 S1_q + n dl
+            ff_add(uh, ul, ph, pl);
+            const float vh = dh * uh, vl = fmaf(dh, uh, -vh) + fmaf(dh, ul, dlo * uh);
+            ff_add(h2, l2, r[i].z, r[i].w);
+            ff_add(h2, l2, vh, vl);
+          }
         }
+        shift = (double)s;
+      } else {
+        const float4* src = reinterpret_cast<const float4*>(a.part) + ((size_t)f * a.G + g) * a.spans;
+        for (int sp0 = 0; sp0 < a.spans; sp0 += 32 * kFinBatch) {
+          float4 q[kFinBatch];
+#pragma unroll
+          for (int i = 0; i < kFinBatch; ++i) {
+            const int sp = sp0 + lane + 32 * i;
+            q[i] = sp < a.spans ? __ldcg(src + sp) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int i = 0; i < kFinBatch; ++i) {  // adding (0, 0) to a normalised pair changes nothing
+            ff_add(h1, l1, q[i].x, q[i].y);
+            ff_add(h2, l2, q[i].z, q[i].w);
+          }
+        }
+        shift = (double)bf16_at(a.x + (size_t)f * a.P * a.C + (size_t)g * cg);
       }
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -346,12 +325,13 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
         ff_add(h1, l1, oh1, ol1);
         ff_add(h2, l2, oh2, ol2);
       }
-      const double s1 = (double)h1 + (double)l1, s2 = (double)h2 + (double)l2;
+      const double s1 = (double)h1 + (double)l1;
+      const double s2 = (double)h2 + (double)l2;
       // fp64 division and square root are slow on this GPU: 1/L comes from the host and
       // 1/sqrt(v) is an fp32 estimate refined by two Newton steps r <- r (3 - v r^2) / 2 in fp64
       // (relative error 2^-22 -> 2^-44 -> below fp64 rounding).
       const double m1 = s1 * a.inv_len;
-      const double mean = (double)bf16_at(a.x + (size_t)f * a.P * a.C + (size_t)g * cg) + m1;
+      const double mean = shift + m1;
       const double v = fmax(s2 * a.inv_len - m1 * m1, 0.0) + (double)a.eps;
       double rstd;
       if (v > 1e-30 && v < 1e30) {
@@ -366,10 +346,12 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
         const double S = (double)a.gamma[c] * rstd;
         const double B = (double)a.beta[c] - mean * S;
         const float shi = (float)S, bhi = (float)B;
-        a.coef[(size_t)f * a.C + c] = make_float4(shi, (float)(S - (double)shi), bhi, (float)(B - (double)bhi));
+        a.coef[(size_t)f * a.C + (a.coef_blocked ? coef_blocked_index(c) : c)] =
+            make_float4(shi, (float)(S - (double)shi), bhi, (float)(B - (double)bhi));
       }
     }
   }
+  if (!a.apply) return;  // coefficients only
   if (!grid_barrier(a.bar, 2 * gridDim.x, a.err, &s_flag)) return;
 
   // ---------------------------------------------------------------- C: apply, newest spans first
@@ -382,7 +364,7 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
   __syncthreads();
   int fcur = -1;
   uint32_t cphase = 0;
-  float2 shi[4], slo[4], bhi[4], blo[4];
+  GnCoef8 k8;
   for (int k = 0; k < cnt; ++k) {
     const int item = a.items - 1 - (int)(blockIdx.x + k * gridDim.x);  // newest spans first
     const int f = item / a.spans;
@@ -399,15 +381,7 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
       cphase ^= 1;
       if (__syncthreads_or(!okc)) return;
       fcur = f;
-      const float4* cf = s_coef + 8 * j;
-#pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const float4 u = cf[2 * w], v = cf[2 * w + 1];
-        shi[w] = make_float2(u.x, v.x);
-        slo[w] = make_float2(u.y, v.y);
-        bhi[w] = make_float2(u.z, v.z);
-        blo[w] = make_float2(u.w, v.w);
-      }
+      k8 = gn_coef8(s_coef + 8 * j);
     }
     // x comes back from L2 (phase A read it from HBM moments ago) with plain 16-byte loads,
     // kApplyUnroll in flight per thread, and no CTA-wide synchronisation.
@@ -428,27 +402,44 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
         for (int u = 0; u < kApplyUnroll; ++u) {
           const int pp = p + u * ppi;
           if (pp >= q1) break;
-          uint32_t wv[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-          float2 z[4];
-          float zmin = 0.f;
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const float2 xv = unpack2(wv[w]);
-            z[w] = __fadd2_rn(__ffma2_rn(xv, shi[w], bhi[w]), __ffma2_rn(xv, slo[w], blo[w]));
-            zmin = fminf(zmin, fminf(z[w].x, z[w].y));
-          }
-          if (zmin >= -80.f) {
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              const float2 o = silu2_fast(z[w]);
-              wv[w] = pack_bf16x2(o.x, o.y);
-            }
-          } else {
-#pragma unroll
-            for (int w = 0; w < 4; ++w) wv[w] = pack_bf16x2(silu_exact_range(z[w].x), silu_exact_range(z[w].y));
-          }
-          stg_v4(dst + (size_t)pp * vpp * 16, make_uint4(wv[0], wv[1], wv[2], wv[3]));
+          stg_v4(dst + (size_t)pp * vpp * 16, gn_silu8(v[u], k8));
         }
+      }
+    }
+  }
+}
+
+// The apply pass alone, on frames [t_lo, T) of every n, with the coefficients a coefficients-only
+// call left in `coef` ([N*T][C], blocked layout): y[n, o + t - t_lo] (y has To frames per n)
+// = silu(x[n, t] S + B). Items are (frame, run of px_per_item pixels); a thread owns one
+// 16-byte channel vector and walks the run's pixels with kApplyUnroll loads in flight.
+__global__ void __launch_bounds__(kThreads) gn_apply_frames_kernel(const wan_bf16* __restrict__ x,
+                                                                   const float4* __restrict__ coef,
+                                                                   wan_bf16* __restrict__ y, int T, int t_lo,
+                                                                   int To, int o, int P, int C, int px_per_item,
+                                                                   int items_per_frame, int items) {
+  const int vpp = C >> 3, ppi = blockDim.x / vpp;
+  const int j = threadIdx.x % vpp, lp = threadIdx.x / vpp;
+  if (lp >= ppi) return;
+  const int nt = T - t_lo;
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    const int fi = item / items_per_frame, n = fi / nt, t = t_lo + fi % nt;
+    const int q0 = (item - fi * items_per_frame) * px_per_item, q1 = min(P, q0 + px_per_item);
+    const GnCoef8 k8 = gn_coef8_blocked(coef + (size_t)(n * T + t) * C + 8 * (j & ~7) + (j & 7));
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(n * T + t) * P * C) + j;
+    char* dst = reinterpret_cast<char*>(y + (size_t)(n * To + o + t - t_lo) * P * C) + (size_t)j * 16;
+    for (int p = q0 + lp; p < q1; p += ppi * kApplyUnroll) {
+      uint4 v[kApplyUnroll];
+#pragma unroll
+      for (int u = 0; u < kApplyUnroll; ++u) {
+        const int pp = p + u * ppi;
+        v[u] = pp < q1 ? __ldg(src + (size_t)pp * vpp) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < kApplyUnroll; ++u) {
+        const int pp = p + u * ppi;
+        if (pp >= q1) break;
+        stg_v4(dst + (size_t)pp * vpp * 16, gn_silu8(v[u], k8));
       }
     }
   }
@@ -498,9 +489,28 @@ bool gn_silu_supported(int C, int G) {
   return (cg % 8 == 0) || (8 % cg == 0);
 }
 
+const float4* gn_silu_coef(const void* ws, int N, int T, int H, int W, int C, int G) {
+  const GnPlan pl = plan(N, T, H, W, C, G);
+  return reinterpret_cast<const float4*>(reinterpret_cast<const char*>(ws) + align256(pl.part_bytes));
+}
+
+cudaError_t gn_apply_frames_launch(const wan_bf16* x, const float4* coef, wan_bf16* y, int N, int T, int H, int W,
+                                   int C, int t_lo, int To, int o, int sms, cudaStream_t stream) {
+  if (t_lo < 0 || t_lo >= T || o < 0 || o + (T - t_lo) > To || C % 8 != 0 || C > 2048) return cudaErrorInvalidValue;
+  const int P = H * W, vpp = C / 8, threads = (kThreads / vpp) * vpp;
+  const int px_per_item = max(1, 65536 / (C * 2));  // about 64 KB of x per item
+  const int items_per_frame = cdiv(P, px_per_item);
+  const long long items = (long long)N * (T - t_lo) * items_per_frame;
+  if (items >= (1LL << 31)) return cudaErrorInvalidValue;
+  const int grid = (int)std::min<long long>(items, (long long)sms * 8);
+  gn_apply_frames_kernel<<<grid, threads, 0, stream>>>(x, coef, y, T, t_lo, To, o, P, C, px_per_item,
+                                                       items_per_frame, (int)items);
+  return cudaGetLastError();
+}
+
 cudaError_t gn_silu_launch(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta,
                            int N, int T, int H, int W, int C, int G, float eps, void* ws, int sms,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, const void* st_buf, int st_q, bool apply, float4* coef_out) {
   const GnPlan pl = plan(N, T, H, W, C, G);
   char* base = reinterpret_cast<char*>(ws);
   GnArgs a;
@@ -509,7 +519,7 @@ cudaError_t gn_silu_launch(const wan_bf16* x, wan_bf16* y, const float* gamma, c
   a.gamma = gamma;
   a.beta = beta;
   a.part = reinterpret_cast<GnPartial*>(base);
-  a.coef = reinterpret_cast<float4*>(base + align256(pl.part_bytes));
+  a.coef = coef_out ? coef_out : reinterpret_cast<float4*>(base + align256(pl.part_bytes));
   a.bar = reinterpret_cast<unsigned*>(base + align256(pl.part_bytes) + align256(pl.coef_bytes));
   a.err = device_error_word();
   if (!a.err) return cudaErrorInvalidValue;
@@ -522,6 +532,11 @@ cudaError_t gn_silu_launch(const wan_bf16* x, wan_bf16* y, const float* gamma, c
   a.items = pl.items;
   a.eps = eps;
   a.inv_len = 1.0 / ((double)pl.P * (C / G));
+  a.ext_rec = reinterpret_cast<const float4*>(st_buf);
+  a.ext_meta = st_buf ? reinterpret_cast<const float2*>(a.ext_rec + (size_t)pl.F * G * st_q) : nullptr;
+  a.ext_q = st_q;
+  a.apply = apply ? 1 : 0;
+  a.coef_blocked = (!apply && C % 64 == 0) ? 1 : 0;
   // Persistent grid: every CTA resident at once (the cooperative launch checks it).
   cudaError_t e = cudaFuncSetAttribute(gn_silu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   if (e != cudaSuccess) return e;
