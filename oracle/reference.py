@@ -19,7 +19,8 @@ __all__ = [
     "round_to_bf16", "bf16_to_f64", "bf16_to_f32", "ulp_distance_bf16",
     "silu_f64", "gn_silu_f64", "gn_silu",
     "causal_conv3d_f64", "causal_conv3d", "conv_at_points_f64",
-    "resblock",
+    "resblock", "conv1x1", "fold_bias", "resblock_shortcut",
+    "time_upsample_f64", "time_upsample",
     "phase_tap_sources", "phase_weights", "phase_weights_f64",
     "phase_conv_f64", "phase_conv", "upsample_nearest_conv_f64", "upsample_nearest_conv",
 ]
@@ -185,6 +186,85 @@ def resblock(x_bits, p: dict, groups: int, eps: float, cache1=None, cache2=None)
     a2 = gn_silu(h, p["gamma2"], p["beta2"], groups, eps)
     out, c2 = causal_conv3d(a2, p["w2"], p["b2"], x_bits, cache2)
     return out, c1, c2
+
+
+# ----------------------------------------------------------------------------------------------
+# Channel-changing ResBlock: the 1x1x1 shortcut with its bias folded into conv2's bias
+# (binding.cpp, `prepare()`: the shortcut bias folded into the second conv's bias;
+# `Decoder::resnet`: skip = conv(x, shortcut) without bias when the block changes channels)
+# ----------------------------------------------------------------------------------------------
+
+def conv1x1(x_bits, w_bits) -> np.ndarray:
+    """skip[n,t,h,w,co] = sum_ci w[co,ci] x[n,t,h,w,ci], rounded once (the shortcut carries no
+    bias of its own: it is folded into the second conv's)."""
+    x = bf16_to_f64(x_bits)
+    w = bf16_to_f64(w_bits)
+    return round_to_bf16(x @ w.T)
+
+
+def fold_bias(b2_bits, bsc_bits) -> np.ndarray:
+    """b2 + b_shortcut, one bf16 rounding of the sum (prepare-time)."""
+    return round_to_bf16(bf16_to_f64(b2_bits) + bf16_to_f64(bsc_bits))
+
+
+def resblock_shortcut(x_bits, p: dict, w_sc, b_sc, groups: int, eps: float, cache1=None, cache2=None):
+    """out = conv2(silu(gn2(h))) + b2' + skip with h = conv1(silu(gn1(x))) (Cin -> Cout),
+    skip = conv1x1(x, w_sc) and b2' = fold_bias(b2, b_sc): the output is one rounding of
+    acc2 + b2' + skip. Returns (out, cache1_out, cache2_out)."""
+    a1 = gn_silu(x_bits, p["gamma1"], p["beta1"], groups, eps)
+    h, c1 = causal_conv3d(a1, p["w1"], p["b1"], None, cache1)
+    a2 = gn_silu(h, p["gamma2"], p["beta2"], groups, eps)
+    skip = conv1x1(x_bits, w_sc)
+    out, c2 = causal_conv3d(a2, p["w2"], fold_bias(p["b2"], b_sc), skip, cache2)
+    return out, c1, c2
+
+
+# ----------------------------------------------------------------------------------------------
+# Causal 3x1x1 time upsample with frame-interleaved output (binding.cpp, `Decoder::up`: the
+# frames after the first of the first chunk are padded in front with the cache (norm_pad's
+# copy-only mode), the cache keeps the last two padded frames (`last_frames`), and
+# time_upsample writes the x2 frames interleaved)
+# ----------------------------------------------------------------------------------------------
+
+def time_upsample_f64(x, w, bias=None, cache=None, first: bool = False) -> np.ndarray:
+    """x [N, T, H, W, C], w [2C, 3, C] (kt, Cin), bias [2C]. With start = 1 if `first` (the
+    first frame of the first chunk passes through) else 0, a = x[:, start:] (nf frames) and
+    P = [cache (2 frames, zeros if absent); a]:
+        z[n, t] = bias + sum_kt w[:, kt, :] . P[n, t + kt]      (2C channels, t < nf)
+    and output frame start + 2t + i holds channels [i C, (i + 1) C) of z[n, t] (i = 0, 1).
+    Returns out [N, start + 2 nf, H, W, C] in fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    N, T, H, W, C = x.shape
+    start = 1 if first else 0
+    nf = T - start
+    cache = np.zeros((N, 2, H, W, C)) if cache is None else np.asarray(cache, dtype=np.float64)
+    P = np.concatenate([cache, x[:, start:]], axis=1)
+    z = np.zeros((N, nf, H, W, 2 * C))
+    for kt in range(3):
+        z += P[:, kt:kt + nf] @ w[:, kt, :].T
+    if bias is not None:
+        z += np.asarray(bias, dtype=np.float64)
+    out = np.zeros((N, start + 2 * nf, H, W, C))
+    if first:
+        out[:, 0] = x[:, 0]
+    out[:, start::2] = z[..., :C]
+    out[:, start + 1::2] = z[..., C:]
+    return out
+
+
+def time_upsample(x_bits, w_bits, bias_bits=None, cache_bits=None, first: bool = False):
+    """bf16 time upsample: returns (out bits, rounded once; the passed-through frame is a copy,
+    cache_out bits = the last two frames of P, copies)."""
+    x_bits = np.asarray(x_bits, dtype=np.uint16)
+    out = time_upsample_f64(bf16_to_f64(x_bits), bf16_to_f64(w_bits),
+                            None if bias_bits is None else bf16_to_f64(bias_bits),
+                            None if cache_bits is None else bf16_to_f64(cache_bits), first)
+    N, T, H, W, C = x_bits.shape
+    start = 1 if first else 0
+    prev = np.zeros((N, 2, H, W, C), np.uint16) if cache_bits is None else np.asarray(cache_bits, np.uint16)
+    cache_out = np.concatenate([prev, x_bits[:, start:]], axis=1)[:, -2:]
+    return round_to_bf16(out), np.ascontiguousarray(cache_out)
 
 
 # ----------------------------------------------------------------------------------------------
