@@ -290,6 +290,69 @@ def job_tflops(flops_per_rank_step, world, ms_per_step):
     return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
 
 
+def time_adjacent(dev, reps=10):
+    """The decoder steps next to the ResBlock, timed on their own (outside the step): the causal
+    3x1x1 time upsample of the widest stage [1,4,44,78,1024] -> [1,8,44,78,1024] with history,
+    and a channel-changing ResBlock 512 -> 256 at [1,4,176,312,512] (1x1x1 shortcut, folded bias).
+    CUDA events around each call, an L2 flush (256 MB written) before each, 3 warm-up calls."""
+    import numpy as np
+    import torch
+    from video_vae_decoder_gb300 import binding as wan, synth
+    bf = torch.bfloat16
+
+    def n(shape, name, mean=0.0, std=1.0, dtype=bf):
+        return synth.normal_torch(shape, 0, name, mean, std, device=dev, dtype=dtype)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ms = []
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        return statistics.mean(ms)
+    out = {}
+    C = 1024
+    x = n((1, 4, 44, 78, C), "bench/tup/x")
+    w = n((2 * C, 3, C), "bench/tup/w", 0.0, float(np.sqrt(1.0 / (3 * C))))
+    b = n((2 * C,), "bench/tup/b", 0.0, 0.01)
+    cache = n((1, 2, 44, 78, C), "bench/tup/c")
+    y = torch.empty((1, 8, 44, 78, C), dtype=bf, device=dev)
+    ms = timed(lambda: wan.wan_time_upsample(x, w, b, False, cache, None, y))
+    fl = 2.0 * 4 * 44 * 78 * 3 * C * 2 * C
+    out["time_upsample_c1024"] = {"ms": ms, "tflops": fl / ms / 1e9, "shape": "[1,4,44,78,1024] -> [1,8,44,78,1024]"}
+    del x, w, b, cache, y
+    Cin, Cout = 512, 256
+    x = n((1, 4, 176, 312, Cin), "bench/rbsc/x")
+    p = {"gamma1": n((Cin,), "bench/rbsc/g1", 1.0, 0.1, torch.float32),
+         "beta1": n((Cin,), "bench/rbsc/be1", 0.0, 0.1, torch.float32),
+         "w1": n((Cout, 3, 3, 3, Cin), "bench/rbsc/w1", 0.0, float(np.sqrt(1.0 / (27 * Cin)))),
+         "b1": n((Cout,), "bench/rbsc/b1", 0.0, 0.01),
+         "gamma2": n((Cout,), "bench/rbsc/g2", 1.0, 0.1, torch.float32),
+         "beta2": n((Cout,), "bench/rbsc/be2", 0.0, 0.1, torch.float32),
+         "w2": n((Cout, 3, 3, 3, Cout), "bench/rbsc/w2", 0.0, float(np.sqrt(1.0 / (27 * Cout))))}
+    p["b2"] = wan.wan_fold_bias(n((Cout,), "bench/rbsc/b2", 0.0, 0.01), n((Cout,), "bench/rbsc/bsc", 0.0, 0.01))
+    w_sc = n((Cout, Cin), "bench/rbsc/wsc", 0.0, float(np.sqrt(1.0 / Cin)))
+    c1 = torch.zeros((1, 2, 176, 312, Cin), dtype=bf, device=dev)
+    c2 = torch.zeros((1, 2, 176, 312, Cout), dtype=bf, device=dev)
+    o = torch.empty((1, 4, 176, 312, Cout), dtype=bf, device=dev)
+    ws = torch.empty(wan.wan_workspace_size(wan.WAN_OP_RESBLOCK_SHORTCUT, 1, 4, 176, 312, Cin, Cout, GROUPS),
+                     dtype=torch.uint8, device=dev)
+    ms = timed(lambda: wan.wan_resblock_shortcut(x, p, w_sc, c1, c2, True, GROUPS, EPS, o, ws))
+    px = 4 * 176 * 312
+    fl = 2.0 * px * (27 * Cin * Cout + 27 * Cout * Cout + Cin * Cout)
+    out["resblock_shortcut_512_to_256"] = {"ms": ms, "tflops": fl / ms / 1e9, "shape": "[1,4,176,312,512] -> 256"}
+    assert wan.wan_device_status() == 0
+    return out
+
+
 def run_ours(args, rank, world, dev):
     import torch
     from video_vae_decoder_gb300 import binding as wan
@@ -418,6 +481,8 @@ def run_ours(args, rank, world, dev):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kernels": kernels, "wall_s_timed": wall, "clocks": clocks, "gpu_launches": launches, "roofline": roof,
     }
+    if args.case == "all" and not args.no_adjacent:
+        out["adjacent_steps"] = time_adjacent(dev)
     if not args.no_e2e and args.case == "all":
         out["e2e"] = run_e2e(args, wl, dev, flops)
     return out
@@ -543,6 +608,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-adjacent", action="store_true", help="skip timing the steps next to the ResBlock")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--head-frames", type=int, default=16,
                     help="frames of the head's input (smaller values make a case small enough for ncu --set full)")

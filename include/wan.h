@@ -56,7 +56,8 @@ typedef enum wan_op {
   WAN_OP_RESBLOCK = 2,
   WAN_OP_UPSAMPLE_PHASE_CONV = 3,
   WAN_OP_GN_STATS = 4,           /* statistics buffer of wan_causal_conv3d_gn_stats (Cout, groups) */
-  WAN_OP_GN_SILU_CONV3D = 5      /* wan_gn_silu_causal_conv3d (Cin, Cout, groups) */
+  WAN_OP_GN_SILU_CONV3D = 5,     /* wan_gn_silu_causal_conv3d (Cin, Cout, groups) */
+  WAN_OP_RESBLOCK_SHORTCUT = 6   /* wan_resblock_shortcut (Cin, Cout, groups) */
 } wan_op;
 
 /* Human-readable name of a status (static storage, never NULL). */
@@ -325,6 +326,53 @@ wan_status wan_resblock(const wan_bf16* x, wan_bf16* out, const wan_resblock_par
                         wan_bf16* cache1, wan_bf16* cache2, int cache_valid,
                         int N, int T, int H, int W, int C, void* ws, size_t ws_bytes,
                         void* stream);
+
+/*
+ * The decoder steps next to the ResBlock (binding.cpp, `Decoder::up` and `Decoder::resnet`).
+ *
+ * wan_time_upsample: the causal 3x1x1 time convolution that doubles the frame rate, written
+ * frame-interleaved. With start = 1 when `first` (the first chunk of a video: its first frame
+ * passes through unchanged and is no part of the time conv's history) and 0 otherwise, the
+ * frames x[:, start:] are padded in front with the two history frames (cache_in, zeros if NULL)
+ * and convolved over time to 2C channels:
+ *     z[n, t] = bias + sum_kt w[:, kt, :] . [history; x[:, start:]][n, t + kt]
+ * and output frame start + 2t + i holds channels [iC, (i + 1)C) of z[n, t] (i = 0, 1).
+ * Source: `Decoder::up` (the narrow to frames start.., norm_pad's copy-only padding with the
+ * cache, last_frames, time_upsample writing the x2 frames interleaved); the channel-half order is
+ * the plainest reading of "frame-interleaved", as no source of time_upsample is on the pages.
+ *   x          [N, T, H, W, C] bf16, C % 256 == 0.
+ *   w, bias    [2C, 3, C] (taps kt = 0..2 meet frames t-2..t) and [2C] (or NULL), bf16.
+ *   y          [N, start + 2 (T - start), H, W, C] bf16.
+ *   cache_in   NULL or [N, 2, H, W, C]; cache_out NULL or the same shape (may equal cache_in):
+ *              the last two frames of [cache_in or zeros; x[:, start:]].
+ *
+ * wan_conv1x1: y = x . w^T per pixel (w [Cout, Cin] bf16, no bias), rounded once: the 1x1x1
+ * shortcut of a channel-changing block. Cin % 64 == 0, Cout >= 256 and even.
+ *
+ * wan_fold_bias: out = b2 + b_shortcut (C values, bf16), rounded once: the shortcut's bias folded
+ * into the block's second conv at prepare time (binding.cpp, prepare()), so the shortcut tensor
+ * needs no bias pass of its own.
+ *
+ * wan_resblock_shortcut: the ResBlock whose output has Cout != Cin channels:
+ *     h = conv1(silu(gn1(x)); cache1) + b1                       (Cin -> Cout)
+ *     out = conv2(silu(gn2(h)); cache2) + p->b2 + conv1x1(x, w_sc)  (one rounding)
+ * with p->b2 already folded (wan_fold_bias(b2, b_shortcut)). gamma1/beta1 have Cin values,
+ * gamma2/beta2 Cout; w1 [Cout, 3, 3, 3, Cin], w2 [Cout, 3, 3, 3, Cout]; cache1 [N, 2, H, W, Cin],
+ * cache2 [N, 2, H, W, Cout]. Cout >= 256. ws >= wan_workspace_size(WAN_OP_RESBLOCK_SHORTCUT, N,
+ * T, H, W, Cin, Cout, groups). Source: `Decoder::resnet` (change = true: skip = conv(x,
+ * shortcut) without bias).
+ */
+wan_status wan_time_upsample(const wan_bf16* x, const wan_bf16* cache_in, wan_bf16* cache_out,
+                             const wan_bf16* w, const wan_bf16* bias, wan_bf16* y, int N, int T,
+                             int H, int W, int C, int first, void* stream);
+wan_status wan_conv1x1(const wan_bf16* x, const wan_bf16* w, wan_bf16* y, int N, int T, int H, int W,
+                       int Cin, int Cout, void* stream);
+wan_status wan_fold_bias(const wan_bf16* b2, const wan_bf16* b_shortcut, wan_bf16* out, int C,
+                         void* stream);
+wan_status wan_resblock_shortcut(const wan_bf16* x, wan_bf16* out, const wan_resblock_params* p,
+                                 const wan_bf16* w_sc, wan_bf16* cache1, wan_bf16* cache2,
+                                 int cache_valid, int N, int T, int H, int W, int Cin, int Cout,
+                                 void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the library's device error word on the

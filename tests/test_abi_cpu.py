@@ -166,6 +166,27 @@ def test_gn_silu_steps_reject_invalid(L):
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers are only passed where no GPU exists")
+def test_adjacent_steps_reject_invalid(L):
+    tu = L.wan_time_upsample
+    assert tu(None, None, None, A * 5, None, A * 9, 1, 2, 8, 16, 256, 1, None) == 1     # no input
+    assert tu(A, None, None, A * 5, None, A * 9, 1, 2, 8, 16, 128, 1, None) == 2       # C % 256 != 0
+    assert tu(A, None, None, MIS, None, A * 9, 1, 2, 8, 16, 256, 1, None) == 3         # misaligned weights
+    assert tu(A, None, None, A * 5, None, A + 4096, 1, 2, 8, 16, 256, 1, None) == 1    # y overlaps x
+    c1 = L.wan_conv1x1
+    assert c1(A, A * 5, A * 9, 1, 2, 8, 16, 96, 256, None) == 2    # Cin % 64 != 0
+    assert c1(A, A * 5, A * 9, 1, 2, 8, 16, 128, 128, None) == 2   # Cout < 256
+    assert c1(A, A * 5, A, 1, 2, 8, 16, 128, 256, None) == 1       # y overlaps x
+    assert L.wan_fold_bias(None, A, A * 2, 256, None) == 1
+    assert L.wan_fold_bias(A, A * 2, A * 3, 0, None) == 1
+    from video_vae_decoder_gb300.binding import ResblockParams
+    p = ResblockParams(A * 2, A * 3, A * 4, None, A * 5, A * 6, A * 7, None, 32, 1e-6)
+    rs = L.wan_resblock_shortcut
+    assert rs(A, A * 40, ctypes.byref(p), None, A * 50, A * 60, 0, 1, 2, 4, 4, 128, 256, A * 70, 1 << 30, None) == 1
+    assert rs(A, A * 40, ctypes.byref(p), A * 45, A * 50, A * 60, 0, 1, 2, 4, 4, 128, 128, A * 70, 1 << 30, None) == 2
+    assert rs(A, A * 40, ctypes.byref(p), A * 45, A * 50, A * 60, 0, 1, 2, 4, 4, 128, 256, A * 70, 16, None) == 4
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers are only passed where no GPU exists")
 def test_resblock_and_upsample_reject_invalid(L):
     from video_vae_decoder_gb300.binding import ResblockParams
     p = ResblockParams(A * 2, A * 3, A * 4, None, A * 5, A * 6, A * 7, None, 32, 1e-6)

@@ -20,6 +20,7 @@ WAN_OP_RESBLOCK = 2
 WAN_OP_UPSAMPLE_PHASE_CONV = 3
 WAN_OP_GN_STATS = 4
 WAN_OP_GN_SILU_CONV3D = 5
+WAN_OP_RESBLOCK_SHORTCUT = 6
 
 STATUS = {0: "WAN_OK", 1: "WAN_ERR_INVALID_ARG", 2: "WAN_ERR_UNSUPPORTED_SHAPE", 3: "WAN_ERR_MISALIGNED",
           4: "WAN_ERR_WORKSPACE", 5: "WAN_ERR_CUDA", 6: "WAN_ERR_TIMEOUT"}
@@ -27,6 +28,7 @@ STATUS = {0: "WAN_OK", 1: "WAN_ERR_INVALID_ARG", 2: "WAN_ERR_UNSUPPORTED_SHAPE",
 EXPORTS = ("wan_status_string", "wan_workspace_size", "wan_gn_silu", "wan_gn_silu_noalloc", "wan_causal_conv3d",
            "wan_causal_conv3d_gn_stats", "wan_gn_silu_from_stats", "wan_gn_silu_causal_conv3d", "wan_gn_silu_coefficients",
            "wan_causal_conv3d_gn_input", "wan_gn_silu_cache_update", "wan_cache_update",
+           "wan_time_upsample", "wan_conv1x1", "wan_fold_bias", "wan_resblock_shortcut",
            "wan_upsample_phase_weights", "wan_upsample_phase_conv", "wan_resblock", "wan_device_status")
 
 
@@ -78,6 +80,14 @@ def lib() -> ctypes.CDLL:
     L.wan_causal_conv3d_gn_input.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P]
     L.wan_gn_silu_cache_update.restype = I
     L.wan_gn_silu_cache_update.argtypes = [P, P, P, P, I, I, I, I, I, P]
+    L.wan_time_upsample.restype = I
+    L.wan_time_upsample.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P]
+    L.wan_conv1x1.restype = I
+    L.wan_conv1x1.argtypes = [P, P, P, I, I, I, I, I, I, P]
+    L.wan_fold_bias.restype = I
+    L.wan_fold_bias.argtypes = [P, P, P, I, P]
+    L.wan_resblock_shortcut.restype = I
+    L.wan_resblock_shortcut.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, P, S, P]
     L.wan_cache_update.restype = I
     L.wan_cache_update.argtypes = [P, P, P, I, I, I, I, I, P]
     L.wan_upsample_phase_weights.restype = I
@@ -329,6 +339,69 @@ def wan_resblock(x, params: dict, cache1, cache2, cache_valid: bool, groups: int
                        groups, eps)
     _check(lib().wan_resblock(_ptr(x), _ptr(out), ctypes.byref(p), _ptr(cache1), _ptr(cache2), int(bool(cache_valid)),
                               N, T, H, W, C, _ptr(ws), need, _stream(stream)), "wan_resblock")
+    return out
+
+
+def wan_time_upsample(x, w, bias=None, first: bool = False, cache_in=None, cache_out=None, y=None, stream=None):
+    """Causal 3x1x1 time conv to 2C channels, written as twice the frames (frame-interleaved); x
+    [N, T, H, W, C], w [2C, 3, C]; with `first` the first frame passes through. Returns y
+    [N, start + 2 (T - start), H, W, C]."""
+    for t, n in ((x, "x"), (w, "w"), (bias, "bias"), (cache_in, "cache_in"), (cache_out, "cache_out")):
+        _need(t, torch.bfloat16, n)
+    N, T, H, W, C = x.shape
+    start = 1 if first else 0
+    y = torch.empty((N, start + 2 * (T - start), H, W, C), dtype=torch.bfloat16, device=x.device) if y is None else y
+    _need(y, torch.bfloat16, "y")
+    _check(lib().wan_time_upsample(_ptr(x), _ptr(cache_in), _ptr(cache_out), _ptr(w), _ptr(bias), _ptr(y), N, T, H, W,
+                                   C, int(bool(first)), _stream(stream)), "wan_time_upsample")
+    return y
+
+
+def wan_conv1x1(x, w, y=None, stream=None):
+    """y = x . w^T per pixel (w [Cout, Cin]), no bias."""
+    _need(x, torch.bfloat16, "x")
+    _need(w, torch.bfloat16, "w")
+    N, T, H, W, Cin = x.shape
+    Cout = w.shape[0]
+    y = torch.empty((N, T, H, W, Cout), dtype=torch.bfloat16, device=x.device) if y is None else y
+    _need(y, torch.bfloat16, "y")
+    _check(lib().wan_conv1x1(_ptr(x), _ptr(w), _ptr(y), N, T, H, W, Cin, Cout, _stream(stream)), "wan_conv1x1")
+    return y
+
+
+def wan_fold_bias(b2, b_shortcut, out=None, stream=None):
+    """bf16(b2 + b_shortcut): the shortcut bias folded into the second conv's."""
+    _need(b2, torch.bfloat16, "b2")
+    _need(b_shortcut, torch.bfloat16, "b_shortcut")
+    out = torch.empty_like(b2) if out is None else out
+    _check(lib().wan_fold_bias(_ptr(b2), _ptr(b_shortcut), _ptr(out), b2.numel(), _stream(stream)), "wan_fold_bias")
+    return out
+
+
+def wan_resblock_shortcut(x, params: dict, w_sc, cache1, cache2, cache_valid: bool, groups: int, eps: float, out=None,
+                          ws=None, stream=None):
+    """The channel-changing ResBlock: params as wan_resblock's with w1 [Cout, 3, 3, 3, Cin] and b2 the folded
+    bias (wan_fold_bias); w_sc [Cout, Cin] the 1x1x1 shortcut."""
+    _need(x, torch.bfloat16, "x")
+    _need(w_sc, torch.bfloat16, "w_sc")
+    _need(cache1, torch.bfloat16, "cache1")
+    _need(cache2, torch.bfloat16, "cache2")
+    for k in ("gamma1", "beta1", "gamma2", "beta2"):
+        _need(params[k], torch.float32, k)
+    for k in ("w1", "b1", "w2", "b2"):
+        _need(params.get(k), torch.bfloat16, k)
+    N, T, H, W, Cin = x.shape
+    Cout = w_sc.shape[0]
+    out = torch.empty((N, T, H, W, Cout), dtype=torch.bfloat16, device=x.device) if out is None else out
+    _need(out, torch.bfloat16, "out")
+    need = wan_workspace_size(WAN_OP_RESBLOCK_SHORTCUT, N, T, H, W, Cin, Cout, groups)
+    ws = _workspace(need, x.device, ws)
+    p = ResblockParams(_ptr(params["gamma1"]), _ptr(params["beta1"]), _ptr(params["w1"]), _ptr(params.get("b1")),
+                       _ptr(params["gamma2"]), _ptr(params["beta2"]), _ptr(params["w2"]), _ptr(params.get("b2")),
+                       groups, eps)
+    _check(lib().wan_resblock_shortcut(_ptr(x), _ptr(out), ctypes.byref(p), _ptr(w_sc), _ptr(cache1), _ptr(cache2),
+                                       int(bool(cache_valid)), N, T, H, W, Cin, Cout, _ptr(ws), need, _stream(stream)),
+           "wan_resblock_shortcut")
     return out
 
 

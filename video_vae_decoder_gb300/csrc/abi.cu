@@ -1,6 +1,8 @@
 // The extern "C" entry points of include/wan.h: host-side validation, workspace layout and the
 // ordering of the kernels on the caller's stream. Nothing here allocates device memory.
 #include <cuda_runtime.h>
+
+#include <algorithm>
 #include <stdint.h>
 #include <string.h>
 
@@ -156,6 +158,14 @@ size_t wan_workspace_size(wan_op op, int N, int T, int H, int W, int Cin, int Co
     case WAN_OP_GN_SILU_CONV3D:
       if (Cout <= 0 || groups <= 0 || Cin % groups || !gn_silu_supported(Cin, groups)) return 0;
       return gn_conv_workspace(N, T, H, W, Cin, Cout, groups);
+    case WAN_OP_RESBLOCK_SHORTCUT: {  // h, the shortcut, then the norm-into-conv workspace
+      if (Cout <= 0 || groups <= 0 || Cin % groups || Cout % groups || !gn_silu_supported(Cin, groups) ||
+          !gn_silu_supported(Cout, groups))
+        return 0;
+      const size_t y = (size_t)N * T * H * W * Cout * sizeof(wan_bf16);
+      return 2 * align256(y) + std::max(gn_conv_workspace(N, T, H, W, Cin, Cout, groups),
+                                        gn_conv_workspace(N, T, H, W, Cout, Cout, groups));
+    }
   }
   return 0;
 }
@@ -426,6 +436,113 @@ wan_status wan_resblock(const wan_bf16* x, wan_bf16* out, const wan_resblock_par
   if (e == cudaSuccess)
     e = gn_conv(h, p->gamma2, p->beta2, p->groups, p->eps, c2_in, cache2, p->w2, p->b2, x, out, N, T, H, W, C, C, gws,
                 err, s);
+  return cuda_status(e);
+}
+
+wan_status wan_time_upsample(const wan_bf16* x, const wan_bf16* cache_in, wan_bf16* cache_out, const wan_bf16* w,
+                             const wan_bf16* bias, wan_bf16* y, int N, int T, int H, int W, int C, int first,
+                             void* stream) {
+  if (!x || !w || !y) return WAN_ERR_INVALID_ARG;
+  if (!positive(N, T, H, W, C)) return WAN_ERR_INVALID_ARG;
+  if (C % 256 != 0 || !fits(N, 2 * T, H, W, C)) return WAN_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(x) || !aligned16(w) || !aligned16(y) || (bias && !aligned16(bias)) ||
+      (cache_in && !aligned16(cache_in)) || (cache_out && !aligned16(cache_out)))
+    return WAN_ERR_MISALIGNED;
+  const int start = first ? 1 : 0, nf = T - start, To = start + 2 * nf;
+  const size_t fb = (size_t)H * W * C * sizeof(wan_bf16);
+  const size_t xbytes = (size_t)N * T * fb, ybytes = (size_t)N * To * fb, cbytes = (size_t)N * 2 * fb;
+  if (overlap(x, xbytes, y, ybytes) || overlap(cache_in, cbytes, y, ybytes) || overlap(cache_out, cbytes, y, ybytes) ||
+      overlap(cache_out, cbytes, x, xbytes) || (cache_in && cache_in != cache_out && overlap(cache_in, cbytes, cache_out, cbytes)))
+    return WAN_ERR_INVALID_ARG;
+  unsigned* err = device_error_word();
+  if (!err) return WAN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  // The first frame of the first chunk passes through.
+  if (first) e = cudaMemcpy2DAsync(y, To * fb, x, T * fb, fb, N, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && nf > 0)
+    e = conv_pair_launch(2, x + (size_t)start * fb / sizeof(wan_bf16), cache_in, w, bias, nullptr, y, N, nf, H, W, C,
+                         2 * C, sm_count(), err, s, nullptr, 0, nullptr, T, To, start);
+  if (e != cudaSuccess || !cache_out) return cuda_status(e);
+  // The new history: the last two frames of [cache_in or zeros; x[:, start:]].
+  const char* xb = reinterpret_cast<const char*>(x);
+  char* cb = reinterpret_cast<char*>(cache_out);
+  if (nf >= 2) {
+    e = cudaMemcpy2DAsync(cb, 2 * fb, xb + (size_t)(T - 2) * fb, T * fb, 2 * fb, N, cudaMemcpyDeviceToDevice, s);
+  } else {
+    const int keep = 2 - nf;  // frames of the old history that stay: its last `keep`
+    if (cache_in)
+      e = cache_in == cache_out && keep == 2 ? cudaSuccess
+                                             : cudaMemcpy2DAsync(cb, 2 * fb, reinterpret_cast<const char*>(cache_in) + (2 - keep) * fb,
+                                                                 2 * fb, keep * fb, N, cudaMemcpyDeviceToDevice, s);
+    else
+      e = cudaMemset2DAsync(cb, 2 * fb, 0, keep * fb, N, s);
+    if (e == cudaSuccess && nf == 1)
+      e = cudaMemcpy2DAsync(cb + fb, 2 * fb, xb + (size_t)(T - 1) * fb, T * fb, fb, N, cudaMemcpyDeviceToDevice, s);
+  }
+  return cuda_status(e);
+}
+
+wan_status wan_conv1x1(const wan_bf16* x, const wan_bf16* w, wan_bf16* y, int N, int T, int H, int W, int Cin,
+                       int Cout, void* stream) {
+  wan_status st = check_conv(x, w, y, N, T, H, W, Cin, Cout);
+  if (st != WAN_OK) return st;
+  if (!conv_pair_supported(Cout)) return WAN_ERR_UNSUPPORTED_SHAPE;
+  if (overlap(x, (size_t)N * T * H * W * Cin * 2, y, (size_t)N * T * H * W * Cout * 2)) return WAN_ERR_INVALID_ARG;
+  unsigned* err = device_error_word();
+  if (!err) return WAN_ERR_CUDA;
+  return cuda_status(conv_pair_launch(3, x, nullptr, w, nullptr, nullptr, y, N, T, H, W, Cin, Cout, sm_count(), err,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+wan_status wan_fold_bias(const wan_bf16* b2, const wan_bf16* b_shortcut, wan_bf16* out, int C, void* stream) {
+  if (!b2 || !b_shortcut || !out || C <= 0) return WAN_ERR_INVALID_ARG;
+  return cuda_status(fold_bias_launch(b2, b_shortcut, out, C, static_cast<cudaStream_t>(stream)));
+}
+
+wan_status wan_resblock_shortcut(const wan_bf16* x, wan_bf16* out, const wan_resblock_params* p, const wan_bf16* w_sc,
+                                 wan_bf16* cache1, wan_bf16* cache2, int cache_valid, int N, int T, int H, int W,
+                                 int Cin, int Cout, void* ws, size_t ws_bytes, void* stream) {
+  if (!p || !cache1 || !cache2 || !w_sc) return WAN_ERR_INVALID_ARG;
+  wan_status st = check_gn(x, out, p->gamma1, p->beta1, N, T, H, W, Cin, p->groups, p->eps);
+  if (st != WAN_OK) return st;
+  st = check_gn(out, out, p->gamma2, p->beta2, N, T, H, W, Cout, p->groups, p->eps);
+  if (st != WAN_OK) return st;
+  st = check_conv(x, p->w1, out, N, T, H, W, Cin, Cout);
+  if (st != WAN_OK) return st;
+  st = check_conv(out, p->w2, out, N, T, H, W, Cout, Cout);
+  if (st != WAN_OK) return st;
+  if (!conv_pair_supported(Cout)) return WAN_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(cache1) || !aligned16(cache2) || !aligned16(w_sc) || (p->b1 && !aligned16(p->b1)) ||
+      (p->b2 && !aligned16(p->b2)))
+    return WAN_ERR_MISALIGNED;
+  const size_t xb = (size_t)N * T * H * W * Cin * 2, yb = (size_t)N * T * H * W * Cout * 2;
+  const size_t c1b = (size_t)N * 2 * H * W * Cin * 2, c2b = (size_t)N * 2 * H * W * Cout * 2;
+  if (overlap(x, xb, out, yb) || overlap(cache1, c1b, cache2, c2b) || overlap(cache1, c1b, out, yb) ||
+      overlap(cache2, c2b, out, yb) || overlap(cache1, c1b, x, xb) || overlap(cache2, c2b, x, xb))
+    return WAN_ERR_INVALID_ARG;
+  const size_t need = wan_workspace_size(WAN_OP_RESBLOCK_SHORTCUT, N, T, H, W, Cin, Cout, p->groups);
+  if (!ws || ws_bytes < need) return WAN_ERR_WORKSPACE;
+  if (!aligned16(ws)) return WAN_ERR_MISALIGNED;
+  unsigned* err = device_error_word();
+  if (!err) return WAN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* base = static_cast<char*>(ws);
+  wan_bf16* h = reinterpret_cast<wan_bf16*>(base);
+  wan_bf16* skip = reinterpret_cast<wan_bf16*>(base + align256(yb));
+  void* gws = base + 2 * align256(yb);
+  const wan_bf16* c1_in = cache_valid ? cache1 : nullptr;
+  const wan_bf16* c2_in = cache_valid ? cache2 : nullptr;
+  // skip = the 1x1x1 conv of x without bias (p->b2 carries the folded shortcut bias), then the
+  // two norm-into-conv steps, the second adding skip as its residual.
+  cudaError_t e = conv_pair_launch(3, x, nullptr, w_sc, nullptr, nullptr, skip, N, T, H, W, Cin, Cout, sm_count(),
+                                   err, s);
+  if (e == cudaSuccess)
+    e = gn_conv(x, p->gamma1, p->beta1, p->groups, p->eps, c1_in, cache1, p->w1, p->b1, nullptr, h, N, T, H, W, Cin,
+                Cout, gws, err, s);
+  if (e == cudaSuccess)
+    e = gn_conv(h, p->gamma2, p->beta2, p->groups, p->eps, c2_in, cache2, p->w2, p->b2, skip, out, N, T, H, W, Cout,
+                Cout, gws, err, s);
   return cuda_status(e);
 }
 

@@ -540,4 +540,24 @@ cudaError_t phase_weights_launch(const wan_bf16* w3, wan_bf16* wp, int Cin, int 
   return cudaGetLastError();
 }
 
+// The channel-changing block's shortcut bias folded into the second conv's (binding.cpp,
+// prepare()): out = b2 + b_shortcut rounded once to bf16. The sum of two bf16 values is exact in
+// fp64; it reaches fp32 rounded to odd (truncate, then set the last bit if anything was lost),
+// from which round-to-nearest-even to bf16 gives the correctly rounded result (Boldo and
+// Melquiond's round-to-odd: 24 bits >= 8 + 2).
+__global__ void fold_bias_kernel(const wan_bf16* __restrict__ b2, const wan_bf16* __restrict__ bsc,
+                                 wan_bf16* __restrict__ out, int C) {
+  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < C; c += gridDim.x * blockDim.x) {
+    const double v = (double)__uint_as_float(((uint32_t)b2[c]) << 16) + (double)__uint_as_float(((uint32_t)bsc[c]) << 16);
+    float r = __double2float_rz(v);
+    if ((double)r != v) r = __uint_as_float(__float_as_uint(r) | 1u);
+    out[c] = (wan_bf16)(pack_bf16x2(r, 0.f) & 0xFFFFu);
+  }
+}
+
+cudaError_t fold_bias_launch(const wan_bf16* b2, const wan_bf16* bsc, wan_bf16* out, int C, cudaStream_t stream) {
+  fold_bias_kernel<<<cdiv(C, 256), 256, 0, stream>>>(b2, bsc, out, C);
+  return cudaGetLastError();
+}
+
 }  // namespace wan

@@ -15,7 +15,13 @@ bool conv_pair_supported(int Cout);
 cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_in, const wan_bf16* w,
                              const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W,
                              int Cin, int Cout, int sms, unsigned* err, cudaStream_t stream,
-                             void* st_buf = nullptr, int st_groups = 0, const float4* coef = nullptr);
+                             void* st_buf = nullptr, int st_groups = 0, const float4* coef = nullptr,
+                             int a_frames = 0, int y_frames = 0, int y_frame0 = 0);
+// Modes of conv_pair_launch beyond conv_launch's: 2, the causal 3x1x1 time conv to Cout = 2 C
+// channels (w [Cout, 3, Cin]) whose output frame t, channel half i lands in frame
+// y_frame0 + 2 t + i of y ([N, y_frames, H, W, Cout / 2]; Cout % 512 == 0, no residual);
+// 3, the 1x1x1 conv (w [Cout, Cin], no cache). a_frames: frames per n of the tensor `a` points
+// into (0: T), so `a` may start at a later frame of a longer video.
 // coef (optional, mode 0): GroupNorm + SiLU of `a` applied to the conv's operand tiles as they
 // arrive (per (frame n*T + t, Cin channel) float4 coefficients as the norm's coefficients-only
 // pass leaves them, blocked layout); the cache frames are used as they are.
@@ -36,4 +42,6 @@ cudaError_t head_launch(const wan_bf16* a, const wan_bf16* cache_in, const wan_b
                         unsigned* err, cudaStream_t stream);
 cudaError_t phase_weights_launch(const wan_bf16* w3, wan_bf16* wp, int Cin, int Cout, int sms,
                                  cudaStream_t stream);
+// out = bf16(b2 + b_shortcut) per channel: the shortcut bias folded into the second conv's.
+cudaError_t fold_bias_launch(const wan_bf16* b2, const wan_bf16* bsc, wan_bf16* out, int C, cudaStream_t stream);
 }  // namespace wan

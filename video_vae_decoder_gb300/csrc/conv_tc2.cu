@@ -96,6 +96,9 @@ struct Conv2Args {
   // A box read from `a` (not the cache).
   const float4* coef;
   const wan_bf16* a;  // the conv input itself (the prologue's rare exact path reads it again)
+  // Mode 2 (time upsample): y has y_frames frames per n of Cout / 2 channels; conv output frame
+  // t, channel half i goes to frame y_frame0 + 2 t + i.
+  int y_frames, y_frame0;
 };
 
 struct PTile {
@@ -133,12 +136,17 @@ __device__ __forceinline__ int item_of(const Conv2Args& a, int r, int cluster, i
 
 // Kernel row `row` of the tap grid: its frame and row offsets, and the input column of the A
 // box's first column relative to the tile. Mode 0: 9 rows (dt, dh) of 3 horizontal taps; mode 1:
-// for phase (pa, pb) the 2 rows u of 2 taps v, reading input (h + pa - 1 + u, w + pb - 1 + v).
+// for phase (pa, pb) the 2 rows u of 2 taps v, reading input (h + pa - 1 + u, w + pb - 1 + v);
+// mode 2 (3x1x1 time conv): 3 rows dt of one tap; mode 3 (1x1x1): one row of one tap.
 __device__ __forceinline__ void row_offsets(const Conv2Args& a, int row, int ph, int& dt, int& dh, int& dw0) {
   if (a.mode == 0) {
     dt = row / 3 - 2;
     dh = row % 3 - 1;
     dw0 = -1;
+  } else if (a.mode >= 2) {  // the current pixel of frame t + dt: mode 2 dt = -2..0, mode 3 dt = 0
+    dt = a.mode == 2 ? row - 2 : 0;
+    dh = 0;
+    dw0 = 0;
   } else {
     dt = 0;
     dh = (ph >> 1) - 1 + row;
@@ -220,8 +228,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
   // rows_in rows, K slice, row in the group): mode 0 takes a kernel frame's 3 rows per K slice, so
   // the taps are added in the order (dt, K slice, dh, dw), the prologue kernel's order too, and
   // the two kernels give the same bits.
-  const int rows = kNorm ? 3 : (args.mode == 0 ? 9 : 2);
-  const int taps_per_row = kNorm ? 9 : (args.mode == 0 ? 3 : 2);
+  const int rows = kNorm ? 3 : (args.mode == 0 ? 9 : args.mode == 1 ? 2 : args.mode == 2 ? 3 : 1);
+  const int taps_per_row = kNorm ? 9 : (args.mode == 0 ? 3 : args.mode == 1 ? 2 : 1);
   const int rows_in = (!kNorm && args.mode == 0) ? 3 : 1;
 
   if (threadIdx.x == 0) {
@@ -425,8 +433,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
     // ------------------------------------------------------------ epilogue (both CTAs, own 128 rows)
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
-    const int Ho = args.mode == 0 ? args.H : 2 * args.H;
-    const int Wo = args.mode == 0 ? args.W : 2 * args.W;
+    const int Ho = args.mode == 1 ? 2 * args.H : args.H;
+    const int Wo = args.mode == 1 ? 2 * args.W : args.W;
+    const int Cy = args.mode == 2 ? args.Cout / 2 : args.Cout;  // channels of a y pixel
     const bool vec8 = (args.Cout % 8) == 0;
     const uint32_t leader_empty0 = mapa_shared(smem_u32(&tmem_empty[0]), 0);
     const uint32_t leader_empty1 = mapa_shared(smem_u32(&tmem_empty[1]), 0);
@@ -443,11 +452,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
       const int tt = t.t0;
       const bool valid = t.valid && hh < args.H && ww < args.W;
       size_t pix;
-      if (args.mode == 0)
-        pix = (((size_t)t.n * args.T + tt) * Ho + hh) * Wo + ww;
-      else
+      wan_bf16* yrow;
+      if (args.mode == 1) {
         pix = (((size_t)t.n * args.T + tt) * Ho + (2 * hh + (t.ph >> 1))) * Wo + (2 * ww + (t.ph & 1));
-      wan_bf16* yrow = args.y + pix * args.Cout;
+        yrow = args.y + pix * args.Cout;
+      } else if (args.mode == 2) {  // channel half i of this N block -> frame y_frame0 + 2 t + i
+        const int half = t.nb * kN / Cy;
+        pix = (((size_t)t.n * args.y_frames + args.y_frame0 + 2 * tt + half) * Ho + hh) * Wo + ww;
+        yrow = args.y + pix * Cy - (size_t)half * Cy;  // + col lands on channel col - half * Cy
+      } else {
+        pix = (((size_t)t.n * args.T + tt) * Ho + hh) * Wo + ww;
+        yrow = args.y + pix * args.Cout;
+      }
       const wan_bf16* rrow = args.residual ? args.residual + pix * args.Cout : nullptr;
       const uint32_t taddr = tmem_base + (uint32_t)(acc * kN) + ((uint32_t)(quarter * 32) << 16);
       // GroupNorm statistics of this tile's output (optional): per group, each lane adds d and d^2
@@ -671,12 +687,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn2() {
 
 // Activations [N, T, H, W, C] addressed as (c, h, w, t, n): H is listed before W, so a box of
 // 8 rows x 18 columns lands in shared memory column by column (row m = h + 8 w).
-bool map_act_hw(CUtensorMap* m, const void* base, int C, int W, int H, int T, int N, int box_h = kTileH) {
+// T frames per n are mapped; consecutive n are n_frames frames apart (n_frames >= T).
+bool map_act_hw(CUtensorMap* m, const void* base, int C, int W, int H, int T, int N, int box_h = kTileH,
+                int n_frames = 0) {
   auto fn = encode_fn2();
   if (!fn) return false;
+  if (n_frames < T) n_frames = T;
   const cuuint64_t dims[5] = {(cuuint64_t)C, (cuuint64_t)H, (cuuint64_t)W, (cuuint64_t)T, (cuuint64_t)N};
   const cuuint64_t e = 2;
-  const cuuint64_t strides[4] = {(cuuint64_t)W * C * e, C * e, (cuuint64_t)H * W * C * e, (cuuint64_t)T * H * W * C * e};
+  const cuuint64_t strides[4] = {(cuuint64_t)W * C * e, C * e, (cuuint64_t)H * W * C * e,
+                                 (cuuint64_t)n_frames * H * W * C * e};
   const cuuint32_t box[5] = {(cuuint32_t)kBlockK, (cuuint32_t)box_h, (cuuint32_t)kBoxW, 1, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
@@ -746,7 +766,10 @@ size_t conv_gn_stats_bytes(int N, int T, int H, int W, int Cout, int groups) {
 cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_in, const wan_bf16* w,
                              const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W,
                              int Cin, int Cout, int sms, unsigned* err, cudaStream_t stream, void* st_buf,
-                             int st_groups, const float4* coef) {
+                             int st_groups, const float4* coef, int a_frames, int y_frames, int y_frame0) {
+  if (mode < 0 || mode > 3) return cudaErrorInvalidValue;
+  if (mode == 2 && (Cout % (2 * kN) != 0 || residual != nullptr)) return cudaErrorInvalidValue;
+  if (mode == 3 && cache_in) return cudaErrorInvalidValue;
   Conv2Args args{};
   args.N = N;
   args.T = T;
@@ -759,7 +782,7 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
   args.px_tiles = N * T * args.tiles_h * args.tiles_w;
   args.px_pairs = cdiv(args.px_tiles, 2);
   args.n_blks = cdiv(Cout, kN);
-  args.phases = mode == 0 ? 1 : 4;
+  args.phases = mode == 1 ? 4 : 1;
   args.items = args.px_pairs * args.phases * args.n_blks;
   args.kb_per_tap = Cin / kBlockK;
   args.mode = mode;
@@ -768,6 +791,8 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
   args.residual = residual;
   args.y = y;
   args.err = err;
+  args.y_frames = y_frames;
+  args.y_frame0 = y_frame0;
   if (st_buf) {
     if (mode != 0 || !conv_gn_stats_supported(Cout, st_groups)) return cudaErrorInvalidValue;
     args.st_rec = reinterpret_cast<float4*>(st_buf);
@@ -777,13 +802,14 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
   }
   CUtensorMap ta, tc, tw;
   const int box_h = coef ? kTallRows : kTileH;  // the prologue kernel loads tall boxes
-  if (!map_act_hw(&ta, a, Cin, W, H, T, N, box_h)) return cudaErrorInvalidValue;
+  if (!map_act_hw(&ta, a, Cin, W, H, T, N, box_h, a_frames)) return cudaErrorInvalidValue;
   if (cache_in) {
     if (!map_act_hw(&tc, cache_in, Cin, W, H, 2, N, box_h)) return cudaErrorInvalidValue;
   } else {
     tc = ta;
   }
-  if (!map_w_half(&tw, w, (mode == 0 ? 27 : 4) * Cin, Cout, args.phases)) return cudaErrorInvalidValue;
+  const int taps = mode == 0 ? 27 : mode == 1 ? 4 : mode == 2 ? 3 : 1;
+  if (!map_w_half(&tw, w, taps * Cin, Cout, args.phases)) return cudaErrorInvalidValue;
   if (coef) {
     if (mode != 0) return cudaErrorInvalidValue;
     args.coef = coef;
