@@ -43,7 +43,7 @@ typedef uint16_t wan_bf16;
 typedef enum wan_status {
   WAN_OK = 0,
   WAN_ERR_INVALID_ARG = 1,       /* null pointer, non-positive size, groups not dividing C ... */
-  WAN_ERR_UNSUPPORTED_SHAPE = 2, /* a size this build has no kernel for (see each call) */
+  WAN_ERR_UNSUPPORTED_SHAPE = 2, /* a size this library has no kernel for (see each call) */
   WAN_ERR_MISALIGNED = 3,        /* a pointer is not 16-byte aligned */
   WAN_ERR_WORKSPACE = 4,         /* ws is NULL or ws_bytes below wan_workspace_size() */
   WAN_ERR_CUDA = 5,              /* a CUDA runtime call or kernel launch failed */
@@ -138,7 +138,7 @@ wan_status wan_gn_silu_noalloc(const wan_bf16* x, wan_bf16* y, const float* gamm
  *              overlap y).
  *   y          [N, T, H, W, Cout] bf16.
  *   Cin % 64 == 0; 1 <= Cout; Cout % 2 == 0.
- *   ws         unused by this build (wan_workspace_size returns 0); may be NULL.
+ *   ws         unused by this version of the library (wan_workspace_size returns 0); may be NULL.
  */
 wan_status wan_causal_conv3d(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out,
                              const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual,
