@@ -113,3 +113,18 @@ def test_conv_full_size_c256(wan):
 def test_conv_full_size_c1024(wan):
     # The widest stage: [1, 4, 44, 78, 1024] -> 1024 channels, sampled outputs.
     _sampled_check(wan, (1, 4, 44, 78, 1024), 1024, "conv/cfg5")
+
+
+def test_conv_c1024_split_last_round_equals_chunks(wan):
+    # [1, 4, 44, 78, 1024]: 240 items (pixel-tile pairs x 4 blocks of 256 output channels). On 76
+    # CTA pairs the last round holds 12 items, which run as 24 halves of 128 channels; two 2-frame
+    # chunks (120 items, a last round of 44) run whole. Both must give the same bits.
+    shape = (1, 4, 44, 78, 1024)
+    a, w, b, _, _ = make(shape, 1024, "conv/split")
+    full, full_cache = run(wan, a, w, b, None, None)
+    parts, cache = [], None
+    for s in range(0, 4, 2):
+        y, cache = run(wan, a[:, s:s + 2], w, b, None, cache)
+        parts.append(y)
+    assert np.array_equal(np.concatenate(parts, 1), full)
+    assert np.array_equal(cache, full_cache)

@@ -87,3 +87,18 @@ def test_decoder_stage_c256_chunked_equals_unchunked(wan):
     assert torch.isfinite(a.float()).all()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
     assert wan.wan_device_status() == 0
+
+
+def test_resblock_c1024_chunked_equals_unchunked(wan):
+    # The widest stage's ResBlock on [1, 4, 44, 78, 1024] (GroupNorm + SiLU in the convs' operand
+    # prologue): one 4-frame call, whose convs split their last round into 128-channel halves,
+    # against two 2-frame chunks, whose convs do not.
+    x = synth.normal_torch((1, 4, 44, 78, 1024), 0, "rb/c1024/x", device="cuda", dtype=torch.bfloat16)
+    params = dev_params(synth.resblock_params(1024, 0, "rb/c1024"))
+    full, f1, f2 = run_chunks(wan, x, params, 32, 4)
+    part, p1, p2 = run_chunks(wan, x, params, 32, 2)
+    assert torch.isfinite(full.float()).all()
+    assert torch.equal(full.view(torch.int16), part.view(torch.int16))
+    assert torch.equal(f1.view(torch.int16), p1.view(torch.int16))
+    assert torch.equal(f2.view(torch.int16), p2.view(torch.int16))
+    assert wan.wan_device_status() == 0

@@ -28,7 +28,19 @@
 // the second (a missing second tile loads zeros and stores nothing). Both tiles of a pair use the
 // same weights, so in mode 1 a pair never mixes phases. Items go to the CTA pairs in snake order
 // (round r: pair c takes item r * P + c, or r * P + P - 1 - c on odd rounds), which evens out
-// items of different cost (the first frames of a chunk without history skip taps).
+// items of different cost (the first frames of a chunk without history skip taps). When the last
+// round holds at most P / 2 items, each of them is scheduled as two halves of 128 output channels
+// (M256 x N128 MMAs, 64 weight rows per SM) on twice as many pairs: that round would otherwise
+// leave most pairs idle (the C=1024 stage's 240 items over 76 pairs). A half computes the same
+// output elements with the same sequence of K steps as the whole item, so the split changes no
+// result.
+//
+// MMA issue. One thread issues every MMA of the pair, and its issue rate, not the tensor pipe, was
+// the limit: with a wait, a fence and a stage release per tap inside a run-time loop, each MMA
+// took ~160 cycles to issue against 128 to execute (M256 x N256 x K16), whatever N was. Each A box
+// is therefore issued as one straight-line burst (9 taps of a tall box, 3 of a plain mode-0 box,
+// 2 of a phase box, two consecutive 1-tap boxes in modes 2 and 3) whose descriptors differ by
+// constants; the B ring is used 9 or 8 stages deep so that no burst wraps it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
@@ -79,6 +91,9 @@ struct Conv2Args {
   int tiles_h, tiles_w;
   int px_tiles, px_pairs;
   int n_blks, phases, items;
+  // Scheduling units: item i < split0 is one unit, items from split0 on are two (their halves of
+  // 128 output channels); units = split0 + 2 (items - split0).
+  int units, split0;
   int kb_per_tap, mode, has_cache;
   const wan_bf16* bias;
   const wan_bf16* residual;
@@ -126,12 +141,22 @@ __device__ __forceinline__ PTile decode_pair(const Conv2Args& a, int item, int w
   return t;
 }
 
-// Snake order of items over the CTA pairs; -1 once this pair has no item in round r.
+// Snake order of scheduling units over the CTA pairs; -1 once this pair has no unit in round r.
 __device__ __forceinline__ int item_of(const Conv2Args& a, int r, int cluster, int nclusters) {
   const int base = r * nclusters;
-  if (base >= a.items) return -1;
-  const int item = base + ((r & 1) ? nclusters - 1 - cluster : cluster);
-  return item < a.items ? item : -2;  // -2: nothing in this (last) round
+  if (base >= a.units) return -1;
+  const int unit = base + ((r & 1) ? nclusters - 1 - cluster : cluster);
+  return unit < a.units ? unit : -2;  // -2: nothing in this (last) round
+}
+
+// Unit -> item, and which 128-channel half of the item's N block it computes (-1: all 256).
+__device__ __forceinline__ int unit_item(const Conv2Args& a, int unit, int& sub) {
+  if (unit < a.split0) {
+    sub = -1;
+    return unit;
+  }
+  sub = (unit - a.split0) & 1;
+  return a.split0 + ((unit - a.split0) >> 1);
 }
 
 // Kernel row `row` of the tap grid: its frame and row offsets, and the input column of the A
@@ -199,10 +224,59 @@ __device__ __forceinline__ void st_reduce8(const float (&vh)[8], const float (&v
   }
 }
 
+// The MMAs of one A box whose kTaps taps read the consecutive B stages starting at full_b[0] /
+// empty_b[0] (no wrap of the ring inside the box): straight-line code whose descriptors differ by
+// constants, with each tap's wait, fence and stage release in place. A probe of the tensor pipe
+// (one issuing thread, M256 x N128 pair MMAs) measured that per-tap wait, fence and commit inside
+// a run-time loop cost ~120 cycles of issue per MMA against ~86 in straight-line code.
+template <int kTaps, bool kTall>
+__device__ __forceinline__ bool mma_box(uint32_t d_tmem, uint32_t a_box, uint32_t b_stage, uint64_t* full_b,
+                                        uint64_t* empty_b, uint32_t phb, uint32_t idesc, bool first, unsigned* err) {
+  const uint64_t a0 = kTall ? smem_desc_sw128(a_box, kTallRows * 128) : smem_desc_sw128(a_box);
+  const uint64_t b0 = smem_desc_sw128(b_stage);
+#pragma unroll
+  for (int j = 0; j < kTaps; ++j) {
+    if (!mbar_wait_cluster(&full_b[j], phb, err, kDevErrTimeoutMma)) return false;
+    tc_fence_after();
+    // Tap j: plain box, the next column (1024 bytes on); tall box, rows dh + 10 dw of its
+    // 10-row columns (tap j = 3 dh + dw), columns 1280 bytes apart.
+    const uint64_t aj = a0 + (kTall ? (uint64_t)(((j % 3) * kTallRows + j / 3) * 8) : (uint64_t)j * kShiftDesc);
+    const uint64_t bj = b0 + (uint64_t)j * (kBBytes >> 4);
+#pragma unroll
+    for (int k = 0; k < kBlockK / 16; ++k)
+      mma_bf16_pair(d_tmem, aj + 2 * k, bj + 2 * k, idesc, (first && j == 0 && k == 0) ? 0u : 1u);
+    mma_commit_pair(&empty_b[j], 0x3);
+  }
+  return true;
+}
+
+// Two consecutive boxes of one tap each (modes 2 and 3: consecutive K blocks of one kernel row):
+// A stages 0, 1 and B stages 0, 1 from the given ones, in straight-line code.
+__device__ __forceinline__ bool mma_two_boxes(uint32_t d_tmem, uint32_t a_box, uint32_t a_stride, uint32_t b_stage,
+                                              uint64_t* full_a, uint64_t* empty_a, uint64_t* full_b,
+                                              uint64_t* empty_b, uint32_t pha, uint32_t phb, uint32_t idesc,
+                                              bool first, unsigned* err) {
+  const uint64_t a0 = smem_desc_sw128(a_box), b0 = smem_desc_sw128(b_stage);
+#pragma unroll
+  for (int g = 0; g < 2; ++g) {
+    if (!mbar_wait_cluster(&full_a[g], pha, err, kDevErrTimeoutMma)) return false;
+    if (!mbar_wait_cluster(&full_b[g], phb, err, kDevErrTimeoutMma)) return false;
+    tc_fence_after();
+    const uint64_t ag = a0 + (uint64_t)g * (a_stride >> 4), bg = b0 + (uint64_t)g * (kBBytes >> 4);
+#pragma unroll
+    for (int k = 0; k < kBlockK / 16; ++k)
+      mma_bf16_pair(d_tmem, ag + 2 * k, bg + 2 * k, idesc, (first && g == 0 && k == 0) ? 0u : 1u);
+    mma_commit_pair(&empty_b[g], 0x3);
+    mma_commit_pair(&empty_a[g], 0x3);
+  }
+  return true;
+}
+
 template <bool kNorm>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads, 1)
     conv_tc2_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_cache,
-                    const __grid_constant__ CUtensorMap tm_w, const Conv2Args args) {
+                    const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_w64,
+                    const Conv2Args args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int kAStages = Cfg<kNorm>::kAStages, kBStages = Cfg<kNorm>::kBStages;
@@ -231,6 +305,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
   const int rows = kNorm ? 3 : (args.mode == 0 ? 9 : args.mode == 1 ? 2 : args.mode == 2 ? 3 : 1);
   const int taps_per_row = kNorm ? 9 : (args.mode == 0 ? 3 : args.mode == 1 ? 2 : 1);
   const int rows_in = (!kNorm && args.mode == 0) ? 3 : 1;
+  // B stages in use: 8 for boxes of 2 taps (mode 1) and of 1 tap (modes 2, 3), so that no box,
+  // and no pair of 1-tap boxes, wraps the ring.
+  const int b_ring = taps_per_row <= 2 ? kBStages - 1 : kBStages;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAStages; ++s) {
@@ -252,6 +329,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
     prefetch_tensormap(&tm_a);
     prefetch_tensormap(&tm_cache);
     prefetch_tensormap(&tm_w);
+    if (args.split0 < args.items) prefetch_tensormap(&tm_w64);
   }
   if (warp == 1) {
     tmem_alloc_pair(tmem_slot, kTmemCols);  // one warp in each CTA of the pair, collectively
@@ -271,12 +349,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
     uint32_t armed_a = 0, parity_a = 0, armed_b = 0, parity_b = 0;  // stages the even CTA armed
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int item = item_of(args, r, cluster, nclusters);
-      if (item == -1) break;
-      if (item < 0) continue;
+      const int unit = item_of(args, r, cluster, nclusters);
+      if (unit == -1) break;
+      if (unit < 0) continue;
+      int sub;
+      const int item = unit_item(args, unit, sub);
       const PTile me = decode_pair(args, item, (int)rank);
       const PTile p0 = decode_pair(args, item, 0), p1 = decode_pair(args, item, 1);
-      const int brow = me.nb * kN + (int)rank * 128;
+      // This CTA's weight rows: half of the N block, or half of the unit's 128-channel half.
+      const int brow = me.nb * kN + (sub < 0 ? (int)rank * 128 : sub * 128 + (int)rank * 64);
+      const CUtensorMap* wmap = sub < 0 ? &tm_w : &tm_w64;
+      const uint32_t b_tx = sub < 0 ? 2 * kBBytes : kBBytes;
       for (int rg = 0; ok && rg < rows; rg += rows_in) {
         for (int kb = 0; ok && kb < args.kb_per_tap; ++kb) {
           for (int row = rg; ok && row < rg + rows_in; ++row) {
@@ -333,14 +416,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
                 break;
               }
               if (leader) {
-                mbar_arrive_expect_tx(&full_b[sb], 2 * kBBytes);
+                mbar_arrive_expect_tx(&full_b[sb], b_tx);
                 armed_b |= 1u << sb;
                 parity_b = (parity_b & ~(1u << sb)) | (phb << sb);
               }
               const int tap = row * taps_per_row + j;
-              tma_load_3d_pair(smem + kBOffset + sb * kBBytes, &tm_w, mapa_shared(smem_u32(&full_b[sb]), 0),
+              tma_load_3d_pair(smem + kBOffset + sb * kBBytes, wmap, mapa_shared(smem_u32(&full_b[sb]), 0),
                                tap * args.Cin + kb * kBlockK, brow, me.ph, w_policy);
-              if (++sb == kBStages) {
+              if (++sb == b_ring) {
                 sb = 0;
                 phb ^= 1;
               }
@@ -357,7 +440,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
       if (armed_b & (1u << s)) mbar_wait(&full_b[s], (parity_b >> s) & 1, args.err, kDevErrTimeoutDrain);
   } else if (warp == 1 && lane == 0 && leader) {
     // ------------------------------------------------------------ MMA issuer (even CTA)
-    constexpr uint32_t idesc = idesc_bf16_f32(256, kN);
+    constexpr uint32_t idesc_full = idesc_bf16_f32(256, kN), idesc_half = idesc_bf16_f32(256, kN / 2);
     const uint32_t a_base = smem_u32(smem), b_base = smem_u32(smem + kBOffset);
     int sa = 0, sb = 0;
     uint32_t pha = 0, phb = 0;
@@ -365,9 +448,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int item = item_of(args, r, cluster, nclusters);
-      if (item == -1) break;
-      if (item < 0) continue;
+      const int unit = item_of(args, r, cluster, nclusters);
+      if (unit == -1) break;
+      if (unit < 0) continue;
+      int sub;
+      const int item = unit_item(args, unit, sub);
+      const uint32_t idesc = sub < 0 ? idesc_full : idesc_half;  // a half: the first 128 columns
       const PTile p0 = decode_pair(args, item, 0), p1 = decode_pair(args, item, 1);
       if (!mbar_wait_cluster(&tmem_empty[acc], acc_phase ^ 1, args.err, kDevErrTimeoutMma)) break;
       tc_fence_after();
@@ -384,33 +470,68 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
                 row_offsets(args, row, p0.ph, dt, dh, dw0);
               if (skip_pair(args, p0, p1, dt)) continue;
             }
+            if (!kNorm && taps_per_row == 1 && rows_in == 1 && (kb & 1) == 0 && kb + 1 < args.kb_per_tap &&
+                (sa & 1) == 0 && (sb & 1) == 0) {
+              // K blocks kb and kb + 1 of this kernel row in one burst (the loop's kb++ skips kb + 1).
+              ok = mma_two_boxes(d_tmem, a_base + sa * kAStride, kAStride, b_base + sb * kBBytes, full_a + sa,
+                                 empty_a + sa, full_b + sb, empty_b + sb, pha, phb, idesc, first, args.err);
+              first = false;
+              if ((sa += 2) == kAStages) {
+                sa = 0;
+                pha ^= 1;
+              }
+              if ((sb += 2) == b_ring) {
+                sb = 0;
+                phb ^= 1;
+              }
+              ++kb;
+              continue;
+            }
             if (!mbar_wait_cluster(kNorm ? &ready_a[sa] : &full_a[sa], pha, args.err, kDevErrTimeoutMma)) {
               ok = false;
               break;
             }
             const uint32_t a_box = a_base + sa * kAStride;
-            const uint64_t a_desc = smem_desc_sw128(a_box);
-            for (int j = 0; j < taps_per_row; ++j) {
-              if (!mbar_wait_cluster(&full_b[sb], phb, args.err, kDevErrTimeoutMma)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              // Tap j of the box: plain, the next column (1024 bytes on); tall box, rows
-              // dh + 10 dw of its 10-row columns (tap j = 3 dh + dw), columns 1280 bytes apart.
-              const uint64_t aj = kNorm ? smem_desc_sw128(a_box + ((j % 3) * kTallRows + j / 3) * 128, kTallRows * 128)
-                                        : a_desc + j * kShiftDesc;
-              const uint64_t b_desc = smem_desc_sw128(b_base + sb * kBBytes);
+            // Boxes of 9 taps (tall), 3 taps (mode 0) or 2 taps (mode 1, an 8-stage ring) never wrap
+            // the B ring: one straight-line burst each. Boxes of 1 tap (modes 2, 3) take the loop.
+            static_assert(kBStages == 9, "9 B stages: whole boxes of 3 and 9 taps");
+            if (kNorm && sb == 0) {
+              ok = mma_box<9, true>(d_tmem, a_box, b_base, full_b, empty_b, phb, idesc, first, args.err);
+              sb = kBStages;
+            } else if (!kNorm && taps_per_row == 3 && sb % 3 == 0) {
+              ok = mma_box<3, false>(d_tmem, a_box, b_base + sb * kBBytes, full_b + sb, empty_b + sb, phb, idesc, first,
+                                     args.err);
+              sb += 3;
+            } else if (!kNorm && taps_per_row == 2 && sb % 2 == 0) {
+              ok = mma_box<2, false>(d_tmem, a_box, b_base + sb * kBBytes, full_b + sb, empty_b + sb, phb, idesc, first,
+                                     args.err);
+              sb += 2;
+            } else {
+              const uint64_t a_desc = smem_desc_sw128(a_box);
+              for (int j = 0; j < taps_per_row; ++j) {
+                if (!mbar_wait_cluster(&full_b[sb], phb, args.err, kDevErrTimeoutMma)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                const uint64_t aj = kNorm ? smem_desc_sw128(a_box + ((j % 3) * kTallRows + j / 3) * 128, kTallRows * 128)
+                                          : a_desc + j * kShiftDesc;
+                const uint64_t b_desc = smem_desc_sw128(b_base + sb * kBBytes);
   #pragma unroll
-              for (int k = 0; k < kBlockK / 16; ++k)
-                mma_bf16_pair(d_tmem, aj + 2 * k, b_desc + 2 * k, idesc, (first && k == 0) ? 0u : 1u);
-              first = false;
-              mma_commit_pair(&empty_b[sb], 0x3);
-              if (++sb == kBStages) {
-                sb = 0;
-                phb ^= 1;
+                for (int k = 0; k < kBlockK / 16; ++k)
+                  mma_bf16_pair(d_tmem, aj + 2 * k, b_desc + 2 * k, idesc, (first && j == 0 && k == 0) ? 0u : 1u);
+                mma_commit_pair(&empty_b[sb], 0x3);
+                if (++sb == b_ring) {
+                  sb = 0;
+                  phb ^= 1;
+                }
               }
             }
+            if (sb == b_ring) {
+              sb = 0;
+              phb ^= 1;
+            }
+            first = false;
             if (!ok) break;
             mma_commit_pair(&empty_a[sa], 0x3);
             if (++sa == kAStages) {
@@ -442,10 +563,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int r = 0;; ++r) {
-      const int item = item_of(args, r, cluster, nclusters);
-      if (item == -1) break;
-      if (item < 0) continue;
+      const int unit = item_of(args, r, cluster, nclusters);
+      if (unit == -1) break;
+      if (unit < 0) continue;
+      int sub;
+      const int item = unit_item(args, unit, sub);
       const PTile t = decode_pair(args, item, (int)rank);
+      const int ncols = sub < 0 ? kN : kN / 2;                  // accumulator columns of the unit
+      const int cbase = t.nb * kN + (sub > 0 ? kN / 2 : 0);     // its first output channel
       if (!mbar_wait_cluster(&tmem_full[acc], acc_phase, args.err, kDevErrTimeoutEpilogue)) break;
       tc_fence_after();
       const int hh = t.h0 + (row & (kTileH - 1)), ww = t.w0 + row / kTileH;  // TMEM row = h + 8 w
@@ -486,12 +611,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
       float sh = 0.f;
       float2 h1 = make_float2(0.f, 0.f), l1 = h1, h2 = h1, l2 = h1;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kN; c0 += 16) {
+      for (int c0 = 0; c0 < ncols; c0 += 16) {
         float v[16];
         uint32_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // the chunk as stored (valid lanes)
         __syncwarp();
         tmem_ld16(taddr + c0, v);
-        const int col = t.nb * kN + c0;
+        const int col = cbase + c0;
         if (valid && col < args.Cout) {
           if (args.bias) {
 #pragma unroll
@@ -601,9 +726,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
     uint32_t pha = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int item = item_of(args, r, cluster, nclusters);
-      if (item == -1) break;
-      if (item < 0) continue;
+      const int unit = item_of(args, r, cluster, nclusters);
+      if (unit == -1) break;
+      if (unit < 0) continue;
+      int sub;
+      const int item = unit_item(args, unit, sub);
       const PTile me = decode_pair(args, item, (int)rank);
       const PTile p0 = decode_pair(args, item, 0), p1 = decode_pair(args, item, 1);
       for (int row = 0; ok && row < rows; ++row) {
@@ -704,12 +831,13 @@ bool map_act_hw(CUtensorMap* m, const void* base, int C, int W, int H, int T, in
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool map_w_half(CUtensorMap* m, const void* base, int K, int Cout, int P) {
+// Weights [P][Cout][K] addressed as (k, cout, p); a box is 64 K x `rows` output channels.
+bool map_w_half(CUtensorMap* m, const void* base, int K, int Cout, int P, int rows) {
   auto fn = encode_fn2();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)Cout, (cuuint64_t)P};
   const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)K * Cout * 2};
-  const cuuint32_t box[3] = {(cuuint32_t)kBlockK, 128, 1};
+  const cuuint32_t box[3] = {(cuuint32_t)kBlockK, (cuuint32_t)rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -719,8 +847,8 @@ bool map_w_half(CUtensorMap* m, const void* base, int K, int Cout, int P) {
 // Persistent grid: as many CTA pairs as the GPU can hold at once (not every SM can be paired:
 // a pair lives in one GPC), so no pair waits for a second wave.
 template <bool kNorm>
-cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tc, const CUtensorMap& tw, const Conv2Args& args,
-                        int sms, cudaStream_t stream) {
+cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tc, const CUtensorMap& tw, const CUtensorMap& tw64,
+                        Conv2Args args, int sms, cudaStream_t stream) {
   constexpr int kSmem = Cfg<kNorm>::kSmemTotal, kThr = Cfg<kNorm>::kThreads;
   cudaError_t e = cudaFuncSetAttribute(conv_tc2_kernel<kNorm>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
@@ -740,9 +868,18 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tc, const CUte
     max_clusters[dev] = n;
   }
   int clusters = (dev >= 0 && dev < 64) ? max_clusters[dev] : sms / 2;
-  if (clusters > args.items) clusters = args.items;
   if (clusters < 1) clusters = 1;
-  conv_tc2_kernel<kNorm><<<2 * clusters, kThr, kSmem, stream>>>(ta, tc, tw, args);
+  // A last round of at most half the pairs' worth of items runs as twice as many 128-channel
+  // halves (not with the epilogue statistics, whose records span 4 groups of a 256-channel block).
+  const int rem = args.items % clusters;
+  args.split0 = args.items;
+  args.units = args.items;
+  if (rem > 0 && 2 * rem <= clusters && args.st_rec == nullptr) {
+    args.split0 = args.items - rem;
+    args.units = args.items + rem;
+  }
+  if (clusters > args.units) clusters = args.units;
+  conv_tc2_kernel<kNorm><<<2 * clusters, kThr, kSmem, stream>>>(ta, tc, tw, tw64, args);
   return cudaGetLastError();
 }
 
@@ -800,7 +937,7 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
     args.st_cg = Cout / st_groups;
     while ((1 << args.st_lg) < args.st_cg) ++args.st_lg;
   }
-  CUtensorMap ta, tc, tw;
+  CUtensorMap ta, tc, tw, tw64;
   const int box_h = coef ? kTallRows : kTileH;  // the prologue kernel loads tall boxes
   if (!map_act_hw(&ta, a, Cin, W, H, T, N, box_h, a_frames)) return cudaErrorInvalidValue;
   if (cache_in) {
@@ -809,14 +946,15 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
     tc = ta;
   }
   const int taps = mode == 0 ? 27 : mode == 1 ? 4 : mode == 2 ? 3 : 1;
-  if (!map_w_half(&tw, w, taps * Cin, Cout, args.phases)) return cudaErrorInvalidValue;
+  if (!map_w_half(&tw, w, taps * Cin, Cout, args.phases, 128)) return cudaErrorInvalidValue;
+  if (!map_w_half(&tw64, w, taps * Cin, Cout, args.phases, 64)) return cudaErrorInvalidValue;
   if (coef) {
     if (mode != 0) return cudaErrorInvalidValue;
     args.coef = coef;
     args.a = a;
-    return launch_pair<true>(ta, tc, tw, args, sms, stream);
+    return launch_pair<true>(ta, tc, tw, tw64, args, sms, stream);
   }
-  return launch_pair<false>(ta, tc, tw, args, sms, stream);
+  return launch_pair<false>(ta, tc, tw, tw64, args, sms, stream);
 }
 
 }  // namespace wan
