@@ -600,7 +600,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
       const int src = vmask ? __ffs(vmask) - 1 : 0;
       const int cg = args.st_cg, lg = args.st_lg;
       const size_t rec_stride = (size_t)args.tiles_h * args.tiles_w * 4;  // between groups
-      const size_t rec0 = ((((size_t)t.n * args.T + tt) * (args.Cout >> lg) + (size_t)t.nb * (kN >> lg)) *
+      const size_t rec0 = ((((size_t)t.n * args.T + tt) * (args.Cout >> lg) + (size_t)(cbase >> lg)) *
                                (size_t)args.tiles_h * args.tiles_w +
                            (size_t)(t.h0 / kTileH) * args.tiles_w + t.w0 / kTileW) * 4 + quarter;
       float wh[8], wl[8], shw[4];  // the window's 4 groups: (sum d, sum d^2) as float-float, shifts
@@ -870,11 +870,11 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tc, const CUte
   int clusters = (dev >= 0 && dev < 64) ? max_clusters[dev] : sms / 2;
   if (clusters < 1) clusters = 1;
   // A last round of at most half the pairs' worth of items runs as twice as many 128-channel
-  // halves (not with the epilogue statistics, whose records span 4 groups of a 256-channel block).
+  // halves (with the epilogue statistics only while a half holds whole windows of 4 groups).
   const int rem = args.items % clusters;
   args.split0 = args.items;
   args.units = args.items;
-  if (rem > 0 && 2 * rem <= clusters && args.st_rec == nullptr) {
+  if (rem > 0 && 2 * rem <= clusters && (args.st_rec == nullptr || 4 * args.st_cg <= kN / 2)) {
     args.split0 = args.items - rem;
     args.units = args.items + rem;
   }
