@@ -161,14 +161,15 @@ __device__ __forceinline__ void store_row(const HeadArgs& args, const float (&ac
     yp[k] = make_uint2(pack_bf16x2(o[4 * k], o[4 * k + 1]), pack_bf16x2(o[4 * k + 2], o[4 * k + 3]));
 }
 
-// Input frame U (tau = t - 2 + U) of an image row of a full item (4 output frames, input frames
-// t-2 .. t+3 all present): it is tap kt = U - o of the output frames o in [max(U-2, 0), min(U, 3)],
-// frame U is written first in the row here (its accumulator released by the epilogue first), and
-// frame U-2 sees its last input. Every burst size, frame, weight tap and barrier is a compile-time
-// constant, so the issuing thread spends no time between bursts on bookkeeping: with run-time
-// bookkeeping between input frames the tensor pipe idled 28% of the time (62.6 cycles per
-// M256 x N112 MMA inside the bursts, 86.7 overall).
-template <int KBPF, int U>
+// Input frame U (tau = t - 2 + U) of an image row of an item of 4 output frames whose input frames
+// t-2+U0 .. t+3 are present (U0 = 0: all of them; U0 = 2: the first quad of a chunk without
+// history, whose frames before t read zeros and are skipped): it is tap kt = U - o of the output
+// frames o in [max(U-2, 0), min(U, 3)], frame o is first written in the row at U = max(o, U0) (its
+// accumulator released by the epilogue first), and frame U-2 sees its last input. Every burst
+// size, frame, weight tap and barrier is a compile-time constant, so the issuing thread spends no
+// time between bursts on bookkeeping: with run-time bookkeeping between input frames the tensor
+// pipe idled 28% of the time (62.6 cycles per M256 x N112 MMA inside the bursts, 86.7 overall).
+template <int KBPF, int U, int U0>
 __device__ __forceinline__ bool head_full_tau(uint32_t tmem_base, uint32_t a_stage0, uint64_t b_desc0, uint64_t* full,
                                               uint64_t* empty, uint64_t* tmem_full, uint64_t* tmem_empty, int& grp,
                                               uint32_t& phase, uint32_t rc, unsigned* err) {
@@ -177,8 +178,11 @@ __device__ __forceinline__ bool head_full_tau(uint32_t tmem_base, uint32_t a_sta
   constexpr int kGroups = kStages / KBPF;
   constexpr int o_lo = U - 2 > 0 ? U - 2 : 0, o_hi = U < kFrames - 1 ? U : kFrames - 1;
   if (!mbar_wait_cluster(&full[grp], phase, err, kDevErrTimeoutMma)) return false;
-  if (U < kFrames) {
-    if (!mbar_wait_cluster(&tmem_empty[U], (rc & 1) ^ 1, err, kDevErrTimeoutMma)) return false;
+#pragma unroll
+  for (int o = o_lo; o <= o_hi; ++o) {
+    if ((o > U0 ? o : U0) == U) {  // first written in this row here
+      if (!mbar_wait_cluster(&tmem_empty[o], (rc & 1) ^ 1, err, kDevErrTimeoutMma)) return false;
+    }
   }
   tc_fence_after();
   const uint64_t a0 = smem_desc_sw128(a_stage0 + (uint32_t)(grp * KBPF * kABytes));
@@ -191,7 +195,7 @@ __device__ __forceinline__ bool head_full_tau(uint32_t tmem_base, uint32_t a_sta
       for (int k = 0; k < 4; ++k)
         mma_bf16_pair(tmem_base + o * kNP, a0 + (uint64_t)kb * (kABytes >> 4) + 2 * k,
                       b_desc0 + (uint64_t)(kt * KBPF + kb) * kBStep + 2 * k, idesc,
-                      (o == U && kb == 0 && k == 0) ? 0u : 1u);
+                      ((o > U0 ? o : U0) == U && kb == 0 && k == 0) ? 0u : 1u);
   }
   mma_commit_pair(&empty[grp], 0x3);
   if (++grp == kGroups) {
@@ -348,24 +352,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const Item it = decode_item(args, item, 0);
       const int nfr = min(kFrames, args.T - it.t);
       const int r1 = row_last(args, it);
-      // Full items (4 output frames, all 6 input frames of a row present) take the compile-time
-      // row below; the first frames of a chunk without history and a short last quad the loop.
+      // Items of 4 output frames with all 6 input frames of a row (full) or with the last 4 (the
+      // first quad of a chunk without history) take the compile-time rows below; a short last
+      // quad takes the loop.
       const bool full_rows = nfr == kFrames && tau_first(args, it) == it.t - 2 && tau_last(args, it) == it.t + 3;
+      const bool first_rows = nfr == kFrames && tau_first(args, it) == it.t && it.t == 0 && !args.has_cache &&
+                              tau_last(args, it) == it.t + 3;
       for (int r = row_first(it); ok && r <= r1; ++r, ++rc) {
+        if (first_rows) {
+          const uint32_t a_stage0 = smem_u32(smem);
+          const uint64_t bd = smem_desc_sw128(b_base);
+          ok = head_full_tau<KBPF, 2, 2>(tmem_base, a_stage0, bd, full, empty, tmem_full, tmem_empty, grp, phase, rc,
+                                         args.err) &&
+               head_full_tau<KBPF, 3, 2>(tmem_base, a_stage0, bd, full, empty, tmem_full, tmem_empty, grp, phase, rc,
+                                         args.err) &&
+               head_full_tau<KBPF, 4, 2>(tmem_base, a_stage0, bd, full, empty, tmem_full, tmem_empty, grp, phase, rc,
+                                         args.err) &&
+               head_full_tau<KBPF, 5, 2>(tmem_base, a_stage0, bd, full, empty, tmem_full, tmem_empty, grp, phase, rc,
+                                         args.err);
+          continue;
+        }
         if (full_rows) {
           const uint32_t a_stage0 = smem_u32(smem);
           const uint64_t bd = smem_desc_sw128(b_base);
-          ok = head_full_tau<KBPF, 0>(tmem_base, a_stage0, bd, full, empty, tmem_full, tmem_empty, grp, phase, rc,
+          ok = head_full_tau<KBPF, 0, 0>(tmem_base, a_stage0, bd, full, empty, tmem_full, tmem_empty, grp, phase, rc,
                                       args.err) &&
-               head_full_tau<KBPF, 1>(tmem_base, a_stage0, bd, full, empty, tmem_full, tmem_empty, grp, phase, rc,
+               head_full_tau<KBPF, 1, 0>(tmem_base, a_stage0, bd, full, empty, tmem_full, tmem_empty, grp, phase, rc,
                                       args.err) &&
-               head_full_tau<KBPF, 2>(tmem_base, a_stage0, bd, full, empty, tmem_full, tmem_empty, grp, phase, rc,
+               head_full_tau<KBPF, 2, 0>(tmem_base, a_stage0, bd, full, empty, tmem_full, tmem_empty, grp, phase, rc,
                                       args.err) &&
-               head_full_tau<KBPF, 3>(tmem_base, a_stage0, bd, full, empty, tmem_full, tmem_empty, grp, phase, rc,
+               head_full_tau<KBPF, 3, 0>(tmem_base, a_stage0, bd, full, empty, tmem_full, tmem_empty, grp, phase, rc,
                                       args.err) &&
-               head_full_tau<KBPF, 4>(tmem_base, a_stage0, bd, full, empty, tmem_full, tmem_empty, grp, phase, rc,
+               head_full_tau<KBPF, 4, 0>(tmem_base, a_stage0, bd, full, empty, tmem_full, tmem_empty, grp, phase, rc,
                                       args.err) &&
-               head_full_tau<KBPF, 5>(tmem_base, a_stage0, bd, full, empty, tmem_full, tmem_empty, grp, phase, rc,
+               head_full_tau<KBPF, 5, 0>(tmem_base, a_stage0, bd, full, empty, tmem_full, tmem_empty, grp, phase, rc,
                                       args.err);
           continue;
         }
