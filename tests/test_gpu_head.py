@@ -32,6 +32,11 @@ def f64(x):
     ((1, 1, 1, 5, 64), False, False, True),         # one row, one frame from the cache
     ((1, 2, 2, 127, 192), True, False, False),      # two rows; width just over one strip
     ((1, 6, 40, 60, 256), False, False, False),     # several row bands
+    # rows issued by compile-time code: the first quad of a chunk without history (input frames
+    # t..t+3) and quads with all six input frames, for 2, 3 and 1 blocks of 64 input channels
+    ((1, 8, 9, 40, 128), True, False, False),
+    ((1, 4, 6, 50, 192), False, False, True),
+    ((1, 8, 5, 20, 64), False, True, True),
 ])
 def test_head_small(wan, shape, bias, residual, cache):
     a, w, b, r, c = make(shape, f"head/{shape}", bias, residual, cache)
