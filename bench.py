@@ -448,7 +448,7 @@ def run_ours(args, rank, world, dev):
         kernels["gn_silu_decode_mid"] = {"ms": gm, "gbs": wl.gn_bytes / gm / 1e6,
                                          "frac_hbm": wl.gn_bytes / gm / 1e6 / pk["hbm_gbs"]}
     gn_total = tot("gn") + tot("c256.coef") + tot("c1024.coef") + tot("c256.cache") + tot("c1024.cache")
-    if gn_total:
+    if gn_total and "gn_silu_decode_mid" in kernels:  # its roofline line is the standalone norm's
         shares["gn_silu"] = gn_total
     dom = max(shares, key=shares.get)
     if dom == "gn_silu":
