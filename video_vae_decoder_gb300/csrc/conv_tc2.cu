@@ -610,18 +610,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
       for (int k = 0; k < 4; ++k) shw[k] = 0.f;
       float sh = 0.f;
       float2 h1 = make_float2(0.f, 0.f), l1 = h1, h2 = h1, l2 = h1;
+      // The TMEM load of the next 16 columns is in flight while this chunk is processed.
+      uint32_t rn[16];
+      __syncwarp();
+      tmem_ld16_issue(taddr, rn);
+      tmem_ld16_wait(rn);
 #pragma unroll 1
       for (int c0 = 0; c0 < ncols; c0 += 16) {
         float v[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(rn[i]);
+        if (c0 + 16 < ncols) {
+          __syncwarp();
+          tmem_ld16_issue(taddr + c0 + 16, rn);
+        }
         uint32_t o[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // the chunk as stored (valid lanes)
-        __syncwarp();
-        tmem_ld16(taddr + c0, v);
         const int col = cbase + c0;
         if (valid && col < args.Cout) {
           if (args.bias) {
+            if (vec8 && col + 16 <= args.Cout) {  // 16 bias values in two 16-byte loads
+              const uint4 b0 = __ldg(reinterpret_cast<const uint4*>(args.bias + col));
+              const uint4 b1 = __ldg(reinterpret_cast<const uint4*>(args.bias + col + 8));
+              const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (col + i < args.Cout) v[i] += __uint_as_float(((uint32_t)args.bias[col + i]) << 16);
+              for (int i = 0; i < 8; ++i) {
+                v[2 * i] += bf16lo_to_f32(bw[i]);
+                v[2 * i + 1] += bf16hi_to_f32(bw[i]);
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                if (col + i < args.Cout) v[i] += __uint_as_float(((uint32_t)args.bias[col + i]) << 16);
+            }
           }
           if (vec8 && col + 16 <= args.Cout) {
             if (rrow) {
@@ -698,6 +718,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
             }
           }
         }
+        if (c0 + 16 < ncols) tmem_ld16_wait(rn);
       }
       // This warp is done with the accumulator: one arrival per warp on the even CTA's barrier.
       tc_fence_before();
