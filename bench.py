@@ -575,13 +575,43 @@ def cpu_threads():
     return os.cpu_count() or 1
 
 
+ONE_THREAD_SHAPE = (1, 1, 8, 312, 256)  # one frame of 8 rows: the smallest unit of the sample
+
+
+def one_thread_sample():
+    """The oracle ResBlock on ONE_THREAD_SHAPE in this process (started with one BLAS thread)."""
+    import numpy as np
+    import oracle
+    from video_vae_decoder_gb300 import synth
+    x = synth.normal_bf16(ONE_THREAD_SHAPE, 0, "bench/c256/x1")
+    p = synth.resblock_params(256, 0, "bench/cpu/block")
+    flops = 2 * conv_flops(*ONE_THREAD_SHAPE, 256)
+    t = time.perf_counter()
+    oracle.resblock(x, p, GROUPS, float(np.float32(EPS)))
+    s = time.perf_counter() - t
+    return {"value": flops / s / 1e12, "unit": "TFLOP/s", "cores": 1,
+            "sample": f"ResBlock on {list(ONE_THREAD_SHAPE)}, {flops / 1e9:.1f} GFLOP of conv work, {s:.2f} s"}
+
+
+def one_thread_baseline():
+    """one_thread_sample() in a fresh interpreter whose BLAS and OpenMP pools have one thread."""
+    import subprocess
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--one-thread-sample"], env=env,
+                       capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return {"unavailable": (r.stderr.strip().splitlines() or ["failed"])[-1][:200]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
 def cpu_baseline(reps=1):
     run, flops = oracle_sample()
     secs = [run() for _ in range(reps)]
     s = min(secs)
     return {"value": flops / s / 1e12, "unit": "TFLOP/s", "cores": cpu_threads(), "kind": "oracle",
             "sample": f"fp64 numpy oracle ResBlock (GN+SiLU, 2 causal convs C=256) on {list(SAMPLE_SHAPE)}, "
-                      f"{flops / 1e9:.0f} GFLOP of conv work, {s:.2f} s"}
+                      f"{flops / 1e9:.0f} GFLOP of conv work, {s:.2f} s",
+            "one_thread": one_thread_baseline()}
 
 
 def run_reference(args):
@@ -614,7 +644,11 @@ def main():
                     help="frames of the head's input (smaller values make a case small enough for ncu --set full)")
     ap.add_argument("--case", default="all", choices=CASES,
                     help="time one part of the step only (profiling captures); the default is the whole step")
+    ap.add_argument("--one-thread-sample", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.one_thread_sample:
+        print(json.dumps(one_thread_sample()))
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
