@@ -81,7 +81,8 @@ def test_time_upsample_decode_size_sampled(wan):
     conv_close(oracle.round_to_bf16(out), ref, "time upsample, sampled")
 
 
-@pytest.mark.parametrize("shape,Cout", [((1, 2, 12, 33, 128), 256), ((2, 3, 9, 17, 256), 512)])
+@pytest.mark.parametrize("shape,Cout", [((1, 2, 12, 33, 128), 256), ((2, 3, 9, 17, 256), 512),
+                                        ((1, 2, 7, 19, 192), 256)])  # an odd count of 64-channel blocks
 def test_conv1x1_matches_oracle(wan, shape, Cout):
     x = synth.normal_bf16(shape, 0, f"c11/{shape}/x")
     w = synth.normal_bf16((Cout, shape[-1]), 0, f"c11/{shape}/w", 0.0, float(np.sqrt(1.0 / shape[-1])))
