@@ -229,15 +229,21 @@ __device__ __forceinline__ void st_reduce8(const float (&vh)[8], const float (&v
 // constants, with each tap's wait, fence and stage release in place. A probe of the tensor pipe
 // (one issuing thread, M256 x N128 pair MMAs) measured that per-tap wait, fence and commit inside
 // a run-time loop cost ~120 cycles of issue per MMA against ~86 in straight-line code.
-template <int kTaps, bool kTall>
+// kGroup > 1 (the 128-channel halves of the last round, whose MMAs are short): the B stages of
+// kGroup consecutive taps land on the first one's barrier and are released together, so one
+// wait and one commit serve kGroup taps.
+template <int kTaps, bool kTall, int kGroup>
 __device__ __forceinline__ bool mma_box(uint32_t d_tmem, uint32_t a_box, uint32_t b_stage, uint64_t* full_b,
                                         uint64_t* empty_b, uint32_t phb, uint32_t idesc, bool first, unsigned* err) {
+  static_assert(kTaps % kGroup == 0, "whole groups of taps");
   const uint64_t a0 = kTall ? smem_desc_sw128(a_box, kTallRows * 128) : smem_desc_sw128(a_box);
   const uint64_t b0 = smem_desc_sw128(b_stage);
 #pragma unroll
   for (int j = 0; j < kTaps; ++j) {
-    if (!mbar_wait_cluster(&full_b[j], phb, err, kDevErrTimeoutMma)) return false;
-    tc_fence_after();
+    if (j % kGroup == 0) {
+      if (!mbar_wait_cluster(&full_b[j], phb, err, kDevErrTimeoutMma)) return false;
+      tc_fence_after();
+    }
     // Tap j: plain box, the next column (1024 bytes on); tall box, rows dh + 10 dw of its
     // 10-row columns (tap j = 3 dh + dw), columns 1280 bytes apart.
     const uint64_t aj = a0 + (kTall ? (uint64_t)(((j % 3) * kTallRows + j / 3) * 8) : (uint64_t)j * kShiftDesc);
@@ -245,7 +251,7 @@ __device__ __forceinline__ bool mma_box(uint32_t d_tmem, uint32_t a_box, uint32_
 #pragma unroll
     for (int k = 0; k < kBlockK / 16; ++k)
       mma_bf16_pair(d_tmem, aj + 2 * k, bj + 2 * k, idesc, (first && j == 0 && k == 0) ? 0u : 1u);
-    mma_commit_pair(&empty_b[j], 0x3);
+    if (j % kGroup == kGroup - 1) mma_commit_pair(&empty_b[j - (kGroup - 1)], 0x3);
   }
   return true;
 }
@@ -347,6 +353,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
     int sa = 0, sb = 0;
     uint32_t pha = 0, phb = 0;
     uint32_t armed_a = 0, parity_a = 0, armed_b = 0, parity_b = 0;  // stages the even CTA armed
+    uint32_t fresh_b = 0xffffffffu;  // B group heads not yet used by a half (see below)
     bool ok = true;
     for (int r = 0; ok; ++r) {
       const int unit = item_of(args, r, cluster, nclusters);
@@ -410,18 +417,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
               sa = 0;
               pha ^= 1;
             }
+            // A half's B stages go in groups of bg (the MMA issuer's mma_box): the group's bytes land
+            // on its first stage's barrier, whose release covers the group. The first time a group's
+            // stages are used this way, the full-item MMAs before may still read any of them: all
+            // their releases are waited for then.
+            const int bg = sub < 0 ? 1 : (taps_per_row % 3 == 0 ? 3 : taps_per_row == 2 ? 2 : 1);
+            int head = sb;
             for (int j = 0; j < taps_per_row; ++j) {
-              if (!mbar_wait_cluster(&empty_b[sb], phb ^ 1, args.err, kDevErrTimeoutProducer)) {
-                ok = false;
-                break;
-              }
-              if (leader) {
-                mbar_arrive_expect_tx(&full_b[sb], b_tx);
-                armed_b |= 1u << sb;
-                parity_b = (parity_b & ~(1u << sb)) | (phb << sb);
+              if (j % bg == 0) {
+                head = sb;
+                const int ng = (bg > 1 && ((fresh_b >> sb) & 1u)) ? bg : 1;
+                for (int g = 0; g < ng; ++g) {
+                  if (!mbar_wait_cluster(&empty_b[sb + g], phb ^ 1, args.err, kDevErrTimeoutProducer)) {
+                    ok = false;
+                    break;
+                  }
+                }
+                if (!ok) break;
+                if (bg > 1) fresh_b &= ~(1u << sb);
+                if (leader) {
+                  mbar_arrive_expect_tx(&full_b[sb], (uint32_t)bg * b_tx);
+                  armed_b |= 1u << sb;
+                  parity_b = (parity_b & ~(1u << sb)) | (phb << sb);
+                }
               }
               const int tap = row * taps_per_row + j;
-              tma_load_3d_pair(smem + kBOffset + sb * kBBytes, wmap, mapa_shared(smem_u32(&full_b[sb]), 0),
+              tma_load_3d_pair(smem + kBOffset + sb * kBBytes, wmap, mapa_shared(smem_u32(&full_b[head]), 0),
                                tap * args.Cin + kb * kBlockK, brow, me.ph, w_policy);
               if (++sb == b_ring) {
                 sb = 0;
@@ -495,16 +516,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
             // Boxes of 9 taps (tall), 3 taps (mode 0) or 2 taps (mode 1, an 8-stage ring) never wrap
             // the B ring: one straight-line burst each. Boxes of 1 tap (modes 2, 3) take the loop.
             static_assert(kBStages == 9, "9 B stages: whole boxes of 3 and 9 taps");
+            // Halves (sub >= 0) take their B stages in groups (mma_box); the producer arms them so.
             if (kNorm && sb == 0) {
-              ok = mma_box<9, true>(d_tmem, a_box, b_base, full_b, empty_b, phb, idesc, first, args.err);
+              ok = sub >= 0 ? mma_box<9, true, 3>(d_tmem, a_box, b_base, full_b, empty_b, phb, idesc, first, args.err)
+                            : mma_box<9, true, 1>(d_tmem, a_box, b_base, full_b, empty_b, phb, idesc, first, args.err);
               sb = kBStages;
             } else if (!kNorm && taps_per_row == 3 && sb % 3 == 0) {
-              ok = mma_box<3, false>(d_tmem, a_box, b_base + sb * kBBytes, full_b + sb, empty_b + sb, phb, idesc, first,
-                                     args.err);
+              const uint32_t bs = b_base + sb * kBBytes;
+              ok = sub >= 0 ? mma_box<3, false, 3>(d_tmem, a_box, bs, full_b + sb, empty_b + sb, phb, idesc, first, args.err)
+                            : mma_box<3, false, 1>(d_tmem, a_box, bs, full_b + sb, empty_b + sb, phb, idesc, first, args.err);
               sb += 3;
             } else if (!kNorm && taps_per_row == 2 && sb % 2 == 0) {
-              ok = mma_box<2, false>(d_tmem, a_box, b_base + sb * kBBytes, full_b + sb, empty_b + sb, phb, idesc, first,
-                                     args.err);
+              const uint32_t bs = b_base + sb * kBBytes;
+              ok = sub >= 0 ? mma_box<2, false, 2>(d_tmem, a_box, bs, full_b + sb, empty_b + sb, phb, idesc, first, args.err)
+                            : mma_box<2, false, 1>(d_tmem, a_box, bs, full_b + sb, empty_b + sb, phb, idesc, first, args.err);
               sb += 2;
             } else {
               const uint64_t a_desc = smem_desc_sw128(a_box);
