@@ -461,9 +461,9 @@ def run_ours(args, rank, world, dev):
                 "frac_of_sustained": kernels[dom]["tflops"] / pk["bf16_tflops_sustained"],
                 "peak_source": f"{pk['source']} {pk_tf_note}"}
     # DRAM bytes (read + write) per launch from one `ncu --set full` capture of the current kernel
-    # build (the conv with the norm prologue, C=256: 172.37 MB read, 76.42 MB written); None for
+    # build (the conv with the norm prologue, C=256: 172.37 MB read, 76.50 MB written); None for
     # kernels without a capture of their current build.
-    traffic = {"conv_c256": 172.368128e6 + 76.424704e6}
+    traffic = {"conv_c256": 172.367104e6 + 76.504064e6}
     roof["traffic"] = traffic.get(roof["kernel"])
     roof["share_of_step"] = shares[dom] / ms
     launches = sum(k for _, k, _ in calls) * args.steps
