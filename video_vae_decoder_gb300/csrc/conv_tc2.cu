@@ -40,7 +40,9 @@
 // took ~160 cycles to issue against 128 to execute (M256 x N256 x K16), whatever N was. Each A box
 // is therefore issued as one straight-line burst (9 taps of a tall box, 3 of a plain mode-0 box,
 // 2 of a phase box, two consecutive 1-tap boxes in modes 2 and 3) whose descriptors differ by
-// constants; the B ring is used 9 or 8 stages deep so that no burst wraps it.
+// constants; the B ring is used 9 or 8 stages deep so that no burst wraps it. The halves of the
+// last round, whose N128 MMAs are short, take their B stages in groups of 3 (2 in phase mode) that
+// land on one barrier and are released by one commit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
