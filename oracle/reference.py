@@ -79,32 +79,34 @@ def silu_f64(z) -> np.ndarray:
     return np.where(z >= 0, z / (1.0 + ez), z * ez / (1.0 + ez))
 
 
-def gn_silu_f64(x, gamma, beta, groups: int, eps: float) -> np.ndarray:
+def gn_silu_f64(x, gamma, beta, groups: int, eps: float, whole_clip: bool = False) -> np.ndarray:
     """silu(group_norm(x)) in fp64, x float [N, T, H, W, C].
 
     Statistics are taken per (n, t, group) over the group's C/groups channels of all H*W pixels
-    of one frame (the per-image GroupNorm of the pages applied to every frame). Two passes:
-    m = sum(x)/L, var = sum((x - m)^2)/L (population variance, divided by the length L as the
-    pages do), z = (x - m)/sqrt(var + eps) * gamma_c + beta_c, output silu(z)."""
+    of one frame (the per-image GroupNorm of the pages applied to every frame); with whole_clip,
+    per (n, group) over all T frames as well (GroupNorm of the whole N C T H W tensor). Two
+    passes: m = sum(x)/L, var = sum((x - m)^2)/L (population variance, divided by the length L
+    as the pages do), z = (x - m)/sqrt(var + eps) * gamma_c + beta_c, output silu(z)."""
     x = np.asarray(x, dtype=np.float64)
     N, T, H, W, C = x.shape
     assert C % groups == 0
     cg = C // groups
-    L = H * W * cg
+    L = H * W * cg * (T if whole_clip else 1)
     xg = x.reshape(N, T, H * W, groups, cg)
-    mean = xg.sum(axis=(2, 4)) / L
-    d = xg - mean[:, :, None, :, None]
-    var = (d * d).sum(axis=(2, 4)) / L
+    axes = (1, 2, 4) if whole_clip else (2, 4)
+    mean = xg.sum(axis=axes, keepdims=True) / L
+    d = xg - mean
+    var = (d * d).sum(axis=axes, keepdims=True) / L
     rstd = 1.0 / np.sqrt(var + float(eps))
     g = np.asarray(gamma, dtype=np.float64).reshape(groups, cg)
     b = np.asarray(beta, dtype=np.float64).reshape(groups, cg)
-    z = d * rstd[:, :, None, :, None] * g + b
+    z = d * rstd * g + b
     return silu_f64(z).reshape(N, T, H, W, C)
 
 
-def gn_silu(x_bits, gamma, beta, groups: int, eps: float) -> np.ndarray:
+def gn_silu(x_bits, gamma, beta, groups: int, eps: float, whole_clip: bool = False) -> np.ndarray:
     """bf16 in, bf16 out: silu(group_norm(x)) rounded once."""
-    return round_to_bf16(gn_silu_f64(bf16_to_f64(x_bits), gamma, beta, groups, eps))
+    return round_to_bf16(gn_silu_f64(bf16_to_f64(x_bits), gamma, beta, groups, eps, whole_clip))
 
 
 # ----------------------------------------------------------------------------------------------

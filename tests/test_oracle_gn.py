@@ -124,3 +124,49 @@ def test_bf16_wrapper_rounds_once():
     back = bf16_to_f64(out)
     step = np.ldexp(1.0, np.frexp(f)[1] - 8)
     assert np.all(np.abs(back - f) <= 0.5 * step + 1e-300)
+
+
+def test_whole_clip_brute_force_tiny():
+    # Whole-clip statistics (per (n, group) over every frame) by element-by-element loops.
+    rng = np.random.default_rng(5)
+    N, T, H, W, C, G = 2, 3, 2, 2, 8, 2
+    x = rng.normal(-0.4, 1.3, size=(N, T, H, W, C))
+    gamma = rng.normal(1, 0.1, size=C)
+    beta = rng.normal(0, 0.1, size=C)
+    eps = 1e-6
+    got = gn_silu_f64(x, gamma, beta, G, eps, whole_clip=True)
+    cg = C // G
+    for n in range(N):
+        for g in range(G):
+            vals = [x[n, t, h, w, c] for t in range(T) for h in range(H) for w in range(W)
+                    for c in range(g * cg, (g + 1) * cg)]
+            m = math.fsum(vals) / len(vals)
+            v = math.fsum((u - m) ** 2 for u in vals) / len(vals)
+            for t in range(T):
+                for h in range(H):
+                    for w in range(W):
+                        for c in range(g * cg, (g + 1) * cg):
+                            z = (x[n, t, h, w, c] - m) / math.sqrt(v + eps) * gamma[c] + beta[c]
+                            s = z / (1 + math.exp(-z))
+                            assert abs(got[n, t, h, w, c] - s) <= 1e-13 * max(1.0, abs(s))
+
+
+def test_whole_clip_matches_torch_group_norm_5d():
+    # PyTorch's group_norm on the N C T H W video (its statistics span the whole clip), fp64.
+    N, T, H, W, C, G = 2, 3, 4, 5, 64, 32
+    x = synth.normal_f32((N, T, H, W, C), 0, "t/gnc/x", 0.5, np.sqrt(2.0)).astype(np.float64)
+    gamma = synth.normal_f32((C,), 0, "t/gnc/g", 1, 0.1)
+    beta = synth.normal_f32((C,), 0, "t/gnc/b", 0, 0.1)
+    ref = torch.nn.functional.group_norm(torch.from_numpy(x).permute(0, 4, 1, 2, 3), G,
+                                         torch.from_numpy(gamma.astype(np.float64)),
+                                         torch.from_numpy(beta.astype(np.float64)), 1e-6)
+    ref = torch.nn.functional.silu(ref).permute(0, 2, 3, 4, 1).numpy()
+    got = gn_silu_f64(x, gamma, beta, G, 1e-6, whole_clip=True)
+    assert np.max(np.abs(got - ref)) < 1e-12
+
+
+def test_whole_clip_of_one_frame_is_per_frame():
+    x = synth.normal_f32((2, 1, 3, 5, 32), 0, "t/gnc1/x").astype(np.float64)
+    g = np.ones(32)
+    b = np.zeros(32)
+    assert np.array_equal(gn_silu_f64(x, g, b, 8, 1e-6, whole_clip=True), gn_silu_f64(x, g, b, 8, 1e-6))
