@@ -90,6 +90,19 @@ wan_status wan_gn_silu(const wan_bf16* x, wan_bf16* y, const float* gamma, const
                        void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * wan_gn_silu_clip: wan_gn_silu with the statistics of each (n, group) taken over the whole clip,
+ * all T frames of n together (the GroupNorm of an N C T H W video as PyTorch computes it), where
+ * wan_gn_silu takes them per frame.
+ *   Same arguments, workspace and limits as wan_gn_silu, and H * W * C / groups < 2^24 (else
+ *   WAN_ERR_UNSUPPORTED_SHAPE).
+ *   Unlike the per-frame norm, the result depends on every frame of the clip, so a video split
+ *   into chunks does not give the bits of one call over the whole video.
+ */
+wan_status wan_gn_silu_clip(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta,
+                            int N, int T, int H, int W, int C, int groups, float eps,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/*
  * wan_gn_silu for callers that cannot allocate device memory. (The pages have no counterpart:
  * this is an interface of this library only.)
  *

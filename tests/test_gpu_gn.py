@@ -82,3 +82,25 @@ def test_gn_very_negative_z(wan):
     assert int(oracle.ulp_distance_bf16(got, ref).max()) <= 1
     tiny = oracle.bf16_to_f64(ref[:, :, 0, 0, :])
     assert np.any((tiny < 0) & (tiny > -1e-30)), "the case must reach the tiny-output range"
+
+
+@pytest.mark.parametrize("shape,groups,mean,std", [
+    ((1, 3, 16, 16, 64), 32, 0.5, np.sqrt(2.0)),     # 2 channels per group
+    ((2, 4, 9, 14, 128), 16, 0.5, np.sqrt(2.0)),     # batch of 2: one clip each
+    ((1, 1, 7, 9, 256), 32, 0.5, np.sqrt(2.0)),      # one frame: the per-frame statistics
+    ((1, 4, 88, 156, 512), 32, 0.5, np.sqrt(2.0)),   # the decode-mid size
+    ((1, 2, 44, 78, 512), 32, 1e4, 64.0),            # large mean, spread of about one ulp
+])
+def test_gn_whole_clip(wan, shape, groups, mean, std):
+    # Statistics per (n, group) over all frames (wan_gn_silu_clip), within one ulp of the oracle.
+    name = f"gnclip/{shape}"
+    x = synth.normal_bf16(shape, 0, f"{name}/x", mean, std)
+    C = shape[-1]
+    g = synth.normal_f32((C,), 0, f"{name}/gamma", 1.0, 0.1)
+    b = synth.normal_f32((C,), 0, f"{name}/beta", 0.0, 0.1)
+    got = bits(wan.wan_gn_silu(to_dev(x), f32_dev(g), f32_dev(b), groups, EPS, whole_clip=True))
+    assert wan.wan_device_status() == 0
+    ref = oracle.gn_silu(x, g, b, groups, EPS, whole_clip=True)
+    assert int(oracle.ulp_distance_bf16(got, ref).max()) <= 1
+    if shape[1] == 1:  # one frame: the same bits as the per-frame call
+        assert np.array_equal(got, bits(wan.wan_gn_silu(to_dev(x), f32_dev(g), f32_dev(b), groups, EPS)))

@@ -25,7 +25,8 @@ WAN_OP_RESBLOCK_SHORTCUT = 6
 STATUS = {0: "WAN_OK", 1: "WAN_ERR_INVALID_ARG", 2: "WAN_ERR_UNSUPPORTED_SHAPE", 3: "WAN_ERR_MISALIGNED",
           4: "WAN_ERR_WORKSPACE", 5: "WAN_ERR_CUDA", 6: "WAN_ERR_TIMEOUT"}
 
-EXPORTS = ("wan_status_string", "wan_workspace_size", "wan_gn_silu", "wan_gn_silu_noalloc", "wan_causal_conv3d",
+EXPORTS = ("wan_status_string", "wan_workspace_size", "wan_gn_silu", "wan_gn_silu_clip", "wan_gn_silu_noalloc",
+           "wan_causal_conv3d",
            "wan_causal_conv3d_gn_stats", "wan_gn_silu_from_stats", "wan_gn_silu_causal_conv3d", "wan_gn_silu_coefficients",
            "wan_causal_conv3d_gn_input", "wan_gn_silu_cache_update", "wan_cache_update",
            "wan_time_upsample", "wan_conv1x1", "wan_fold_bias", "wan_resblock_shortcut",
@@ -64,6 +65,8 @@ def lib() -> ctypes.CDLL:
     L.wan_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
     L.wan_gn_silu.restype = I
     L.wan_gn_silu.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, S, P]
+    L.wan_gn_silu_clip.restype = I
+    L.wan_gn_silu_clip.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P, S, P]
     L.wan_gn_silu_noalloc.restype = I
     L.wan_gn_silu_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P]
     L.wan_causal_conv3d.restype = I
@@ -140,8 +143,9 @@ def _workspace(nbytes: int, device, ws=None):
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
 
-def wan_gn_silu(x, gamma, beta, groups: int, eps: float, y=None, ws=None, stream=None):
-    """y = silu(group_norm(x)) per (n, t, group); x [N, T, H, W, C] bf16."""
+def wan_gn_silu(x, gamma, beta, groups: int, eps: float, y=None, ws=None, stream=None, whole_clip: bool = False):
+    """y = silu(group_norm(x)) per (n, t, group), or per (n, group) over all frames with
+    whole_clip; x [N, T, H, W, C] bf16."""
     _need(x, torch.bfloat16, "x")
     _need(gamma, torch.float32, "gamma")
     _need(beta, torch.float32, "beta")
@@ -150,8 +154,10 @@ def wan_gn_silu(x, gamma, beta, groups: int, eps: float, y=None, ws=None, stream
     _need(y, torch.bfloat16, "y")
     need = wan_workspace_size(WAN_OP_GN_SILU, N, T, H, W, C, 0, groups)
     ws = _workspace(need, x.device, ws)
-    _check(lib().wan_gn_silu(_ptr(x), _ptr(y), _ptr(gamma), _ptr(beta), N, T, H, W, C, groups, eps,
-                             _ptr(ws), need if ws is not None else 0, _stream(stream)), "wan_gn_silu")
+    fn = lib().wan_gn_silu_clip if whole_clip else lib().wan_gn_silu
+    _check(fn(_ptr(x), _ptr(y), _ptr(gamma), _ptr(beta), N, T, H, W, C, groups, eps,
+              _ptr(ws), need if ws is not None else 0, _stream(stream)),
+           "wan_gn_silu_clip" if whole_clip else "wan_gn_silu")
     return y
 
 

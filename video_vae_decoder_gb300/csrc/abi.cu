@@ -183,6 +183,20 @@ wan_status wan_gn_silu(const wan_bf16* x, wan_bf16* y, const float* gamma, const
                                     static_cast<cudaStream_t>(stream)));
 }
 
+wan_status wan_gn_silu_clip(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta, int N, int T,
+                            int H, int W, int C, int groups, float eps, void* ws, size_t ws_bytes, void* stream) {
+  wan_status st = check_gn(x, y, gamma, beta, N, T, H, W, C, groups, eps);
+  if (st != WAN_OK) return st;
+  const size_t bytes = (size_t)N * T * H * W * C * sizeof(wan_bf16);
+  if (overlap(x, bytes, y, bytes)) return WAN_ERR_INVALID_ARG;
+  if ((double)H * W * (C / groups) >= 16777216.0) return WAN_ERR_UNSUPPORTED_SHAPE;  // a frame's count exact in fp32
+  const size_t need = wan_workspace_size(WAN_OP_GN_SILU, N, T, H, W, C, 0, groups);
+  if (!ws || ws_bytes < need) return WAN_ERR_WORKSPACE;
+  if (!aligned16(ws)) return WAN_ERR_MISALIGNED;
+  return cuda_status(gn_silu_launch(x, y, gamma, beta, N, T, H, W, C, groups, eps, ws, sm_count(),
+                                    static_cast<cudaStream_t>(stream), nullptr, 0, true, nullptr, true));
+}
+
 wan_status wan_gn_silu_from_stats(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta, int N,
                                   int T, int H, int W, int C, int groups, float eps, const void* stats,
                                   size_t stats_bytes, void* ws, size_t ws_bytes, void* stream) {

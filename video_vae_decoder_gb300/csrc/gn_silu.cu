@@ -111,6 +111,8 @@ struct GnArgs {
   const float4* ext_rec;
   const float2* ext_meta;
   int ext_q;
+  // Whole-clip statistics: 0 per frame; T: per (n, group) over the T frames of each n (F = N T).
+  int clip_T;
   int apply;  // 0: stop after the coefficients (phase B), the caller applies them elsewhere
   // 1: coefficients in the blocked layout (coef_blocked_index), for readers that take 8
   // consecutive channels per thread with 8 threads side by side (apply == 0 only).
@@ -261,7 +263,78 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
   {
     const int warps = blockDim.x >> 5, warp = tid >> 5, lane = tid & 31;
     // pair p -> CTA p % grid, warp (p / grid) % warps: the few pairs spread over many SMs.
-    for (int pr = warp * gridDim.x + blockIdx.x; pr < a.F * a.G; pr += gridDim.x * warps) {
+    const int pairs = a.clip_T ? (a.F / a.clip_T) * a.G : a.F * a.G;
+    for (int pr = warp * gridDim.x + blockIdx.x; pr < pairs; pr += gridDim.x * warps) {
+      if (a.clip_T) {
+        // Whole clip: each frame's span partials merged as below (fixed order), then moved exactly
+        // from the frame's own shift s_t to frame 0's shift s, in float-float (dl = s_t - s by
+        // TwoSum, n dl by an FMA product error):
+        //   sum (x - s) = S1_t + n dl,  sum (x - s)^2 = S2_t + dl (2 S1_t + n dl),
+        // and added in frame order. n = H W C/G per frame.
+        const int nn = pr / a.G, g = pr - nn * a.G;
+        const int f0 = nn * a.clip_T;
+        const float s = bf16_at(a.x + (size_t)f0 * a.P * a.C + (size_t)g * cg);
+        const float nf = (float)a.P * (float)cg;
+        float h1 = 0.f, l1 = 0.f, h2 = 0.f, l2 = 0.f;
+        for (int t = 0; t < a.clip_T; ++t) {
+          const int f = f0 + t;
+          const float4* src = reinterpret_cast<const float4*>(a.part) + ((size_t)f * a.G + g) * a.spans;
+          float fh1 = 0.f, fl1 = 0.f, fh2 = 0.f, fl2 = 0.f;
+          for (int sp0 = 0; sp0 < a.spans; sp0 += 32 * kFinBatch) {
+            float4 q[kFinBatch];
+#pragma unroll
+            for (int i = 0; i < kFinBatch; ++i) {
+              const int sp = sp0 + lane + 32 * i;
+              q[i] = sp < a.spans ? __ldcg(src + sp) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int i = 0; i < kFinBatch; ++i) {
+              ff_add(fh1, fl1, q[i].x, q[i].y);
+              ff_add(fh2, fl2, q[i].z, q[i].w);
+            }
+          }
+#pragma unroll
+          for (int off = 1; off < 32; off <<= 1) {
+            const float oh1 = __shfl_xor_sync(0xffffffffu, fh1, off), ol1 = __shfl_xor_sync(0xffffffffu, fl1, off);
+            const float oh2 = __shfl_xor_sync(0xffffffffu, fh2, off), ol2 = __shfl_xor_sync(0xffffffffu, fl2, off);
+            ff_add(fh1, fl1, oh1, ol1);
+            ff_add(fh2, fl2, oh2, ol2);
+          }
+          float dh = bf16_at(a.x + (size_t)f * a.P * a.C + (size_t)g * cg), dlo = 0.f;
+          ff_add(dh, dlo, -s, 0.f);  // s_t - s exactly
+          const float ph = nf * dh, pl = fmaf(nf, dh, -ph) + nf * dlo;
+          ff_add(h1, l1, fh1, fl1);
+          ff_add(h1, l1, ph, pl);
+          float uh = 2.f * fh1, ul = 2.f * fl1;  // 2 S1_t + n dl
+          ff_add(uh, ul, ph, pl);
+          const float vh = dh * uh, vl = fmaf(dh, uh, -vh) + fmaf(dh, ul, dlo * uh);
+          ff_add(h2, l2, fh2, fl2);
+          ff_add(h2, l2, vh, vl);
+        }
+        const double s1 = (double)h1 + (double)l1;
+        const double s2 = (double)h2 + (double)l2;
+        const double m1 = s1 * a.inv_len;
+        const double mean = (double)s + m1;
+        const double v = fmax(s2 * a.inv_len - m1 * m1, 0.0) + (double)a.eps;
+        double rstd;
+        if (v > 1e-30 && v < 1e30) {
+          rstd = (double)rsqrtf((float)v);
+          rstd = rstd * (1.5 - 0.5 * v * rstd * rstd);
+          rstd = rstd * (1.5 - 0.5 * v * rstd * rstd);
+        } else {
+          rstd = 1.0 / sqrt(v);
+        }
+        for (int kk = lane; kk < cg; kk += 32) {
+          const int c = g * cg + kk;
+          const double S = (double)a.gamma[c] * rstd;
+          const double B = (double)a.beta[c] - mean * S;
+          const float shi = (float)S, bhi = (float)B;
+          const float4 cf = make_float4(shi, (float)(S - (double)shi), bhi, (float)(B - (double)bhi));
+          for (int t = 0; t < a.clip_T; ++t)
+            a.coef[(size_t)(f0 + t) * a.C + (a.coef_blocked ? coef_blocked_index(c) : c)] = cf;
+        }
+        continue;
+      }
       const int f = pr / a.G, g = pr - f * a.G;
       // Float-float sums (fp64 issue is scarce on this GPU): lane-strided, then a butterfly.
       // The float-float add is commutative bit for bit (TwoSum's error term is unique), so every
@@ -510,7 +583,9 @@ cudaError_t gn_apply_frames_launch(const wan_bf16* x, const float4* coef, wan_bf
 
 cudaError_t gn_silu_launch(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta,
                            int N, int T, int H, int W, int C, int G, float eps, void* ws, int sms,
-                           cudaStream_t stream, const void* st_buf, int st_q, bool apply, float4* coef_out) {
+                           cudaStream_t stream, const void* st_buf, int st_q, bool apply, float4* coef_out,
+                           bool whole_clip) {
+  if (whole_clip && st_buf) return cudaErrorInvalidValue;
   const GnPlan pl = plan(N, T, H, W, C, G);
   char* base = reinterpret_cast<char*>(ws);
   GnArgs a;
@@ -531,7 +606,8 @@ cudaError_t gn_silu_launch(const wan_bf16* x, wan_bf16* y, const float* gamma, c
   a.spans = pl.spans;
   a.items = pl.items;
   a.eps = eps;
-  a.inv_len = 1.0 / ((double)pl.P * (C / G));
+  a.clip_T = whole_clip ? T : 0;
+  a.inv_len = 1.0 / ((double)pl.P * (C / G) * (whole_clip ? T : 1));
   a.ext_rec = reinterpret_cast<const float4*>(st_buf);
   a.ext_meta = st_buf ? reinterpret_cast<const float2*>(a.ext_rec + (size_t)pl.F * G * st_q) : nullptr;
   a.ext_q = st_q;

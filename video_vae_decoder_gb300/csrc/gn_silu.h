@@ -11,7 +11,7 @@ size_t gn_silu_workspace(int N, int T, int H, int W, int C, int groups, int sms)
 cudaError_t gn_silu_launch(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta,
                            int N, int T, int H, int W, int C, int groups, float eps, void* ws,
                            int sms, cudaStream_t stream, const void* st_buf = nullptr, int st_q = 0,
-                           bool apply = true, float4* coef_out = nullptr);
+                           bool apply = true, float4* coef_out = nullptr, bool whole_clip = false);
 // st_buf (optional): statistics of x produced with it, as the CTA-pair conv's epilogue emits them
 // (per frame, group and part q < st_q the float-float sums of d and d^2 of d = x - shift as a
 // float4, then the (shift, count) pairs; part 0 has count > 0); the statistics pass is skipped.
@@ -19,6 +19,8 @@ cudaError_t gn_silu_launch(const wan_bf16* x, wan_bf16* y, const float* gamma, c
 // into the workspace: gn_silu_coef), y is not touched; C % 64 == 0 then, and the coefficients of
 // a frame are in the blocked layout (coef_blocked_index: 64-channel slices, channel 8 j + m at
 // 8 m + j).
+// whole_clip: statistics per (n, group) over all T frames of n instead of per frame (not with
+// st_buf); every frame of n gets the same coefficients.
 // Coefficients (S_hi, S_lo, B_hi, B_lo) per (frame, channel), [N*T][C] float4, inside ws.
 const float4* gn_silu_coef(const void* ws, int N, int T, int H, int W, int C, int groups);
 // The apply pass alone on frames [t_lo, T): y[n, o + t - t_lo] = silu(x[n, t] S + B), y with To
