@@ -95,6 +95,21 @@ def test_gn_rejects_invalid(L):
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers are only passed where no GPU exists")
+def test_gn_clip_rejects_invalid(L):
+    f = L.wan_gn_silu_clip
+
+    def call(x=A, y=A * 3, N=1, T=2, H=4, W=4, C=64, G=32, eps=1e-6, ws=A * 9, wsb=1 << 30):
+        return f(x, y, A * 5, A * 7, N, T, H, W, C, G, ctypes.c_float(eps), ws, wsb, None)
+    assert call(x=None) == 1
+    assert call(T=0) == 1
+    assert call(G=24) == 1                     # does not divide 64
+    assert call(y=A) == 1                      # y overlaps x
+    assert call(x=MIS) == 3
+    assert call(wsb=8) == 4                    # workspace too small
+    assert call(y=1 << 40, H=4096, W=4096, C=64, G=2) == 2  # a frame count of 2^29 is not exact in fp32
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers are only passed where no GPU exists")
 def test_conv_rejects_invalid(L):
     f = L.wan_causal_conv3d
     ok = (A, None, None, A * 5, None, None, A * 9)
