@@ -126,3 +126,19 @@ def test_resblock_shortcut_with_identity_equals_resblock():
     out_s, c1_s, c2_s = oracle.resblock_shortcut(x, p, eye, zero, 32, float(np.float32(1e-6)))
     out, c1, c2 = oracle.resblock(x, p, 32, float(np.float32(1e-6)))
     assert np.array_equal(out_s, out) and np.array_equal(c1_s, c1) and np.array_equal(c2_s, c2)
+
+
+def test_time_upsample_matches_torch_conv3d():
+    # The time conv against PyTorch's conv3d with a (3, 1, 1) kernel on [history; frames], fp64.
+    import torch
+    N, T, H, W, C = 2, 3, 3, 4, 8
+    x = oracle.bf16_to_f64(synth.normal_bf16((N, T, H, W, C), 0, "t/tu/torch/x"))
+    w = oracle.bf16_to_f64(synth.normal_bf16((2 * C, 3, C), 0, "t/tu/torch/w", 0.0, 0.2))
+    b = oracle.bf16_to_f64(synth.normal_bf16((2 * C,), 0, "t/tu/torch/b", 0.0, 0.1))
+    cache = oracle.bf16_to_f64(synth.normal_bf16((N, 2, H, W, C), 0, "t/tu/torch/c"))
+    got = oracle.time_upsample_f64(x, w, b, cache, first=False)
+    p = torch.from_numpy(np.concatenate([cache, x], 1)).permute(0, 4, 1, 2, 3)          # N C T H W
+    z = torch.nn.functional.conv3d(p, torch.from_numpy(w).permute(0, 2, 1)[..., None, None], torch.from_numpy(b))
+    z = z.permute(0, 2, 3, 4, 1).numpy()                                              # [N, T, H, W, 2C]
+    ref = np.stack([z[..., :C], z[..., C:]], 2).reshape(N, 2 * T, H, W, C)            # half i -> frame 2t + i
+    assert np.max(np.abs(got - ref)) < 1e-12

@@ -72,3 +72,17 @@ def test_bf16_phase_weights_brute_force():
                                     s = np.float32(s + wf[co, r, c, ci])
                             want = round_to_bf16(np.array([float(s)]))[0]
                             assert got[2 * a + b, co, u, v, ci] == want
+
+
+def test_definition_matches_torch_nearest_and_conv2d():
+    # The definition against PyTorch: nearest-x2 interpolation, then conv2d with padding 1 (fp64).
+    import torch
+    x = synth.normal_f32((1, 2, 5, 7, 16), 0, "t/up/torch/x").astype(np.float64)
+    w3 = synth.normal_f32((24, 3, 3, 16), 0, "t/up/torch/w", 0.0, 0.2).astype(np.float64)
+    b = synth.normal_f32((24,), 0, "t/up/torch/b", 0.0, 0.1).astype(np.float64)
+    got = upsample_nearest_conv_f64(x, w3, b)
+    xt = torch.from_numpy(x).reshape(2, 5, 7, 16).permute(0, 3, 1, 2)      # frames as images, NCHW
+    up = torch.nn.functional.interpolate(xt, scale_factor=2, mode="nearest")
+    ref = torch.nn.functional.conv2d(up, torch.from_numpy(w3).permute(0, 3, 1, 2), torch.from_numpy(b), padding=1)
+    ref = ref.permute(0, 2, 3, 1).reshape(1, 2, 10, 14, 24).numpy()
+    assert np.max(np.abs(got - ref)) < 1e-12
