@@ -114,9 +114,11 @@ wan_status wan_gn_silu_clip(const wan_bf16* x, wan_bf16* y, const float* gamma, 
  * until the process exits. The call allocates nothing.
  *   - Sizes whose scratch exceeds 4 MiB are refused with WAN_ERR_WORKSPACE (nothing is
  *     launched). The scratch needed is wan_workspace_size(WAN_OP_GN_SILU, ...); for example
- *     [1, 4, 88, 156, 512] with 32 groups needs about 0.7 MiB.
+ *     [1, 4, 88, 156, 512] with 32 groups needs about 0.45 MiB.
  *   - The first call on each device looks up the array's device address (cudaGetSymbolAddress)
- *     with that device current; make that first call before any stream capture.
+ *     with that device current, and keeps it for the life of the process; make that first call
+ *     before any stream capture. After cudaDeviceReset() of a device the kept address is stale:
+ *     do not call this entry point on that device again in the same process.
  *   - All calls share the one array: calls that may overlap on the GPU (on different streams,
  *     or from different threads without ordering) race on it and must be serialised by the
  *     caller. Each call clears, on its stream, the one scratch word that must start at zero
@@ -386,6 +388,24 @@ wan_status wan_resblock_shortcut(const wan_bf16* x, wan_bf16* out, const wan_res
                                  const wan_bf16* w_sc, wan_bf16* cache1, wan_bf16* cache2,
                                  int cache_valid, int N, int T, int H, int W, int Cin, int Cout,
                                  void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Self-test of the failure detection of the bounded device waits (the pages have no counterpart:
+ * the waits and their error word belong to this library). It makes a wait run out on purpose, with
+ * a short bound, so that a caller can check that the kernel gives up, winds down and reports
+ * WAN_ERR_TIMEOUT through wan_device_status(), and that the next calls work normally.
+ *   which = 0  wan_gn_silu's cooperative kernel on the given tensors, with its first grid
+ *              barrier set one arrival beyond what the grid can give: every CTA waits
+ *              `wait_cycles` SM cycles, records the timeout and returns; y is not written.
+ *              The other arguments, their checks and errors are wan_gn_silu's.
+ *   which = 1  one thread waits on an mbarrier (the tensor-core pipelines' wait) that never
+ *              completes; the tensor and workspace arguments are ignored (may be NULL).
+ *   wait_cycles  the bound, 1e3 .. 1e8 SM cycles (at most ~50 ms), else WAN_ERR_INVALID_ARG.
+ * Nothing faults and nothing waits without bound.
+ */
+wan_status wan_selftest_wait_timeout(int which, long long wait_cycles, const wan_bf16* x, wan_bf16* y,
+                                     const float* gamma, const float* beta, int N, int T, int H, int W,
+                                     int C, int groups, float eps, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Synchronises `stream`, then reads and clears the library's device error word on the

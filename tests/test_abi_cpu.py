@@ -227,3 +227,16 @@ def test_gn_noalloc_refuses_sizes_beyond_its_static_scratch(L):
     assert f(x, y, A * 5, A * 7, 1, 64, 176, 312, 256, 32, ctypes.c_float(1e-6), None) == 4
     assert f(None, y, A * 5, A * 7, 1, 4, 8, 8, 256, 32, ctypes.c_float(1e-6), None) == 1
     assert f(MIS, y, A * 5, A * 7, 1, 4, 8, 8, 256, 32, ctypes.c_float(1e-6), None) == 3
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers are only passed where no GPU exists")
+def test_selftest_wait_timeout_rejects_invalid(L):
+    f = L.wan_selftest_wait_timeout
+    eps = ctypes.c_float(1e-6)
+    assert f(2, 100000, None, None, None, None, 0, 0, 0, 0, 0, 0, eps, None, 0, None) == 1        # no such wait
+    assert f(1, 10, None, None, None, None, 0, 0, 0, 0, 0, 0, eps, None, 0, None) == 1            # bound too short
+    assert f(1, 10 ** 9, None, None, None, None, 0, 0, 0, 0, 0, 0, eps, None, 0, None) == 1       # too long
+    # which = 0 checks its tensors as wan_gn_silu does, before anything is enqueued
+    assert f(0, 100000, None, A * 3, A * 5, A * 7, 1, 2, 4, 4, 64, 32, eps, A * 9, 1 << 30, None) == 1
+    assert f(0, 100000, MIS, A * 3, A * 5, A * 7, 1, 2, 4, 4, 64, 32, eps, A * 9, 1 << 30, None) == 3
+    assert f(0, 100000, A, A * 3, A * 5, A * 7, 1, 2, 4, 4, 64, 32, eps, A * 9, 8, None) == 4

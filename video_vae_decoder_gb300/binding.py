@@ -30,7 +30,8 @@ EXPORTS = ("wan_status_string", "wan_workspace_size", "wan_gn_silu", "wan_gn_sil
            "wan_causal_conv3d_gn_stats", "wan_gn_silu_from_stats", "wan_gn_silu_causal_conv3d", "wan_gn_silu_coefficients",
            "wan_causal_conv3d_gn_input", "wan_gn_silu_cache_update", "wan_cache_update",
            "wan_time_upsample", "wan_conv1x1", "wan_fold_bias", "wan_resblock_shortcut",
-           "wan_upsample_phase_weights", "wan_upsample_phase_conv", "wan_resblock", "wan_device_status")
+           "wan_upsample_phase_weights", "wan_upsample_phase_conv", "wan_resblock", "wan_selftest_wait_timeout",
+           "wan_device_status")
 
 
 class WanError(RuntimeError):
@@ -99,6 +100,8 @@ def lib() -> ctypes.CDLL:
     L.wan_upsample_phase_conv.argtypes = [P, P, P, P, I, I, I, I, I, I, P]
     L.wan_resblock.restype = I
     L.wan_resblock.argtypes = [P, P, ctypes.POINTER(ResblockParams), P, P, I, I, I, I, I, I, P, S, P]
+    L.wan_selftest_wait_timeout.restype = I
+    L.wan_selftest_wait_timeout.argtypes = [I, ctypes.c_longlong, P, P, P, P, I, I, I, I, I, I, F, P, S, P]
     L.wan_device_status.restype = I
     L.wan_device_status.argtypes = [P]
     _lib = L
@@ -409,6 +412,25 @@ def wan_resblock_shortcut(x, params: dict, w_sc, cache1, cache2, cache_valid: bo
                                        int(bool(cache_valid)), N, T, H, W, Cin, Cout, _ptr(ws), need, _stream(stream)),
            "wan_resblock_shortcut")
     return out
+
+
+def wan_selftest_wait_timeout(which: int, wait_cycles: int, x=None, gamma=None, beta=None, groups: int = 0,
+                              eps: float = 1e-6, y=None, ws=None, stream=None) -> int:
+    """Makes one bounded device wait run out on purpose (which 0: the GroupNorm kernel's grid
+    barrier on x; which 1: an mbarrier wait); returns the call's status (the timeout itself is
+    reported by wan_device_status)."""
+    if which == 0:
+        _need(x, torch.bfloat16, "x")
+        _need(gamma, torch.float32, "gamma")
+        _need(beta, torch.float32, "beta")
+        N, T, H, W, C = x.shape
+        y = torch.empty_like(x) if y is None else y
+        need = wan_workspace_size(WAN_OP_GN_SILU, N, T, H, W, C, 0, groups)
+        ws = _workspace(need, x.device, ws)
+        return int(lib().wan_selftest_wait_timeout(0, wait_cycles, _ptr(x), _ptr(y), _ptr(gamma), _ptr(beta),
+                                                   N, T, H, W, C, groups, eps, _ptr(ws), need, _stream(stream)))
+    return int(lib().wan_selftest_wait_timeout(which, wait_cycles, None, None, None, None, 0, 0, 0, 0, 0, 0, eps,
+                                               None, 0, _stream(stream)))
 
 
 def wan_device_status(stream=None) -> int:

@@ -6,6 +6,7 @@
 #include <stdint.h>
 #include <string.h>
 
+#include "abi_util.h"
 #include "common.cuh"
 #include "conv_tc.h"
 #include "gn_silu.h"
@@ -25,6 +26,8 @@ int current_device() {
   if (cudaGetDevice(&d) != cudaSuccess) return -1;
   return d;
 }
+
+}  // namespace
 
 int sm_count() {
   static int cached[kMaxDevices] = {0};
@@ -46,6 +49,10 @@ bool overlap(const void* a, size_t abytes, const void* b, size_t bbytes) {
   return a0 < b0 + bbytes && b0 < a0 + abytes;
 }
 
+wan_status cuda_status(cudaError_t e) { return e == cudaSuccess ? WAN_OK : WAN_ERR_CUDA; }
+
+namespace {
+
 size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 bool positive(int a, int b, int c, int d, int e) { return a > 0 && b > 0 && c > 0 && d > 0 && e > 0; }
@@ -56,7 +63,7 @@ bool fits(int N, int T, int H, int W, int C) {
   return px * C < (1LL << 31) && (long long)N * T * 4 < (1LL << 31) && C <= 65536;
 }
 
-wan_status cuda_status(cudaError_t e) { return e == cudaSuccess ? WAN_OK : WAN_ERR_CUDA; }
+}  // namespace
 
 wan_status check_gn(const void* x, const void* y, const float* gamma, const float* beta, int N, int T,
                     int H, int W, int C, int groups, float eps) {
@@ -67,6 +74,8 @@ wan_status check_gn(const void* x, const void* y, const float* gamma, const floa
   if (!aligned16(x) || !aligned16(y) || !aligned16(gamma) || !aligned16(beta)) return WAN_ERR_MISALIGNED;
   return WAN_OK;
 }
+
+namespace {
 
 wan_status check_conv(const void* a, const void* w, const void* y, int N, int T, int H, int W, int Cin,
                       int Cout) {

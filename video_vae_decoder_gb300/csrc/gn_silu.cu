@@ -61,8 +61,9 @@ __device__ __forceinline__ float bf16_at(const wan_bf16* p) { return __uint_as_f
 
 // Grid-wide barrier for a cooperative launch (all CTAs co-resident). `ctr` counts arrivals
 // over the whole call (cleared before the launch); barrier k waits for k * gridDim.x arrivals.
-// The wait is bounded: on timeout it records kDevErrTimeoutGrid and returns false everywhere.
-__device__ bool grid_barrier(unsigned* ctr, unsigned target, unsigned* err, int* s_flag) {
+// The wait is bounded by `limit` SM cycles: on timeout it records kDevErrTimeoutGrid and returns
+// false everywhere.
+__device__ bool grid_barrier(unsigned* ctr, unsigned target, unsigned* err, int* s_flag, long long limit) {
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
@@ -73,7 +74,7 @@ __device__ bool grid_barrier(unsigned* ctr, unsigned target, unsigned* err, int*
       unsigned v;
       asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
       if (v >= target) break;
-      if (clock64() - start > kWaitCycles) {
+      if (clock64() - start > limit) {
         atomicOr(err, kDevErrTimeoutGrid);
         ok = 0;
         break;
@@ -113,6 +114,11 @@ struct GnArgs {
   int ext_q;
   // Whole-clip statistics: 0 per frame; T: per (n, group) over the T frames of each n (F = N T).
   int clip_T;
+  // Bound of the grid-barrier waits in SM cycles, and arrivals the first barrier waits for beyond
+  // the grid's own: kWaitCycles and 0, except in the self-test of the timeout path, which sets a
+  // short bound and a target the grid cannot reach.
+  long long wait_cycles;
+  unsigned bar_extra;
   int apply;  // 0: stop after the coefficients (phase B), the caller applies them elsewhere
   // 1: coefficients in the blocked layout (coef_blocked_index), for readers that take 8
   // consecutive channels per thread with 8 threads side by side (apply == 0 only).
@@ -257,7 +263,7 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
     }
     __syncthreads();  // red is reused by the next item
   }
-  if (!grid_barrier(a.bar, gridDim.x, a.err, &s_flag)) return;
+  if (!grid_barrier(a.bar, gridDim.x + a.bar_extra, a.err, &s_flag, a.wait_cycles)) return;
 
   // ---------------------------------------------------------------- B: finalize per (frame, group)
   {
@@ -425,7 +431,7 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
     }
   }
   if (!a.apply) return;  // coefficients only
-  if (!grid_barrier(a.bar, 2 * gridDim.x, a.err, &s_flag)) return;
+  if (!grid_barrier(a.bar, 2 * gridDim.x, a.err, &s_flag, a.wait_cycles)) return;
 
   // ---------------------------------------------------------------- C: apply, newest spans first
   // The frame's coefficients reach shared memory with one bulk copy per CTA (a per-thread load
@@ -584,7 +590,7 @@ cudaError_t gn_apply_frames_launch(const wan_bf16* x, const float4* coef, wan_bf
 cudaError_t gn_silu_launch(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta,
                            int N, int T, int H, int W, int C, int G, float eps, void* ws, int sms,
                            cudaStream_t stream, const void* st_buf, int st_q, bool apply, float4* coef_out,
-                           bool whole_clip) {
+                           bool whole_clip, long long wait_cycles, unsigned bar_extra) {
   if (whole_clip && st_buf) return cudaErrorInvalidValue;
   const GnPlan pl = plan(N, T, H, W, C, G);
   char* base = reinterpret_cast<char*>(ws);
@@ -611,6 +617,8 @@ cudaError_t gn_silu_launch(const wan_bf16* x, wan_bf16* y, const float* gamma, c
   a.ext_rec = reinterpret_cast<const float4*>(st_buf);
   a.ext_meta = st_buf ? reinterpret_cast<const float2*>(a.ext_rec + (size_t)pl.F * G * st_q) : nullptr;
   a.ext_q = st_q;
+  a.wait_cycles = wait_cycles > 0 ? wait_cycles : kWaitCycles;
+  a.bar_extra = bar_extra;
   a.apply = apply ? 1 : 0;
   a.coef_blocked = (!apply && C % 64 == 0) ? 1 : 0;
   // Persistent grid: every CTA resident at once (the cooperative launch checks it).

@@ -7,11 +7,14 @@
 // the fixed-size array below, a file-scope __device__ array that every GPU which loads this
 // library holds from module load until the process exits.
 //
-// The computation is the one of wan_gn_silu (the same kernels, launched by the same code); only
-// the place of the scratch differs.
+// The computation is the one of wan_gn_silu (the same argument checks, the same kernels launched
+// by the same code); only the place of the scratch differs.
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <stdint.h>
 
+#include "abi_util.h"
 #include "gn_silu.h"
 #include "wan.h"
 
@@ -26,28 +29,20 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 constexpr int kMaxDevices = 64;
 
-// Device address of the scratch on the current device (looked up on the first call made on
-// each device), or nullptr if the lookup failed.
+// Device address of the scratch on the current device, looked up (with that device current) on
+// the first call made on each device and kept for the life of the process; nullptr if the
+// lookup failed.
 void* scratch_address() {
-  static void* cached[kMaxDevices] = {nullptr};
+  static std::atomic<void*> cached[kMaxDevices];
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!cached[dev]) {
-    void* p = nullptr;
+  void* p = cached[dev].load(std::memory_order_acquire);
+  if (!p) {
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    cached[dev] = p;
+    cached[dev].store(p, std::memory_order_release);
   }
-  return cached[dev];
+  return p;
 }
-
-int sm_count_noalloc() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
-  return n;
-}
-
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
 }  // namespace wan
@@ -55,16 +50,11 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 extern "C" wan_status wan_gn_silu_noalloc(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta,
                                           int N, int T, int H, int W, int C, int groups, float eps, void* stream) {
   using namespace wan;
-  if (!x || !y || !gamma || !beta) return WAN_ERR_INVALID_ARG;
-  if (N <= 0 || T <= 0 || H <= 0 || W <= 0 || C <= 0 || groups <= 0 || C % groups != 0) return WAN_ERR_INVALID_ARG;
-  if (!(eps > 0.0f) || eps > 3.0e38f) return WAN_ERR_INVALID_ARG;
-  if (!gn_silu_supported(C, groups) || (long long)H * W * C >= (1LL << 31) || (long long)N * T * 4 >= (1LL << 31))
-    return WAN_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned16(x) || !aligned16(y) || !aligned16(gamma) || !aligned16(beta)) return WAN_ERR_MISALIGNED;
-  const size_t bytes = (size_t)N * T * H * W * C * 2;
-  const uintptr_t xa = reinterpret_cast<uintptr_t>(x), ya = reinterpret_cast<uintptr_t>(y);
-  if (xa < ya + bytes && ya < xa + bytes) return WAN_ERR_INVALID_ARG;
-  const int sms = sm_count_noalloc();
+  wan_status st = check_gn(x, y, gamma, beta, N, T, H, W, C, groups, eps);
+  if (st != WAN_OK) return st;
+  const size_t bytes = (size_t)N * T * H * W * C * sizeof(wan_bf16);
+  if (overlap(x, bytes, y, bytes)) return WAN_ERR_INVALID_ARG;
+  const int sms = sm_count();
   // Sizes whose scratch does not fit the static array are refused, never truncated.
   if (gn_silu_workspace(N, T, H, W, C, groups, sms) > kNoAllocScratchBytes) return WAN_ERR_WORKSPACE;
   void* scratch = scratch_address();
@@ -72,8 +62,6 @@ extern "C" wan_status wan_gn_silu_noalloc(const wan_bf16* x, wan_bf16* y, const 
   // The launcher clears the one scratch word that must start at zero (a grid-barrier counter)
   // at the start of every call; every other word the kernel reads it has written earlier in the
   // same call (the per-span partial sums, then the per-channel coefficients).
-  return gn_silu_launch(x, y, gamma, beta, N, T, H, W, C, groups, eps, scratch, sms,
-                        static_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? WAN_OK
-             : WAN_ERR_CUDA;
+  return cuda_status(gn_silu_launch(x, y, gamma, beta, N, T, H, W, C, groups, eps, scratch, sms,
+                                    static_cast<cudaStream_t>(stream)));
 }
