@@ -18,7 +18,7 @@ import numpy as np
 __all__ = [
     "round_to_bf16", "bf16_to_f64", "bf16_to_f32", "ulp_distance_bf16",
     "silu_f64", "gn_silu_f64", "gn_silu",
-    "causal_conv3d_f64", "causal_conv3d", "conv_at_points_f64",
+    "causal_conv3d_f64", "causal_conv3d", "causal_conv3d_products_f64", "conv_at_points_f64",
     "resblock", "conv1x1", "fold_bias", "resblock_shortcut",
     "time_upsample_f64", "time_upsample",
     "phase_tap_sources", "phase_weights", "phase_weights_f64",
@@ -160,6 +160,42 @@ def causal_conv3d(a_bits, w_bits, bias_bits=None, residual_bits=None, cache_bits
     prev = np.zeros((N, 2, H, W, C), np.uint16) if cache_bits is None else np.asarray(cache_bits)
     cache_out = np.concatenate([prev, np.asarray(a_bits, dtype=np.uint16)], axis=1)[:, -2:]
     return round_to_bf16(y), np.ascontiguousarray(cache_out)
+
+
+def causal_conv3d_products_f64(a, w, bias=None, residual=None, cache=None) -> np.ndarray:
+    """The sum of causal_conv3d_f64 grouped by input frame, for convolutions with few output
+    channels: every frame tau of the padded input P is contracted ONCE with the weights of all 27
+    taps,
+        Q_tau[h, w, (kt, kh, kw), co] = sum_ci P[n, tau, h, w, ci] * w[co, kt, kh, kw, ci],
+    and each output adds its 27 shifted products in the definition's tap order,
+        y[n, t, h, w, co] = sum_{kt, kh, kw} Q_{t+kt}[h+kh, w+kw, (kt, kh, kw), co] (+ bias + residual).
+    The products and the order of the 27-term sum are those of the definition; only the contraction
+    is one matrix product per frame with 27 * Cout columns instead of 27 with Cout."""
+    a = np.asarray(a, dtype=np.float64)
+    w = np.asarray(w, dtype=np.float64)
+    N, T, H, W, Ci = a.shape
+    Co = w.shape[0]
+    P = _padded_input(a, None if cache is None else np.asarray(cache, dtype=np.float64))
+    w_all = w.reshape(Co, 27, Ci).transpose(1, 0, 2).reshape(27 * Co, Ci)  # row tap * Co + co
+    y = np.zeros((N, T, H, W, Co), dtype=np.float64)
+    for n in range(N):
+        Q = {}
+        for tau in range(T + 2):
+            Q[tau] = (P[n, tau].reshape(-1, Ci) @ w_all.T).reshape(H + 2, W + 2, 27, Co)
+            t = tau - 2  # the output frame whose last input frame is tau
+            if t < 0:
+                continue
+            for kt in range(3):
+                for kh in range(3):
+                    for kw in range(3):
+                        tap = (kt * 3 + kh) * 3 + kw
+                        y[n, t] += Q[t + kt][kh:kh + H, kw:kw + W, tap, :]
+            del Q[t]
+    if bias is not None:
+        y += np.asarray(bias, dtype=np.float64)
+    if residual is not None:
+        y += np.asarray(residual, dtype=np.float64)
+    return y
 
 
 def conv_at_points_f64(patches, w, bias=None, residual=None) -> np.ndarray:

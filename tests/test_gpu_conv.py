@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import oracle
-from util import to_dev, bits, conv_close, padded, sample_points
+from util import to_dev, bits, conv_close
 from video_vae_decoder_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -90,29 +90,6 @@ def test_conv_cache_aliasing_in_place(wan):
         torch.cuda.synchronize()
         assert np.array_equal(bits(cd), ref_cache)
         conv_close(bits(y), ref, "alias")
-
-
-def _sampled_check(wan, shape, Cout, name, count=160):
-    rng = np.random.default_rng(0)
-    a, w, b, _, _ = make(shape, Cout, name)
-    got, _ = run(wan, a, w, b, None, None, with_cache_out=False)
-    P = padded(a)
-    N, T, H, W, _ = shape
-    pts = sample_points(rng, N, T, H, W, count)
-    patches = np.stack([P[n, t:t + 3, h:h + 3, x:x + 3] for n, t, h, x in pts])
-    ref = oracle.conv_at_points_f64(patches, oracle.bf16_to_f64(w), oracle.bf16_to_f64(b))
-    sel = np.stack([got[n, t, h, x] for n, t, h, x in pts])
-    conv_close(sel, ref, name)
-
-
-def test_conv_full_size_c256(wan):
-    # One 4-frame chunk of the C=256 decoder stage: [1, 4, 176, 312, 256], sampled outputs.
-    _sampled_check(wan, (1, 4, 176, 312, 256), 256, "conv/cfg4")
-
-
-def test_conv_full_size_c1024(wan):
-    # The widest stage: [1, 4, 44, 78, 1024] -> 1024 channels, sampled outputs.
-    _sampled_check(wan, (1, 4, 44, 78, 1024), 1024, "conv/cfg5")
 
 
 def test_conv_c1024_split_last_round_equals_chunks(wan):

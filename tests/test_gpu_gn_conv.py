@@ -67,10 +67,16 @@ def test_fused_equals_unfused(wan, shape, Cout, history, residual):
         assert same(c_io, c_ref)
 
 
-def test_fused_matches_oracle(wan):
-    shape, Cout = (1, 3, 11, 21, 64), 256
-    x, g, be, w, b, c, _ = inputs(shape, Cout, "gnconv/oracle")
-    c_out = torch.empty((1, 2, 11, 21, 64), dtype=torch.bfloat16, device="cuda")
+@pytest.mark.parametrize("shape,Cout", [
+    ((1, 3, 11, 21, 64), 256),
+    ((1, 2, 9, 17, 256), 256),     # 8 channels per group
+    ((1, 2, 9, 17, 1024), 1024),   # the widest stage's Cin: 16 K blocks per tap, 32 channels per group
+    ((1, 3, 8, 20, 1024), 256),
+])
+def test_fused_matches_oracle(wan, shape, Cout):
+    x, g, be, w, b, c, _ = inputs(shape, Cout, f"gnconv/oracle/{shape}/{Cout}")
+    N, T, H, W, Cin = shape
+    c_out = torch.empty((N, 2, H, W, Cin), dtype=torch.bfloat16, device="cuda")
     y = wan.wan_gn_silu_causal_conv3d(to_dev(x), f32_dev(g), f32_dev(be), G, EPS, to_dev(w), to_dev(b), None,
                                       to_dev(c), c_out)
     torch.cuda.synchronize()

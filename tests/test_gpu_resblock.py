@@ -55,6 +55,19 @@ def test_resblock_medium_with_history(wan):
     check_caches(c1, c2, r1, r2)
 
 
+def test_resblock_c1024_small_with_history_matches_oracle(wan):
+    # The widest stage's ResBlock (Cin = Cout = 1024: the norm applied in the conv's operand prologue
+    # over 16 K blocks per tap) on small frames, two chunks (2 + 2 frames) carrying the caches.
+    x = synth.normal_bf16((1, 4, 12, 20, 1024), 0, "rb/c1024s/x")
+    p = synth.resblock_params(1024, 0, "rb/c1024s")
+    out, c1, c2 = run_chunks(wan, to_dev(x), dev_params(p), 32, 2)
+    r_a, r1, r2 = oracle.resblock(x[:, :2], p, 32, EPS)
+    r_b, r1, r2 = oracle.resblock(x[:, 2:], p, 32, EPS, r1, r2)
+    conv_close(bits(out), np.concatenate([r_a, r_b], 1), "resblock C=1024 chunks")
+    check_caches(c1, c2, r1, r2)
+    assert wan.wan_device_status() == 0
+
+
 def test_resblock_chunked_equals_unchunked_small(wan):
     x = to_dev(synth.normal_bf16((1, 12, 24, 40, 256), 0, "rb/chunk/x"))
     params = dev_params(synth.resblock_params(256, 0, "rb/chunk"))

@@ -2,8 +2,8 @@
 import numpy as np
 import torch
 
-from oracle import (causal_conv3d, causal_conv3d_f64, conv_at_points_f64, resblock,
-                    bf16_to_f64, round_to_bf16)
+from oracle import (causal_conv3d, causal_conv3d_f64, causal_conv3d_products_f64, conv_at_points_f64,
+                    resblock, bf16_to_f64, round_to_bf16)
 from video_vae_decoder_gb300 import synth
 
 
@@ -137,3 +137,58 @@ def test_residual_and_bias_rounded_once():
     y, _ = causal_conv3d(a, w, b, r)
     exact = causal_conv3d_f64(bf16_to_f64(a), bf16_to_f64(w), bf16_to_f64(b), bf16_to_f64(r))
     np.testing.assert_array_equal(y, round_to_bf16(exact))
+
+
+def test_products_form_matches_torch_conv3d():
+    # The frame-grouped form against torch's conv3d (fp64) on the front-padded input: batch 2,
+    # 12 output channels, a cache, bias and residual; asymmetric random weights, so a transposed
+    # tap index (kh <-> kw) or a reversed temporal tap would show.
+    N, T, H, W, Ci, Co = 2, 5, 6, 7, 16, 12
+    a = _rand((N, T, H, W, Ci), 11)
+    cache = _rand((N, 2, H, W, Ci), 12)
+    w = _rand((Co, 3, 3, 3, Ci), 13, 0.1)
+    bias = _rand((Co,), 14)
+    res = _rand((N, T, H, W, Co), 15)
+    ours = causal_conv3d_products_f64(a, w, bias, res, cache)
+    seq = np.concatenate([cache, a], axis=1)
+    xt = torch.from_numpy(seq).permute(0, 4, 1, 2, 3)
+    wt = torch.from_numpy(w).permute(0, 4, 1, 2, 3)
+    ref = torch.nn.functional.conv3d(xt, wt, torch.from_numpy(bias), padding=(0, 1, 1))
+    ref = ref.permute(0, 2, 3, 4, 1).numpy() + res
+    np.testing.assert_allclose(ours, ref, rtol=1e-12, atol=1e-12)
+    # without a cache the history is zero
+    ref0 = torch.nn.functional.conv3d(torch.from_numpy(np.concatenate([np.zeros_like(cache), a], 1))
+                                      .permute(0, 4, 1, 2, 3), wt, padding=(0, 1, 1)).permute(0, 2, 3, 4, 1).numpy()
+    np.testing.assert_allclose(causal_conv3d_products_f64(a, w), ref0, rtol=1e-12, atol=1e-12)
+
+
+def test_products_form_brute_force_points():
+    N, T, H, W, Ci, Co = 1, 3, 4, 5, 3, 2
+    a = _rand((N, T, H, W, Ci), 16)
+    w = _rand((Co, 3, 3, 3, Ci), 17)
+    ours = causal_conv3d_products_f64(a, w)
+    for (t, h, x, co) in [(0, 0, 0, 0), (2, 3, 4, 1), (1, 2, 0, 1), (2, 0, 3, 0)]:
+        s = 0.0
+        for kt in range(3):
+            for kh in range(3):
+                for kw in range(3):
+                    tt, hh, ww = t + kt - 2, h + kh - 1, x + kw - 1
+                    if tt < 0 or not (0 <= hh < H) or not (0 <= ww < W):
+                        continue
+                    for ci in range(Ci):
+                        s += w[co, kt, kh, kw, ci] * a[0, tt, hh, ww, ci]
+        assert abs(ours[0, t, h, x, co] - s) < 1e-12
+
+
+def test_conv_rows_depend_only_on_neighbouring_input_rows():
+    # Output rows [r0, r1) read input rows [r0 - 1, r1 + 1) only (zero padding at the frame's
+    # edge): the conv of that band of the input, minus its first and last row where they are halo,
+    # is those rows of the full output. The full-size tests split a frame into such bands.
+    N, T, H, W, Ci, Co = 1, 3, 11, 6, 8, 5
+    a = _rand((N, T, H, W, Ci), 18)
+    w = _rand((Co, 3, 3, 3, Ci), 19, 0.2)
+    full = causal_conv3d_products_f64(a, w)
+    for r0, r1 in ((0, 4), (4, 8), (8, 11), (3, 4)):
+        lo, hi = max(r0 - 1, 0), min(r1 + 1, H)
+        band = causal_conv3d_products_f64(a[:, :, lo:hi], w)
+        np.testing.assert_allclose(band[:, :, r0 - lo:r0 - lo + (r1 - r0)], full[:, :, r0:r1], rtol=1e-13, atol=1e-13)

@@ -1,18 +1,24 @@
-"""Why the Winograd variant of the spatial 3x3 taps is not built: its accuracy, on the CPU.
+"""The accuracy of Winograd variants of the spatial 3x3 taps, on the CPU: which one may replace the
+direct tcgen05 conv "at equal accuracy".
 
-The decoder pages run their expensive spatial 3x3 convolutions as Winograd F(4x4, 3x3)
-(FastVideo wan22_vae_decode, binding.cpp: `Decoder::conv`, the Winograd weights of `prepare()`),
-and the scope's next row asks for that variant at the direct tcgen05 conv's accuracy. A
-tensor-core kernel has to store the transformed input B^T d B and the transformed weights
-G g G^T in a 16-bit input format before the channel GEMM. This test computes one frame's 3x3
-correlation exactly (fp64) and through the Winograd algorithm of Lavin and Gray ("Fast Algorithms
-for Convolutional Neural Networks", 2016: Y = A^T [(G g G^T) . (B^T d B)] A, with their F(2,3)
-and F(4,3) matrices), rounding only where such a kernel would store (the transformed operands,
-then the bf16 output; the channel sums and both transforms are kept exact, which only favours
-Winograd), and compares both with the conv criterion: relative L2 <= 4e-3 and
-max |err| <= 2^-7 max |ref|.
+The decoder pages run their expensive spatial 3x3 convolutions as Winograd F(4x4, 3x3) with bf16
+operands (FastVideo wan22_vae_decode, binding.cpp: `Decoder::conv`, the Winograd weights of
+`prepare()`). A tensor-core kernel has to store the transformed input B^T d B and the transformed
+weights G g G^T in a 16-bit input format before the channel GEMM. This test computes one frame's
+3x3 correlation exactly (fp64) and through the Winograd algorithm of Lavin and Gray ("Fast
+Algorithms for Convolutional Neural Networks", 2016: Y = A^T [(G g G^T) . (B^T d B)] A, with their
+F(2,3) and F(4,3) matrices), rounding only where such a kernel stores (the transformed operands,
+then the bf16 output; the channel sums and both transforms kept exact), over several seeds and for
+inputs drawn as N(0, 1) and as SiLU of such values (what a ResBlock's conv reads), and compares the
+errors with the direct conv's, whose only rounding is its output's.
+
+Outcome: F(2x2, 3x3) with fp16 operands has the direct conv's error (relative L2 within 5%, max
+within 15%): the variant that is built. F(4x4, 3x3) misses: about 15x the error with bf16 operands
+(the pages' choice), about 2x (L2) and 2-5x (max) with fp16 operands, and a power-of-two scale per
+component changes nothing for fp16 (a floating format; the operands are far from its range limits).
 """
 import numpy as np
+import pytest
 
 import oracle
 from video_vae_decoder_gb300 import synth
@@ -33,9 +39,11 @@ H = W = 16
 C = 256
 
 
-def inputs():
-    d = oracle.bf16_to_f64(synth.normal_bf16((H, W, C), 0, "winograd/d"))
-    g = oracle.bf16_to_f64(synth.normal_bf16((C, 3, 3, C), 0, "winograd/g", 0.0, float(np.sqrt(1.0 / (9 * C)))))
+def inputs(seed=0, act=False):
+    d = oracle.bf16_to_f64(synth.normal_bf16((H, W, C), seed, "winograd/d"))
+    if act:  # SiLU of N(0.3, 1), stored in bf16: the activated input of a ResBlock's conv
+        d = oracle.bf16_to_f64(oracle.round_to_bf16(oracle.silu_f64(d + 0.3)))
+    g = oracle.bf16_to_f64(synth.normal_bf16((C, 3, 3, C), seed, "winograd/g", 0.0, float(np.sqrt(1.0 / (9 * C)))))
     return d, g
 
 
@@ -82,20 +90,35 @@ def test_winograd_matrices_are_exact():
         assert rel < 1e-12 and mx < 1e-12
 
 
-def test_winograd_misses_the_direct_convs_accuracy():
-    d, g = inputs()
+def fp16_scaled(x):
+    """fp16 storage with a power-of-two scale per component (the leading two axes), chosen so that
+    the component's largest magnitude lands in [2^14, 2^15)."""
+    x = np.asarray(x, np.float64)
+    m = np.abs(x).max(axis=tuple(range(2, x.ndim)), keepdims=True)
+    scale = 2.0 ** (14 - np.floor(np.log2(np.maximum(m, 1e-300))))
+    return np.asarray(x * scale, np.float16).astype(np.float64) / scale
+
+
+@pytest.mark.parametrize("seed,act", [(0, False), (1, False), (0, True), (1, True)])
+def test_winograd_variants_against_the_direct_conv(seed, act):
+    d, g = inputs(seed, act)
     ref = direct(d, g)
     bf16 = lambda x: oracle.bf16_to_f64(oracle.round_to_bf16(x))  # noqa: E731
     out = lambda y: oracle.bf16_to_f64(oracle.round_to_bf16(y))   # noqa: E731  (the stored output)
     direct_rel, direct_max = errors(out(ref), ref)
+    f2_fp16 = errors(out(winograd(d, g, BT2, G2, AT2, to_fp16)), ref)
+    f2_bf16 = errors(out(winograd(d, g, BT2, G2, AT2, bf16)), ref)
     f4_bf16 = errors(out(winograd(d, g, BT4, G4, AT4, bf16)), ref)
     f4_fp16 = errors(out(winograd(d, g, BT4, G4, AT4, to_fp16)), ref)
-    f2_bf16 = errors(out(winograd(d, g, BT2, G2, AT2, bf16)), ref)
+    f4_fp16s = errors(out(winograd(d, g, BT4, G4, AT4, fp16_scaled)), ref)
     # the direct conv, whose only rounding is the output's, meets the criterion with room to spare
     assert direct_rel <= REL_L2_MAX / 2 and direct_max <= MAX_ABS_FRAC / 2
-    # F(4x4) with bf16 operands misses it outright (about 15x the direct conv's error)
+    # F(2x2) with fp16 operands: the direct conv's accuracy
+    assert f2_fp16[0] <= 1.05 * direct_rel and f2_fp16[1] <= 1.15 * direct_max
+    # with bf16 operands F(2x2) has 2.4-2.6x the direct conv's L2 error
+    assert f2_bf16[0] > 2 * direct_rel
+    # F(4x4) with bf16 operands misses the criterion outright (about 15x the direct conv's error)
     assert f4_bf16[0] > REL_L2_MAX and f4_bf16[1] > MAX_ABS_FRAC
-    # with fp16 operands, and F(2x2) with bf16 ones, the error is two to three times the direct
-    # conv's: within a few percent of the bound (F(2x2) crosses the L2 bound on this sample)
-    assert f4_fp16[0] > 1.8 * direct_rel and f4_fp16[1] > 2.5 * direct_max
-    assert f2_bf16[0] > 2 * direct_rel and f2_bf16[1] > 1.5 * direct_max
+    # with fp16 operands, scaled per component or not, about twice the L2 and 2-5x the max error
+    for f4 in (f4_fp16, f4_fp16s):
+        assert f4[0] > 1.8 * direct_rel and f4[1] > 1.9 * direct_max

@@ -55,3 +55,52 @@ def sample_points(rng, N, T, H, W, count):
     while len(pts) < count:
         pts.add((int(rng.integers(N)), int(rng.integers(T)), int(rng.integers(H)), int(rng.integers(W))))
     return sorted(pts)
+
+
+class ConvErr:
+    """The conv acceptance criterion over an output compared piece by piece (for outputs whose
+    oracle is computed in bands): relative L2 over the whole output and max |err| against
+    2^-7 * max |ref| over the whole output."""
+
+    def __init__(self, what="", max_abs_frac=MAX_ABS_FRAC):
+        self.what = what
+        self.max_abs_frac = max_abs_frac
+        self.err2 = 0.0
+        self.ref2 = 0.0
+        self.maxerr = 0.0
+        self.maxref = 0.0
+        self.count = 0
+
+    def add(self, got_bits, ref):
+        got = oracle.bf16_to_f64(got_bits)
+        ref = oracle.bf16_to_f64(ref) if ref.dtype == np.uint16 else np.asarray(ref, np.float64)
+        assert got.shape == ref.shape, f"{self.what}: shapes {got.shape} vs {ref.shape}"
+        assert np.all(np.isfinite(got)), f"{self.what}: non-finite output"
+        diff = got - ref
+        self.err2 += float(np.sum(diff * diff))
+        self.ref2 += float(np.sum(ref * ref))
+        if diff.size:
+            self.maxerr = max(self.maxerr, float(np.max(np.abs(diff))))
+            self.maxref = max(self.maxref, float(np.max(np.abs(ref))))
+        self.count += got.size
+
+    def rel_and_max(self):
+        return float(np.sqrt(self.err2) / max(np.sqrt(self.ref2), 1e-300)), self.maxerr
+
+    def check(self):
+        rel = float(np.sqrt(self.err2) / max(np.sqrt(self.ref2), 1e-300))
+        bound = self.max_abs_frac * self.maxref
+        assert rel <= REL_L2_MAX, f"{self.what}: relative L2 {rel:.3e} > {REL_L2_MAX}"
+        assert self.maxerr <= bound, f"{self.what}: max abs err {self.maxerr:.3e} > {bound:.3e}"
+        return rel, self.maxerr
+
+
+def ulp_report(got_bits, ref_bits):
+    """Counts of elements by bf16 ulp distance (0, 1, 2, 3, more) and where the largest is."""
+    d = oracle.ulp_distance_bf16(got_bits, ref_bits)
+    counts = {k: int(np.count_nonzero(d == k)) for k in range(4)}
+    counts[">3"] = int(np.count_nonzero(d > 3))
+    i = int(np.argmax(d))
+    return {"counts": counts, "max_ulp": int(d.flat[i]), "at": tuple(int(v) for v in np.unravel_index(i, d.shape)),
+            "got": float(oracle.bf16_to_f64(np.asarray(got_bits).flat[i])),
+            "ref": float(oracle.bf16_to_f64(np.asarray(ref_bits).flat[i]))}
