@@ -23,6 +23,7 @@ __all__ = [
     "time_upsample_f64", "time_upsample",
     "phase_tap_sources", "phase_weights", "phase_weights_f64",
     "phase_conv_f64", "phase_conv", "upsample_nearest_conv_f64", "upsample_nearest_conv",
+    "f32_to_f16_bits", "f16_to_f64", "winograd_weights", "winograd_weights_f64", "winograd_causal_conv3d_f64",
 ]
 
 _BF16_OVERFLOW = 2.0 ** 128  # |value| rounded to 2^128 or above is out of bf16 range
@@ -408,3 +409,89 @@ def upsample_nearest_conv_f64(x, w3, bias=None) -> np.ndarray:
 def upsample_nearest_conv(x_bits, w3_bits, bias_bits=None) -> np.ndarray:
     return round_to_bf16(upsample_nearest_conv_f64(bf16_to_f64(x_bits), bf16_to_f64(w3_bits),
                                                    None if bias_bits is None else bf16_to_f64(bias_bits)))
+
+
+# ----------------------------------------------------------------------------------------------
+# Winograd F(2x2, 3x3) variant of the spatial taps  (binding.cpp, `prepare()`: the Winograd weights
+# of the up blocks, each component keeping the causal 3-tap temporal conv; `Decoder::conv`: only the
+# spatial 3x3 convolutions use Winograd, the transformed input, one conv per component, and the
+# epilogue that applies the output transform). Transform matrices: Lavin and Gray, "Fast
+# Algorithms for Convolutional Neural Networks" (2016), F(2x2, 3x3):
+#   Y = A^T [ (G g G^T) . (B^T d B) ] A  for a 4x4 input tile d and a 3x3 kernel g.
+# ----------------------------------------------------------------------------------------------
+
+WINO_BT = np.array([[1, 0, -1, 0], [0, 1, 1, 0], [0, -1, 1, 0], [0, 1, 0, -1]], dtype=np.float64)
+WINO_G = np.array([[1, 0, 0], [0.5, 0.5, 0.5], [0.5, -0.5, 0.5], [0, 0, 1]], dtype=np.float64)
+WINO_AT = np.array([[1, 1, 1, 0], [0, 1, -1, -1]], dtype=np.float64)
+
+
+def f32_to_f16_bits(x) -> np.ndarray:
+    """fp32 -> IEEE half bits, round to nearest even (numpy's conversion)."""
+    return np.asarray(x, dtype=np.float32).astype(np.float16).view(np.uint16)
+
+
+def f16_to_f64(bits) -> np.ndarray:
+    return np.asarray(bits, dtype=np.uint16).view(np.float16).astype(np.float64)
+
+
+def winograd_weights(w_bits) -> np.ndarray:
+    """[Cout, 3, 3, 3, Cin] bf16 -> [16, Cout, 3, Cin] fp16 bits: component (x, y) = 4 x + y of
+    G g G^T for every temporal tap kt, i.e. the sum over the spatial taps (r, c) with a non-zero
+    coefficient G[x, r] G[y, c] of coefficient * w[:, kt, r, c, :], formed in fp32 in the pages'
+    order (r outer, c inner, from zero), then rounded once to fp16. The coefficients are 1, 1/2,
+    1/4 with signs, so each product is exact and only the fp32 sums and the final rounding round."""
+    w = bf16_to_f32(w_bits)
+    Co, _, _, _, Ci = w.shape
+    out = np.zeros((16, Co, 3, Ci), dtype=np.float32)
+    for x in range(4):
+        for y in range(4):
+            s = np.zeros((Co, 3, Ci), dtype=np.float32)
+            for r in range(3):
+                for c in range(3):
+                    k = WINO_G[x, r] * WINO_G[y, c]
+                    if k != 0:
+                        s = (s + np.float32(k) * w[:, :, r, c, :]).astype(np.float32)
+            out[4 * x + y] = s
+    return f32_to_f16_bits(out)
+
+
+def winograd_weights_f64(w) -> np.ndarray:
+    """The same transform with exact sums: [16, Cout, 3, Cin] fp64."""
+    w = np.asarray(w, dtype=np.float64)
+    return np.einsum("xr,oarci,yc->xyoai", WINO_G, w, WINO_G).reshape(16, w.shape[0], 3, w.shape[4])
+
+
+def winograd_causal_conv3d_f64(a, u, bias=None, residual=None, cache=None, store=None) -> np.ndarray:
+    """The causal 3x3x3 convolution through F(2x2, 3x3) on the spatial taps, with transformed
+    weights u [16, Cout, 3, Cin] (fp64 values): per frame tau of P = [cache or zeros; a] and 2x2
+    output tile (i, j), the 4x4 input tile d = P[tau, 2i-1 .. 2i+2, 2j-1 .. 2j+2] (zero outside the
+    frame) is transformed to V = B^T d B (then passed through `store`, e.g. a rounding to fp16, if
+    given); per component the products are summed over the temporal taps and channels,
+        M[t, tile, xy, co] = sum_{kt, ci} u[xy, co, kt, ci] V[t + kt, tile, xy, ci],
+    and Y = A^T M A gives the 2x2 outputs, + bias + residual, in fp64."""
+    a = np.asarray(a, dtype=np.float64)
+    u = np.asarray(u, dtype=np.float64)
+    N, T, H, W, Ci = a.shape
+    Co = u.shape[1]
+    Ht, Wt = (H + 1) // 2, (W + 1) // 2
+    cache = np.zeros((N, 2, H, W, Ci)) if cache is None else np.asarray(cache, dtype=np.float64)
+    P = np.concatenate([cache, a], axis=1)
+    Pp = np.zeros((N, T + 2, 2 * Ht + 2, 2 * Wt + 2, Ci))
+    Pp[:, :, 1:H + 1, 1:W + 1] = P
+    # d[n, tau, i, j, r, c, ci] = Pp[n, tau, 2i + r, 2j + c, ci]
+    d = np.stack([np.stack([Pp[:, :, r:r + 2 * Ht:2, c:c + 2 * Wt:2] for c in range(4)], axis=4)
+                  for r in range(4)], axis=4)
+    V = np.einsum("xr,ntijrcz,yc->ntijxyz", WINO_BT, d, WINO_BT)
+    if store is not None:
+        V = store(V)
+    V = V.reshape(N, T + 2, Ht, Wt, 16, Ci)
+    M = np.zeros((N, T, Ht, Wt, 16, Co))
+    for kt in range(3):
+        M += np.einsum("ntijkz,koz->ntijko", V[:, kt:kt + T], u[:, :, kt, :])
+    Y = np.einsum("ax,ntijxyo,by->ntiajbo", WINO_AT, M.reshape(N, T, Ht, Wt, 4, 4, Co), WINO_AT)
+    y = Y.reshape(N, T, 2 * Ht, 2 * Wt, Co)[:, :, :H, :W]
+    if bias is not None:
+        y = y + np.asarray(bias, dtype=np.float64)
+    if residual is not None:
+        y = y + np.asarray(residual, dtype=np.float64)
+    return y
