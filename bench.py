@@ -9,7 +9,9 @@ each op at the decoder shape it is quoted on:
           GN+SiLU, causal conv + residual, cache update, per block)
   up      phase-weight transform [512, 3, 3, 512] and the nearest-x2 + 3x3 upsample as four phase
           convs, [1, 4, 44, 78, 512] -> [1, 4, 88, 156, 512]
-  c1024   two causal ResBlocks at C=1024 on [1, 4, 44, 78, 1024] with carried caches
+  c1024   two causal ResBlocks at C=1024 on [1, 4, 44, 78, 1024] with carried caches, their convs
+          through Winograd F(2x2, 3x3) with fp16 operands (weights transformed once, as the
+          pages' prepare() does; FLOPs counted as the direct conv's)
   head    causal 3x3x3 conv 256 -> 12 channels on [1, 16, 704, 1248, 256] (zero history)
 value = useful convolution FLOPs of the step / step time (TFLOP/s); the per-op times, GN GB/s,
 ResBlock ms and the dominant kernel's roofline fraction are reported beside it. The step's
@@ -52,6 +54,12 @@ def peaks():
 
 def conv_flops(N, T, H, W, Cin, Cout):
     return 2.0 * N * T * H * W * Cout * 27 * Cin
+
+
+def wino_flops(N, T, H, W, Cin, Cout):
+    """Tensor work of the Winograd F(2x2, 3x3) causal conv: per 2x2 output tile, 16 component
+    products over 3 temporal taps x Cin input channels for each output channel."""
+    return 2.0 * N * T * ((H + 1) // 2) * ((W + 1) // 2) * 16 * Cout * 3 * Cin
 
 
 def phase_flops(N, T, H, W, Cin, Cout):
@@ -180,6 +188,12 @@ class Workload:
         self.c4, self.o4, self.k4, self.h4 = stage_bufs(self.x4, 3)
         self.c5, self.o5, self.k5, self.h5 = stage_bufs(self.x5, 2)
         from video_vae_decoder_gb300 import binding as wan
+        # the C=1024 convs' Winograd weights, transformed once per weight set (prepare)
+        self.u5 = [(wan.wan_winograd_weights(p["w1"]), wan.wan_winograd_weights(p["w2"])) for p in self.blocks5]
+        self.wino_ws = torch.empty(wan.wan_workspace_size(wan.WAN_OP_WINOGRAD_CONV3D, *self.x5.shape, self.x5.shape[-1],
+                                                          0), dtype=torch.uint8, device=dev)
+        self.rbw_ws = torch.empty(wan.wan_workspace_size(wan.WAN_OP_RESBLOCK_WINOGRAD, *self.x5.shape, self.x5.shape[-1],
+                                                         GROUPS), dtype=torch.uint8, device=dev)
         need = max(wan.wan_workspace_size(wan.WAN_OP_GN_SILU, *t.shape, 0, GROUPS)
                    for t in (self.gn_x, self.x4, self.x5))
         self.gn_ws = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -209,17 +223,21 @@ class Workload:
             calls.append(("gn", 1, lambda: wan.wan_gn_silu(self.gn_x, self.gn_g, self.gn_b, GROUPS, EPS, self.gn_y,
                                                            self.gn_ws)))
 
-        def stage(tag, x, blocks, caches, outs, coef, h):
-            # Each ResBlock as the calls wan_resblock makes, twice (GroupNorm + SiLU into each conv):
-            # the norm's coefficients (one pass over its input), the conv normalising its operand
-            # tiles as they arrive, then the last two normalised frames into the conv's cache.
+        def stage(tag, x, blocks, caches, outs, coef, h, us=None):
+            # Each ResBlock as the calls wan_resblock (wan_resblock_winograd with `us`) makes, twice
+            # (GroupNorm + SiLU into each conv): the norm's coefficients (one pass over its input),
+            # the conv normalising its operand tiles as they arrive (or its input as it is
+            # transformed), then the last two normalised frames into the conv's cache.
             cur = x
             for i, (p, (c1, c2), out) in enumerate(zip(blocks, caches, outs)):
                 def n1(cur=cur, p=p):
                     wan.wan_gn_silu_coefficients(cur, p["gamma1"], p["beta1"], GROUPS, EPS, coef, self.gn_ws)
 
-                def k1(cur=cur, p=p, c1=c1):
-                    wan.wan_causal_conv3d_gn_input(cur, coef, p["w1"], p["b1"], None, c1, h)
+                def k1(cur=cur, p=p, c1=c1, i=i):
+                    if us is not None:
+                        wan.wan_causal_conv3d_winograd(cur, us[i][0], coef, p["b1"], None, c1, None, h, self.wino_ws)
+                    else:
+                        wan.wan_causal_conv3d_gn_input(cur, coef, p["w1"], p["b1"], None, c1, h)
 
                 def u1(cur=cur, c1=c1):
                     wan.wan_gn_silu_cache_update(cur, coef, c1, c1)
@@ -227,13 +245,17 @@ class Workload:
                 def n2(p=p):
                     wan.wan_gn_silu_coefficients(h, p["gamma2"], p["beta2"], GROUPS, EPS, coef, self.gn_ws)
 
-                def k2(cur=cur, p=p, c2=c2, out=out):
-                    wan.wan_causal_conv3d_gn_input(h, coef, p["w2"], p["b2"], cur, c2, out)
+                def k2(cur=cur, p=p, c2=c2, out=out, i=i):
+                    if us is not None:
+                        wan.wan_causal_conv3d_winograd(h, us[i][1], coef, p["b2"], cur, c2, None, out, self.wino_ws)
+                    else:
+                        wan.wan_causal_conv3d_gn_input(h, coef, p["w2"], p["b2"], cur, c2, out)
 
                 def u2(c2=c2):
                     wan.wan_gn_silu_cache_update(h, coef, c2, c2)
-                calls.extend([(f"{tag}.coef", 1, n1), (f"{tag}.conv", 1, k1), (f"{tag}.cache", 1, u1),
-                              (f"{tag}.coef", 1, n2), (f"{tag}.conv", 1, k2), (f"{tag}.cache", 1, u2)])
+                kc = 3 if us is not None else 1  # Winograd: input transform, component GEMMs, output transform
+                calls.extend([(f"{tag}.coef", 1, n1), (f"{tag}.conv", kc, k1), (f"{tag}.cache", 1, u1),
+                              (f"{tag}.coef", 1, n2), (f"{tag}.conv", kc, k2), (f"{tag}.cache", 1, u2)])
                 cur = out
 
         if want("c256"):
@@ -242,7 +264,7 @@ class Workload:
             calls.append(("up.weights", 1, lambda: wan.wan_upsample_phase_weights(self.w3, self.wp)))
             calls.append(("up.conv", 1, lambda: wan.wan_upsample_phase_conv(self.x3, self.wp, None, self.y3)))
         if want("c1024"):
-            stage("c1024", self.x5, self.blocks5, self.c5, self.o5, self.k5, self.h5)
+            stage("c1024", self.x5, self.blocks5, self.c5, self.o5, self.k5, self.h5, self.u5)
         if want("head"):
             calls.append(("head.conv", 1, lambda: wan.wan_causal_conv3d(self.xh, self.wh, None, None, None, None,
                                                                         self.yh)))
@@ -266,8 +288,8 @@ class Workload:
         wan.wan_upsample_phase_conv(x3, self.wp, None, self.y3)
         wait(3)
         cur = x5
-        for p, (c1, c2), out in zip(self.blocks5, self.c5, self.o5):
-            wan.wan_resblock(cur, p, c1, c2, True, GROUPS, EPS, out, self.rb_ws)
+        for p, (u1, u2), (c1, c2), out in zip(self.blocks5, self.u5, self.c5, self.o5):
+            wan.wan_resblock_winograd(cur, p, u1, u2, c1, c2, True, GROUPS, EPS, out, self.rbw_ws)
             cur = out
         wait(4)
         wan.wan_causal_conv3d(xh, self.wh, None, None, None, None, self.yh)
@@ -436,7 +458,12 @@ def run_ours(args, rank, world, dev):
         hbm_kernel("gn_cache_frames_c256", per_launch("c256.cache"), 2.0 * wl.x4.numel(), tot("c256.cache"))
         kernels["resblock_c256_ms"] = (tot("c256.coef") + tot("c256.conv") + tot("c256.cache")) / 3.0
     if "c1024.conv" in per_tag:
-        tensor_kernel("conv_c1024", per_launch("c1024.conv"), conv_flops(1, 4, 44, 78, 1024, 1024), tot("c1024.conv"))
+        # Winograd F(2x2, 3x3): 16 component products of 3 temporal taps x Cin per 2x2 outputs, the
+        # algorithm's tensor work (its three kernels timed together as one call); the direct
+        # conv's count per call gives the equivalent rate.
+        cm = per_launch("c1024.conv")
+        tensor_kernel("conv_c1024_winograd", cm, wino_flops(1, 4, 44, 78, 1024, 1024), tot("c1024.conv"))
+        kernels["conv_c1024_winograd"]["direct_equivalent_tflops"] = conv_flops(1, 4, 44, 78, 1024, 1024) / cm / 1e9
         hbm_kernel("gn_coef_c1024", per_launch("c1024.coef"), 2.0 * wl.x5.numel(), tot("c1024.coef"))
         hbm_kernel("gn_cache_frames_c1024", per_launch("c1024.cache"), 2.0 * wl.x5.numel(), tot("c1024.cache"))
         kernels["resblock_c1024_ms"] = (tot("c1024.coef") + tot("c1024.conv") + tot("c1024.cache")) / 2.0
@@ -484,9 +511,10 @@ def run_ours(args, rank, world, dev):
         "data": "synthetic (seeded counter-based normals; random-init weights of the decoder shapes)",
         "config": {"workload": "decoder hot path, one steady-state 4-frame chunk: GN+SiLU [1,4,88,156,512]; "
                                "3 causal ResBlocks C=256 [1,4,176,312,256]; nearest-x2+3x3 upsample as 4 phase convs "
-                               "[1,4,44,78,512]->[1,4,88,156,512]; 2 causal ResBlocks C=1024 [1,4,44,78,1024]; "
-                               "head conv 256->12 [1,16,704,1248,256]",
-                   "useful_tflop_per_step": flops / 1e12, "l2": "no flush: the step's working set (~8 GB) exceeds L2",
+                               "[1,4,44,78,512]->[1,4,88,156,512]; 2 causal ResBlocks C=1024 [1,4,44,78,1024] (convs through "
+                               "Winograd F(2x2,3x3), fp16 operands); head conv 256->12 [1,16,704,1248,256]",
+                   "useful_tflop_per_step": flops / 1e12,
+                   "flop_count": "direct-convolution FLOPs (2 M N K) for every conv, the Winograd ones included", "l2": "no flush: the step's working set (~8 GB) exceeds L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kernels": kernels, "wall_s_timed": wall, "clocks": clocks, "gpu_launches": launches, "roofline": roof,
         "rooflines": rooflines,
@@ -551,7 +579,8 @@ def run_e2e(args, wl, dev, flops):
     ms = e0.elapsed_time(e1) / steps
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms, "steps": steps,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "api": "wan_gn_silu, wan_resblock x5, wan_upsample_phase_weights, wan_upsample_phase_conv, "
+            "api": "wan_gn_silu, wan_resblock x3, wan_resblock_winograd x2, wan_upsample_phase_weights, "
+                   "wan_upsample_phase_conv, "
                    "wan_causal_conv3d from pinned host buffers; copies on their own streams, double-buffered "
                    "device inputs (host link measured at ~211 GB/s in, ~193 GB/s out)"}
 

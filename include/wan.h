@@ -39,6 +39,7 @@ extern "C" {
 #endif
 
 typedef uint16_t wan_bf16;
+typedef uint16_t wan_fp16;  /* 16-bit patterns of IEEE half-precision values */
 
 typedef enum wan_status {
   WAN_OK = 0,
@@ -57,7 +58,9 @@ typedef enum wan_op {
   WAN_OP_UPSAMPLE_PHASE_CONV = 3,
   WAN_OP_GN_STATS = 4,           /* statistics buffer of wan_causal_conv3d_gn_stats (Cout, groups) */
   WAN_OP_GN_SILU_CONV3D = 5,     /* wan_gn_silu_causal_conv3d (Cin, Cout, groups) */
-  WAN_OP_RESBLOCK_SHORTCUT = 6   /* wan_resblock_shortcut (Cin, Cout, groups) */
+  WAN_OP_RESBLOCK_SHORTCUT = 6,  /* wan_resblock_shortcut (Cin, Cout, groups) */
+  WAN_OP_WINOGRAD_CONV3D = 7,    /* wan_causal_conv3d_winograd (Cin, Cout) */
+  WAN_OP_RESBLOCK_WINOGRAD = 8   /* wan_resblock_winograd (Cin = C, groups) */
 } wan_op;
 
 /* Human-readable name of a status (static storage, never NULL). */
@@ -388,6 +391,54 @@ wan_status wan_resblock_shortcut(const wan_bf16* x, wan_bf16* out, const wan_res
                                  const wan_bf16* w_sc, wan_bf16* cache1, wan_bf16* cache2,
                                  int cache_valid, int N, int T, int H, int W, int Cin, int Cout,
                                  void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The causal 3x3x3 convolution with its spatial 3x3 taps through Winograd F(2x2, 3x3), fp16
+ * transformed operands, fp32 accumulation, one rounding to bf16.
+ *
+ * Source: binding.cpp, `prepare()` (the Winograd weights G g G^T, each component keeping the
+ * causal 3-tap temporal convolution, summed in fp32) and `Decoder::conv` (only the spatial 3x3
+ * convolutions use Winograd: the padded input transformed once, one convolution per component,
+ * an epilogue applying the output transform with bias and residual). Transforms: Lavin and Gray
+ * (2016), Y = A^T [(G g G^T) . (B^T d B)] A. The pages run F(4x4, 3x3) with bf16 operands; this
+ * library runs F(2x2, 3x3) with fp16 operands, whose error equals the direct conv's (F(4x4) with
+ * bf16 operands has about 15 times it). The result is that of wan_causal_conv3d within the conv
+ * tolerance, not bit for bit; it does not depend on the chunking of the frames.
+ *
+ * wan_winograd_weights: u[xy][co][kt][ci] (component xy = 4 x + y of 16) = fp16 of
+ *     sum over (r, c) with G[x][r] G[y][c] != 0 of G[x][r] G[y][c] w[co][kt][r][c][ci],
+ *   G = [[1,0,0],[1/2,1/2,1/2],[1/2,-1/2,1/2],[0,0,1]], summed in fp32 in the order r outer, c inner,
+ *   from zero (each product is exact), rounded once to nearest even. Once per weight set.
+ *     w  [Cout, 3, 3, 3, Cin] bf16.   u  [16, Cout, 3, Cin] fp16 (16 * Cout * 3 * Cin values).
+ *     Cin % 64 == 0, Cout % 256 == 0.
+ *
+ * wan_causal_conv3d_winograd: y = conv(A; cache_in) + bias + residual with the definition of
+ *   wan_causal_conv3d, where A = silu(a S + B) if `coef` is given (the coefficients of a from
+ *   wan_gn_silu_coefficients: the GroupNorm + SiLU applied to the conv's input as it is
+ *   transformed) and A = a otherwise; cache_in holds already-activated frames (or NULL: zeros).
+ *   cache_out (NULL or [N, 2, H, W, Cin], may equal cache_in) receives the last two frames of
+ *   [cache_in or zeros; A] bit for bit as wan_gn_silu_cache_update / wan_cache_update write them.
+ *     u     from wan_winograd_weights.   Cin % 64 == 0, Cin <= 2048, Cout % 256 == 0.
+ *     ws    >= wan_workspace_size(WAN_OP_WINOGRAD_CONV3D, N, T, H, W, Cin, Cout, 0) bytes: the
+ *           transformed input (16 N (T + 2) ceil(H/2) ceil(W/2) Cin fp16) and the component
+ *           products (16 N T ceil(H/2) ceil(W/2) Cout fp32); may not overlap the tensors.
+ *   Values: the transformed input and weights must fit fp16 (|values| below about 16000 at the
+ *   input, which GroupNorm + SiLU outputs are for any gamma, beta of moderate size).
+ *
+ * wan_resblock_winograd: wan_resblock with both convolutions through Winograd (u1, u2 from
+ *   wan_winograd_weights of w1, w2; p->w1 and p->w2 are not read). Same definition, caches and
+ *   conditions as wan_resblock, and C % 256 == 0.
+ *     ws  >= wan_workspace_size(WAN_OP_RESBLOCK_WINOGRAD, N, T, H, W, C, C, groups) bytes.
+ */
+wan_status wan_winograd_weights(const wan_bf16* w, wan_fp16* u, int Cin, int Cout, void* stream);
+wan_status wan_causal_conv3d_winograd(const wan_bf16* a, const void* coef, const wan_bf16* cache_in,
+                                      wan_bf16* cache_out, const wan_fp16* u, const wan_bf16* bias,
+                                      const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W,
+                                      int Cin, int Cout, void* ws, size_t ws_bytes, void* stream);
+wan_status wan_resblock_winograd(const wan_bf16* x, wan_bf16* out, const wan_resblock_params* p,
+                                 const wan_fp16* u1, const wan_fp16* u2, wan_bf16* cache1, wan_bf16* cache2,
+                                 int cache_valid, int N, int T, int H, int W, int C, void* ws,
+                                 size_t ws_bytes, void* stream);
 
 /*
  * Self-test of the failure detection of the bounded device waits (the pages have no counterpart:

@@ -6,7 +6,7 @@ import pytest
 import torch
 
 import oracle
-from util import to_dev, f32_dev, bits, conv_close
+from util import to_dev, f32_dev, bits, conv_close, cache2_close
 from video_vae_decoder_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -138,7 +138,7 @@ def test_resblock_shortcut_matches_oracle(wan):
     r_b, r1, r2 = oracle.resblock_shortcut(x[:, 3:], p, w_sc, b_sc, 32, EPS, r1, r2)
     conv_close(bits(out), np.concatenate([r_a, r_b], 1), "channel-changing resblock")
     assert int(oracle.ulp_distance_bf16(bits(c1), r1).max()) <= 1
-    conv_close(bits(c2), r2, "cache 2")
+    cache2_close(bits(c2), r2, "cache 2")
 
 
 def test_resblock_shortcut_chunked_equals_unchunked(wan):

@@ -4,9 +4,9 @@ way the GPU runs them (the same chunks, the same carried caches):
   * the C=256 decoder stage: three causal ResBlocks on [1, 12, 176, 312, 256] as three 4-frame
     chunks carrying their six caches (binding.cpp, `Decoder::resnet`; `decode_video`: the history
     crosses passes in the cache);
-  * the widest stage: two causal ResBlocks on [1, 4, 44, 78, 1024] with carried history (the norm
-    applied in the convs' operand prologue at Cin = 1024, the last round of tile pairs split into
-    halves of 128 channels);
+  * the widest stage: two causal ResBlocks on [1, 4, 44, 78, 1024] with carried history, through
+    the direct convs (the norm applied in their operand prologue at Cin = 1024, the last round of
+    tile pairs split into halves of 128 channels) and through the Winograd F(2x2, 3x3) convs;
   * the causal convs alone at both sizes, with history, bias and residual;
   * the 256 -> 12 output head on [1, 16, 704, 1248, 256] (every one of its 168 M outputs; the
     oracle runs in bands of rows, each convolved with its one-row halo).
@@ -22,7 +22,7 @@ import pytest
 import torch
 
 import oracle
-from util import MAX_ABS_FRAC, to_dev, f32_dev, bits, conv_close, ConvErr, ulp_report
+from util import MAX_ABS_FRAC, to_dev, f32_dev, bits, conv_close, cache2_close, ConvErr, ulp_report
 from video_vae_decoder_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -65,7 +65,7 @@ def check_block(got, ref, what):
     rel, mx = conv_close(out, r_out, what)
     print(f"{what}: rel L2 {rel:.3e}, max |err| {mx:.4g}, ulps {ulp_report(out, r_out)['counts']}")
     assert int(oracle.ulp_distance_bf16(c1, r1).max()) <= 1, f"{what}: cache 1"
-    conv_close(c2, r2, f"{what}: cache 2")
+    cache2_close(c2, r2, f"{what}: cache 2")
 
 
 def dev_params(p):
@@ -109,29 +109,44 @@ def test_stage_c256_three_resblocks_in_chunks_matches_oracle(wan):
     check_chain(chained, ref, "C=256 stage")
 
 
+def run_block_winograd(wan, x_bits, p_dev, us, c1_bits, c2_bits, valid):
+    """One wan_resblock_winograd call on host inputs; returns (out, cache1, cache2) as bf16 bits."""
+    c1, c2 = to_dev(c1_bits), to_dev(c2_bits)
+    out = wan.wan_resblock_winograd(to_dev(x_bits), p_dev, us[0], us[1], c1, c2, valid, G, EPS)
+    return bits(out), bits(c1), bits(c2)
+
+
 def test_stage_c1024_two_resblocks_with_history_matches_oracle(wan):
+    # Both GPU paths of the widest stage against one oracle run: the direct convs (norm in the
+    # operand prologue) and the Winograd F(2x2, 3x3) convs (norm in the input transform).
     shape = (1, 4, 44, 78, 1024)
     N, T, H, W, C = shape
     xh = synth.normal_bf16(shape, 0, "stage5/x")
     host_blocks = [synth.resblock_params(C, 0, f"stage5/block{i}") for i in range(2)]
     blocks = [dev_params(p) for p in host_blocks]
+    us = [(wan.wan_winograd_weights(b["w1"]), wan.wan_winograd_weights(b["w2"])) for b in blocks]
     # the history left by a previous chunk (activated values of each conv's input)
     hist = [(synth.normal_bf16((N, 2, H, W, C), 0, f"stage5/block{i}/c1", 0.1, 0.6),
              synth.normal_bf16((N, 2, H, W, C), 0, f"stage5/block{i}/c2", 0.1, 0.6)) for i in range(2)]
-    chained = []
-    h = xh
+    chained, chained_w = [], []
+    h = hw = xh
     for k, (c1, c2) in enumerate(hist):
         h, _, _ = run_block(wan, h, blocks[k], c1, c2, True)
+        hw, _, _ = run_block_winograd(wan, hw, blocks[k], us[k], c1, c2, True)
         chained.append([h])
+        chained_w.append([hw])
     r = xh
     ref = []
     for k, (p, (c1, c2)) in enumerate(zip(host_blocks, hist)):
         got = run_block(wan, r, blocks[k], c1, c2, True)
+        got_w = run_block_winograd(wan, r, blocks[k], us[k], c1, c2, True)
         r, c1o, c2o = oracle.resblock(r, p, G, EPS, c1, c2)
         check_block(got, (r, c1o, c2o), f"C=1024 block {k}")
+        check_block(got_w, (r, c1o, c2o), f"C=1024 Winograd block {k}")
         ref.append([r])
     assert wan.wan_device_status() == 0
     check_chain(chained, ref, "C=1024 stage")
+    check_chain(chained_w, ref, "C=1024 Winograd stage")
 
 
 @pytest.mark.parametrize("shape,Cout", [((1, 4, 176, 312, 256), 256), ((1, 4, 44, 78, 1024), 1024)])

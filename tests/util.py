@@ -36,6 +36,20 @@ def conv_close(got_bits, ref, what=""):
     return rel, mx
 
 
+def cache2_close(got_bits, ref, what=""):
+    """The second conv's cache of a ResBlock holds silu(gn(h)) of the first conv's output h: h's
+    conv error (up to one bf16 step at its largest magnitude), carried through the normalisation,
+    then the norm's own rounding: relative L2 <= 4e-3 and max |err| <= 2 * 2^-7 max |ref|."""
+    got = oracle.bf16_to_f64(got_bits)
+    ref = oracle.bf16_to_f64(ref) if ref.dtype == np.uint16 else np.asarray(ref, np.float64)
+    diff = got - ref
+    rel = float(np.linalg.norm(diff) / max(np.linalg.norm(ref), 1e-300))
+    mx = float(np.max(np.abs(diff))) if diff.size else 0.0
+    assert rel <= REL_L2_MAX, f"{what}: relative L2 {rel:.3e} > {REL_L2_MAX}"
+    assert mx <= 2 * MAX_ABS_FRAC * float(np.max(np.abs(ref))), f"{what}: max abs err {mx:.3e}"
+    return rel, mx
+
+
 def padded(a_bits, cache_bits=None):
     """fp64 padded input P = [cache or zeros; a], zero-padded by 1 in H and W: [N, T+2, H+2, W+2, C]."""
     a = oracle.bf16_to_f64(a_bits)

@@ -21,6 +21,8 @@ WAN_OP_UPSAMPLE_PHASE_CONV = 3
 WAN_OP_GN_STATS = 4
 WAN_OP_GN_SILU_CONV3D = 5
 WAN_OP_RESBLOCK_SHORTCUT = 6
+WAN_OP_WINOGRAD_CONV3D = 7
+WAN_OP_RESBLOCK_WINOGRAD = 8
 
 STATUS = {0: "WAN_OK", 1: "WAN_ERR_INVALID_ARG", 2: "WAN_ERR_UNSUPPORTED_SHAPE", 3: "WAN_ERR_MISALIGNED",
           4: "WAN_ERR_WORKSPACE", 5: "WAN_ERR_CUDA", 6: "WAN_ERR_TIMEOUT"}
@@ -30,7 +32,8 @@ EXPORTS = ("wan_status_string", "wan_workspace_size", "wan_gn_silu", "wan_gn_sil
            "wan_causal_conv3d_gn_stats", "wan_gn_silu_from_stats", "wan_gn_silu_causal_conv3d", "wan_gn_silu_coefficients",
            "wan_causal_conv3d_gn_input", "wan_gn_silu_cache_update", "wan_cache_update",
            "wan_time_upsample", "wan_conv1x1", "wan_fold_bias", "wan_resblock_shortcut",
-           "wan_upsample_phase_weights", "wan_upsample_phase_conv", "wan_resblock", "wan_selftest_wait_timeout",
+           "wan_upsample_phase_weights", "wan_upsample_phase_conv", "wan_resblock", "wan_winograd_weights",
+           "wan_causal_conv3d_winograd", "wan_resblock_winograd", "wan_selftest_wait_timeout",
            "wan_device_status")
 
 
@@ -100,6 +103,12 @@ def lib() -> ctypes.CDLL:
     L.wan_upsample_phase_conv.argtypes = [P, P, P, P, I, I, I, I, I, I, P]
     L.wan_resblock.restype = I
     L.wan_resblock.argtypes = [P, P, ctypes.POINTER(ResblockParams), P, P, I, I, I, I, I, I, P, S, P]
+    L.wan_winograd_weights.restype = I
+    L.wan_winograd_weights.argtypes = [P, P, I, I, P]
+    L.wan_causal_conv3d_winograd.restype = I
+    L.wan_causal_conv3d_winograd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, S, P]
+    L.wan_resblock_winograd.restype = I
+    L.wan_resblock_winograd.argtypes = [P, P, ctypes.POINTER(ResblockParams), P, P, P, P, I, I, I, I, I, I, P, S, P]
     L.wan_selftest_wait_timeout.restype = I
     L.wan_selftest_wait_timeout.argtypes = [I, ctypes.c_longlong, P, P, P, P, I, I, I, I, I, I, F, P, S, P]
     L.wan_device_status.restype = I
@@ -411,6 +420,53 @@ def wan_resblock_shortcut(x, params: dict, w_sc, cache1, cache2, cache_valid: bo
     _check(lib().wan_resblock_shortcut(_ptr(x), _ptr(out), ctypes.byref(p), _ptr(w_sc), _ptr(cache1), _ptr(cache2),
                                        int(bool(cache_valid)), N, T, H, W, Cin, Cout, _ptr(ws), need, _stream(stream)),
            "wan_resblock_shortcut")
+    return out
+
+
+def wan_winograd_weights(w, u=None, stream=None):
+    """u [16, Cout, 3, Cin] fp16 (as torch.float16) = G g G^T per temporal tap of w [Cout, 3, 3, 3, Cin]."""
+    _need(w, torch.bfloat16, "w")
+    Cout, Cin = w.shape[0], w.shape[-1]
+    u = torch.empty((16, Cout, 3, Cin), dtype=torch.float16, device=w.device) if u is None else u
+    _need(u, torch.float16, "u")
+    _check(lib().wan_winograd_weights(_ptr(w), _ptr(u), Cin, Cout, _stream(stream)), "wan_winograd_weights")
+    return u
+
+
+def wan_causal_conv3d_winograd(a, u, coef=None, bias=None, residual=None, cache_in=None, cache_out=None, y=None,
+                               ws=None, stream=None):
+    """The causal conv of a (or of silu(a S + B) with GroupNorm coefficients `coef`) through
+    Winograd F(2x2, 3x3) with weights u from wan_winograd_weights."""
+    for t, n in ((a, "a"), (bias, "bias"), (residual, "residual"), (cache_in, "cache_in"), (cache_out, "cache_out")):
+        _need(t, torch.bfloat16, n)
+    _need(u, torch.float16, "u")
+    N, T, H, W, Cin = a.shape
+    Cout = u.shape[1]
+    y = torch.empty((N, T, H, W, Cout), dtype=torch.bfloat16, device=a.device) if y is None else y
+    _need(y, torch.bfloat16, "y")
+    need = wan_workspace_size(WAN_OP_WINOGRAD_CONV3D, N, T, H, W, Cin, Cout, 0)
+    ws = _workspace(need, a.device, ws)
+    _check(lib().wan_causal_conv3d_winograd(_ptr(a), _ptr(coef), _ptr(cache_in), _ptr(cache_out), _ptr(u), _ptr(bias),
+                                            _ptr(residual), _ptr(y), N, T, H, W, Cin, Cout, _ptr(ws), need,
+                                            _stream(stream)), "wan_causal_conv3d_winograd")
+    return y
+
+
+def wan_resblock_winograd(x, params, u1, u2, cache1, cache2, cache_valid, groups: int, eps: float, out=None, ws=None,
+                          stream=None):
+    """wan_resblock with both convs through Winograd F(2x2, 3x3) (u1, u2 from wan_winograd_weights)."""
+    _need(x, torch.bfloat16, "x")
+    _need(u1, torch.float16, "u1")
+    _need(u2, torch.float16, "u2")
+    N, T, H, W, C = x.shape
+    out = torch.empty_like(x) if out is None else out
+    need = wan_workspace_size(WAN_OP_RESBLOCK_WINOGRAD, N, T, H, W, C, C, groups)
+    ws = _workspace(need, x.device, ws)
+    p = ResblockParams(_ptr(params["gamma1"]), _ptr(params["beta1"]), None, _ptr(params.get("b1")),
+                       _ptr(params["gamma2"]), _ptr(params["beta2"]), None, _ptr(params.get("b2")), groups, eps)
+    _check(lib().wan_resblock_winograd(_ptr(x), _ptr(out), ctypes.byref(p), _ptr(u1), _ptr(u2), _ptr(cache1),
+                                       _ptr(cache2), int(bool(cache_valid)), N, T, H, W, C, _ptr(ws), need,
+                                       _stream(stream)), "wan_resblock_winograd")
     return out
 
 

@@ -11,6 +11,7 @@
 #include "conv_tc.h"
 #include "gn_silu.h"
 #include "wan.h"
+#include "winograd.h"
 
 namespace wan {
 
@@ -167,6 +168,14 @@ size_t wan_workspace_size(wan_op op, int N, int T, int H, int W, int Cin, int Co
     case WAN_OP_GN_SILU_CONV3D:
       if (Cout <= 0 || groups <= 0 || Cin % groups || !gn_silu_supported(Cin, groups)) return 0;
       return gn_conv_workspace(N, T, H, W, Cin, Cout, groups);
+    case WAN_OP_WINOGRAD_CONV3D:
+      if (!wino_supported(Cin, Cout)) return 0;
+      return wino_workspace(N, T, H, W, Cin, Cout);
+    case WAN_OP_RESBLOCK_WINOGRAD: {  // h, the coefficients, the norm's workspace, the conv's
+      if (groups <= 0 || Cin % groups || !gn_silu_supported(Cin, groups) || !wino_supported(Cin, Cin)) return 0;
+      return align256((size_t)N * T * H * W * Cin * sizeof(wan_bf16)) + align256((size_t)N * T * Cin * 16) +
+             align256(gn_silu_workspace(N, T, H, W, Cin, groups, sm_count())) + wino_workspace(N, T, H, W, Cin, Cin);
+    }
     case WAN_OP_RESBLOCK_SHORTCUT: {  // h, the shortcut, then the norm-into-conv workspace
       if (Cout <= 0 || groups <= 0 || Cin % groups || Cout % groups || !gn_silu_supported(Cin, groups) ||
           !gn_silu_supported(Cout, groups))
@@ -566,6 +575,91 @@ wan_status wan_resblock_shortcut(const wan_bf16* x, wan_bf16* out, const wan_res
   if (e == cudaSuccess)
     e = gn_conv(h, p->gamma2, p->beta2, p->groups, p->eps, c2_in, cache2, p->w2, p->b2, skip, out, N, T, H, W, Cout,
                 Cout, gws, err, s);
+  return cuda_status(e);
+}
+
+wan_status wan_winograd_weights(const wan_bf16* w, wan_fp16* u, int Cin, int Cout, void* stream) {
+  if (!w || !u || Cin <= 0 || Cout <= 0) return WAN_ERR_INVALID_ARG;
+  if (!wino_supported(Cin, Cout) || (long long)Cin * Cout * 27 >= (1LL << 40)) return WAN_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(w) || !aligned16(u)) return WAN_ERR_MISALIGNED;
+  if (overlap(w, (size_t)Cout * 27 * Cin * 2, u, (size_t)16 * Cout * 3 * Cin * 2)) return WAN_ERR_INVALID_ARG;
+  return cuda_status(wino_weights_launch(w, u, Cin, Cout, sm_count(), static_cast<cudaStream_t>(stream)));
+}
+
+wan_status wan_causal_conv3d_winograd(const wan_bf16* a, const void* coef, const wan_bf16* cache_in,
+                                      wan_bf16* cache_out, const wan_fp16* u, const wan_bf16* bias,
+                                      const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W, int Cin,
+                                      int Cout, void* ws, size_t ws_bytes, void* stream) {
+  wan_status st = check_conv(a, u, y, N, T, H, W, Cin, Cout);
+  if (st != WAN_OK) return st;
+  if (!wino_supported(Cin, Cout) || Cin > 2048) return WAN_ERR_UNSUPPORTED_SHAPE;
+  if ((coef && !aligned16(coef)) || (cache_in && !aligned16(cache_in)) || (cache_out && !aligned16(cache_out)) ||
+      (bias && !aligned16(bias)) || (residual && !aligned16(residual)))
+    return WAN_ERR_MISALIGNED;
+  const size_t abytes = (size_t)N * T * H * W * Cin * 2, ybytes = (size_t)N * T * H * W * Cout * 2;
+  const size_t cbytes = (size_t)N * 2 * H * W * Cin * 2;
+  const size_t need = wino_workspace(N, T, H, W, Cin, Cout);
+  if (overlap(a, abytes, y, ybytes) || overlap(residual, ybytes, y, ybytes) || overlap(cache_in, cbytes, y, ybytes) ||
+      overlap(cache_out, cbytes, y, ybytes) || overlap(cache_out, cbytes, a, abytes) ||
+      overlap(coef, (size_t)N * T * Cin * 16, y, ybytes) ||
+      (cache_in && cache_out && cache_in != cache_out && overlap(cache_in, cbytes, cache_out, cbytes)) ||
+      overlap(ws, need, a, abytes) || overlap(ws, need, y, ybytes) || overlap(ws, need, u, (size_t)96 * Cout * Cin))
+    return WAN_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < need) return WAN_ERR_WORKSPACE;
+  if (!aligned16(ws)) return WAN_ERR_MISALIGNED;
+  unsigned* err = device_error_word();
+  if (!err) return WAN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float4* cf = static_cast<const float4*>(coef);
+  cudaError_t e = wino_conv_launch(a, cf, cache_in, u, bias, residual, y, N, T, H, W, Cin, Cout, ws, sm_count(), err, s);
+  if (e != cudaSuccess || !cache_out) return cuda_status(e);
+  if (cf) return cuda_status(gn_cache_update(a, cf, cache_in, cache_out, N, T, H, W, Cin, sm_count(), s));
+  return cuda_status(cache_update_launch(a, cache_in, cache_out, N, T, H, W, Cin, sm_count(), s));
+}
+
+wan_status wan_resblock_winograd(const wan_bf16* x, wan_bf16* out, const wan_resblock_params* p, const wan_fp16* u1,
+                                 const wan_fp16* u2, wan_bf16* cache1, wan_bf16* cache2, int cache_valid, int N, int T,
+                                 int H, int W, int C, void* ws, size_t ws_bytes, void* stream) {
+  if (!p || !cache1 || !cache2 || !u1 || !u2) return WAN_ERR_INVALID_ARG;
+  wan_status st = check_gn(x, out, p->gamma1, p->beta1, N, T, H, W, C, p->groups, p->eps);
+  if (st != WAN_OK) return st;
+  st = check_gn(x, out, p->gamma2, p->beta2, N, T, H, W, C, p->groups, p->eps);
+  if (st != WAN_OK) return st;
+  st = check_conv(x, u1, out, N, T, H, W, C, C);
+  if (st != WAN_OK) return st;
+  if (!wino_supported(C, C)) return WAN_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(cache1) || !aligned16(cache2) || !aligned16(u2) || (p->b1 && !aligned16(p->b1)) ||
+      (p->b2 && !aligned16(p->b2)))
+    return WAN_ERR_MISALIGNED;
+  const size_t bytes = (size_t)N * T * H * W * C * 2, cbytes = (size_t)N * 2 * H * W * C * 2;
+  if (overlap(x, bytes, out, bytes) || overlap(cache1, cbytes, cache2, cbytes) || overlap(cache1, cbytes, out, bytes) ||
+      overlap(cache2, cbytes, out, bytes) || overlap(cache1, cbytes, x, bytes) || overlap(cache2, cbytes, x, bytes))
+    return WAN_ERR_INVALID_ARG;
+  const size_t need = wan_workspace_size(WAN_OP_RESBLOCK_WINOGRAD, N, T, H, W, C, C, p->groups);
+  if (!ws || ws_bytes < need) return WAN_ERR_WORKSPACE;
+  if (!aligned16(ws)) return WAN_ERR_MISALIGNED;
+  unsigned* err = device_error_word();
+  if (!err) return WAN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int sms = sm_count();
+  char* base = static_cast<char*>(ws);
+  wan_bf16* h = reinterpret_cast<wan_bf16*>(base);
+  float4* coef = reinterpret_cast<float4*>(base + align256(bytes));
+  void* gws = base + align256(bytes) + align256((size_t)N * T * C * 16);
+  void* wws = static_cast<char*>(gws) + align256(gn_silu_workspace(N, T, H, W, C, p->groups, sms));
+  const wan_bf16* c1_in = cache_valid ? cache1 : nullptr;
+  const wan_bf16* c2_in = cache_valid ? cache2 : nullptr;
+  // Each norm's coefficients, the Winograd conv applying them to its input tiles, then the
+  // norm's last two frames into that conv's cache (after the conv has read the old ones).
+  cudaError_t e = gn_silu_launch(x, nullptr, p->gamma1, p->beta1, N, T, H, W, C, p->groups, p->eps, gws, sms, s,
+                                 nullptr, 0, false, coef);
+  if (e == cudaSuccess) e = wino_conv_launch(x, coef, c1_in, u1, p->b1, nullptr, h, N, T, H, W, C, C, wws, sms, err, s);
+  if (e == cudaSuccess) e = gn_cache_update(x, coef, c1_in, cache1, N, T, H, W, C, sms, s);
+  if (e == cudaSuccess)
+    e = gn_silu_launch(h, nullptr, p->gamma2, p->beta2, N, T, H, W, C, p->groups, p->eps, gws, sms, s, nullptr, 0,
+                       false, coef);
+  if (e == cudaSuccess) e = wino_conv_launch(h, coef, c2_in, u2, p->b2, x, out, N, T, H, W, C, C, wws, sms, err, s);
+  if (e == cudaSuccess) e = gn_cache_update(h, coef, c2_in, cache2, N, T, H, W, C, sms, s);
   return cuda_status(e);
 }
 

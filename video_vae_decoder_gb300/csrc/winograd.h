@@ -1,0 +1,20 @@
+// Internal interface of the Winograd F(2x2, 3x3) causal convolution (winograd.cu).
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "wan.h"
+
+namespace wan {
+// Sizes the variant takes: Cin % 64 == 0, Cout % 256 == 0.
+bool wino_supported(int Cin, int Cout);
+// Workspace of one call: the transformed input V (fp16) and the component products M (fp32).
+size_t wino_workspace(int N, int T, int H, int W, int Cin, int Cout);
+// u[16][Cout][3][Cin] (fp16 bits) = G g G^T of w[Cout][3][3][3][Cin] per temporal tap.
+cudaError_t wino_weights_launch(const wan_bf16* w, uint16_t* u, int Cin, int Cout, int sms, cudaStream_t s);
+// y = causal conv of a (silu(a S + B) with the blocked GroupNorm coefficients `coef`, if given;
+// the cache frames as they are) through F(2x2, 3x3) with the transformed weights u.
+cudaError_t wino_conv_launch(const wan_bf16* a, const float4* coef, const wan_bf16* cache_in, const uint16_t* u,
+                             const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W,
+                             int Cin, int Cout, void* ws, int sms, unsigned* err, cudaStream_t s);
+}  // namespace wan
