@@ -104,6 +104,7 @@ struct GnArgs {
   unsigned* bar;    // grid-barrier arrival counter, zero at launch
   unsigned* err;
   int P, C, G, F, piece_px, spans, items;
+  int cthreads;     // compute threads of a CTA (a multiple of C / 8); one more warp loads x
   float eps;
   double inv_len;   // 1 / (H * W * C / G)
   // Statistics produced elsewhere (null: phase A computes them): per (frame, group, part q < ext_q)
@@ -133,31 +134,47 @@ __device__ __forceinline__ void piece_range(const GnArgs& a, int item, int j, in
   q1 = min(a.P, q0 + a.piece_px);
 }
 
-__global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
+// OR of `v` over the `nthreads` threads (a multiple of 32) that use named barrier `id`; the barrier
+// also orders their shared-memory accesses like __syncthreads does.
+__device__ __forceinline__ bool bar_red_or(int id, int nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+__global__ void __launch_bounds__(kThreads + 32, 2) gn_silu_kernel(const GnArgs a) {
   extern __shared__ __align__(128) uint8_t gsm[];
   uint8_t* slots = gsm;                                                  // kSlots x piece bytes
   const int vpp = a.C >> 3;
-  const int ppi = blockDim.x / vpp;
+  const int ct = a.cthreads;        // compute threads (a multiple of vpp); the last warp loads x
+  const int cw = (ct + 31) >> 5;    // compute warps
+  const int ppi = ct / vpp;
   const int piece_bytes = a.piece_px * a.C * 2;
-  float* red = reinterpret_cast<float*>(gsm + kSlots * piece_bytes);   // [blockDim][slots][4]
-  float* s_shift = red + (size_t)blockDim.x * (a.C / a.G >= 8 ? 1 : 8 / (a.C / a.G)) * 4;  // [G]
+  const int cg = a.C / a.G;
+  const int nslot = cg >= 8 ? 1 : 8 / cg;
+  float* red = reinterpret_cast<float*>(gsm + kSlots * piece_bytes);   // [2][32 cw][nslot][4]
   float4* s_coef = reinterpret_cast<float4*>(slots);  // [C], phase C only (the slots are idle then)
-  __shared__ uint64_t full[kSlots];
+  __shared__ uint64_t full[kSlots], empty[kSlots];
   __shared__ uint64_t cbar;
   __shared__ int s_flag;
   const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
   const int j = tid % vpp;
   const int lp = tid / vpp;
   const bool active = lp < ppi;
-  const int cg = a.C / a.G;
-  const int nslot = cg >= 8 ? 1 : 8 / cg;
   const int cnt = (a.items - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;  // items of this CTA
 
   // The CTA's stream of pieces: its statistics items (item = blockIdx + k * grid), kPiecesPerSpan
-  // pieces each; piece n is piece n % kPiecesPerSpan of the (n / kPiecesPerSpan)-th item.
+  // pieces each; piece n is piece n % kPiecesPerSpan of the (n / kPiecesPerSpan)-th item. One
+  // thread of the last warp issues them into kSlots slots; each compute warp releases a slot on
+  // `empty` once it has read it, so warps never wait for one another while streaming.
   const int cnt_a = a.ext_rec ? 0 : cnt;  // statistics items (none when they come with x)
-  auto issue = [&](int n) {  // thread 0: start loading piece n of the stream
-    if (n >= cnt_a * kPiecesPerSpan) return;
+  auto issue = [&](int n) {
     const int k = n / kPiecesPerSpan, jj = n - k * kPiecesPerSpan;
     uint64_t* bar = &full[n % kSlots];
     int f, q0, q1;
@@ -171,98 +188,145 @@ __global__ void __launch_bounds__(kThreads) gn_silu_kernel(const GnArgs a) {
     }
   };
   if (tid == 0) {
-    for (int s = 0; s < kSlots; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], cw);
+    }
     fence_mbarrier_init();
-    for (int n = 0; n < kSlots; ++n) issue(n);
+    s_flag = 0;
   }
   __syncthreads();
-  int n = 0;  // next piece of the stream to consume
-
-  // Waits for piece n (all threads), bounded; the failure is made CTA-uniform by the caller.
-  auto wait_piece = [&](int nn) -> bool {
-    return mbar_wait(&full[nn % kSlots], (uint32_t)((nn / kSlots) & 1), a.err, kDevErrTimeoutGrid);
-  };
 
   // ---------------------------------------------------------------- A: statistics
-  for (int k = 0; k < cnt_a; ++k) {
-    const int item = blockIdx.x + k * gridDim.x;
-    const int f = item / a.spans, span = item - f * a.spans;
-    // The group shifts (each group's first value in the frame), loaded once per CTA: a
-    // per-thread load would send every thread of the grid to the same few L2 lines.
-    const wan_bf16* xf = a.x + (size_t)f * a.P * a.C;
-    for (int g = tid; g < a.G; g += blockDim.x) s_shift[g] = bf16_at(xf + (size_t)g * cg);
-    __syncthreads();
-    float2 s1h[4], s1l[4], s2h[4], s2l[4], sh[4];
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      s1h[w] = s1l[w] = s2h[w] = s2l[w] = make_float2(0.f, 0.f);
-      const int c0 = 8 * j + 2 * w;
-      sh[w] = active ? make_float2(s_shift[c0 / cg], s_shift[(c0 + 1) / cg]) : make_float2(0.f, 0.f);
+  if (warp == cw) {
+    if (lane == 0) {
+      const int npieces = cnt_a * kPiecesPerSpan;
+      for (int n = 0; n < npieces; ++n) {
+        if (n >= kSlots &&
+            !mbar_wait(&empty[n % kSlots], (uint32_t)(((n / kSlots) - 1) & 1), a.err, kDevErrTimeoutGrid))
+          break;  // the compute warps time out on the pieces that never come
+        issue(n);
+      }
     }
-    for (int pj = 0; pj < kPiecesPerSpan; ++pj, ++n) {
-      const bool ok = wait_piece(n);
-      int f2, q0, q1;
-      piece_range(a, item, pj, f2, q0, q1);
-      if (ok && active) {
-        const uint8_t* src = slots + (n % kSlots) * piece_bytes + (size_t)j * 16;
+  } else if (cnt_a > 0) {
+    int n = 0, buf = 0;  // next piece of the stream; reduction buffer of this item
+    bool fail = false;
+    for (int k = 0; k < cnt_a; ++k) {
+      const int item = blockIdx.x + k * gridDim.x;
+      const int f = item / a.spans, span = item - f * a.spans;
+      // Each group's shift: its first value in the frame (a 2-byte load per group and thread; the
+      // warp's loads fall in the frame's first pixel).
+      const wan_bf16* xf = a.x + (size_t)f * a.P * a.C;
+      float2 s1h[4], s1l[4], s2h[4], s2l[4], sh[4];
 #pragma unroll
-        for (int i = 0; i < kVecPerThread; ++i) {
-          const int pl = lp + i * ppi;
-          if (q0 + pl >= q1) break;
-          const uint4 v = *reinterpret_cast<const uint4*>(src + (size_t)pl * vpp * 16);
-          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+      for (int w = 0; w < 4; ++w) {
+        s1h[w] = s1l[w] = s2h[w] = s2l[w] = make_float2(0.f, 0.f);
+        const int c0 = 8 * j + 2 * w;
+        sh[w] = active ? make_float2(bf16_at(xf + (size_t)(c0 / cg) * cg), bf16_at(xf + (size_t)((c0 + 1) / cg) * cg))
+                       : make_float2(0.f, 0.f);
+      }
+      for (int pj = 0; pj < kPiecesPerSpan; ++pj, ++n) {
+        const bool ok = !fail && mbar_wait(&full[n % kSlots], (uint32_t)((n / kSlots) & 1), a.err, kDevErrTimeoutGrid);
+        fail = !ok;
+        int f2, q0, q1;
+        piece_range(a, item, pj, f2, q0, q1);
+        if (ok && active) {
+          // This thread's run of up to kVecPerThread pixels of the piece: plain fp32 sums of d
+          // and d^2 over the run, then one error-free addition of each run sum into the span's
+          // float-float accumulators. The deviations of nearby bf16 values carry few bits, so a
+          // run sum is exact unless the run mixes values more than about 12 binades apart.
+          const uint8_t* src = slots + (n % kSlots) * piece_bytes + (size_t)j * 16;
+          float2 rs[4], rq[4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) rs[w] = rq[w] = make_float2(0.f, 0.f);
+          if (q1 - q0 == a.piece_px) {  // a whole piece: all loads first
+            uint4 v[kVecPerThread];
+#pragma unroll
+            for (int i = 0; i < kVecPerThread; ++i)
+              v[i] = *reinterpret_cast<const uint4*>(src + (size_t)(lp + i * ppi) * vpp * 16);
+#pragma unroll
+            for (int i = 0; i < kVecPerThread; ++i) {
+              const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                const float2 d = sub2(unpack2(wv[w]), sh[w]);
+                rs[w] = __fadd2_rn(rs[w], d);
+                rq[w] = __ffma2_rn(d, d, rq[w]);
+              }
+            }
+          } else {
+            for (int i = 0; i < kVecPerThread; ++i) {
+              const int pl = lp + i * ppi;
+              if (q0 + pl >= q1) break;
+              const uint4 v = *reinterpret_cast<const uint4*>(src + (size_t)pl * vpp * 16);
+              const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int w = 0; w < 4; ++w) {
+                const float2 d = sub2(unpack2(wv[w]), sh[w]);
+                rs[w] = __fadd2_rn(rs[w], d);
+                rq[w] = __ffma2_rn(d, d, rq[w]);
+              }
+            }
+          }
 #pragma unroll
           for (int w = 0; w < 4; ++w) {
-            const float2 d = sub2(unpack2(wv[w]), sh[w]);
-            two_sum2(s1h[w], s1l[w], d);
-            fast_two_sum2(s2h[w], s2l[w], __fmul2_rn(d, d));
+            two_sum2(s1h[w], s1l[w], rs[w]);
+            fast_two_sum2(s2h[w], s2l[w], rq[w]);
           }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[n % kSlots]);  // this warp is done with the slot
       }
-      if (__syncthreads_or(!ok)) return;  // every thread is done with the slot
-      if (tid == 0) issue(n + kSlots);
-    }
-    (void)span;
-    // Fold this thread's 8 channel partials by group slot (channels of a group are consecutive:
-    // a vector holds 8/cg groups when cg < 8, else part of one group).
-    float* mine = red + (size_t)tid * nslot * 4;
-    for (int q = 0; q < nslot; ++q) {
-      float ah = 0.f, al = 0.f, bh = 0.f, bl = 0.f;
-      if (active) {
+      // Fold this thread's 8 channel partials by group slot (channels of a group are consecutive:
+      // a vector holds 8/cg groups when cg < 8, else part of one group).
+      float* rb = red + (size_t)buf * 32 * cw * nslot * 4;
+      float* mine = rb + (size_t)tid * nslot * 4;
+      for (int q = 0; q < nslot; ++q) {
+        float ah = 0.f, al = 0.f, bh = 0.f, bl = 0.f;
+        if (active) {
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          if ((cg >= 8 ? 0 : c / cg) != q) continue;
-          const int w = c >> 1;
-          ff_add(ah, al, (c & 1) ? s1h[w].y : s1h[w].x, (c & 1) ? s1l[w].y : s1l[w].x);
-          ff_add(bh, bl, (c & 1) ? s2h[w].y : s2h[w].x, (c & 1) ? s2l[w].y : s2l[w].x);
+          for (int c = 0; c < 8; ++c) {
+            if ((cg >= 8 ? 0 : c / cg) != q) continue;
+            const int w = c >> 1;
+            ff_add(ah, al, (c & 1) ? s1h[w].y : s1h[w].x, (c & 1) ? s1l[w].y : s1l[w].x);
+            ff_add(bh, bl, (c & 1) ? s2h[w].y : s2h[w].x, (c & 1) ? s2l[w].y : s2l[w].x);
+          }
         }
+        mine[q * 4 + 0] = ah;
+        mine[q * 4 + 1] = al;
+        mine[q * 4 + 2] = bh;
+        mine[q * 4 + 3] = bl;
       }
-      mine[q * 4 + 0] = ah;
-      mine[q * 4 + 1] = al;
-      mine[q * 4 + 2] = bh;
-      mine[q * 4 + 3] = bl;
+      // The compute warps only (the loading warp runs ahead on its own): the buffer is complete,
+      // and whether any warp gave up a wait, so that all leave the loop at the same item.
+      if (bar_red_or(1, 32 * cw, fail)) {
+        fail = true;
+        break;
+      }
+      // One thread per group adds the contributions of the threads holding it, in thread order.
+      for (int g = tid; g < a.G; g += 32 * cw) {
+        float ah = 0.f, al = 0.f, bh = 0.f, bl = 0.f;
+        const int c_first = g * cg, c_last = c_first + cg - 1;
+        const int q = cg >= 8 ? 0 : (c_first % 8) / cg;
+        for (int jj = c_first / 8; jj <= c_last / 8; ++jj)
+          for (int l = 0; l < ppi; ++l) {
+            const float* r = rb + ((size_t)(l * vpp + jj) * nslot + q) * 4;
+            ff_add(ah, al, r[0], r[1]);
+            ff_add(bh, bl, r[2], r[3]);
+          }
+        GnPartial out;
+        out.s1_hi = ah;
+        out.s1_lo = al;
+        out.s2_hi = bh;
+        out.s2_lo = bl;
+        a.part[((size_t)f * a.G + g) * a.spans + span] = out;
+      }
+      buf ^= 1;  // the next item fills the other buffer; the one after waits for its barrier
     }
-    __syncthreads();
-    // One thread per group adds the contributions of the threads holding it, in thread order.
-    for (int g = tid; g < a.G; g += blockDim.x) {
-      float ah = 0.f, al = 0.f, bh = 0.f, bl = 0.f;
-      const int c_first = g * cg, c_last = c_first + cg - 1;
-      const int q = cg >= 8 ? 0 : (c_first % 8) / cg;
-      for (int jj = c_first / 8; jj <= c_last / 8; ++jj)
-        for (int l = 0; l < ppi; ++l) {
-          const float* r = red + ((size_t)(l * vpp + jj) * nslot + q) * 4;
-          ff_add(ah, al, r[0], r[1]);
-          ff_add(bh, bl, r[2], r[3]);
-        }
-      GnPartial out;
-      out.s1_hi = ah;
-      out.s1_lo = al;
-      out.s2_hi = bh;
-      out.s2_lo = bl;
-      a.part[((size_t)f * a.G + g) * a.spans + span] = out;
-    }
-    __syncthreads();  // red is reused by the next item
+    if (fail && tid == 0) s_flag = 1;
   }
+  __syncthreads();
+  if (s_flag) return;  // a wait gave up (recorded in the error word): no coefficients from here
   if (!grid_barrier(a.bar, gridDim.x + a.bar_extra, a.err, &s_flag, a.wait_cycles)) return;
 
   // ---------------------------------------------------------------- B: finalize per (frame, group)
@@ -525,7 +589,7 @@ __global__ void __launch_bounds__(kThreads) gn_apply_frames_kernel(const wan_bf1
 }
 
 struct GnPlan {
-  int P, F, threads, ppi, piece_px, spans, items, slots;
+  int P, F, threads, ppi, piece_px, spans, items, slots, launch_threads;
   size_t part_bytes, coef_bytes, smem;
 };
 
@@ -546,8 +610,9 @@ GnPlan plan(int N, int T, int H, int W, int C, int G) {
   pl.slots = cg >= 8 ? 1 : 8 / cg;
   pl.part_bytes = (size_t)pl.F * pl.spans * G * sizeof(GnPartial);
   pl.coef_bytes = (size_t)pl.F * C * sizeof(float4);
-  pl.smem = (size_t)kSlots * pl.piece_px * C * 2 + (size_t)pl.threads * pl.slots * 4 * sizeof(float) +
-            (size_t)G * sizeof(float);
+  const int cw = (pl.threads + 31) / 32;
+  pl.smem = (size_t)kSlots * pl.piece_px * C * 2 + (size_t)2 * 32 * cw * pl.slots * 4 * sizeof(float);
+  pl.launch_threads = 32 * (cw + 1);
   return pl;
 }
 
@@ -611,6 +676,7 @@ cudaError_t gn_silu_launch(const wan_bf16* x, wan_bf16* y, const float* gamma, c
   a.piece_px = pl.piece_px;
   a.spans = pl.spans;
   a.items = pl.items;
+  a.cthreads = pl.threads;
   a.eps = eps;
   a.clip_T = whole_clip ? T : 0;
   a.inv_len = 1.0 / ((double)pl.P * (C / G) * (whole_clip ? T : 1));
@@ -625,7 +691,7 @@ cudaError_t gn_silu_launch(const wan_bf16* x, wan_bf16* y, const float* gamma, c
   cudaError_t e = cudaFuncSetAttribute(gn_silu_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pl.smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gn_silu_kernel, pl.threads, pl.smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, gn_silu_kernel, pl.launch_threads, pl.smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   // As many CTAs as fit, then evened out so every CTA gets the same number of items (a CTA with
@@ -639,7 +705,7 @@ cudaError_t gn_silu_launch(const wan_bf16* x, wan_bf16* y, const float* gamma, c
   e = cudaMemsetAsync(a.bar, 0, sizeof(unsigned), stream);
   if (e != cudaSuccess) return e;
   void* args[] = {&a};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(gn_silu_kernel), dim3(grid), dim3(pl.threads),
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(gn_silu_kernel), dim3(grid), dim3(pl.launch_threads),
                                      args, pl.smem, stream);
 }
 

@@ -115,6 +115,7 @@ constexpr int kInTileCols = 40;
 constexpr int kInRows = 2 * kInTileRows + 2;  // pixel rows staged per CTA
 constexpr int kInCols = 2 * kInTileCols + 2;  // pixel columns staged per CTA (at most)
 constexpr int kInThreads = 256;
+constexpr int kInLoads = 4;  // 16-byte loads in flight per thread while staging
 
 struct WinoInArgs {
   const wan_bf16* x;       // [N, T, H, W, C]
@@ -150,15 +151,25 @@ __global__ void __launch_bounds__(kInThreads) wino_input_kernel(const WinoInArgs
     GnCoef8 k8;
     if (cf) k8 = gn_coef8_blocked(cf + v);  // the blocked layout: channels 8 v .. 8 v + 7 of the slice
     const int npx = kInRows * cols;
-    for (int p = threadIdx.x >> 3; p < npx; p += kInThreads / 8) {
-      const int r = p / cols, c = p - r * cols;
-      const int hh = 2 * i0 - 1 + r, ww = 2 * j0 - 1 + c;
-      uint4 q = make_uint4(0, 0, 0, 0);
-      if (src && hh >= 0 && hh < a.H && ww >= 0 && ww < a.W) {
-        q = __ldg(reinterpret_cast<const uint4*>(src + ((size_t)hh * a.W + ww) * a.C + slice * 64) + v);
-        if (cf) q = gn_silu8(q, k8);
+    constexpr int kStride = kInThreads / 8;
+    for (int p0 = threadIdx.x >> 3; p0 < npx; p0 += kStride * kInLoads) {
+      uint4 q[kInLoads];
+      bool in[kInLoads];
+#pragma unroll
+      for (int u = 0; u < kInLoads; ++u) {  // kInLoads loads in flight before any is used
+        const int p = p0 + u * kStride;
+        const int r = p / cols, c = p - r * cols;
+        const int hh = 2 * i0 - 1 + r, ww = 2 * j0 - 1 + c;
+        in[u] = p < npx && src && hh >= 0 && hh < a.H && ww >= 0 && ww < a.W;
+        q[u] = in[u] ? __ldg(reinterpret_cast<const uint4*>(src + ((size_t)hh * a.W + ww) * a.C + slice * 64) + v)
+                     : make_uint4(0, 0, 0, 0);
       }
-      *reinterpret_cast<uint4*>(sm_in + (size_t)p * 128 + v * 16) = q;
+#pragma unroll
+      for (int u = 0; u < kInLoads; ++u) {
+        const int p = p0 + u * kStride;
+        if (cf && in[u]) q[u] = gn_silu8(q[u], k8);
+        if (p < npx) *reinterpret_cast<uint4*>(sm_in + (size_t)p * 128 + v * 16) = q[u];
+      }
     }
   }
   __syncthreads();
