@@ -5,8 +5,9 @@ A step is one steady-state pass of every op of the path over one batch of synthe
 each op at the decoder shape it is quoted on:
   gn      GroupNorm+SiLU standalone, x [1, 4, 88, 156, 512] ~ N(0.5, var 2), 32 groups
   c256    three causal ResBlocks at C=256 on a 4-frame chunk [1, 4, 176, 312, 256] with the
-          two-frame caches carried from the previous chunk (GN+SiLU, causal conv, cache update,
-          GN+SiLU, causal conv + residual, cache update, per block)
+          two-frame caches carried from the previous chunk (per block: the norm's coefficients, the
+          causal conv normalising its input and writing the new history, the same for conv 2 with
+          the residual; each conv's history alternates between two buffers)
   up      phase-weight transform [512, 3, 3, 512] and the nearest-x2 + 3x3 upsample as four phase
           convs, [1, 4, 44, 78, 512] -> [1, 4, 88, 156, 512]
   c1024   two causal ResBlocks at C=1024 on [1, 4, 44, 78, 1024] with carried caches, their convs
@@ -182,11 +183,16 @@ class Workload:
             N, T, H, W, C = x.shape
             caches = [(torch.zeros((N, 2, H, W, C), dtype=bf, device=dev),
                        torch.zeros((N, 2, H, W, C), dtype=bf, device=dev)) for _ in range(nblk)]
+            # the second buffer of each conv's history: the step's convs read one and write the other
+            self.alt.extend(torch.zeros((N, 2, H, W, C), dtype=bf, device=dev) for _ in range(2 * nblk))
             outs = [torch.empty_like(x) for _ in range(nblk)]
             coef = torch.empty(N * T * C * 16, dtype=torch.uint8, device=dev)  # GroupNorm coefficients
             return caches, outs, coef, torch.empty_like(x)
+        self.alt = []
         self.c4, self.o4, self.k4, self.h4 = stage_bufs(self.x4, 3)
+        self.alt4, self.alt = self.alt, []
         self.c5, self.o5, self.k5, self.h5 = stage_bufs(self.x5, 2)
+        self.alt5, self.alt = self.alt, []
         from video_vae_decoder_gb300 import binding as wan
         # the C=1024 convs' Winograd weights, transformed once per weight set (prepare)
         self.u5 = [(wan.wan_winograd_weights(p["w1"]), wan.wan_winograd_weights(p["w2"])) for p in self.blocks5]
@@ -223,48 +229,48 @@ class Workload:
             calls.append(("gn", 1, lambda: wan.wan_gn_silu(self.gn_x, self.gn_g, self.gn_b, GROUPS, EPS, self.gn_y,
                                                            self.gn_ws)))
 
-        def stage(tag, x, blocks, caches, outs, coef, h, us=None):
+        def stage(tag, x, blocks, caches, outs, coef, h, alt, us=None):
             # Each ResBlock as the calls wan_resblock (wan_resblock_winograd with `us`) makes, twice
             # (GroupNorm + SiLU into each conv): the norm's coefficients (one pass over its input),
-            # the conv normalising its operand tiles as they arrive (or its input as it is
-            # transformed), then the last two normalised frames into the conv's cache.
+            # then the conv normalising its operand tiles as they arrive (or its input as it is
+            # transformed), which also writes the conv's new history: each conv has two history
+            # buffers, reads one and writes the other, and they swap every step.
             cur = x
             for i, (p, (c1, c2), out) in enumerate(zip(blocks, caches, outs)):
+                h1 = [c1, alt[2 * i]]      # conv 1's history: [read, write]
+                h2 = [c2, alt[2 * i + 1]]  # conv 2's
+
                 def n1(cur=cur, p=p):
                     wan.wan_gn_silu_coefficients(cur, p["gamma1"], p["beta1"], GROUPS, EPS, coef, self.gn_ws)
 
-                def k1(cur=cur, p=p, c1=c1, i=i):
+                def k1(cur=cur, p=p, hb=h1, i=i):
                     if us is not None:
-                        wan.wan_causal_conv3d_winograd(cur, us[i][0], coef, p["b1"], None, c1, None, h, self.wino_ws)
+                        wan.wan_causal_conv3d_winograd(cur, us[i][0], coef, p["b1"], None, hb[0], hb[1], h, self.wino_ws)
                     else:
-                        wan.wan_causal_conv3d_gn_input(cur, coef, p["w1"], p["b1"], None, c1, h)
-
-                def u1(cur=cur, c1=c1):
-                    wan.wan_gn_silu_cache_update(cur, coef, c1, c1)
+                        wan.wan_causal_conv3d_gn_input(cur, coef, p["w1"], p["b1"], None, hb[0], h, cache_out=hb[1])
+                    hb.reverse()
 
                 def n2(p=p):
                     wan.wan_gn_silu_coefficients(h, p["gamma2"], p["beta2"], GROUPS, EPS, coef, self.gn_ws)
 
-                def k2(cur=cur, p=p, c2=c2, out=out, i=i):
+                def k2(cur=cur, p=p, hb=h2, out=out, i=i):
                     if us is not None:
-                        wan.wan_causal_conv3d_winograd(h, us[i][1], coef, p["b2"], cur, c2, None, out, self.wino_ws)
+                        wan.wan_causal_conv3d_winograd(h, us[i][1], coef, p["b2"], cur, hb[0], hb[1], out, self.wino_ws)
                     else:
-                        wan.wan_causal_conv3d_gn_input(h, coef, p["w2"], p["b2"], cur, c2, out)
-
-                def u2(c2=c2):
-                    wan.wan_gn_silu_cache_update(h, coef, c2, c2)
+                        wan.wan_causal_conv3d_gn_input(h, coef, p["w2"], p["b2"], cur, hb[0], out, cache_out=hb[1])
+                    hb.reverse()
                 kc = 3 if us is not None else 1  # Winograd: input transform, component GEMMs, output transform
-                calls.extend([(f"{tag}.coef", 1, n1), (f"{tag}.conv", kc, k1), (f"{tag}.cache", 1, u1),
-                              (f"{tag}.coef", 1, n2), (f"{tag}.conv", kc, k2), (f"{tag}.cache", 1, u2)])
+                calls.extend([(f"{tag}.coef", 1, n1), (f"{tag}.conv", kc, k1),
+                              (f"{tag}.coef", 1, n2), (f"{tag}.conv", kc, k2)])
                 cur = out
 
         if want("c256"):
-            stage("c256", self.x4, self.blocks4, self.c4, self.o4, self.k4, self.h4)
+            stage("c256", self.x4, self.blocks4, self.c4, self.o4, self.k4, self.h4, self.alt4)
         if want("up"):
             calls.append(("up.weights", 1, lambda: wan.wan_upsample_phase_weights(self.w3, self.wp)))
             calls.append(("up.conv", 1, lambda: wan.wan_upsample_phase_conv(self.x3, self.wp, None, self.y3)))
         if want("c1024"):
-            stage("c1024", self.x5, self.blocks5, self.c5, self.o5, self.k5, self.h5, self.u5)
+            stage("c1024", self.x5, self.blocks5, self.c5, self.o5, self.k5, self.h5, self.alt5, self.u5)
         if want("head"):
             calls.append(("head.conv", 1, lambda: wan.wan_causal_conv3d(self.xh, self.wh, None, None, None, None,
                                                                         self.yh)))
@@ -455,8 +461,7 @@ def run_ours(args, rank, world, dev):
         # the norm's coefficients: one read of its input (2 bytes per element); the cache frames:
         # 2 of the 4 frames read and written
         hbm_kernel("gn_coef_c256", per_launch("c256.coef"), 2.0 * wl.x4.numel(), tot("c256.coef"))
-        hbm_kernel("gn_cache_frames_c256", per_launch("c256.cache"), 2.0 * wl.x4.numel(), tot("c256.cache"))
-        kernels["resblock_c256_ms"] = (tot("c256.coef") + tot("c256.conv") + tot("c256.cache")) / 3.0
+        kernels["resblock_c256_ms"] = (tot("c256.coef") + tot("c256.conv")) / 3.0
     if "c1024.conv" in per_tag:
         # Winograd F(2x2, 3x3): 16 component products of 3 temporal taps x Cin per 2x2 outputs, the
         # algorithm's tensor work (its three kernels timed together as one call); the direct
@@ -465,8 +470,7 @@ def run_ours(args, rank, world, dev):
         tensor_kernel("conv_c1024_winograd", cm, wino_flops(1, 4, 44, 78, 1024, 1024), tot("c1024.conv"))
         kernels["conv_c1024_winograd"]["direct_equivalent_tflops"] = conv_flops(1, 4, 44, 78, 1024, 1024) / cm / 1e9
         hbm_kernel("gn_coef_c1024", per_launch("c1024.coef"), 2.0 * wl.x5.numel(), tot("c1024.coef"))
-        hbm_kernel("gn_cache_frames_c1024", per_launch("c1024.cache"), 2.0 * wl.x5.numel(), tot("c1024.cache"))
-        kernels["resblock_c1024_ms"] = (tot("c1024.coef") + tot("c1024.conv") + tot("c1024.cache")) / 2.0
+        kernels["resblock_c1024_ms"] = (tot("c1024.coef") + tot("c1024.conv")) / 2.0
     if "head.conv" in per_tag:
         # Bound by whichever takes longer at the measured peaks: its useful MMAs or its HBM bytes.
         hm = per_launch("head.conv")

@@ -216,7 +216,8 @@ wan_status wan_gn_silu_from_stats(const wan_bf16* x, wan_bf16* y, const float* g
  * calls return.
  * For Cout >= 256 a is never stored: the norm's pass over x writes per-(frame, channel)
  * coefficients only, the conv normalises each operand tile of x in shared memory as it arrives,
- * and the last two frames of a are written once, straight into cache_out.
+ * and the last two frames of a are written once into cache_out: by the conv itself when
+ * cache_out is a buffer apart from cache_in, else by a pass after the conv.
  *
  *   x          [N, T, H, W, Cin] bf16 (the norm's input); gamma, beta, groups, eps as wan_gn_silu.
  *   cache_in   NULL (zero history) or [N, 2, H, W, Cin] bf16, already activated (a previous
@@ -251,14 +252,19 @@ wan_status wan_gn_silu_causal_conv3d(const wan_bf16* x, const float* gamma, cons
  *                             wan_workspace_size(WAN_OP_GN_SILU, ...)).
  *   wan_causal_conv3d_gn_input  cache_in (activated history, or NULL), w, bias, residual, y as
  *                             wan_causal_conv3d; Cout < 256 gives WAN_ERR_UNSUPPORTED_SHAPE.
+ *                             cache_out (NULL, or [N, 2, H, W, Cin]) receives step 3's result: a
+ *                             buffer apart from cache_in is written by the conv's operand
+ *                             prologue from its normalised tiles (no pass of its own); cache_out
+ *                             == cache_in is updated after the conv, as step 3 does.
  *   wan_gn_silu_cache_update  cache_out may equal cache_in; must not overlap x or coef.
  */
 wan_status wan_gn_silu_coefficients(const wan_bf16* x, const float* gamma, const float* beta, int N, int T,
                                     int H, int W, int C, int groups, float eps, void* coef, void* ws,
                                     size_t ws_bytes, void* stream);
 wan_status wan_causal_conv3d_gn_input(const wan_bf16* x, const void* coef, const wan_bf16* cache_in,
-                                      const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual,
-                                      wan_bf16* y, int N, int T, int H, int W, int Cin, int Cout, void* stream);
+                                      wan_bf16* cache_out, const wan_bf16* w, const wan_bf16* bias,
+                                      const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W, int Cin,
+                                      int Cout, void* stream);
 wan_status wan_gn_silu_cache_update(const wan_bf16* x, const void* coef, const wan_bf16* cache_in,
                                     wan_bf16* cache_out, int N, int T, int H, int W, int C, void* stream);
 
@@ -417,7 +423,8 @@ wan_status wan_resblock_shortcut(const wan_bf16* x, wan_bf16* out, const wan_res
  *   wan_gn_silu_coefficients: the GroupNorm + SiLU applied to the conv's input as it is
  *   transformed) and A = a otherwise; cache_in holds already-activated frames (or NULL: zeros).
  *   cache_out (NULL or [N, 2, H, W, Cin], may equal cache_in) receives the last two frames of
- *   [cache_in or zeros; A] bit for bit as wan_gn_silu_cache_update / wan_cache_update write them.
+ *   [cache_in or zeros; A] bit for bit as wan_gn_silu_cache_update / wan_cache_update write them
+ *   (apart from cache_in it is written by the input transform, in place by a pass after the conv).
  *     u     from wan_winograd_weights.   Cin % 64 == 0, Cin <= 2048, Cout % 256 == 0.
  *     ws    >= wan_workspace_size(WAN_OP_WINOGRAD_CONV3D, N, T, H, W, Cin, Cout, 0) bytes: the
  *           transformed input (16 N (T + 2) ceil(H/2) ceil(W/2) Cin fp16) and the component

@@ -169,10 +169,12 @@ def test_gn_silu_steps_reject_invalid(L):
     assert co(A, A * 2, A * 3, 1, 2, 16, 16, 256, 32, 1e-6, None, A * 5, big, None) == 1  # no coefficient buffer
     assert co(A, A * 2, A * 3, 1, 2, 16, 16, 256, 32, 1e-6, A * 4, None, 0, None) == 4    # no workspace
     cv = L.wan_causal_conv3d_gn_input
-    assert cv(A, None, None, A * 5, None, None, A * 9, 1, 2, 16, 16, 256, 256, None) == 1  # no coefficients
-    assert cv(A, A * 4, None, A * 5, None, None, A * 9, 1, 2, 16, 16, 256, 128, None) == 2  # Cout < 256
-    assert cv(A, MIS, None, A * 5, None, None, A * 9, 1, 2, 16, 16, 256, 256, None) == 3    # misaligned coefficients
-    assert cv(A, A * 4, None, A * 5, None, None, A, 1, 2, 16, 16, 256, 256, None) == 1      # y overlaps x
+    assert cv(A, None, None, None, A * 5, None, None, A * 9, 1, 2, 16, 16, 256, 256, None) == 1  # no coefficients
+    assert cv(A, A * 4, None, None, A * 5, None, None, A * 9, 1, 2, 16, 16, 256, 128, None) == 2  # Cout < 256
+    assert cv(A, MIS, None, None, A * 5, None, None, A * 9, 1, 2, 16, 16, 256, 256, None) == 3    # misaligned coefficients
+    assert cv(A, A * 4, None, None, A * 5, None, None, A, 1, 2, 16, 16, 256, 256, None) == 1      # y overlaps x
+    assert cv(A, A * 4, None, A + 4096, A * 5, None, None, A * 9, 1, 2, 16, 16, 256, 256, None) == 1  # cache_out on x
+    assert cv(A, A * 4, A * 20, A * 20 + 64, A * 5, None, None, A * 9, 1, 2, 16, 16, 256, 256, None) == 1  # caches overlap
     cu = L.wan_gn_silu_cache_update
     assert cu(A, A * 4, None, None, 1, 2, 16, 16, 256, None) == 1        # no cache_out
     assert cu(A, A * 4, None, A * 20, 1, 2, 16, 16, 96, None) == 2       # C % 64 != 0

@@ -135,6 +135,9 @@ def test_steps_equal_fused(wan, shape, history, in_place):
     c_f = torch.empty((shape[0], 2) + shape[2:], dtype=torch.bfloat16, device="cuda")
     y_f = wan.wan_gn_silu_causal_conv3d(xd, gd, bed, G, EPS, wd, bd, rd, cd, c_f)
     coef = wan.wan_gn_silu_coefficients(xd, gd, bed, G, EPS)
+    # the conv writing the new history itself (a cache_out apart from the history it reads)
+    c_d = torch.empty_like(c_f)
+    y_d = wan.wan_causal_conv3d_gn_input(xd, coef, wd, bd, rd, cd, cache_out=c_d)
     y = wan.wan_causal_conv3d_gn_input(xd, coef, wd, bd, rd, cd)
     if in_place:
         c_s = cd.clone()
@@ -143,6 +146,30 @@ def test_steps_equal_fused(wan, shape, history, in_place):
         c_s = torch.empty_like(c_f)
         wan.wan_gn_silu_cache_update(xd, coef, c_s, cd)
     torch.cuda.synchronize()
+    assert same(y_d, y_f) and same(c_d, c_f)
     assert wan.wan_device_status() == 0
     assert same(y, y_f)
     assert same(c_s, c_f)
+
+
+@pytest.mark.parametrize("shape", [(1, 4, 176, 312, 256), (1, 2, 44, 78, 1024)])
+def test_history_written_by_the_conv_equals_the_pass_after_it(wan, shape):
+    # At the decoder's sizes: the conv storing the normalised last two frames from its operand
+    # prologue (cache_out apart from cache_in) writes the bits that the pass after the conv writes
+    # (cache_out == cache_in), and the same y.
+    N, T, H, W, C = shape
+    x = synth.normal_torch(shape, 0, f"gnconv/hist/{C}/x", device="cuda", dtype=torch.bfloat16)
+    g = f32_dev(synth.normal_f32((C,), 0, f"gnconv/hist/{C}/g", 1.0, 0.1))
+    be = f32_dev(synth.normal_f32((C,), 0, f"gnconv/hist/{C}/b", 0.0, 0.1))
+    w = synth.normal_torch((C, 3, 3, 3, C), 0, f"gnconv/hist/{C}/w", 0.0, float(np.sqrt(1.0 / (27 * C))),
+                           device="cuda", dtype=torch.bfloat16)
+    hist = synth.normal_torch((N, 2, H, W, C), 0, f"gnconv/hist/{C}/c", 0.1, 0.6, device="cuda", dtype=torch.bfloat16)
+    coef = wan.wan_gn_silu_coefficients(x, g, be, G, EPS)
+    c_direct = torch.empty_like(hist)
+    y_direct = wan.wan_causal_conv3d_gn_input(x, coef, w, None, None, hist, cache_out=c_direct)
+    c_place = hist.clone()
+    y_place = wan.wan_causal_conv3d_gn_input(x, coef, w, None, None, c_place, cache_out=c_place)
+    torch.cuda.synchronize()
+    assert wan.wan_device_status() == 0
+    assert same(y_direct, y_place)
+    assert same(c_direct, c_place)

@@ -84,7 +84,7 @@ def lib() -> ctypes.CDLL:
     L.wan_gn_silu_coefficients.restype = I
     L.wan_gn_silu_coefficients.argtypes = [P, P, P, I, I, I, I, I, I, F, P, P, S, P]
     L.wan_causal_conv3d_gn_input.restype = I
-    L.wan_causal_conv3d_gn_input.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, P]
+    L.wan_causal_conv3d_gn_input.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, P]
     L.wan_gn_silu_cache_update.restype = I
     L.wan_gn_silu_cache_update.argtypes = [P, P, P, P, I, I, I, I, I, P]
     L.wan_time_upsample.restype = I
@@ -276,17 +276,20 @@ def wan_gn_silu_coefficients(x, gamma, beta, groups: int, eps: float, coef=None,
     return coef
 
 
-def wan_causal_conv3d_gn_input(x, coef, w, bias=None, residual=None, cache_in=None, y=None, stream=None):
+def wan_causal_conv3d_gn_input(x, coef, w, bias=None, residual=None, cache_in=None, y=None, stream=None,
+                               cache_out=None):
     """y = causal_conv3d(silu(x S + B); cache_in) + bias + residual with coefficients from
-    wan_gn_silu_coefficients(x, ...); Cout >= 256."""
-    for t, n in ((x, "x"), (w, "w"), (bias, "bias"), (residual, "residual"), (cache_in, "cache_in")):
+    wan_gn_silu_coefficients(x, ...); Cout >= 256. cache_out (optional) receives the new history
+    (written by the conv itself when it is not cache_in)."""
+    for t, n in ((x, "x"), (w, "w"), (bias, "bias"), (residual, "residual"), (cache_in, "cache_in"),
+                 (cache_out, "cache_out")):
         _need(t, torch.bfloat16, n)
     N, T, H, W, Cin = x.shape
     Cout = w.shape[0]
     y = torch.empty((N, T, H, W, Cout), dtype=torch.bfloat16, device=x.device) if y is None else y
     _need(y, torch.bfloat16, "y")
-    _check(lib().wan_causal_conv3d_gn_input(_ptr(x), _ptr(coef), _ptr(cache_in), _ptr(w), _ptr(bias), _ptr(residual),
-                                            _ptr(y), N, T, H, W, Cin, Cout, _stream(stream)),
+    _check(lib().wan_causal_conv3d_gn_input(_ptr(x), _ptr(coef), _ptr(cache_in), _ptr(cache_out), _ptr(w), _ptr(bias),
+                                            _ptr(residual), _ptr(y), N, T, H, W, Cin, Cout, _stream(stream)),
            "wan_causal_conv3d_gn_input")
     return y
 

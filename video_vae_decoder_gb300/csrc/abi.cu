@@ -115,6 +115,16 @@ cudaError_t gn_cache_update(const wan_bf16* x, const float4* coef, const wan_bf1
   return gn_apply_frames_launch(x, coef, cache_out, N, 1, H, W, C, 0, 2, 1, sms, s);
 }
 
+// cache_out[:, 0] = cache_in[:, 1] (zeros without cache_in): the part of a one-frame chunk's new
+// history that the conv's prologue does not write.
+cudaError_t cache_keep_last(const wan_bf16* cache_in, wan_bf16* cache_out, int N, int H, int W, int C,
+                            cudaStream_t s) {
+  const size_t fb = (size_t)H * W * C * sizeof(wan_bf16);
+  return cache_in ? cudaMemcpy2DAsync(cache_out, 2 * fb, cache_in + fb / sizeof(wan_bf16), 2 * fb, fb, N,
+                                      cudaMemcpyDeviceToDevice, s)
+                  : cudaMemset2DAsync(cache_out, 2 * fb, 0, fb, N, s);
+}
+
 }  // namespace
 
 unsigned* device_error_word() {
@@ -290,9 +300,14 @@ cudaError_t gn_conv(const wan_bf16* x, const float* gamma, const float* beta, in
   }
   e = gn_silu_launch(x, nullptr, gamma, beta, N, T, H, W, Cin, groups, eps, ws, sms, s, nullptr, 0, false);
   const float4* coef = gn_silu_coef(ws, N, T, H, W, Cin, groups);
+  // A cache_out apart from cache_in is written by the conv's prologue itself; in place, the new
+  // history can only be written once the conv has read the old one.
+  const bool direct = cache_out && cache_out != cache_in;
+  if (e == cudaSuccess && direct && T == 1) e = cache_keep_last(cache_in, cache_out, N, H, W, Cin, s);
   if (e == cudaSuccess)
-    e = conv_pair_launch(0, x, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, sms, err, s, nullptr, 0, coef);
-  if (e != cudaSuccess || !cache_out) return e;
+    e = conv_pair_launch(0, x, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, sms, err, s, nullptr, 0, coef, 0,
+                         0, 0, direct ? cache_out : nullptr);
+  if (e != cudaSuccess || !cache_out || direct) return e;
   return gn_cache_update(x, coef, cache_in, cache_out, N, T, H, W, Cin, sms, s);
 }
 
@@ -363,25 +378,35 @@ wan_status wan_gn_silu_coefficients(const wan_bf16* x, const float* gamma, const
                                     static_cast<float4*>(coef)));
 }
 
-wan_status wan_causal_conv3d_gn_input(const wan_bf16* x, const void* coef, const wan_bf16* cache_in, const wan_bf16* w,
-                                      const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H,
-                                      int W, int Cin, int Cout, void* stream) {
+wan_status wan_causal_conv3d_gn_input(const wan_bf16* x, const void* coef, const wan_bf16* cache_in, wan_bf16* cache_out,
+                                      const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y,
+                                      int N, int T, int H, int W, int Cin, int Cout, void* stream) {
   if (!coef) return WAN_ERR_INVALID_ARG;
   wan_status st = check_conv(x, w, y, N, T, H, W, Cin, Cout);
   if (st != WAN_OK) return st;
   if (!gn_conv_fused(Cout)) return WAN_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned16(coef) || (cache_in && !aligned16(cache_in)) || (bias && !aligned16(bias)) ||
-      (residual && !aligned16(residual)))
+  if (!aligned16(coef) || (cache_in && !aligned16(cache_in)) || (cache_out && !aligned16(cache_out)) ||
+      (bias && !aligned16(bias)) || (residual && !aligned16(residual)))
     return WAN_ERR_MISALIGNED;
   const size_t xbytes = (size_t)N * T * H * W * Cin * 2, ybytes = (size_t)N * T * H * W * Cout * 2;
-  if (overlap(x, xbytes, y, ybytes) || overlap(residual, ybytes, y, ybytes) ||
-      overlap(cache_in, (size_t)N * 2 * H * W * Cin * 2, y, ybytes) || overlap(coef, (size_t)N * T * Cin * 16, y, ybytes))
+  const size_t cbytes = (size_t)N * 2 * H * W * Cin * 2;
+  if (overlap(x, xbytes, y, ybytes) || overlap(residual, ybytes, y, ybytes) || overlap(cache_in, cbytes, y, ybytes) ||
+      overlap(coef, (size_t)N * T * Cin * 16, y, ybytes) || overlap(cache_out, cbytes, y, ybytes) ||
+      overlap(cache_out, cbytes, x, xbytes) || overlap(cache_out, cbytes, coef, (size_t)N * T * Cin * 16) ||
+      (cache_in && cache_out && cache_in != cache_out && overlap(cache_in, cbytes, cache_out, cbytes)))
     return WAN_ERR_INVALID_ARG;
   unsigned* err = device_error_word();
   if (!err) return WAN_ERR_CUDA;
-  return cuda_status(conv_pair_launch(0, x, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, sm_count(), err,
-                                      static_cast<cudaStream_t>(stream), nullptr, 0,
-                                      static_cast<const float4*>(coef)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float4* cf = static_cast<const float4*>(coef);
+  const bool direct = cache_out && cache_out != cache_in;
+  cudaError_t e = cudaSuccess;
+  if (direct && T == 1) e = cache_keep_last(cache_in, cache_out, N, H, W, Cin, s);
+  if (e == cudaSuccess)
+    e = conv_pair_launch(0, x, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, sm_count(), err, s, nullptr, 0,
+                         cf, 0, 0, 0, direct ? cache_out : nullptr);
+  if (e != cudaSuccess || !cache_out || direct) return cuda_status(e);
+  return cuda_status(gn_cache_update(x, cf, cache_in, cache_out, N, T, H, W, Cin, sm_count(), s));
 }
 
 wan_status wan_gn_silu_cache_update(const wan_bf16* x, const void* coef, const wan_bf16* cache_in, wan_bf16* cache_out,
@@ -611,8 +636,14 @@ wan_status wan_causal_conv3d_winograd(const wan_bf16* a, const void* coef, const
   if (!err) return WAN_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const float4* cf = static_cast<const float4*>(coef);
-  cudaError_t e = wino_conv_launch(a, cf, cache_in, u, bias, residual, y, N, T, H, W, Cin, Cout, ws, sm_count(), err, s);
-  if (e != cudaSuccess || !cache_out) return cuda_status(e);
+  // A cache_out apart from cache_in is written by the input transform from its staged pixels.
+  const bool direct = cache_out && cache_out != cache_in;
+  cudaError_t e = cudaSuccess;
+  if (direct && T == 1) e = cache_keep_last(cache_in, cache_out, N, H, W, Cin, s);
+  if (e == cudaSuccess)
+    e = wino_conv_launch(a, cf, cache_in, u, bias, residual, y, N, T, H, W, Cin, Cout, ws, sm_count(), err, s,
+                         direct ? cache_out : nullptr);
+  if (e != cudaSuccess || !cache_out || direct) return cuda_status(e);
   if (cf) return cuda_status(gn_cache_update(a, cf, cache_in, cache_out, N, T, H, W, Cin, sm_count(), s));
   return cuda_status(cache_update_launch(a, cache_in, cache_out, N, T, H, W, Cin, sm_count(), s));
 }

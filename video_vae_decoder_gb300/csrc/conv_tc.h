@@ -16,7 +16,7 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
                              const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W,
                              int Cin, int Cout, int sms, unsigned* err, cudaStream_t stream,
                              void* st_buf = nullptr, int st_groups = 0, const float4* coef = nullptr,
-                             int a_frames = 0, int y_frames = 0, int y_frame0 = 0);
+                             int a_frames = 0, int y_frames = 0, int y_frame0 = 0, wan_bf16* cache_out = nullptr);
 // Modes of conv_pair_launch beyond conv_launch's: 2, the causal 3x1x1 time conv to Cout = 2 C
 // channels (w [Cout, 3, Cin]) whose output frame t, channel half i lands in frame
 // y_frame0 + 2 t + i of y ([N, y_frames, H, W, Cout / 2]; Cout % 512 == 0, no residual);
@@ -25,6 +25,8 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
 // coef (optional, mode 0): GroupNorm + SiLU of `a` applied to the conv's operand tiles as they
 // arrive (per (frame n*T + t, Cin channel) float4 coefficients as the norm's coefficients-only
 // pass leaves them, blocked layout); the cache frames are used as they are.
+// cache_out (optional, with coef; never cache_in): receives frames max(T - 2, 0) .. T - 1 of
+// silu(a S + B) at cache frames t - T + 2, written by the prologue from its normalised tiles.
 // GroupNorm statistics of the causal conv's output, emitted by the CTA-pair kernel's epilogue
 // (Cout a multiple of 256, channels per group a power of two from 4 to 64): per (frame, group,
 // 8 x 16-pixel tile, epilogue warp) the float-float sums of d and d^2 of d = y - s as a float4,

@@ -113,6 +113,10 @@ struct Conv2Args {
   // A box read from `a` (not the cache).
   const float4* coef;
   const wan_bf16* a;  // the conv input itself (the prologue's rare exact path reads it again)
+  // Optional, with the prologue: the new history [N, 2, H, W, Cin] (never the cache being read).
+  // The tiles of frames T - 2 and T - 1 store their own normalised pixels there (frame
+  // t - T + 2 of cache_out) from the box of their current frame, so no pass over x rewrites them.
+  wan_bf16* cache_out;
   // Mode 2 (time upsample): y has y_frames frames per n of Cout / 2 channels; conv output frame
   // t, channel half i goes to frame y_frame0 + 2 t + i.
   int y_frames, y_frame0;
@@ -320,7 +324,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
   if (threadIdx.x == 0) {
     for (int s = 0; s < kAStages; ++s) {
       mbar_init(&full_a[s], 1);
-      mbar_init(&empty_a[s], 1);
+      // with the prologue, an A stage is free once the pair's MMAs (one commit) and this CTA's 8
+      // prologue warps (which may still copy the box's pixels to the new history) are done with it
+      mbar_init(&empty_a[s], kNorm ? 9 : 1);
     }
     for (int s = 0; s < kBStages; ++s) {
       mbar_init(&full_b[s], 1);
@@ -786,6 +792,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
         if (skip_pair(args, p0, p1, dt)) continue;
         const int tau = me.t0 + dt;
         const bool xf = me.valid && tau >= 0;  // this box holds x
+        // this box's tile pixels are the new history (once per pixel: the current frame's box of
+        // the first N block, not the second half of a split item)
+        const bool wcache = args.cache_out && xf && dt == 0 && tau >= args.T - 2 && me.nb == 0 && sub <= 0;
         for (int kb = 0; kb < args.kb_per_tap; ++kb) {
           if (!mbar_wait(&full_a[sa], pha, args.err, kDevErrTimeoutPrologue)) {
             ok = false;
@@ -833,6 +842,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
             else
               mbar_arrive_remote_cta(ready0 + 8u * (uint32_t)sa);
           }
+          if (wcache) {  // while the MMAs run: the tile's own pixels of the box to the new history
+            const uint8_t* box = smem + sa * kAStride + chunk_off;
+            wan_bf16* dst = args.cache_out + ((size_t)me.n * 2 + (tau - args.T + 2)) * args.H * args.W * args.Cin +
+                            (size_t)kb * kBlockK + 8 * jl;
+#pragma unroll
+            for (int i = 0; i < 6; ++i) {
+              const int rr = r0 + 32 * i, rh = rr % kTallRows, rc = rr / kTallRows;
+              const int hh = me.h0 - 1 + rh, ww = me.w0 - 1 + rc;
+              if (rr < kRows && rh >= 1 && rh <= kTileH && rc >= 1 && rc <= kTileW && hh < args.H && ww < args.W)
+                __stcs(reinterpret_cast<int4*>(dst + ((size_t)hh * args.W + ww) * args.Cin),
+                       *reinterpret_cast<const int4*>(box + i * 4096));  // streamed: L2 keeps the conv's operands
+            }
+            __syncwarp();
+          }
+          if (lane == 0) mbar_arrive(&empty_a[sa]);  // this warp is done reading the stage
           if (++sa == kAStages) {
             sa = 0;
             pha ^= 1;
@@ -951,7 +975,8 @@ size_t conv_gn_stats_bytes(int N, int T, int H, int W, int Cout, int groups) {
 cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_in, const wan_bf16* w,
                              const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W,
                              int Cin, int Cout, int sms, unsigned* err, cudaStream_t stream, void* st_buf,
-                             int st_groups, const float4* coef, int a_frames, int y_frames, int y_frame0) {
+                             int st_groups, const float4* coef, int a_frames, int y_frames, int y_frame0,
+                             wan_bf16* cache_out) {
   if (mode < 0 || mode > 3) return cudaErrorInvalidValue;
   if (mode == 2 && (Cout % (2 * kN) != 0 || residual != nullptr)) return cudaErrorInvalidValue;
   if (mode == 3 && cache_in) return cudaErrorInvalidValue;
@@ -996,10 +1021,12 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
   const int taps = mode == 0 ? 27 : mode == 1 ? 4 : mode == 2 ? 3 : 1;
   if (!map_w_half(&tw, w, taps * Cin, Cout, args.phases, 128)) return cudaErrorInvalidValue;
   if (!map_w_half(&tw64, w, taps * Cin, Cout, args.phases, 64)) return cudaErrorInvalidValue;
+  if (cache_out && (!coef || cache_out == cache_in)) return cudaErrorInvalidValue;
   if (coef) {
     if (mode != 0) return cudaErrorInvalidValue;
     args.coef = coef;
     args.a = a;
+    args.cache_out = cache_out;
     return launch_pair<true>(ta, tc, tw, tw64, args, sms, stream);
   }
   return launch_pair<false>(ta, tc, tw, tw64, args, sms, stream);

@@ -122,6 +122,7 @@ struct WinoInArgs {
   const float4* coef;      // blocked GroupNorm coefficients per (n T + t, c), or null
   const wan_bf16* cache;   // [N, 2, H, W, C] or null (zeros)
   uint16_t* v;             // [16][N (T + 2) tiles][C] fp16
+  wan_bf16* cache_out;     // [N, 2, H, W, C] or null: the new history, from the staged pixels
   int N, T, H, W, C, Ht, Wt, tiles, col_groups;
   long long rows;          // N (T + 2) tiles
 };
@@ -133,10 +134,15 @@ __global__ void __launch_bounds__(kInThreads) wino_input_kernel(const WinoInArgs
   const int j0 = (blockIdx.y % a.col_groups) * kInTileCols;  // first tile column
   const int ncols = min(kInTileCols, a.Wt - j0);
   const int cols = 2 * ncols + 2;                   // staged pixel columns
+  const int nrows = min(kInTileRows, a.Ht - i0);
   const int ft = blockIdx.z;                        // n (T + 2) + tau
   const int tau = ft % (a.T + 2), n = ft / (a.T + 2);
   const wan_bf16* src = nullptr;
   const float4* cf = nullptr;
+  // frames T - 2 and T - 1 of the input are the new history: each CTA stores the pixels of its own
+  // tiles (not the halo) of its 64 channels
+  const bool wcache = a.cache_out && tau >= 2 && tau - 2 >= a.T - 2;
+  wan_bf16* cdst = wcache ? a.cache_out + ((size_t)n * 2 + (tau - a.T)) * a.H * a.W * a.C + slice * 64 : nullptr;
   if (tau < 2) {
     if (a.cache) src = a.cache + ((size_t)n * 2 + tau) * a.H * a.W * a.C;
   } else {
@@ -169,13 +175,17 @@ __global__ void __launch_bounds__(kInThreads) wino_input_kernel(const WinoInArgs
         const int p = p0 + u * kStride;
         if (cf && in[u]) q[u] = gn_silu8(q[u], k8);
         if (p < npx) *reinterpret_cast<uint4*>(sm_in + (size_t)p * 128 + v * 16) = q[u];
+        if (wcache && in[u]) {
+          const int r = p / cols, c = p - r * cols;
+          if (r >= 1 && r <= 2 * nrows && c >= 1 && c <= 2 * ncols)
+            *reinterpret_cast<uint4*>(cdst + ((size_t)(2 * i0 - 1 + r) * a.W + (2 * j0 - 1 + c)) * a.C + v * 8) = q[u];
+        }
       }
     }
   }
   __syncthreads();
   // 2. V = B^T d B per channel, B^T = [[1, 0, -1, 0], [0, 1, 1, 0], [0, -1, 1, 0], [0, 1, 0, -1]]:
   // rows first (s = B^T d), then columns (V = s B), in fp32, rounded once to fp16.
-  const int nrows = min(kInTileRows, a.Ht - i0);
   const int work = nrows * ncols * 16;
   for (int idx = threadIdx.x; idx < work; idx += kInThreads) {
     const int q = idx & 15;  // channels 4 q .. 4 q + 3 of the slice
@@ -572,8 +582,9 @@ cudaError_t wino_weights_launch(const wan_bf16* w, uint16_t* u, int Cin, int Cou
 
 cudaError_t wino_conv_launch(const wan_bf16* a, const float4* coef, const wan_bf16* cache_in, const uint16_t* u,
                              const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W,
-                             int Cin, int Cout, void* ws, int sms, unsigned* err, cudaStream_t s) {
-  if (!wino_supported(Cin, Cout)) return cudaErrorInvalidValue;
+                             int Cin, int Cout, void* ws, int sms, unsigned* err, cudaStream_t s,
+                             wan_bf16* cache_out) {
+  if (!wino_supported(Cin, Cout) || (cache_out && cache_out == cache_in)) return cudaErrorInvalidValue;
   const WinoPlan p = wplan(N, T, H, W, Cin, Cout);
   uint16_t* v = static_cast<uint16_t*>(ws);
   float* mbuf = reinterpret_cast<float*>(static_cast<char*>(ws) + p.v_bytes);
@@ -583,6 +594,7 @@ cudaError_t wino_conv_launch(const wan_bf16* a, const float4* coef, const wan_bf
   ia.coef = coef;
   ia.cache = cache_in;
   ia.v = v;
+  ia.cache_out = cache_out;
   ia.N = N;
   ia.T = T;
   ia.H = H;

@@ -16,5 +16,8 @@ cudaError_t wino_weights_launch(const wan_bf16* w, uint16_t* u, int Cin, int Cou
 // the cache frames as they are) through F(2x2, 3x3) with the transformed weights u.
 cudaError_t wino_conv_launch(const wan_bf16* a, const float4* coef, const wan_bf16* cache_in, const uint16_t* u,
                              const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W,
-                             int Cin, int Cout, void* ws, int sms, unsigned* err, cudaStream_t s);
+                             int Cin, int Cout, void* ws, int sms, unsigned* err, cudaStream_t s,
+                             wan_bf16* cache_out = nullptr);
+// cache_out (optional, never cache_in): receives frames max(T - 2, 0) .. T - 1 of the conv's
+// input (silu(a S + B) with coef) at cache frames t - T + 2, from the input transform's staging.
 }  // namespace wan
