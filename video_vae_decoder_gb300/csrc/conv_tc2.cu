@@ -65,28 +65,36 @@ constexpr int kTmemCols = 512;          // 2 accumulators x 256 columns
 constexpr uint32_t kShiftDesc = (kTileH * 128) >> 4;  // one column of the box, in descriptor units
 constexpr int kCoefBytes = kBlockK * 16;                // GroupNorm coefficients of one A stage
 constexpr int kTallRows = kTileH + 2;                   // rows of a tall A box (one halo row per side)
+constexpr int kPhaseRows = kTileH + 1;                  // rows of a phase box (taps u = 0, 1)
 
 static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
 // Stage rings and shared memory. The plain kernel: producer, MMA issuer, 4 epilogue warps. With
 // the GroupNorm + SiLU operand prologue: 8 more warps that normalise each A box in place between
 // its arrival and the MMAs.
-template <bool kNorm>
+// Kernel kinds: 0 plain, 1 with the GroupNorm + SiLU operand prologue (mode 0), 2 the phase
+// convolutions of mode 1 with one tall A box per K block.
+template <int kKind>
 struct Cfg {
+  static constexpr bool kNorm = kKind == 1;
+  static constexpr bool kPhase = kKind == 2;
   static constexpr int kThreads = kNorm ? 448 : 192;  // + 8 prologue warps
   // kNorm: one tall A box per (kernel frame, 64 channels), 10 x 18 pixels, serves all 9 taps of
   // that frame (the plain kernel loads one 8 x 18 box per kernel row, for its 3 taps), so every
   // pixel is normalised once per box instead of three times.
-  static constexpr int kABox = kNorm ? kTallRows * kBoxW * 128 : kABytes;
+  // kPhase: one 9 x 18 box per 64 channels serves the 4 taps (u, v) of a phase, at row offsets
+  // u + 9 v (the plain kernel loads one 8 x 18 box per tap row u, for its 2 taps).
+  static constexpr int kABox = kNorm ? kTallRows * kBoxW * 128 : kPhase ? kPhaseRows * kBoxW * 128 : kABytes;
   static constexpr int kAStride = (kABox + 1023) / 1024 * 1024;
   static constexpr int kAStages = kNorm ? 3 : 4;
-  static constexpr int kBStages = 9;
+  static constexpr int kBStages = kPhase ? 8 : 9;  // 4-tap boxes: two per ring
   static constexpr int kBOffset = kAStages * kAStride;
   // kNorm: each A stage's 64 channels of coefficients (16 bytes each) arrive with the box.
   static constexpr int kCoefOffset = kBOffset + kBStages * kBBytes;
   static constexpr int kBarOffset = kCoefOffset + (kNorm ? kAStages * kCoefBytes : 0);
   static constexpr int kSmemTotal = kBarOffset + 512 + 1024;
 };
-static_assert(Cfg<false>::kSmemTotal <= 232448 && Cfg<true>::kSmemTotal <= 232448, "shared memory per CTA");
+static_assert(Cfg<0>::kSmemTotal <= 232448 && Cfg<1>::kSmemTotal <= 232448 && Cfg<2>::kSmemTotal <= 232448,
+              "shared memory per CTA");
 
 struct Conv2Args {
   int N, T, H, W, Cin, Cout;
@@ -238,11 +246,13 @@ __device__ __forceinline__ void st_reduce8(const float (&vh)[8], const float (&v
 // kGroup > 1 (the 128-channel halves of the last round, whose MMAs are short): the B stages of
 // kGroup consecutive taps land on the first one's barrier and are released together, so one
 // wait and one commit serve kGroup taps.
-template <int kTaps, bool kTall, int kGroup>
+// kTallR > 0: a tall box of kTallR-row columns whose tap j = kTapW dh + dw starts at row dh + kTallR dw
+// (8-row groups kTallR * 128 bytes apart); kTallR = 0: a plain box, tap j one column (1024 bytes) on.
+template <int kTaps, int kTallR, int kTapW, int kGroup>
 __device__ __forceinline__ bool mma_box(uint32_t d_tmem, uint32_t a_box, uint32_t b_stage, uint64_t* full_b,
                                         uint64_t* empty_b, uint32_t phb, uint32_t idesc, bool first, unsigned* err) {
   static_assert(kTaps % kGroup == 0, "whole groups of taps");
-  const uint64_t a0 = kTall ? smem_desc_sw128(a_box, kTallRows * 128) : smem_desc_sw128(a_box);
+  const uint64_t a0 = kTallR ? smem_desc_sw128(a_box, kTallR * 128) : smem_desc_sw128(a_box);
   const uint64_t b0 = smem_desc_sw128(b_stage);
 #pragma unroll
   for (int j = 0; j < kTaps; ++j) {
@@ -250,9 +260,8 @@ __device__ __forceinline__ bool mma_box(uint32_t d_tmem, uint32_t a_box, uint32_
       if (!mbar_wait_cluster(&full_b[j], phb, err, kDevErrTimeoutMma)) return false;
       tc_fence_after();
     }
-    // Tap j: plain box, the next column (1024 bytes on); tall box, rows dh + 10 dw of its
-    // 10-row columns (tap j = 3 dh + dw), columns 1280 bytes apart.
-    const uint64_t aj = a0 + (kTall ? (uint64_t)(((j % 3) * kTallRows + j / 3) * 8) : (uint64_t)j * kShiftDesc);
+    const uint64_t aj =
+        a0 + (kTallR ? (uint64_t)(((j % kTapW) * kTallR + j / kTapW) * 8) : (uint64_t)j * kShiftDesc);
     const uint64_t bj = b0 + (uint64_t)j * (kBBytes >> 4);
 #pragma unroll
     for (int k = 0; k < kBlockK / 16; ++k)
@@ -284,16 +293,17 @@ __device__ __forceinline__ bool mma_two_boxes(uint32_t d_tmem, uint32_t a_box, u
   return true;
 }
 
-template <bool kNorm>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads, 1)
+template <int kKind>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kKind>::kThreads, 1)
     conv_tc2_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_cache,
                     const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_w64,
                     const Conv2Args args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  constexpr int kAStages = Cfg<kNorm>::kAStages, kBStages = Cfg<kNorm>::kBStages;
-  constexpr int kBOffset = Cfg<kNorm>::kBOffset, kAStride = Cfg<kNorm>::kAStride, kABox = Cfg<kNorm>::kABox;
-  uint64_t* full_a = reinterpret_cast<uint64_t*>(smem + Cfg<kNorm>::kBarOffset);
+  constexpr bool kNorm = Cfg<kKind>::kNorm, kPhase = Cfg<kKind>::kPhase;
+  constexpr int kAStages = Cfg<kKind>::kAStages, kBStages = Cfg<kKind>::kBStages;
+  constexpr int kBOffset = Cfg<kKind>::kBOffset, kAStride = Cfg<kKind>::kAStride, kABox = Cfg<kKind>::kABox;
+  uint64_t* full_a = reinterpret_cast<uint64_t*>(smem + Cfg<kKind>::kBarOffset);
   uint64_t* empty_a = full_a + kAStages;
   uint64_t* full_b = empty_a + kAStages;
   uint64_t* empty_b = full_b + kBStages;
@@ -314,8 +324,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
   // rows_in rows, K slice, row in the group): mode 0 takes a kernel frame's 3 rows per K slice, so
   // the taps are added in the order (dt, K slice, dh, dw), the prologue kernel's order too, and
   // the two kernels give the same bits.
-  const int rows = kNorm ? 3 : (args.mode == 0 ? 9 : args.mode == 1 ? 2 : args.mode == 2 ? 3 : 1);
-  const int taps_per_row = kNorm ? 9 : (args.mode == 0 ? 3 : args.mode == 1 ? 2 : 1);
+  const int rows = kNorm ? 3 : kPhase ? 1 : (args.mode == 0 ? 9 : args.mode == 1 ? 2 : args.mode == 2 ? 3 : 1);
+  const int taps_per_row = kNorm ? 9 : kPhase ? 4 : (args.mode == 0 ? 3 : args.mode == 1 ? 2 : 1);
   const int rows_in = (!kNorm && args.mode == 0) ? 3 : 1;
   // B stages in use: 8 for boxes of 2 taps (mode 1) and of 1 tap (modes 2, 3), so that no box,
   // and no pair of 1-tap boxes, wraps the ring.
@@ -401,7 +411,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
               // wait for both.
               mbar_arrive_expect_tx(&full_a[sa], kABox + kCoefBytes);
               const int fc = min(max(tau, 0), args.T - 1);
-              bulk_load(smem + Cfg<kNorm>::kCoefOffset + sa * kCoefBytes,
+              bulk_load(smem + Cfg<kKind>::kCoefOffset + sa * kCoefBytes,
                         args.coef + ((size_t)me.n * args.T + fc) * args.Cin + kb * kBlockK, kCoefBytes, &full_a[sa]);
               armed_a |= 1u << sa;
               parity_a = (parity_a & ~(1u << sa)) | (pha << sa);
@@ -411,7 +421,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
                 tma_load_5d(a_dst, &tm_a, &full_a[sa], kb * kBlockK, hh, ww, tau, me.n);
             } else {
               if (leader) {
-                mbar_arrive_expect_tx(&full_a[sa], 2 * kABytes);  // both CTAs' bytes land on it
+                mbar_arrive_expect_tx(&full_a[sa], 2 * kABox);  // both CTAs' bytes land on it
                 armed_a |= 1u << sa;
                 parity_a = (parity_a & ~(1u << sa)) | (pha << sa);
               }
@@ -429,7 +439,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
             // on its first stage's barrier, whose release covers the group. The first time a group's
             // stages are used this way, the full-item MMAs before may still read any of them: all
             // their releases are waited for then.
-            const int bg = sub < 0 ? 1 : (taps_per_row % 3 == 0 ? 3 : taps_per_row == 2 ? 2 : 1);
+            const int bg = sub < 0 ? 1 : (taps_per_row % 3 == 0 ? 3 : taps_per_row == 4 ? 4 : taps_per_row == 2 ? 2 : 1);
             int head = sb;
             for (int j = 0; j < taps_per_row; ++j) {
               if (j % bg == 0) {
@@ -523,21 +533,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
             const uint32_t a_box = a_base + sa * kAStride;
             // Boxes of 9 taps (tall), 3 taps (mode 0) or 2 taps (mode 1, an 8-stage ring) never wrap
             // the B ring: one straight-line burst each. Boxes of 1 tap (modes 2, 3) take the loop.
-            static_assert(kBStages == 9, "9 B stages: whole boxes of 3 and 9 taps");
+            static_assert(kBStages == (kPhase ? 8 : 9), "whole boxes of 3, 4 and 9 taps");
             // Halves (sub >= 0) take their B stages in groups (mma_box); the producer arms them so.
             if (kNorm && sb == 0) {
-              ok = sub >= 0 ? mma_box<9, true, 3>(d_tmem, a_box, b_base, full_b, empty_b, phb, idesc, first, args.err)
-                            : mma_box<9, true, 1>(d_tmem, a_box, b_base, full_b, empty_b, phb, idesc, first, args.err);
+              ok = sub >= 0 ? mma_box<9, kTallRows, 3, 3>(d_tmem, a_box, b_base, full_b, empty_b, phb, idesc, first, args.err)
+                            : mma_box<9, kTallRows, 3, 1>(d_tmem, a_box, b_base, full_b, empty_b, phb, idesc, first, args.err);
               sb = kBStages;
-            } else if (!kNorm && taps_per_row == 3 && sb % 3 == 0) {
+            } else if (kPhase && sb % 4 == 0) {
               const uint32_t bs = b_base + sb * kBBytes;
-              ok = sub >= 0 ? mma_box<3, false, 3>(d_tmem, a_box, bs, full_b + sb, empty_b + sb, phb, idesc, first, args.err)
-                            : mma_box<3, false, 1>(d_tmem, a_box, bs, full_b + sb, empty_b + sb, phb, idesc, first, args.err);
+              ok = sub >= 0 ? mma_box<4, kPhaseRows, 2, 4>(d_tmem, a_box, bs, full_b + sb, empty_b + sb, phb, idesc, first, args.err)
+                            : mma_box<4, kPhaseRows, 2, 1>(d_tmem, a_box, bs, full_b + sb, empty_b + sb, phb, idesc, first, args.err);
+              sb += 4;
+            } else if (!kNorm && !kPhase && taps_per_row == 3 && sb % 3 == 0) {
+              const uint32_t bs = b_base + sb * kBBytes;
+              ok = sub >= 0 ? mma_box<3, 0, 3, 3>(d_tmem, a_box, bs, full_b + sb, empty_b + sb, phb, idesc, first, args.err)
+                            : mma_box<3, 0, 3, 1>(d_tmem, a_box, bs, full_b + sb, empty_b + sb, phb, idesc, first, args.err);
               sb += 3;
-            } else if (!kNorm && taps_per_row == 2 && sb % 2 == 0) {
+            } else if (!kNorm && !kPhase && taps_per_row == 2 && sb % 2 == 0) {
               const uint32_t bs = b_base + sb * kBBytes;
-              ok = sub >= 0 ? mma_box<2, false, 2>(d_tmem, a_box, bs, full_b + sb, empty_b + sb, phb, idesc, first, args.err)
-                            : mma_box<2, false, 1>(d_tmem, a_box, bs, full_b + sb, empty_b + sb, phb, idesc, first, args.err);
+              ok = sub >= 0 ? mma_box<2, 0, 2, 2>(d_tmem, a_box, bs, full_b + sb, empty_b + sb, phb, idesc, first, args.err)
+                            : mma_box<2, 0, 2, 1>(d_tmem, a_box, bs, full_b + sb, empty_b + sb, phb, idesc, first, args.err);
               sb += 2;
             } else {
               const uint64_t a_desc = smem_desc_sw128(a_box);
@@ -547,8 +562,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
                   break;
                 }
                 tc_fence_after();
-                const uint64_t aj = kNorm ? smem_desc_sw128(a_box + ((j % 3) * kTallRows + j / 3) * 128, kTallRows * 128)
-                                          : a_desc + j * kShiftDesc;
+                const uint64_t aj = kNorm    ? smem_desc_sw128(a_box + ((j % 3) * kTallRows + j / 3) * 128, kTallRows * 128)
+                                    : kPhase ? smem_desc_sw128(a_box + ((j % 2) * kPhaseRows + j / 2) * 128, kPhaseRows * 128)
+                                             : a_desc + j * kShiftDesc;
                 const uint64_t b_desc = smem_desc_sw128(b_base + sb * kBBytes);
   #pragma unroll
                 for (int k = 0; k < kBlockK / 16; ++k)
@@ -775,7 +791,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kNorm>::kThreads
     const int jl = pt & 7, r0 = pt >> 3;
     const uint32_t chunk_off = (uint32_t)r0 * 128 + ((uint32_t)(jl ^ (r0 & 7)) << 4);
     const uint32_t ready0 = mapa_shared(smem_u32(&ready_a[0]), 0);
-    const float4* coef_sm = reinterpret_cast<const float4*>(smem + Cfg<kNorm>::kCoefOffset) + jl;  // blocked
+    const float4* coef_sm = reinterpret_cast<const float4*>(smem + Cfg<kKind>::kCoefOffset) + jl;  // blocked
     int sa = 0;
     uint32_t pha = 0;
     bool ok = true;
@@ -918,11 +934,11 @@ bool map_w_half(CUtensorMap* m, const void* base, int K, int Cout, int P, int ro
 
 // Persistent grid: as many CTA pairs as the GPU can hold at once (not every SM can be paired:
 // a pair lives in one GPC), so no pair waits for a second wave.
-template <bool kNorm>
+template <int kKind>
 cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tc, const CUtensorMap& tw, const CUtensorMap& tw64,
                         Conv2Args args, int sms, cudaStream_t stream) {
-  constexpr int kSmem = Cfg<kNorm>::kSmemTotal, kThr = Cfg<kNorm>::kThreads;
-  cudaError_t e = cudaFuncSetAttribute(conv_tc2_kernel<kNorm>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  constexpr int kSmem = Cfg<kKind>::kSmemTotal, kThr = Cfg<kKind>::kThreads;
+  cudaError_t e = cudaFuncSetAttribute(conv_tc2_kernel<kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   static int max_clusters[64] = {0};
   int dev = 0;
@@ -933,7 +949,7 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tc, const CUte
     cfg.blockDim = dim3(kThr, 1, 1);
     cfg.dynamicSmemBytes = kSmem;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, conv_tc2_kernel<kNorm>, &cfg) != cudaSuccess || n <= 0) {
+    if (cudaOccupancyMaxActiveClusters(&n, conv_tc2_kernel<kKind>, &cfg) != cudaSuccess || n <= 0) {
       cudaGetLastError();
       n = sms / 2;
     }
@@ -951,7 +967,7 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tc, const CUte
     args.units = args.items + rem;
   }
   if (clusters > args.units) clusters = args.units;
-  conv_tc2_kernel<kNorm><<<2 * clusters, kThr, kSmem, stream>>>(ta, tc, tw, tw64, args);
+  conv_tc2_kernel<kKind><<<2 * clusters, kThr, kSmem, stream>>>(ta, tc, tw, tw64, args);
   return cudaGetLastError();
 }
 
@@ -1011,7 +1027,7 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
     while ((1 << args.st_lg) < args.st_cg) ++args.st_lg;
   }
   CUtensorMap ta, tc, tw, tw64;
-  const int box_h = coef ? kTallRows : kTileH;  // the prologue kernel loads tall boxes
+  const int box_h = coef ? kTallRows : mode == 1 ? kPhaseRows : kTileH;  // tall boxes: prologue and phase kernels
   if (!map_act_hw(&ta, a, Cin, W, H, T, N, box_h, a_frames)) return cudaErrorInvalidValue;
   if (cache_in) {
     if (!map_act_hw(&tc, cache_in, Cin, W, H, 2, N, box_h)) return cudaErrorInvalidValue;
@@ -1027,9 +1043,10 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
     args.coef = coef;
     args.a = a;
     args.cache_out = cache_out;
-    return launch_pair<true>(ta, tc, tw, tw64, args, sms, stream);
+    return launch_pair<1>(ta, tc, tw, tw64, args, sms, stream);
   }
-  return launch_pair<false>(ta, tc, tw, tw64, args, sms, stream);
+  if (mode == 1) return launch_pair<2>(ta, tc, tw, tw64, args, sms, stream);
+  return launch_pair<0>(ta, tc, tw, tw64, args, sms, stream);
 }
 
 }  // namespace wan
