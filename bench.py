@@ -381,6 +381,36 @@ def time_adjacent(dev, reps=10):
     return out
 
 
+def timed_graph_steps(calls, steps, stream):
+    """Capture two consecutive steps as two CUDA graphs and time `steps` steps replaying them in
+    turn (CUDA events on the stream around the whole timed region)."""
+    import torch
+    try:
+        graphs = []
+        side = torch.cuda.Stream()  # capture runs on a stream of its own; replays go on `stream`
+        side.wait_stream(stream)
+        for _ in range(2):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for _, _, fn in calls:
+                    fn()
+            graphs.append(g)
+        stream.wait_stream(side)
+        for k in range(4):  # warm-up replays
+            graphs[k % 2].replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for k in range(steps):
+            graphs[k % 2].replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return {"ms_per_step": e0.elapsed_time(e1) / steps, "graphs": 2}
+    except Exception as exc:  # capture refused: the eager timing stands
+        torch.cuda.synchronize()
+        return {"unavailable": str(exc).splitlines()[0][:200]}
+
+
 def run_ours(args, rank, world, dev):
     import torch
     from video_vae_decoder_gb300 import binding as wan
@@ -417,6 +447,13 @@ def run_ours(args, rank, world, dev):
     wall = time.perf_counter() - t0
     if world > 1:
         torch.distributed.barrier()
+    assert wan.wan_device_status() == 0
+    # Optionally the same step replayed from CUDA graphs (one per direction of the histories' two
+    # buffers, replayed alternately, so every timed step reads the history the step before wrote),
+    # reported beside the eager step time.
+    graph = timed_graph_steps(calls, args.steps, stream) if args.graph else None
+    if world > 1:
+        torch.distributed.barrier()
     clocks = sampler.stop()
     assert wan.wan_device_status() == 0
 
@@ -426,7 +463,8 @@ def run_ours(args, rank, world, dev):
         step_ms.append(ev[s][0].elapsed_time(ev[s][-1]))
         for i, (tag, _, _) in enumerate(calls):
             per_tag.setdefault(tag, []).append(ev[s][i].elapsed_time(ev[s][i + 1]))
-    ms = max_over_ranks(statistics.mean(step_ms), world, dev)
+    ms_eager = statistics.mean(step_ms)
+    ms = max_over_ranks(ms_eager, world, dev)
     flops = sum(wl.flops.values())
     pk = peaks()
 
@@ -500,7 +538,7 @@ def run_ours(args, rank, world, dev):
             achieved = peak * k["frac"]
         rooflines.append({"kernel": name, "bound": k["bound"], "achieved": achieved, "peak": peak,
                           "unit": "TFLOP/s" if tensor else "GB/s", "frac": k["frac"],
-                          "traffic": traffic.get(name), "share_of_step": k["total_ms"] / ms,
+                          "traffic": traffic.get(name), "share_of_step": k["total_ms"] / ms_eager,
                           "peak_source": (f"{pk['source']} burst bf16 GEMM" if tensor else f"{pk['source']} HBM copy")})
     dom = max(shares, key=shares.get)
     roof = dict(next(r for r in rooflines if r["kernel"] == dom))
@@ -521,6 +559,7 @@ def run_ours(args, rank, world, dev):
                    "flop_count": "direct-convolution FLOPs (2 M N K) for every conv, the Winograd ones included", "l2": "no flush: the step's working set (~8 GB) exceeds L2",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "kernels": kernels, "wall_s_timed": wall, "clocks": clocks, "gpu_launches": launches, "roofline": roof,
+        "ms_per_step_eager": ms_eager, "cuda_graph": graph,
         "rooflines": rooflines,
     }
     if args.case == "all" and not args.no_adjacent:
@@ -683,6 +722,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-adjacent", action="store_true", help="skip timing the steps next to the ResBlock")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step replayed from CUDA graphs (measured no faster: launches are not the limit)")
     ap.add_argument("--head-frames", type=int, default=16,
                     help="frames of the head's input (smaller values make a case small enough for ncu --set full)")
     ap.add_argument("--case", default="all", choices=CASES,
