@@ -524,9 +524,14 @@ def run_ours(args, rank, world, dev):
         tensor_kernel("upsample_phase_conv", per_launch("up.conv"), wl.flops["up"], tot("up.conv"))
     if "gn" in per_tag:
         hbm_kernel("gn_silu_decode_mid", per_launch("gn"), wl.gn_bytes, tot("gn"))
-    # DRAM bytes (read + write) per launch from one `ncu --set full` capture of the current build of
-    # each kernel (profiles/); None where there is none.
-    traffic = {"conv_c256": 172.367104e6 + 76.504064e6}
+    # DRAM bytes (read + write) per launch from `ncu --set full` captures of the current build of
+    # each kernel (profiles/); the head's from a single-pass capture of the 16-frame launch; the
+    # Winograd conv's is its three kernels' sum.
+    traffic = {"conv_c256": 172.434944e6 + 123.60192e6, "gn_coef_c256": 112.545024e6 + 3.172352e6,
+               "gn_coef_c1024": 28.198912e6, "conv_c1024_winograd": (43.088384e6 + 120.969728e6) +
+               (270.3232e6 + 182.370816e6) + (253.05856e6 + 4.851968e6),
+               "upsample_phase_conv": 22.552064e6 + 4.372736e6, "gn_silu_decode_mid": 72.582912e6 + 11.582208e6,
+               "head_256_to_12": 9.9e9 + 0.343e9}
     rooflines = []
     for name, k in kernels.items():
         if not isinstance(k, dict) or "frac" not in k:
