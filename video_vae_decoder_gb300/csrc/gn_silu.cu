@@ -498,24 +498,40 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gn_silu_kernel(const GnArgs 
   if (!grid_barrier(a.bar, 2 * gridDim.x, a.err, &s_flag, a.wait_cycles)) return;
 
   // ---------------------------------------------------------------- C: apply, newest spans first
-  // The frame's coefficients reach shared memory with one bulk copy per CTA (a per-thread load
-  // would send every thread of the grid to the same few L2 lines).
+  // The coefficients reach shared memory with bulk copies (a per-thread load would send every
+  // thread of the grid to the same few L2 lines): those of every frame at once when they fit the
+  // idle slots (a CTA's successive spans usually lie in different frames), else the frame's as
+  // the frame changes.
+  const bool all_coef = (size_t)a.F * a.C * 16 <= (size_t)kSlots * piece_bytes;
   if (tid == 0) {
     mbar_init(&cbar, 1);
     fence_mbarrier_init();
+    if (all_coef) {
+      // Written by other CTAs with ordinary stores (ordered before the grid barrier); the copy
+      // reads them through the async proxy.
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      mbar_arrive_expect_tx(&cbar, (uint32_t)a.F * a.C * 16u);
+      bulk_load(s_coef, a.coef, (uint32_t)a.F * a.C * 16u, &cbar);
+    }
   }
   __syncthreads();
   int fcur = -1;
   uint32_t cphase = 0;
+  if (all_coef) {
+    const bool okc = mbar_wait(&cbar, cphase, a.err, kDevErrTimeoutGrid);
+    cphase ^= 1;
+    if (__syncthreads_or(!okc)) return;
+  }
   GnCoef8 k8;
   for (int k = 0; k < cnt; ++k) {
     const int item = a.items - 1 - (int)(blockIdx.x + k * gridDim.x);  // newest spans first
     const int f = item / a.spans;
-    if (f != fcur) {
+    if (f != fcur && all_coef) {
+      fcur = f;
+      k8 = gn_coef8(s_coef + (size_t)f * a.C + 8 * j);
+    } else if (f != fcur) {
       __syncthreads();  // the previous frame's coefficients have been read
       if (tid == 0) {
-        // Written by other CTAs with ordinary stores (ordered before the grid barrier); the copy
-        // reads them through the async proxy.
         asm volatile("fence.proxy.async.global;" ::: "memory");
         mbar_arrive_expect_tx(&cbar, (uint32_t)a.C * 16u);
         bulk_load(s_coef, a.coef + (size_t)f * a.C, (uint32_t)a.C * 16u, &cbar);
