@@ -321,7 +321,8 @@ def job_tflops(flops_per_rank_step, world, ms_per_step):
 def time_adjacent(dev, reps=10):
     """The decoder steps next to the ResBlock, timed on their own (outside the step): the causal
     3x1x1 time upsample of the widest stage [1,4,44,78,1024] -> [1,8,44,78,1024] with history,
-    and a channel-changing ResBlock 512 -> 256 at [1,4,176,312,512] (1x1x1 shortcut, folded bias).
+    a channel-changing ResBlock 512 -> 256 at [1,4,176,312,512] (1x1x1 shortcut, folded bias), and
+    GroupNorm + SiLU applied on its own at the C=256 chunk size [1,4,176,312,256] (225 MB moved).
     CUDA events around each call, an L2 flush (256 MB written) before each, 3 warm-up calls."""
     import numpy as np
     import torch
@@ -377,6 +378,17 @@ def time_adjacent(dev, reps=10):
     px = 4 * 176 * 312
     fl = 2.0 * px * (27 * Cin * Cout + 27 * Cout * Cout + Cin * Cout)
     out["resblock_shortcut_512_to_256"] = {"ms": ms, "tflops": fl / ms / 1e9, "shape": "[1,4,176,312,512] -> 256"}
+    del x, p, w_sc, c1, c2, o, ws
+    C = 256
+    x = n((1, 4, 176, 312, C), "bench/gn256/x", 0.5, float(np.sqrt(2.0)))
+    g = n((C,), "bench/gn256/gamma", 1.0, 0.1, torch.float32)
+    be = n((C,), "bench/gn256/beta", 0.0, 0.1, torch.float32)
+    y = torch.empty_like(x)
+    ws = torch.empty(wan.wan_workspace_size(wan.WAN_OP_GN_SILU, *x.shape, 0, GROUPS), dtype=torch.uint8, device=dev)
+    ms = timed(lambda: wan.wan_gn_silu(x, g, be, GROUPS, EPS, y, ws))
+    gbs = 4.0 * x.numel() / ms / 1e6
+    out["gn_silu_c256_chunk"] = {"ms": ms, "gbs": gbs, "frac": gbs / peaks()["hbm_gbs"],
+                                 "shape": "[1,4,176,312,256], 4 B per element (x read, y written)"}
     assert wan.wan_device_status() == 0
     return out
 
@@ -527,10 +539,10 @@ def run_ours(args, rank, world, dev):
     # DRAM bytes (read + write) per launch from `ncu --set full` captures of the current build of
     # each kernel (profiles/); the head's from a single-pass capture of the 16-frame launch; the
     # Winograd conv's is its three kernels' sum.
-    traffic = {"conv_c256": 172.434944e6 + 123.60192e6, "gn_coef_c256": 112.545024e6 + 3.172352e6,
+    traffic = {"conv_c256": 172.434944e6 + 123.60192e6, "gn_coef_c256": 112.548352e6 + 3.560192e6,
                "gn_coef_c1024": 28.198912e6, "conv_c1024_winograd": (43.088384e6 + 120.969728e6) +
                (270.3232e6 + 182.370816e6) + (253.05856e6 + 4.851968e6),
-               "upsample_phase_conv": 22.552064e6 + 4.372736e6, "gn_silu_decode_mid": 72.582912e6 + 11.582208e6,
+               "upsample_phase_conv": 22.552064e6 + 4.372736e6, "gn_silu_decode_mid": 72.386816e6 + 12.526336e6,
                "head_256_to_12": 9.9e9 + 0.343e9}
     rooflines = []
     for name, k in kernels.items():

@@ -93,6 +93,7 @@ constexpr int kVecPerThread = 8;   // 16-byte vectors per thread per piece
 constexpr int kPiecesPerSpan = 2;  // a statistics partial covers 2 pieces (about 64 KB)
 constexpr int kApplyUnroll = 8;    // 16-byte loads in flight per thread in the apply phase
 constexpr int kFinBatch = 8;       // partials in flight per lane in the finalize
+constexpr int kFinBatchSpans = 16; // the same for the span partials (one round of loads up to 512 spans)
 
 struct GnArgs {
   const wan_bf16* x;
@@ -406,6 +407,10 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gn_silu_kernel(const GnArgs 
         continue;
       }
       const int f = pr / a.G, g = pr - f * a.G;
+      // The lane's gamma and beta (and below, the group's shift) are loaded with the partials, not
+      // after them: the finalize is a chain of round trips to L2, one of them instead of three.
+      const float gam0 = lane < cg ? __ldg(a.gamma + g * cg + lane) : 0.f;
+      const float bet0 = lane < cg ? __ldg(a.beta + g * cg + lane) : 0.f;
       // Float-float sums (fp64 issue is scarce on this GPU): lane-strided, then a butterfly.
       // The float-float add is commutative bit for bit (TwoSum's error term is unique), so every
       // lane ends with the same bits.
@@ -446,20 +451,21 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gn_silu_kernel(const GnArgs 
         shift = (double)s;
       } else {
         const float4* src = reinterpret_cast<const float4*>(a.part) + ((size_t)f * a.G + g) * a.spans;
-        for (int sp0 = 0; sp0 < a.spans; sp0 += 32 * kFinBatch) {
-          float4 q[kFinBatch];
+        const float sh = bf16_at(a.x + (size_t)f * a.P * a.C + (size_t)g * cg);
+        for (int sp0 = 0; sp0 < a.spans; sp0 += 32 * kFinBatchSpans) {
+          float4 q[kFinBatchSpans];
 #pragma unroll
-          for (int i = 0; i < kFinBatch; ++i) {
+          for (int i = 0; i < kFinBatchSpans; ++i) {
             const int sp = sp0 + lane + 32 * i;
             q[i] = sp < a.spans ? __ldcg(src + sp) : make_float4(0.f, 0.f, 0.f, 0.f);
           }
 #pragma unroll
-          for (int i = 0; i < kFinBatch; ++i) {  // adding (0, 0) to a normalised pair changes nothing
+          for (int i = 0; i < kFinBatchSpans; ++i) {  // adding (0, 0) to a normalised pair changes nothing
             ff_add(h1, l1, q[i].x, q[i].y);
             ff_add(h2, l2, q[i].z, q[i].w);
           }
         }
-        shift = (double)bf16_at(a.x + (size_t)f * a.P * a.C + (size_t)g * cg);
+        shift = (double)sh;
       }
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -486,8 +492,8 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gn_silu_kernel(const GnArgs 
       }
       for (int kk = lane; kk < cg; kk += 32) {
         const int c = g * cg + kk;
-        const double S = (double)a.gamma[c] * rstd;
-        const double B = (double)a.beta[c] - mean * S;
+        const double S = (double)(kk == lane ? gam0 : a.gamma[c]) * rstd;
+        const double B = (double)(kk == lane ? bet0 : a.beta[c]) - mean * S;
         const float shi = (float)S, bhi = (float)B;
         a.coef[(size_t)f * a.C + (a.coef_blocked ? coef_blocked_index(c) : c)] =
             make_float4(shi, (float)(S - (double)shi), bhi, (float)(B - (double)bhi));
