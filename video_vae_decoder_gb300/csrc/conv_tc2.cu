@@ -72,18 +72,30 @@ static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "stages keep the 1024-
 // the GroupNorm + SiLU operand prologue: 8 more warps that normalise each A box in place between
 // its arrival and the MMAs.
 // Kernel kinds: 0 plain, 1 with the GroupNorm + SiLU operand prologue (mode 0), 2 the phase
-// convolutions of mode 1 with one tall A box per K block.
+// convolutions of mode 1 with one tall A box per K block, 3 kind 1 on tiles of 16 rows x 8
+// columns (boxes stored row by row; chosen where it pads the frame less, e.g. 176 x 312).
 template <int kKind>
 struct Cfg {
-  static constexpr bool kNorm = kKind == 1;
+  static constexpr bool kNorm = kKind == 1 || kKind == 3;
   static constexpr bool kPhase = kKind == 2;
+  // Tile orientation. kWFast: the tile is 16 rows x 8 columns and its boxes land in shared memory
+  // row by row (the tensor map lists W before H), TMEM row m = w + 8 h; otherwise 8 rows x 16
+  // columns, column by column, m = h + 8 w. Either way an 8-row swizzle atom is 8 consecutive
+  // pixels along the fast dimension.
+  static constexpr bool kWFast = kKind == 3;
+  static constexpr int kTH = kWFast ? 16 : kTileH, kTW = kWFast ? 8 : kTileW;
+  // The norm kernel's tall box: the tile plus one halo pixel on each side in both dimensions;
+  // kSlow = its pixels along the fast dimension (the stride, in 128-byte rows, from one line of
+  // the box to the next, and the descriptors' 8-row group stride).
+  static constexpr int kBoxRowsH = kTH + 2, kBoxColsW = kTW + 2;
+  static constexpr int kSlow = kWFast ? kBoxColsW : kBoxRowsH;
   static constexpr int kThreads = kNorm ? 448 : 192;  // + 8 prologue warps
   // kNorm: one tall A box per (kernel frame, 64 channels), 10 x 18 pixels, serves all 9 taps of
   // that frame (the plain kernel loads one 8 x 18 box per kernel row, for its 3 taps), so every
   // pixel is normalised once per box instead of three times.
   // kPhase: one 9 x 18 box per 64 channels serves the 4 taps (u, v) of a phase, at row offsets
   // u + 9 v (the plain kernel loads one 8 x 18 box per tap row u, for its 2 taps).
-  static constexpr int kABox = kNorm ? kTallRows * kBoxW * 128 : kPhase ? kPhaseRows * kBoxW * 128 : kABytes;
+  static constexpr int kABox = kNorm ? kBoxRowsH * kBoxColsW * 128 : kPhase ? kPhaseRows * kBoxW * 128 : kABytes;
   static constexpr int kAStride = (kABox + 1023) / 1024 * 1024;
   static constexpr int kAStages = kNorm ? 3 : 4;
   static constexpr int kBStages = kPhase ? 8 : 9;  // 4-tap boxes: two per ring
@@ -93,8 +105,11 @@ struct Cfg {
   static constexpr int kBarOffset = kCoefOffset + (kNorm ? kAStages * kCoefBytes : 0);
   static constexpr int kSmemTotal = kBarOffset + 512 + 1024;
 };
-static_assert(Cfg<0>::kSmemTotal <= 232448 && Cfg<1>::kSmemTotal <= 232448 && Cfg<2>::kSmemTotal <= 232448,
+static_assert(Cfg<0>::kSmemTotal <= 232448 && Cfg<1>::kSmemTotal <= 232448 && Cfg<2>::kSmemTotal <= 232448 &&
+                  Cfg<3>::kSmemTotal <= 232448,
               "shared memory per CTA");
+static_assert(Cfg<1>::kABox == Cfg<3>::kABox && Cfg<3>::kBoxRowsH == 18 && Cfg<3>::kBoxColsW == 10,
+              "both orientations of the norm kernel use 180-pixel tall boxes");
 
 struct Conv2Args {
   int N, T, H, W, Cin, Cout;
@@ -137,6 +152,7 @@ struct PTile {
 
 // item -> N block (fastest), phase, pixel pair; `which` picks the pair's first or second tile.
 // Pixel tiles are numbered frame-fastest, so concurrently running pairs share input frames in L2.
+template <int kKind>
 __device__ __forceinline__ PTile decode_pair(const Conv2Args& a, int item, int which) {
   PTile t;
   t.nb = item % a.n_blks;
@@ -148,9 +164,9 @@ __device__ __forceinline__ PTile decode_pair(const Conv2Args& a, int item, int w
   if (!t.valid) px = 2 * item;
   t.t0 = px % a.T;
   px /= a.T;
-  t.w0 = (px % a.tiles_w) * kTileW;
+  t.w0 = (px % a.tiles_w) * Cfg<kKind>::kTW;
   px /= a.tiles_w;
-  t.h0 = (px % a.tiles_h) * kTileH;
+  t.h0 = (px % a.tiles_h) * Cfg<kKind>::kTH;
   t.n = px / a.tiles_h;
   return t;
 }
@@ -248,7 +264,9 @@ __device__ __forceinline__ void st_reduce8(const float (&vh)[8], const float (&v
 // wait and one commit serve kGroup taps.
 // kTallR > 0: a tall box of kTallR-row columns whose tap j = kTapW dh + dw starts at row dh + kTallR dw
 // (8-row groups kTallR * 128 bytes apart); kTallR = 0: a plain box, tap j one column (1024 bytes) on.
-template <int kTaps, int kTallR, int kTapW, int kGroup>
+// kRowMajor: the box is stored row by row with kTallR pixels per row, so tap j starts at row
+// kTallR dh + dw (8-row groups one box row apart).
+template <int kTaps, int kTallR, int kTapW, int kGroup, bool kRowMajor = false>
 __device__ __forceinline__ bool mma_box(uint32_t d_tmem, uint32_t a_box, uint32_t b_stage, uint64_t* full_b,
                                         uint64_t* empty_b, uint32_t phb, uint32_t idesc, bool first, unsigned* err) {
   static_assert(kTaps % kGroup == 0, "whole groups of taps");
@@ -261,7 +279,8 @@ __device__ __forceinline__ bool mma_box(uint32_t d_tmem, uint32_t a_box, uint32_
       tc_fence_after();
     }
     const uint64_t aj =
-        a0 + (kTallR ? (uint64_t)(((j % kTapW) * kTallR + j / kTapW) * 8) : (uint64_t)j * kShiftDesc);
+        a0 + (kTallR ? (uint64_t)((kRowMajor ? (j / kTapW) * kTallR + j % kTapW : (j % kTapW) * kTallR + j / kTapW) * 8)
+                     : (uint64_t)j * kShiftDesc);
     const uint64_t bj = b0 + (uint64_t)j * (kBBytes >> 4);
 #pragma unroll
     for (int k = 0; k < kBlockK / 16; ++k)
@@ -379,8 +398,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kKind>::kThreads
       if (unit < 0) continue;
       int sub;
       const int item = unit_item(args, unit, sub);
-      const PTile me = decode_pair(args, item, (int)rank);
-      const PTile p0 = decode_pair(args, item, 0), p1 = decode_pair(args, item, 1);
+      const PTile me = decode_pair<kKind>(args, item, (int)rank);
+      const PTile p0 = decode_pair<kKind>(args, item, 0), p1 = decode_pair<kKind>(args, item, 1);
       // This CTA's weight rows: half of the N block, or half of the unit's 128-channel half.
       const int brow = me.nb * kN + (sub < 0 ? (int)rank * 128 : sub * 128 + (int)rank * 64);
       const CUtensorMap* wmap = sub < 0 ? &tm_w : &tm_w64;
@@ -415,10 +434,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kKind>::kThreads
                         args.coef + ((size_t)me.n * args.T + fc) * args.Cin + kb * kBlockK, kCoefBytes, &full_a[sa]);
               armed_a |= 1u << sa;
               parity_a = (parity_a & ~(1u << sa)) | (pha << sa);
+              // the tensor map lists the box's fast dimension first: (c, h, w) or, kWFast, (c, w, h)
+              const int d1 = Cfg<kKind>::kWFast ? ww : hh, d2 = Cfg<kKind>::kWFast ? hh : ww;
               if (tau < 0 && args.has_cache)
-                tma_load_5d(a_dst, &tm_cache, &full_a[sa], kb * kBlockK, hh, ww, tau + 2, me.n);
+                tma_load_5d(a_dst, &tm_cache, &full_a[sa], kb * kBlockK, d1, d2, tau + 2, me.n);
               else
-                tma_load_5d(a_dst, &tm_a, &full_a[sa], kb * kBlockK, hh, ww, tau, me.n);
+                tma_load_5d(a_dst, &tm_a, &full_a[sa], kb * kBlockK, d1, d2, tau, me.n);
             } else {
               if (leader) {
                 mbar_arrive_expect_tx(&full_a[sa], 2 * kABox);  // both CTAs' bytes land on it
@@ -493,7 +514,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kKind>::kThreads
       int sub;
       const int item = unit_item(args, unit, sub);
       const uint32_t idesc = sub < 0 ? idesc_full : idesc_half;  // a half: the first 128 columns
-      const PTile p0 = decode_pair(args, item, 0), p1 = decode_pair(args, item, 1);
+      const PTile p0 = decode_pair<kKind>(args, item, 0), p1 = decode_pair<kKind>(args, item, 1);
       if (!mbar_wait_cluster(&tmem_empty[acc], acc_phase ^ 1, args.err, kDevErrTimeoutMma)) break;
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * kN;
@@ -536,8 +557,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kKind>::kThreads
             static_assert(kBStages == (kPhase ? 8 : 9), "whole boxes of 3, 4 and 9 taps");
             // Halves (sub >= 0) take their B stages in groups (mma_box); the producer arms them so.
             if (kNorm && sb == 0) {
-              ok = sub >= 0 ? mma_box<9, kTallRows, 3, 3>(d_tmem, a_box, b_base, full_b, empty_b, phb, idesc, first, args.err)
-                            : mma_box<9, kTallRows, 3, 1>(d_tmem, a_box, b_base, full_b, empty_b, phb, idesc, first, args.err);
+              constexpr int kS = Cfg<kKind>::kSlow;
+              constexpr bool kR = Cfg<kKind>::kWFast;
+              ok = sub >= 0 ? mma_box<9, kS, 3, 3, kR>(d_tmem, a_box, b_base, full_b, empty_b, phb, idesc, first, args.err)
+                            : mma_box<9, kS, 3, 1, kR>(d_tmem, a_box, b_base, full_b, empty_b, phb, idesc, first, args.err);
               sb = kBStages;
             } else if (kPhase && sb % 4 == 0) {
               const uint32_t bs = b_base + sb * kBBytes;
@@ -562,7 +585,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kKind>::kThreads
                   break;
                 }
                 tc_fence_after();
-                const uint64_t aj = kNorm    ? smem_desc_sw128(a_box + ((j % 3) * kTallRows + j / 3) * 128, kTallRows * 128)
+                const uint64_t aj = kNorm    ? smem_desc_sw128(a_box + (Cfg<kKind>::kWFast ? (j / 3) * Cfg<kKind>::kSlow + j % 3
+                                                                                    : (j % 3) * Cfg<kKind>::kSlow + j / 3) * 128,
+                                                               Cfg<kKind>::kSlow * 128)
                                     : kPhase ? smem_desc_sw128(a_box + ((j % 2) * kPhaseRows + j / 2) * 128, kPhaseRows * 128)
                                              : a_desc + j * kShiftDesc;
                 const uint64_t b_desc = smem_desc_sw128(b_base + sb * kBBytes);
@@ -617,12 +642,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kKind>::kThreads
       if (unit < 0) continue;
       int sub;
       const int item = unit_item(args, unit, sub);
-      const PTile t = decode_pair(args, item, (int)rank);
+      const PTile t = decode_pair<kKind>(args, item, (int)rank);
       const int ncols = sub < 0 ? kN : kN / 2;                  // accumulator columns of the unit
       const int cbase = t.nb * kN + (sub > 0 ? kN / 2 : 0);     // its first output channel
       if (!mbar_wait_cluster(&tmem_full[acc], acc_phase, args.err, kDevErrTimeoutEpilogue)) break;
       tc_fence_after();
-      const int hh = t.h0 + (row & (kTileH - 1)), ww = t.w0 + row / kTileH;  // TMEM row = h + 8 w
+      // TMEM row = h + 8 w, or w + 8 h for the 16 x 8 tiles
+      const int hh = t.h0 + (Cfg<kKind>::kWFast ? row / 8 : row & 7), ww = t.w0 + (Cfg<kKind>::kWFast ? row & 7 : row / 8);
       const int tt = t.t0;
       const bool valid = t.valid && hh < args.H && ww < args.W;
       size_t pix;
@@ -785,8 +811,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kKind>::kThreads
     // would have written). Boxes of the cache (already normalised) and rows of zero padding are
     // left as loaded. Thread t of the 256 owns the 16-byte chunk jl = t % 8 (channels 8 jl ..
     // 8 jl + 7 of the box's 64) of rows r0 + 32 i, r0 = t / 8, of the box's 180 rows
-    // (row = h + 10 c, c the column); the swizzle puts the chunk at jl ^ (row % 8) = jl ^ (r0 % 8).
-    constexpr int kRows = kTallRows * kBoxW;
+    // (row = h + 10 c for the 8 x 16 tiles' 10 x 18 boxes, c the column; row = c + 10 h for the
+    // 16 x 8 tiles' 18 x 10 boxes); the swizzle puts the chunk at jl ^ (row % 8) = jl ^ (r0 % 8).
+    constexpr int kRows = Cfg<kKind>::kBoxRowsH * Cfg<kKind>::kBoxColsW;
+    constexpr int kSl = Cfg<kKind>::kSlow;
+    constexpr bool kWF = Cfg<kKind>::kWFast;
     const int pt = (int)threadIdx.x - 192;
     const int jl = pt & 7, r0 = pt >> 3;
     const uint32_t chunk_off = (uint32_t)r0 * 128 + ((uint32_t)(jl ^ (r0 & 7)) << 4);
@@ -801,8 +830,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kKind>::kThreads
       if (unit < 0) continue;
       int sub;
       const int item = unit_item(args, unit, sub);
-      const PTile me = decode_pair(args, item, (int)rank);
-      const PTile p0 = decode_pair(args, item, 0), p1 = decode_pair(args, item, 1);
+      const PTile me = decode_pair<kKind>(args, item, (int)rank);
+      const PTile p0 = decode_pair<kKind>(args, item, 0), p1 = decode_pair<kKind>(args, item, 1);
       for (int row = 0; ok && row < rows; ++row) {
         const int dt = row - 2;
         if (skip_pair(args, p0, p1, dt)) continue;
@@ -826,7 +855,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kKind>::kThreads
 #pragma unroll
             for (int i = 0; i < 6; ++i) {
               const int rr = r0 + 32 * i;
-              const int hh = me.h0 - 1 + rr % kTallRows, ww = me.w0 - 1 + rr / kTallRows;
+              const int hh = me.h0 - 1 + (kWF ? rr / kSl : rr % kSl), ww = me.w0 - 1 + (kWF ? rr % kSl : rr / kSl);
               if (rr < kRows && hh >= 0 && hh < args.H && ww >= 0 && ww < args.W) {
                 bool sl;
                 uint4* q = reinterpret_cast<uint4*>(box + i * 4096);
@@ -840,7 +869,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kKind>::kThreads
               for (int i = 0; i < 6; ++i) {
                 if ((slow >> i) & 1) {
                   const int rr = r0 + 32 * i;
-                  const int hh = me.h0 - 1 + rr % kTallRows, ww = me.w0 - 1 + rr / kTallRows;
+                  const int hh = me.h0 - 1 + (kWF ? rr / kSl : rr % kSl), ww = me.w0 - 1 + (kWF ? rr % kSl : rr / kSl);
                   const size_t px = (((size_t)me.n * args.T + tau) * args.H + hh) * args.W + ww;
                   const uint4 xv = *reinterpret_cast<const uint4*>(src + px * args.Cin);
                   *reinterpret_cast<uint4*>(box + i * 4096) = gn_silu8(xv, k8);
@@ -864,9 +893,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kKind>::kThreads
                             (size_t)kb * kBlockK + 8 * jl;
 #pragma unroll
             for (int i = 0; i < 6; ++i) {
-              const int rr = r0 + 32 * i, rh = rr % kTallRows, rc = rr / kTallRows;
+              const int rr = r0 + 32 * i, rh = kWF ? rr / kSl : rr % kSl, rc = kWF ? rr % kSl : rr / kSl;
               const int hh = me.h0 - 1 + rh, ww = me.w0 - 1 + rc;
-              if (rr < kRows && rh >= 1 && rh <= kTileH && rc >= 1 && rc <= kTileW && hh < args.H && ww < args.W)
+              if (rr < kRows && rh >= 1 && rh <= Cfg<kKind>::kTH && rc >= 1 && rc <= Cfg<kKind>::kTW && hh < args.H &&
+                  ww < args.W)
                 __stcs(reinterpret_cast<int4*>(dst + ((size_t)hh * args.W + ww) * args.Cin),
                        *reinterpret_cast<const int4*>(box + i * 4096));  // streamed: L2 keeps the conv's operands
             }
@@ -913,6 +943,23 @@ bool map_act_hw(CUtensorMap* m, const void* base, int C, int W, int H, int T, in
   const cuuint64_t strides[4] = {(cuuint64_t)W * C * e, C * e, (cuuint64_t)H * W * C * e,
                                  (cuuint64_t)n_frames * H * W * C * e};
   const cuuint32_t box[5] = {(cuuint32_t)kBlockK, (cuuint32_t)box_h, (cuuint32_t)kBoxW, 1, 1};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same activations addressed as (c, w, h, t, n) for the 16 x 8 tiles: a box of 18 rows x 10
+// columns lands in shared memory row by row (row m = w + 10 h).
+bool map_act_wh(CUtensorMap* m, const void* base, int C, int W, int H, int T, int N, int n_frames = 0) {
+  auto fn = encode_fn2();
+  if (!fn) return false;
+  if (n_frames < T) n_frames = T;
+  const cuuint64_t dims[5] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)N};
+  const cuuint64_t e = 2;
+  const cuuint64_t strides[4] = {C * e, (cuuint64_t)W * C * e, (cuuint64_t)H * W * C * e,
+                                 (cuuint64_t)n_frames * H * W * C * e};
+  const cuuint32_t box[5] = {(cuuint32_t)kBlockK, (cuuint32_t)Cfg<3>::kBoxColsW, (cuuint32_t)Cfg<3>::kBoxRowsH, 1, 1};
   const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -1003,8 +1050,13 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
   args.W = W;
   args.Cin = Cin;
   args.Cout = Cout;
-  args.tiles_h = cdiv(H, kTileH);
-  args.tiles_w = cdiv(W, kTileW);
+  // The norm kernel takes 16 x 8 tiles where they cover the frame with fewer tiles than 8 x 16 ones
+  // (176 x 312: 429 tiles against 440, whose last column is half padding). Every output element
+  // gets the same K steps in the same order either way.
+  const bool wfast = coef != nullptr && mode == 0 &&
+                     (long long)cdiv(H, Cfg<3>::kTH) * cdiv(W, Cfg<3>::kTW) < (long long)cdiv(H, kTileH) * cdiv(W, kTileW);
+  args.tiles_h = cdiv(H, wfast ? Cfg<3>::kTH : kTileH);
+  args.tiles_w = cdiv(W, wfast ? Cfg<3>::kTW : kTileW);
   args.px_tiles = N * T * args.tiles_h * args.tiles_w;
   args.px_pairs = cdiv(args.px_tiles, 2);
   args.n_blks = cdiv(Cout, kN);
@@ -1019,8 +1071,8 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
   args.err = err;
   args.y_frames = y_frames;
   args.y_frame0 = y_frame0;
-  if (st_buf) {
-    if (mode != 0 || !conv_gn_stats_supported(Cout, st_groups)) return cudaErrorInvalidValue;
+  if (st_buf) {  // the plain kernel's epilogue (not with the operand prologue)
+    if (mode != 0 || coef || !conv_gn_stats_supported(Cout, st_groups)) return cudaErrorInvalidValue;
     args.st_rec = reinterpret_cast<float4*>(st_buf);
     args.st_meta = reinterpret_cast<float2*>(args.st_rec + (size_t)N * T * st_groups * conv_gn_stats_parts(H, W));
     args.st_cg = Cout / st_groups;
@@ -1028,9 +1080,11 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
   }
   CUtensorMap ta, tc, tw, tw64;
   const int box_h = coef ? kTallRows : mode == 1 ? kPhaseRows : kTileH;  // tall boxes: prologue and phase kernels
-  if (!map_act_hw(&ta, a, Cin, W, H, T, N, box_h, a_frames)) return cudaErrorInvalidValue;
+  if (wfast ? !map_act_wh(&ta, a, Cin, W, H, T, N, a_frames) : !map_act_hw(&ta, a, Cin, W, H, T, N, box_h, a_frames))
+    return cudaErrorInvalidValue;
   if (cache_in) {
-    if (!map_act_hw(&tc, cache_in, Cin, W, H, 2, N, box_h)) return cudaErrorInvalidValue;
+    if (wfast ? !map_act_wh(&tc, cache_in, Cin, W, H, 2, N) : !map_act_hw(&tc, cache_in, Cin, W, H, 2, N, box_h))
+      return cudaErrorInvalidValue;
   } else {
     tc = ta;
   }
@@ -1043,7 +1097,7 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
     args.coef = coef;
     args.a = a;
     args.cache_out = cache_out;
-    return launch_pair<1>(ta, tc, tw, tw64, args, sms, stream);
+    return wfast ? launch_pair<3>(ta, tc, tw, tw64, args, sms, stream) : launch_pair<1>(ta, tc, tw, tw64, args, sms, stream);
   }
   if (mode == 1) return launch_pair<2>(ta, tc, tw, tw64, args, sms, stream);
   return launch_pair<0>(ta, tc, tw, tw64, args, sms, stream);
