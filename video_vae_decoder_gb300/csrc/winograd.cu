@@ -201,23 +201,26 @@ __global__ void __launch_bounds__(kInThreads) wino_input_kernel(const WinoInArgs
         e[r][c][0] = unpack2(wv.x);
         e[r][c][1] = unpack2(wv.y);
       }
+    // Two channels per packed fp32x2 operation (sub2 = an FMA by -1: the same rounding as a - b).
     uint32_t out[16][2];
 #pragma unroll
     for (int w = 0; w < 2; ++w) {
       float2 sr[4][4];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        sr[0][c] = make_float2(e[0][c][w].x - e[2][c][w].x, e[0][c][w].y - e[2][c][w].y);
-        sr[1][c] = make_float2(e[1][c][w].x + e[2][c][w].x, e[1][c][w].y + e[2][c][w].y);
-        sr[2][c] = make_float2(e[2][c][w].x - e[1][c][w].x, e[2][c][w].y - e[1][c][w].y);
-        sr[3][c] = make_float2(e[1][c][w].x - e[3][c][w].x, e[1][c][w].y - e[3][c][w].y);
+        sr[0][c] = sub2(e[0][c][w], e[2][c][w]);
+        sr[1][c] = __fadd2_rn(e[1][c][w], e[2][c][w]);
+        sr[2][c] = sub2(e[2][c][w], e[1][c][w]);
+        sr[3][c] = sub2(e[1][c][w], e[3][c][w]);
       }
 #pragma unroll
       for (int x = 0; x < 4; ++x) {
-        out[4 * x + 0][w] = pack_f16x2(sr[x][0].x - sr[x][2].x, sr[x][0].y - sr[x][2].y);
-        out[4 * x + 1][w] = pack_f16x2(sr[x][1].x + sr[x][2].x, sr[x][1].y + sr[x][2].y);
-        out[4 * x + 2][w] = pack_f16x2(sr[x][2].x - sr[x][1].x, sr[x][2].y - sr[x][1].y);
-        out[4 * x + 3][w] = pack_f16x2(sr[x][1].x - sr[x][3].x, sr[x][1].y - sr[x][3].y);
+        const float2 o0 = sub2(sr[x][0], sr[x][2]), o1 = __fadd2_rn(sr[x][1], sr[x][2]);
+        const float2 o2 = sub2(sr[x][2], sr[x][1]), o3 = sub2(sr[x][1], sr[x][3]);
+        out[4 * x + 0][w] = pack_f16x2(o0.x, o0.y);
+        out[4 * x + 1][w] = pack_f16x2(o1.x, o1.y);
+        out[4 * x + 2][w] = pack_f16x2(o2.x, o2.y);
+        out[4 * x + 3][w] = pack_f16x2(o3.x, o3.y);
       }
     }
     const size_t row = (size_t)ft * a.tiles + (size_t)(i0 + il) * a.Wt + j0 + tj;
