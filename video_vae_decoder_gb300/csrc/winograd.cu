@@ -460,6 +460,18 @@ __global__ void __launch_bounds__(256) wino_output_kernel(const WinoOutArgs a) {
 #pragma unroll
     for (int xy = 0; xy < 16; ++xy)
       M[xy] = __ldcs(reinterpret_cast<const float4*>(a.mbuf + ((size_t)xy * a.mrows + m) * a.Cout) + q);
+    // the residual of the tile's 4 pixels, loaded with the products rather than after them
+    uint2 res[2][2];
+#pragma unroll
+    for (int pa = 0; pa < 2; ++pa)
+#pragma unroll
+      for (int pb = 0; pb < 2; ++pb) {
+        const int hh = 2 * ti + pa, ww = 2 * tj + pb;
+        res[pa][pb] = (a.residual && hh < a.H && ww < a.W)
+                          ? *reinterpret_cast<const uint2*>(a.residual + (((size_t)f * a.H + hh) * a.W + ww) * a.Cout +
+                                                            (size_t)q * 4)
+                          : make_uint2(0u, 0u);
+      }
     // A^T = [[1, 1, 1, 0], [0, 1, -1, -1]]: z = A^T M (rows), then Y = z A (columns).
     float4 z[2][4];
 #pragma unroll
@@ -501,7 +513,7 @@ __global__ void __launch_bounds__(256) wino_output_kernel(const WinoOutArgs a) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) v[i] += bv[i];
         if (a.residual) {
-          const uint2 r = *reinterpret_cast<const uint2*>(a.residual + px * a.Cout + (size_t)q * 4);
+          const uint2 r = res[pa][pb];
           v[0] += bf16lo_to_f32(r.x);
           v[1] += bf16hi_to_f32(r.x);
           v[2] += bf16lo_to_f32(r.y);
