@@ -540,8 +540,8 @@ def run_ours(args, rank, world, dev):
     # each kernel (profiles/); the head's from a single-pass capture of the 16-frame launch; the
     # Winograd conv's is its three kernels' sum.
     traffic = {"conv_c256": 172.643328e6 + 125.374976e6, "gn_coef_c256": 112.548352e6 + 3.560192e6,
-               "gn_coef_c1024": 28.202752e6, "conv_c1024_winograd": (42.909184e6 + 121.512192e6) +
-               (270.09664e6 + 181.595392e6) + (253.0624e6 + 4.858368e6),
+               "gn_coef_c1024": 28.202496e6, "conv_c1024_winograd": (42.893824e6 + 120.870912e6) +
+               (270.27328e6 + 182.016512e6) + (253.05728e6 + 4.976128e6),
                "upsample_phase_conv": 22.552064e6 + 4.372736e6, "gn_silu_decode_mid": 72.386816e6 + 12.526336e6,
                "head_256_to_12": 9.9e9 + 0.343e9}
     rooflines = []
