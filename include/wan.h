@@ -171,10 +171,11 @@ wan_status wan_causal_conv3d(const wan_bf16* a, const wan_bf16* cache_in, wan_bf
  * cross-op fusion the scope lists after the hot path itself.
  *
  * y and the cache are exactly those of wan_causal_conv3d with the same arguments. stats receives,
- * per (frame, group, 32-pixel quarter of an 8 x 16-pixel tile of the frame), the fp32 sums of d
- * and d^2 of d = y - s over the quarter's pixels and the group's channels, s being one value of
- * the group there, with s and the count; its exact layout is private to this library: pass it
- * unchanged to wan_gn_silu_from_stats with the same N, T, H, W, C = Cout and groups.
+ * per (frame, group, 32-pixel quarter of a 128-pixel tile of the frame), the float-float sums of
+ * d and d^2 of d = y - s over the quarter's pixels and the group's channels, s being one value of
+ * the group there, with s and the count, and a header with the number of such parts; its exact layout is private to this library: pass it
+ * unchanged to wan_gn_silu_from_stats or wan_gn_silu_coefficients_from_stats with the same N, T,
+ * H, W, C = Cout and groups.
  *
  *   groups     GroupNorm groups of the following norm; Cout % 256 == 0, groups divides Cout and
  *              the channels per group are a power of two from 4 to 64 (else
@@ -190,10 +191,11 @@ wan_status wan_causal_conv3d_gn_stats(const wan_bf16* a, const wan_bf16* cache_i
 
 /*
  * GroupNorm + SiLU of x (the definition of wan_gn_silu, per (n, t, group)) using the statistics
- * that wan_causal_conv3d_gn_stats emitted when it wrote x: the per-part sums are moved to one
- * shift and added as float-float pairs in a fixed part order, so the result depends only on x's
- * frames (the same bits in any chunking of the video). y is within one bf16 ulp of the exact
- * (fp64, rounded once) GroupNorm + SiLU, like wan_gn_silu's.
+ * that wan_causal_conv3d_gn_stats (or wan_causal_conv3d_gn_input_stats) emitted when it wrote x:
+ * the per-part sums are moved to one shift and added as float-float pairs in a fixed part order,
+ * so the result depends only on x's frames (the same bits in any chunking of the video). y is
+ * within one bf16 ulp of the exact (fp64, rounded once) GroupNorm + SiLU, like wan_gn_silu's.
+ * A stats buffer not written for these sizes is reported by wan_device_status.
  *
  *   x, y, gamma, beta, groups, eps, ws  as wan_gn_silu (ws >= wan_workspace_size(WAN_OP_GN_SILU,
  *              N, T, H, W, C, 0, groups)).
@@ -204,6 +206,25 @@ wan_status wan_gn_silu_from_stats(const wan_bf16* x, wan_bf16* y, const float* g
                                   int N, int T, int H, int W, int C, int groups, float eps,
                                   const void* stats, size_t stats_bytes, void* ws, size_t ws_bytes,
                                   void* stream);
+
+/*
+ * The per-(frame, channel) coefficients of x's GroupNorm (those wan_gn_silu_coefficients computes
+ * with a pass over x) from the statistics a conv emitted when it wrote x, for a following
+ * wan_causal_conv3d_gn_input: the norm then reads nothing of x beyond what its conv reads. Per
+ * (frame, group) the parts are moved to one shift and added as float-float pairs in a fixed
+ * order (so the result depends only on x's frames), then the mean and variance follow in fp64 as
+ * in wan_gn_silu. The coefficients are those of wan_gn_silu_coefficients up to the rounding of
+ * the sums (a few units in the 24th bit).
+ *
+ *   stats, stats_bytes  as wan_gn_silu_from_stats (C, groups: the conv's Cout and groups).
+ *   gamma, beta, eps    as wan_gn_silu.
+ *   coef       N*T*C*16 bytes, 16-byte aligned, caller-owned: the coefficients, in the layout
+ *              wan_gn_silu_coefficients writes.
+ * A stats buffer not written for these sizes is reported by wan_device_status.
+ */
+wan_status wan_gn_silu_coefficients_from_stats(const void* stats, size_t stats_bytes, const float* gamma,
+                                               const float* beta, int N, int T, int H, int W, int C, int groups,
+                                               float eps, void* coef, void* stream);
 
 /*
  * GroupNorm + SiLU feeding a causal conv, the pair that every ResBlock of the decoder runs twice:
@@ -267,6 +288,24 @@ wan_status wan_causal_conv3d_gn_input(const wan_bf16* x, const void* coef, const
                                       int Cout, void* stream);
 wan_status wan_gn_silu_cache_update(const wan_bf16* x, const void* coef, const wan_bf16* cache_in,
                                     wan_bf16* cache_out, int N, int T, int H, int W, int C, void* stream);
+
+/*
+ * wan_causal_conv3d_gn_input that also emits the GroupNorm statistics of its output y (as
+ * wan_causal_conv3d_gn_stats does for wan_causal_conv3d), so that the norm of the next ResBlock
+ * step gets its coefficients from wan_gn_silu_coefficients_from_stats without a pass over y.
+ * y and cache_out are bit for bit those of wan_causal_conv3d_gn_input.
+ *
+ *   groups, stats, stats_bytes  as wan_causal_conv3d_gn_stats (Cout % 256 == 0, channels per
+ *              group a power of two from 4 to 64; stats_bytes >= wan_workspace_size(
+ *              WAN_OP_GN_STATS, N, T, H, W, Cin, Cout, groups)); stats must not overlap the other
+ *              buffers.
+ *   Other arguments as wan_causal_conv3d_gn_input.
+ */
+wan_status wan_causal_conv3d_gn_input_stats(const wan_bf16* x, const void* coef, const wan_bf16* cache_in,
+                                            wan_bf16* cache_out, const wan_bf16* w, const wan_bf16* bias,
+                                            const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W,
+                                            int Cin, int Cout, int groups, void* stats, size_t stats_bytes,
+                                            void* stream);
 
 /*
  * Temporal-cache update (the cache manager of the causal convolutions), on its own.
@@ -468,7 +507,9 @@ wan_status wan_selftest_wait_timeout(int which, long long wait_cycles, const wan
 /*
  * Synchronises `stream`, then reads and clears the library's device error word on the
  * current device. Returns WAN_ERR_TIMEOUT if a kernel gave up a bounded wait since the last
- * call, WAN_ERR_CUDA if the synchronisation failed, else WAN_OK.
+ * call, else WAN_ERR_INVALID_ARG if a statistics buffer given to wan_gn_silu_from_stats or
+ * wan_gn_silu_coefficients_from_stats did not hold statistics of the call's sizes (the
+ * coefficients were then not written), WAN_ERR_CUDA if the synchronisation failed, else WAN_OK.
  */
 wan_status wan_device_status(void* stream);
 

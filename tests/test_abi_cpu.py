@@ -47,9 +47,12 @@ def test_workspace_sizes(L):
     rb = b.wan_workspace_size(b.WAN_OP_RESBLOCK, 1, 4, 16, 16, 64, 64, 32)
     assert rb >= 2 * 4 * 16 * 16 * 64 * 2
     assert b.wan_workspace_size(b.WAN_OP_GN_SILU, 1, 4, 8, 8, 60, 0, 32) == 0   # groups do not divide C
-    # statistics of a conv output: one (fp64 pair + float pair) per (frame, group, 8x16 tile)
+    # statistics of a conv output: a 256-byte header, then a float4 + float2 per (frame, group, tile,
+    # epilogue warp) for the tiling with more tiles (8 x 16: 22 x 20 at 176 x 312; 16 x 8: 11 x 39)
     st = b.wan_workspace_size(b.WAN_OP_GN_STATS, 1, 4, 176, 312, 256, 256, 32)
-    assert st == 4 * 32 * (22 * 20 * 4) * 24  # float4 + float2 per (frame, group, tile, warp)
+    assert st == 256 + 4 * 32 * (22 * 20 * 4) * 24
+    st = b.wan_workspace_size(b.WAN_OP_GN_STATS, 1, 4, 88, 156, 256, 256, 32)
+    assert st == 256 + 4 * 32 * (6 * 20 * 4) * 24  # 16 x 8 tiles need more here (120 against 110)
     assert b.wan_workspace_size(b.WAN_OP_GN_STATS, 1, 4, 16, 16, 64, 320, 32) == 0   # Cout % 256 != 0
     assert b.wan_workspace_size(b.WAN_OP_GN_STATS, 1, 4, 16, 16, 64, 256, 128) == 0  # 2 channels per group
     assert b.wan_workspace_size(b.WAN_OP_GN_STATS, 1, 4, 16, 16, 64, 768, 64) == 0   # 12 channels per group

@@ -31,6 +31,7 @@ EXPORTS = ("wan_status_string", "wan_workspace_size", "wan_gn_silu", "wan_gn_sil
            "wan_causal_conv3d",
            "wan_causal_conv3d_gn_stats", "wan_gn_silu_from_stats", "wan_gn_silu_causal_conv3d", "wan_gn_silu_coefficients",
            "wan_causal_conv3d_gn_input", "wan_gn_silu_cache_update", "wan_cache_update",
+           "wan_causal_conv3d_gn_input_stats", "wan_gn_silu_coefficients_from_stats",
            "wan_time_upsample", "wan_conv1x1", "wan_fold_bias", "wan_resblock_shortcut",
            "wan_upsample_phase_weights", "wan_upsample_phase_conv", "wan_resblock", "wan_winograd_weights",
            "wan_causal_conv3d_winograd", "wan_resblock_winograd", "wan_selftest_wait_timeout",
@@ -87,6 +88,10 @@ def lib() -> ctypes.CDLL:
     L.wan_causal_conv3d_gn_input.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, P]
     L.wan_gn_silu_cache_update.restype = I
     L.wan_gn_silu_cache_update.argtypes = [P, P, P, P, I, I, I, I, I, P]
+    L.wan_causal_conv3d_gn_input_stats.restype = I
+    L.wan_causal_conv3d_gn_input_stats.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, S, P]
+    L.wan_gn_silu_coefficients_from_stats.restype = I
+    L.wan_gn_silu_coefficients_from_stats.argtypes = [P, S, P, P, I, I, I, I, I, I, F, P, P]
     L.wan_time_upsample.restype = I
     L.wan_time_upsample.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P]
     L.wan_conv1x1.restype = I
@@ -292,6 +297,42 @@ def wan_causal_conv3d_gn_input(x, coef, w, bias=None, residual=None, cache_in=No
                                             _ptr(residual), _ptr(y), N, T, H, W, Cin, Cout, _stream(stream)),
            "wan_causal_conv3d_gn_input")
     return y
+
+
+def wan_causal_conv3d_gn_input_stats(x, coef, w, groups: int, bias=None, residual=None, cache_in=None, y=None,
+                                     stats=None, stream=None, cache_out=None):
+    """wan_causal_conv3d_gn_input that also emits the GroupNorm statistics of y (for `groups` groups)
+    for wan_gn_silu_coefficients_from_stats / wan_gn_silu_from_stats. Returns (y, stats)."""
+    for t, n in ((x, "x"), (w, "w"), (bias, "bias"), (residual, "residual"), (cache_in, "cache_in"),
+                 (cache_out, "cache_out")):
+        _need(t, torch.bfloat16, n)
+    N, T, H, W, Cin = x.shape
+    Cout = w.shape[0]
+    y = torch.empty((N, T, H, W, Cout), dtype=torch.bfloat16, device=x.device) if y is None else y
+    _need(y, torch.bfloat16, "y")
+    need = wan_workspace_size(WAN_OP_GN_STATS, N, T, H, W, Cin, Cout, groups)
+    if need == 0:
+        raise WanError(2, "wan_causal_conv3d_gn_input_stats")
+    stats = _workspace(need, x.device, stats)
+    _check(lib().wan_causal_conv3d_gn_input_stats(_ptr(x), _ptr(coef), _ptr(cache_in), _ptr(cache_out), _ptr(w),
+                                                  _ptr(bias), _ptr(residual), _ptr(y), N, T, H, W, Cin, Cout, groups,
+                                                  _ptr(stats), stats.numel() * stats.element_size(), _stream(stream)),
+           "wan_causal_conv3d_gn_input_stats")
+    return y, stats
+
+
+def wan_gn_silu_coefficients_from_stats(stats, gamma, beta, shape, groups: int, eps: float, coef=None, stream=None):
+    """The GroupNorm + SiLU coefficients of x (shape [N, T, H, W, C]) from the statistics the conv
+    that wrote x emitted: a uint8 device buffer of N*T*C*16 bytes, as wan_gn_silu_coefficients'."""
+    _need(gamma, torch.float32, "gamma")
+    _need(beta, torch.float32, "beta")
+    N, T, H, W, C = shape
+    coef = torch.empty(N * T * C * 16, dtype=torch.uint8, device=stats.device) if coef is None else coef
+    _check(lib().wan_gn_silu_coefficients_from_stats(_ptr(stats), stats.numel() * stats.element_size(), _ptr(gamma),
+                                                     _ptr(beta), N, T, H, W, C, groups, eps, _ptr(coef),
+                                                     _stream(stream)),
+           "wan_gn_silu_coefficients_from_stats")
+    return coef
 
 
 def wan_gn_silu_cache_update(x, coef, cache_out, cache_in=None, stream=None):

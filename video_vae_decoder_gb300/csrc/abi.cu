@@ -222,7 +222,7 @@ wan_status wan_gn_silu_clip(const wan_bf16* x, wan_bf16* y, const float* gamma, 
   if (!ws || ws_bytes < need) return WAN_ERR_WORKSPACE;
   if (!aligned16(ws)) return WAN_ERR_MISALIGNED;
   return cuda_status(gn_silu_launch(x, y, gamma, beta, N, T, H, W, C, groups, eps, ws, sm_count(),
-                                    static_cast<cudaStream_t>(stream), nullptr, 0, true, nullptr, true));
+                                    static_cast<cudaStream_t>(stream), true, nullptr, true));
 }
 
 wan_status wan_gn_silu_from_stats(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta, int N,
@@ -239,8 +239,37 @@ wan_status wan_gn_silu_from_stats(const wan_bf16* x, wan_bf16* y, const float* g
   const size_t need = wan_workspace_size(WAN_OP_GN_SILU, N, T, H, W, C, 0, groups);
   if (!ws || ws_bytes < need) return WAN_ERR_WORKSPACE;
   if (!aligned16(ws)) return WAN_ERR_MISALIGNED;
-  return cuda_status(gn_silu_launch(x, y, gamma, beta, N, T, H, W, C, groups, eps, ws, sm_count(),
-                                    static_cast<cudaStream_t>(stream), stats, conv_gn_stats_parts(H, W)));
+  if (overlap(stats, stats_bytes, y, bytes) || overlap(ws, ws_bytes, y, bytes) || overlap(ws, ws_bytes, stats, stats_bytes))
+    return WAN_ERR_INVALID_ARG;
+  unsigned* err = device_error_word();
+  if (!err) return WAN_ERR_CUDA;
+  // The coefficients from the statistics (into the workspace's coefficient area, blocked), then
+  // the apply pass over every frame.
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float4* coef = const_cast<float4*>(gn_silu_coef(ws, N, T, H, W, C, groups));
+  cudaError_t e = gn_coef_from_stats_launch(stats, stats_bytes, gamma, beta, N, T, H, W, C, groups, eps, coef, true,
+                                            err, s);
+  if (e == cudaSuccess) e = gn_apply_frames_launch(x, coef, y, N, T, H, W, C, 0, T, 0, sm_count(), s);
+  return cuda_status(e);
+}
+
+wan_status wan_gn_silu_coefficients_from_stats(const void* stats, size_t stats_bytes, const float* gamma,
+                                               const float* beta, int N, int T, int H, int W, int C, int groups,
+                                               float eps, void* coef, void* stream) {
+  if (!stats || !gamma || !beta || !coef) return WAN_ERR_INVALID_ARG;
+  if (!positive(N, T, H, W, C) || groups <= 0 || C % groups != 0) return WAN_ERR_INVALID_ARG;
+  if (!(eps > 0.0f) || eps != eps || eps > 3.0e38f) return WAN_ERR_INVALID_ARG;  // as check_gn
+  if (!conv_gn_stats_supported(C, groups) || !gn_silu_supported(C, groups) || !fits(N, T, H, W, C))
+    return WAN_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(stats) || !aligned16(coef) || !aligned16(gamma) || !aligned16(beta)) return WAN_ERR_MISALIGNED;
+  if (stats_bytes < conv_gn_stats_bytes(N, T, H, W, C, groups)) return WAN_ERR_INVALID_ARG;
+  const size_t cbytes = (size_t)N * T * C * 16;
+  if (overlap(stats, stats_bytes, coef, cbytes)) return WAN_ERR_INVALID_ARG;
+  unsigned* err = device_error_word();
+  if (!err) return WAN_ERR_CUDA;
+  return cuda_status(gn_coef_from_stats_launch(stats, stats_bytes, gamma, beta, N, T, H, W, C, groups, eps,
+                                               static_cast<float4*>(coef), true, err,
+                                               static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"
@@ -298,7 +327,7 @@ cudaError_t gn_conv(const wan_bf16* x, const float* gamma, const float* beta, in
     if (e == cudaSuccess && cache_out) e = cache_update_launch(act, cache_in, cache_out, N, T, H, W, Cin, sms, s);
     return e;
   }
-  e = gn_silu_launch(x, nullptr, gamma, beta, N, T, H, W, Cin, groups, eps, ws, sms, s, nullptr, 0, false);
+  e = gn_silu_launch(x, nullptr, gamma, beta, N, T, H, W, Cin, groups, eps, ws, sms, s, false);
   const float4* coef = gn_silu_coef(ws, N, T, H, W, Cin, groups);
   // A cache_out apart from cache_in is written by the conv's prologue itself; in place, the new
   // history can only be written once the conv has read the old one.
@@ -374,17 +403,28 @@ wan_status wan_gn_silu_coefficients(const wan_bf16* x, const float* gamma, const
   if (!ws || ws_bytes < need) return WAN_ERR_WORKSPACE;
   if (!aligned16(ws)) return WAN_ERR_MISALIGNED;
   return cuda_status(gn_silu_launch(x, nullptr, gamma, beta, N, T, H, W, C, groups, eps, ws, sm_count(),
-                                    static_cast<cudaStream_t>(stream), nullptr, 0, false,
-                                    static_cast<float4*>(coef)));
+                                    static_cast<cudaStream_t>(stream), false, static_cast<float4*>(coef)));
 }
 
-wan_status wan_causal_conv3d_gn_input(const wan_bf16* x, const void* coef, const wan_bf16* cache_in, wan_bf16* cache_out,
-                                      const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y,
-                                      int N, int T, int H, int W, int Cin, int Cout, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// wan_causal_conv3d_gn_input and its statistics-emitting form (stats: null, or a buffer of
+// stats_bytes for `groups` groups of y).
+wan_status gn_input_conv(const wan_bf16* x, const void* coef, const wan_bf16* cache_in, wan_bf16* cache_out,
+                         const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T,
+                         int H, int W, int Cin, int Cout, int groups, void* stats, size_t stats_bytes, void* stream) {
   if (!coef) return WAN_ERR_INVALID_ARG;
   wan_status st = check_conv(x, w, y, N, T, H, W, Cin, Cout);
   if (st != WAN_OK) return st;
   if (!gn_conv_fused(Cout)) return WAN_ERR_UNSUPPORTED_SHAPE;
+  if (stats) {
+    if (groups <= 0) return WAN_ERR_INVALID_ARG;
+    if (!conv_gn_stats_supported(Cout, groups)) return WAN_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(stats)) return WAN_ERR_MISALIGNED;
+    if (stats_bytes < conv_gn_stats_bytes(N, T, H, W, Cout, groups)) return WAN_ERR_INVALID_ARG;
+  }
   if (!aligned16(coef) || (cache_in && !aligned16(cache_in)) || (cache_out && !aligned16(cache_out)) ||
       (bias && !aligned16(bias)) || (residual && !aligned16(residual)))
     return WAN_ERR_MISALIGNED;
@@ -395,6 +435,11 @@ wan_status wan_causal_conv3d_gn_input(const wan_bf16* x, const void* coef, const
       overlap(cache_out, cbytes, x, xbytes) || overlap(cache_out, cbytes, coef, (size_t)N * T * Cin * 16) ||
       (cache_in && cache_out && cache_in != cache_out && overlap(cache_in, cbytes, cache_out, cbytes)))
     return WAN_ERR_INVALID_ARG;
+  if (stats && (overlap(stats, stats_bytes, y, ybytes) || overlap(stats, stats_bytes, x, xbytes) ||
+                overlap(stats, stats_bytes, coef, (size_t)N * T * Cin * 16) ||
+                overlap(stats, stats_bytes, cache_out, cbytes) || overlap(stats, stats_bytes, residual, ybytes) ||
+                overlap(stats, stats_bytes, cache_in, cbytes)))
+    return WAN_ERR_INVALID_ARG;
   unsigned* err = device_error_word();
   if (!err) return WAN_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -403,10 +448,30 @@ wan_status wan_causal_conv3d_gn_input(const wan_bf16* x, const void* coef, const
   cudaError_t e = cudaSuccess;
   if (direct && T == 1) e = cache_keep_last(cache_in, cache_out, N, H, W, Cin, s);
   if (e == cudaSuccess)
-    e = conv_pair_launch(0, x, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, sm_count(), err, s, nullptr, 0,
-                         cf, 0, 0, 0, direct ? cache_out : nullptr);
+    e = conv_pair_launch(0, x, cache_in, w, bias, residual, y, N, T, H, W, Cin, Cout, sm_count(), err, s, stats,
+                         stats ? groups : 0, cf, 0, 0, 0, direct ? cache_out : nullptr);
   if (e != cudaSuccess || !cache_out || direct) return cuda_status(e);
   return cuda_status(gn_cache_update(x, cf, cache_in, cache_out, N, T, H, W, Cin, sm_count(), s));
+}
+
+}  // namespace
+
+extern "C" {
+
+wan_status wan_causal_conv3d_gn_input(const wan_bf16* x, const void* coef, const wan_bf16* cache_in, wan_bf16* cache_out,
+                                      const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y,
+                                      int N, int T, int H, int W, int Cin, int Cout, void* stream) {
+  return gn_input_conv(x, coef, cache_in, cache_out, w, bias, residual, y, N, T, H, W, Cin, Cout, 0, nullptr, 0,
+                       stream);
+}
+
+wan_status wan_causal_conv3d_gn_input_stats(const wan_bf16* x, const void* coef, const wan_bf16* cache_in,
+                                            wan_bf16* cache_out, const wan_bf16* w, const wan_bf16* bias,
+                                            const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W, int Cin,
+                                            int Cout, int groups, void* stats, size_t stats_bytes, void* stream) {
+  if (!stats) return WAN_ERR_INVALID_ARG;
+  return gn_input_conv(x, coef, cache_in, cache_out, w, bias, residual, y, N, T, H, W, Cin, Cout, groups, stats,
+                       stats_bytes, stream);
 }
 
 wan_status wan_gn_silu_cache_update(const wan_bf16* x, const void* coef, const wan_bf16* cache_in, wan_bf16* cache_out,
@@ -683,12 +748,11 @@ wan_status wan_resblock_winograd(const wan_bf16* x, wan_bf16* out, const wan_res
   // Each norm's coefficients, the Winograd conv applying them to its input tiles, then the
   // norm's last two frames into that conv's cache (after the conv has read the old ones).
   cudaError_t e = gn_silu_launch(x, nullptr, p->gamma1, p->beta1, N, T, H, W, C, p->groups, p->eps, gws, sms, s,
-                                 nullptr, 0, false, coef);
+                                 false, coef);
   if (e == cudaSuccess) e = wino_conv_launch(x, coef, c1_in, u1, p->b1, nullptr, h, N, T, H, W, C, C, wws, sms, err, s);
   if (e == cudaSuccess) e = gn_cache_update(x, coef, c1_in, cache1, N, T, H, W, C, sms, s);
   if (e == cudaSuccess)
-    e = gn_silu_launch(h, nullptr, p->gamma2, p->beta2, N, T, H, W, C, p->groups, p->eps, gws, sms, s, nullptr, 0,
-                       false, coef);
+    e = gn_silu_launch(h, nullptr, p->gamma2, p->beta2, N, T, H, W, C, p->groups, p->eps, gws, sms, s, false, coef);
   if (e == cudaSuccess) e = wino_conv_launch(h, coef, c2_in, u2, p->b2, x, out, N, T, H, W, C, C, wws, sms, err, s);
   if (e == cudaSuccess) e = gn_cache_update(h, coef, c2_in, cache2, N, T, H, W, C, sms, s);
   return cuda_status(e);
@@ -701,7 +765,7 @@ wan_status wan_device_status(void* stream) {
   if (v) {
     const unsigned zero = 0;
     if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return WAN_ERR_CUDA;
-    return WAN_ERR_TIMEOUT;
+    return (v & ~kDevErrBadStats) ? WAN_ERR_TIMEOUT : WAN_ERR_INVALID_ARG;
   }
   return WAN_OK;
 }

@@ -28,12 +28,16 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
 // cache_out (optional, with coef; never cache_in): receives frames max(T - 2, 0) .. T - 1 of
 // silu(a S + B) at cache frames t - T + 2, written by the prologue from its normalised tiles.
 // GroupNorm statistics of the causal conv's output, emitted by the CTA-pair kernel's epilogue
-// (Cout a multiple of 256, channels per group a power of two from 4 to 64): per (frame, group,
-// 8 x 16-pixel tile, epilogue warp) the float-float sums of d and d^2 of d = y - s as a float4,
-// followed by the (s, count) pairs as float2.
+// (Cout a multiple of 256, channels per group a power of two from 4 to 64; with or without the
+// operand prologue). The buffer: a header of kGnStatsHeader bytes whose first int is q, the
+// records per (frame, group) (pixel tiles x 4 epilogue warps of the launch that wrote them), then
+// per (frame, group, part < q) the float-float sums of d and d^2 of d = y - s as a float4, then
+// the (s, count) pairs as float2 in the same order.
+constexpr size_t kGnStatsHeader = 256;
 bool conv_gn_stats_supported(int Cout, int groups);
-size_t conv_gn_stats_bytes(int N, int T, int H, int W, int Cout, int groups);
-int conv_gn_stats_parts(int H, int W);  // parts (pixel tiles x 4 warps) per (frame, group)
+size_t conv_gn_stats_bytes(int N, int T, int H, int W, int Cout, int groups);  // for either tiling
+// The record counts q of the two tilings a launch at H x W may use (8 x 16 and 16 x 8 pixels).
+void conv_gn_stats_records(int H, int W, int* q_a, int* q_b);
 // cache_out[n, j] = ([cache_in or zeros; a])[n, T + j], j = 0, 1.
 cudaError_t cache_update_launch(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out,
                                 int N, int T, int H, int W, int C, int sms, cudaStream_t stream);

@@ -48,6 +48,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "conv_tc.h"
 
@@ -127,10 +129,13 @@ struct Conv2Args {
   // GroupNorm statistics of y (null: none): one record per (frame, group, pixel tile, epilogue
   // warp): st_rec = float-float (sum d, sum d^2) over the warp's valid pixels x the group's
   // cg = 2^st_lg channels, d = y - s as stored (bf16); st_meta = (s, count), s the group's first
-  // channel at the warp's first valid pixel (all zero for a warp without valid pixels).
+  // channel at the warp's first valid pixel (all zero for a warp without valid pixels). st_hdr:
+  // the buffer's header, which receives the records per (frame, group) (st_parts) so that their
+  // reader needs no knowledge of this launch's tiles.
   float4* st_rec;
   float2* st_meta;
-  int st_cg, st_lg;
+  int* st_hdr;
+  int st_cg, st_lg, st_parts;
   // Operand prologue (the kNorm kernel): per (frame n*T + t, input channel) the GroupNorm + SiLU
   // coefficients (S_hi, S_lo, B_hi, B_lo), blocked layout (coef_blocked_index), applied to every
   // A box read from `a` (not the cache).
@@ -366,6 +371,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kKind>::kThreads
       mbar_init(&tmem_empty[s], 8);  // 4 epilogue warps in each CTA of the pair
     }
     mbar_init(mma_done, 1);
+    if (blockIdx.x == 0 && args.st_hdr) *args.st_hdr = args.st_parts;  // the statistics' record count
     if (kNorm)
       for (int s = 0; s < kAStages; ++s) mbar_init(&ready_a[s], 16);  // 8 prologue warps per CTA
     fence_mbarrier_init();
@@ -677,7 +683,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kKind>::kThreads
       const size_t rec_stride = (size_t)args.tiles_h * args.tiles_w * 4;  // between groups
       const size_t rec0 = ((((size_t)t.n * args.T + tt) * (args.Cout >> lg) + (size_t)(cbase >> lg)) *
                                (size_t)args.tiles_h * args.tiles_w +
-                           (size_t)(t.h0 / kTileH) * args.tiles_w + t.w0 / kTileW) * 4 + quarter;
+                           (size_t)(t.h0 / Cfg<kKind>::kTH) * args.tiles_w + t.w0 / Cfg<kKind>::kTW) * 4 + quarter;
       float wh[8], wl[8], shw[4];  // the window's 4 groups: (sum d, sum d^2) as float-float, shifts
 #pragma unroll
       for (int k = 0; k < 8; ++k) wh[k] = wl[k] = 0.f;
@@ -1028,11 +1034,16 @@ bool conv_gn_stats_supported(int Cout, int groups) {
   return cg >= 4 && cg <= 64 && (cg & (cg - 1)) == 0;
 }
 
-int conv_gn_stats_parts(int H, int W) { return cdiv(H, kTileH) * cdiv(W, kTileW) * 4; }
+void conv_gn_stats_records(int H, int W, int* q_a, int* q_b) {
+  *q_a = cdiv(H, kTileH) * cdiv(W, kTileW) * 4;      // 8 x 16 tiles, 4 epilogue warps each
+  *q_b = cdiv(H, Cfg<3>::kTH) * cdiv(W, Cfg<3>::kTW) * 4;  // 16 x 8 tiles
+}
 
 size_t conv_gn_stats_bytes(int N, int T, int H, int W, int Cout, int groups) {
   (void)Cout;
-  return (size_t)N * T * groups * conv_gn_stats_parts(H, W) * (sizeof(float4) + sizeof(float2));
+  int q_a, q_b;
+  conv_gn_stats_records(H, W, &q_a, &q_b);
+  return kGnStatsHeader + (size_t)N * T * groups * std::max(q_a, q_b) * (sizeof(float4) + sizeof(float2));
 }
 
 cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_in, const wan_bf16* w,
@@ -1071,10 +1082,12 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
   args.err = err;
   args.y_frames = y_frames;
   args.y_frame0 = y_frame0;
-  if (st_buf) {  // the plain kernel's epilogue (not with the operand prologue)
-    if (mode != 0 || coef || !conv_gn_stats_supported(Cout, st_groups)) return cudaErrorInvalidValue;
-    args.st_rec = reinterpret_cast<float4*>(st_buf);
-    args.st_meta = reinterpret_cast<float2*>(args.st_rec + (size_t)N * T * st_groups * conv_gn_stats_parts(H, W));
+  if (st_buf) {
+    if (mode != 0 || !conv_gn_stats_supported(Cout, st_groups)) return cudaErrorInvalidValue;
+    args.st_parts = args.tiles_h * args.tiles_w * 4;
+    args.st_hdr = reinterpret_cast<int*>(st_buf);
+    args.st_rec = reinterpret_cast<float4*>(static_cast<char*>(st_buf) + kGnStatsHeader);
+    args.st_meta = reinterpret_cast<float2*>(args.st_rec + (size_t)N * T * st_groups * args.st_parts);
     args.st_cg = Cout / st_groups;
     while ((1 << args.st_lg) < args.st_cg) ++args.st_lg;
   }

@@ -40,6 +40,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "conv_tc.h"
 #include "gn_silu.h"
 
 namespace wan {
@@ -108,12 +109,6 @@ struct GnArgs {
   int cthreads;     // compute threads of a CTA (a multiple of C / 8); one more warp loads x
   float eps;
   double inv_len;   // 1 / (H * W * C / G)
-  // Statistics produced elsewhere (null: phase A computes them): per (frame, group, part q < ext_q)
-  // ext_rec = float-float (sum d, sum d^2) of d = x - s around the part's own shift s and
-  // ext_meta = (s, count); part 0 has count > 0.
-  const float4* ext_rec;
-  const float2* ext_meta;
-  int ext_q;
   // Whole-clip statistics: 0 per frame; T: per (n, group) over the T frames of each n (F = N T).
   int clip_T;
   // Bound of the grid-barrier waits in SM cycles, and arrivals the first barrier waits for beyond
@@ -174,7 +169,6 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gn_silu_kernel(const GnArgs 
   // pieces each; piece n is piece n % kPiecesPerSpan of the (n / kPiecesPerSpan)-th item. One
   // thread of the last warp issues them into kSlots slots; each compute warp releases a slot on
   // `empty` once it has read it, so warps never wait for one another while streaming.
-  const int cnt_a = a.ext_rec ? 0 : cnt;  // statistics items (none when they come with x)
   auto issue = [&](int n) {
     const int k = n / kPiecesPerSpan, jj = n - k * kPiecesPerSpan;
     uint64_t* bar = &full[n % kSlots];
@@ -201,7 +195,7 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gn_silu_kernel(const GnArgs 
   // ---------------------------------------------------------------- A: statistics
   if (warp == cw) {
     if (lane == 0) {
-      const int npieces = cnt_a * kPiecesPerSpan;
+      const int npieces = cnt * kPiecesPerSpan;
       for (int n = 0; n < npieces; ++n) {
         if (n >= kSlots &&
             !mbar_wait(&empty[n % kSlots], (uint32_t)(((n / kSlots) - 1) & 1), a.err, kDevErrTimeoutGrid))
@@ -209,10 +203,10 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gn_silu_kernel(const GnArgs 
         issue(n);
       }
     }
-  } else if (cnt_a > 0) {
+  } else if (cnt > 0) {
     int n = 0, buf = 0;  // next piece of the stream; reduction buffer of this item
     bool fail = false;
-    for (int k = 0; k < cnt_a; ++k) {
+    for (int k = 0; k < cnt; ++k) {
       const int item = blockIdx.x + k * gridDim.x;
       const int f = item / a.spans, span = item - f * a.spans;
       // Each group's shift: its first value in the frame (a 2-byte load per group and thread; the
@@ -416,57 +410,22 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gn_silu_kernel(const GnArgs 
       // lane ends with the same bits.
       // A lane adds items lane, lane + 32, ... in order, loading kFinBatch of them at a time.
       float h1 = 0.f, l1 = 0.f, h2 = 0.f, l2 = 0.f;
-      double shift;
-      if (a.ext_rec) {
-        // Parts with their own shifts s_q, moved exactly to the first part's shift s, all in
-        // float-float (dl = s_q - s by TwoSum, n dl by an FMA product error):
-        //   sum (x - s) = S1_q + n dl,  sum (x - s)^2 = S2_q + dl (2 S1_q + n dl).
-        const float4* ep = a.ext_rec + ((size_t)f * a.G + g) * a.ext_q;
-        const float2* em = a.ext_meta + ((size_t)f * a.G + g) * a.ext_q;
-        const float s = __ldcg(em).x;
-        for (int q0 = 0; q0 < a.ext_q; q0 += 32 * kFinBatch) {
-          float4 r[kFinBatch];
-          float2 m[kFinBatch];
+      const float4* src = reinterpret_cast<const float4*>(a.part) + ((size_t)f * a.G + g) * a.spans;
+      const float sh = bf16_at(a.x + (size_t)f * a.P * a.C + (size_t)g * cg);
+      for (int sp0 = 0; sp0 < a.spans; sp0 += 32 * kFinBatchSpans) {
+        float4 q[kFinBatchSpans];
 #pragma unroll
-          for (int i = 0; i < kFinBatch; ++i) {
-            const int q = q0 + lane + 32 * i;
-            r[i] = q < a.ext_q ? __ldcg(ep + q) : make_float4(0.f, 0.f, 0.f, 0.f);
-            m[i] = q < a.ext_q ? __ldcg(em + q) : make_float2(s, 0.f);
-          }
-#pragma unroll
-          for (int i = 0; i < kFinBatch; ++i) {
-            float dh = m[i].x, dlo = 0.f;
-            ff_add(dh, dlo, -s, 0.f);  // s_q - s exactly
-            const float n = m[i].y;
-            const float ph = n * dh, pl = fmaf(n, dh, -ph) + n * dlo;  // n dl (n < 2^24)
-            ff_add(h1, l1, r[i].x, r[i].y);
-            ff_add(h1, l1, ph, pl);
-            float uh = 2.f * r[i].x, ul = 2.f * r[i].y;  // 2 S1_q + n dl
-            ff_add(uh, ul, ph, pl);
-            const float vh = dh * uh, vl = fmaf(dh, uh, -vh) + fmaf(dh, ul, dlo * uh);
-            ff_add(h2, l2, r[i].z, r[i].w);
-            ff_add(h2, l2, vh, vl);
-          }
+        for (int i = 0; i < kFinBatchSpans; ++i) {
+          const int sp = sp0 + lane + 32 * i;
+          q[i] = sp < a.spans ? __ldcg(src + sp) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        shift = (double)s;
-      } else {
-        const float4* src = reinterpret_cast<const float4*>(a.part) + ((size_t)f * a.G + g) * a.spans;
-        const float sh = bf16_at(a.x + (size_t)f * a.P * a.C + (size_t)g * cg);
-        for (int sp0 = 0; sp0 < a.spans; sp0 += 32 * kFinBatchSpans) {
-          float4 q[kFinBatchSpans];
 #pragma unroll
-          for (int i = 0; i < kFinBatchSpans; ++i) {
-            const int sp = sp0 + lane + 32 * i;
-            q[i] = sp < a.spans ? __ldcg(src + sp) : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-#pragma unroll
-          for (int i = 0; i < kFinBatchSpans; ++i) {  // adding (0, 0) to a normalised pair changes nothing
-            ff_add(h1, l1, q[i].x, q[i].y);
-            ff_add(h2, l2, q[i].z, q[i].w);
-          }
+        for (int i = 0; i < kFinBatchSpans; ++i) {  // adding (0, 0) to a normalised pair changes nothing
+          ff_add(h1, l1, q[i].x, q[i].y);
+          ff_add(h2, l2, q[i].z, q[i].w);
         }
-        shift = (double)sh;
       }
+      const double shift = (double)sh;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const float oh1 = __shfl_xor_sync(0xffffffffu, h1, off), ol1 = __shfl_xor_sync(0xffffffffu, l1, off);
@@ -574,6 +533,102 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gn_silu_kernel(const GnArgs 
   }
 }
 
+// Coefficients from the conv epilogue's statistics: one CTA per (frame, group). Its threads take
+// the group's records q = t, t + 256, ... in order, each moved exactly to record 0's shift s in
+// float-float (dl = s_q - s by TwoSum, n dl by an FMA product error):
+//   sum (x - s) = S1_q + n dl,  sum (x - s)^2 = S2_q + dl (2 S1_q + n dl),
+// then the threads' pairs are added in a fixed order (warp butterflies, then the warps in turn)
+// and the mean, variance and coefficients follow as in the norm's own finalize.
+constexpr int kStatThreads = 256;
+constexpr int kStatBatch = 8;  // records in flight per thread
+
+__global__ void __launch_bounds__(kStatThreads) gn_coef_from_stats_kernel(const char* __restrict__ stats, int q_max,
+                                                                          int q_a, int q_b, const float* __restrict__ gamma,
+                                                                          const float* __restrict__ beta, float4* coef,
+                                                                          int F, int C, int G, double inv_len, float eps,
+                                                                          int blocked, unsigned* err) {
+  __shared__ float red[kStatThreads / 32][4];
+  const int q = __ldcg(reinterpret_cast<const int*>(stats));
+  if (q <= 0 || q > q_max || (q != q_a && q != q_b)) {  // not statistics of these sizes
+    if (threadIdx.x == 0) atomicOr(err, kDevErrBadStats);
+    return;
+  }
+  const int pr = blockIdx.x, f = pr / G, g = pr - f * G, cg = C / G;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float4* rec = reinterpret_cast<const float4*>(stats + kGnStatsHeader) + (size_t)pr * q;
+  const float2* meta = reinterpret_cast<const float2*>(stats + kGnStatsHeader + (size_t)F * G * q * sizeof(float4)) +
+                       (size_t)pr * q;
+  const float gam0 = lane < cg ? __ldg(gamma + g * cg + lane) : 0.f;
+  const float bet0 = lane < cg ? __ldg(beta + g * cg + lane) : 0.f;
+  const float s = __ldcg(meta).x;
+  float h1 = 0.f, l1 = 0.f, h2 = 0.f, l2 = 0.f;
+  for (int q0 = 0; q0 < q; q0 += kStatThreads * kStatBatch) {
+    float4 r[kStatBatch];
+    float2 m[kStatBatch];
+#pragma unroll
+    for (int i = 0; i < kStatBatch; ++i) {
+      const int k = q0 + (int)threadIdx.x + kStatThreads * i;
+      r[i] = k < q ? __ldcg(rec + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+      m[i] = k < q ? __ldcg(meta + k) : make_float2(s, 0.f);
+    }
+#pragma unroll
+    for (int i = 0; i < kStatBatch; ++i) {
+      float dh = m[i].x, dlo = 0.f;
+      ff_add(dh, dlo, -s, 0.f);  // s_q - s exactly
+      const float n = m[i].y;
+      const float ph = n * dh, pl = fmaf(n, dh, -ph) + n * dlo;  // n dl (n < 2^24)
+      ff_add(h1, l1, r[i].x, r[i].y);
+      ff_add(h1, l1, ph, pl);
+      float uh = 2.f * r[i].x, ul = 2.f * r[i].y;  // 2 S1_q + n dl
+      ff_add(uh, ul, ph, pl);
+      const float vh = dh * uh, vl = fmaf(dh, uh, -vh) + fmaf(dh, ul, dlo * uh);
+      ff_add(h2, l2, r[i].z, r[i].w);
+      ff_add(h2, l2, vh, vl);
+    }
+  }
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float oh1 = __shfl_xor_sync(0xffffffffu, h1, off), ol1 = __shfl_xor_sync(0xffffffffu, l1, off);
+    const float oh2 = __shfl_xor_sync(0xffffffffu, h2, off), ol2 = __shfl_xor_sync(0xffffffffu, l2, off);
+    ff_add(h1, l1, oh1, ol1);
+    ff_add(h2, l2, oh2, ol2);
+  }
+  if (lane == 0) {
+    red[warp][0] = h1;
+    red[warp][1] = l1;
+    red[warp][2] = h2;
+    red[warp][3] = l2;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  h1 = red[0][0], l1 = red[0][1], h2 = red[0][2], l2 = red[0][3];
+  for (int w = 1; w < kStatThreads / 32; ++w) {
+    ff_add(h1, l1, red[w][0], red[w][1]);
+    ff_add(h2, l2, red[w][2], red[w][3]);
+  }
+  const double s1 = (double)h1 + (double)l1;
+  const double s2 = (double)h2 + (double)l2;
+  const double m1 = s1 * inv_len;
+  const double mean = (double)s + m1;
+  const double v = fmax(s2 * inv_len - m1 * m1, 0.0) + (double)eps;
+  double rstd;
+  if (v > 1e-30 && v < 1e30) {  // an fp32 estimate refined by two Newton steps in fp64
+    rstd = (double)rsqrtf((float)v);
+    rstd = rstd * (1.5 - 0.5 * v * rstd * rstd);
+    rstd = rstd * (1.5 - 0.5 * v * rstd * rstd);
+  } else {
+    rstd = 1.0 / sqrt(v);
+  }
+  for (int kk = lane; kk < cg; kk += 32) {
+    const int c = g * cg + kk;
+    const double S = (double)(kk == lane ? gam0 : gamma[c]) * rstd;
+    const double B = (double)(kk == lane ? bet0 : beta[c]) - mean * S;
+    const float shi = (float)S, bhi = (float)B;
+    coef[(size_t)f * C + (blocked ? coef_blocked_index(c) : c)] =
+        make_float4(shi, (float)(S - (double)shi), bhi, (float)(B - (double)bhi));
+  }
+}
+
 // The apply pass alone, on frames [t_lo, T) of every n, with the coefficients a coefficients-only
 // call left in `coef` ([N*T][C], blocked layout): y[n, o + t - t_lo] (y has To frames per n)
 // = silu(x[n, t] S + B). Items are (frame, run of px_per_item pixels); a thread owns one
@@ -674,11 +729,26 @@ cudaError_t gn_apply_frames_launch(const wan_bf16* x, const float4* coef, wan_bf
   return cudaGetLastError();
 }
 
+cudaError_t gn_coef_from_stats_launch(const void* stats, size_t stats_bytes, const float* gamma, const float* beta,
+                                      int N, int T, int H, int W, int C, int G, float eps, float4* coef, bool blocked,
+                                      unsigned* err, cudaStream_t stream) {
+  if (!stats || !coef || !err || G <= 0 || C % G != 0) return cudaErrorInvalidValue;
+  const long long F = (long long)N * T;
+  const long long pairs = F * G;
+  if (pairs >= (1LL << 31) || stats_bytes < kGnStatsHeader) return cudaErrorInvalidValue;
+  int q_a, q_b;  // the record counts of the two tilings the conv may have used
+  conv_gn_stats_records(H, W, &q_a, &q_b);
+  const long long q_max = (long long)((stats_bytes - kGnStatsHeader) / ((size_t)pairs * (sizeof(float4) + sizeof(float2))));
+  gn_coef_from_stats_kernel<<<(unsigned)pairs, kStatThreads, 0, stream>>>(
+      static_cast<const char*>(stats), (int)std::min<long long>(q_max, 1 << 30), q_a, q_b, gamma, beta, coef, (int)F, C,
+      G, 1.0 / ((double)H * W * (C / G)), eps, blocked ? 1 : 0, err);
+  return cudaGetLastError();
+}
+
 cudaError_t gn_silu_launch(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta,
                            int N, int T, int H, int W, int C, int G, float eps, void* ws, int sms,
-                           cudaStream_t stream, const void* st_buf, int st_q, bool apply, float4* coef_out,
+                           cudaStream_t stream, bool apply, float4* coef_out,
                            bool whole_clip, long long wait_cycles, unsigned bar_extra) {
-  if (whole_clip && st_buf) return cudaErrorInvalidValue;
   const GnPlan pl = plan(N, T, H, W, C, G);
   char* base = reinterpret_cast<char*>(ws);
   GnArgs a;
@@ -702,9 +772,6 @@ cudaError_t gn_silu_launch(const wan_bf16* x, wan_bf16* y, const float* gamma, c
   a.eps = eps;
   a.clip_T = whole_clip ? T : 0;
   a.inv_len = 1.0 / ((double)pl.P * (C / G) * (whole_clip ? T : 1));
-  a.ext_rec = reinterpret_cast<const float4*>(st_buf);
-  a.ext_meta = st_buf ? reinterpret_cast<const float2*>(a.ext_rec + (size_t)pl.F * G * st_q) : nullptr;
-  a.ext_q = st_q;
   a.wait_cycles = wait_cycles > 0 ? wait_cycles : kWaitCycles;
   a.bar_extra = bar_extra;
   a.apply = apply ? 1 : 0;

@@ -57,6 +57,6 @@ extern "C" wan_status wan_selftest_wait_timeout(int which, long long wait_cycles
   }
   // wan_gn_silu's kernel with its first grid barrier one arrival beyond the grid: every CTA
   // arrives, waits `wait_cycles`, records the timeout and returns before writing y.
-  return cuda_status(gn_silu_launch(x, y, gamma, beta, N, T, H, W, C, groups, eps, ws, sm_count(), s, nullptr, 0,
-                                    true, nullptr, false, wait_cycles, 1u));
+  return cuda_status(gn_silu_launch(x, y, gamma, beta, N, T, H, W, C, groups, eps, ws, sm_count(), s, true, nullptr,
+                                    false, wait_cycles, 1u));
 }
