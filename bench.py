@@ -539,10 +539,10 @@ def run_ours(args, rank, world, dev):
     # DRAM bytes (read + write) per launch from `ncu --set full` captures of the current build of
     # each kernel (profiles/); the head's from a single-pass capture of the 16-frame launch; the
     # Winograd conv's is its three kernels' sum.
-    traffic = {"conv_c256": 172.643328e6 + 125.374976e6, "gn_coef_c256": 112.548352e6 + 3.560192e6,
+    traffic = {"conv_c256": 172.575744e6 + 125.743872e6, "gn_coef_c256": 112.540416e6 + 3.522304e6,
                "gn_coef_c1024": 28.202496e6, "conv_c1024_winograd": (42.893824e6 + 120.870912e6) +
                (270.27328e6 + 182.016512e6) + (253.05728e6 + 4.976128e6),
-               "upsample_phase_conv": 22.552064e6 + 4.372736e6, "gn_silu_decode_mid": 72.386816e6 + 12.526336e6,
+               "upsample_phase_conv": 22.552064e6 + 4.372736e6, "gn_silu_decode_mid": 68.827392e6 + 11.028992e6,
                "head_256_to_12": 9.9e9 + 0.343e9}
     rooflines = []
     for name, k in kernels.items():
