@@ -583,8 +583,8 @@ wan_status wan_time_upsample(const wan_bf16* x, const wan_bf16* cache_in, wan_bf
   // The first frame of the first chunk passes through.
   if (first) e = cudaMemcpy2DAsync(y, To * fb, x, T * fb, fb, N, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess && nf > 0)
-    e = conv_pair_launch(2, x + (size_t)start * fb / sizeof(wan_bf16), cache_in, w, bias, nullptr, y, N, nf, H, W, C,
-                         2 * C, sm_count(), err, s, nullptr, 0, nullptr, T, To, start);
+    e = time_up_launch(x + (size_t)start * fb / sizeof(wan_bf16), cache_in, w, bias, y, N, nf, H, W, C, T, To, start,
+                       sm_count(), err, s);
   if (e != cudaSuccess || !cache_out) return cuda_status(e);
   // The new history: the last two frames of [cache_in or zeros; x[:, start:]].
   const char* xb = reinterpret_cast<const char*>(x);

@@ -38,6 +38,14 @@ bool conv_gn_stats_supported(int Cout, int groups);
 size_t conv_gn_stats_bytes(int N, int T, int H, int W, int Cout, int groups);  // for either tiling
 // The record counts q of the two tilings a launch at H x W may use (8 x 16 and 16 x 8 pixels).
 void conv_gn_stats_records(int H, int W, int* q_a, int* q_b);
+// The causal 3x1x1 time conv of the time upsample (time_up_tc2.cu), two output frames per CTA:
+// conv output frame t of x's nf frames (x: frame stride a_frames per n; frames before it from
+// cache_in [N, 2, H, W, C], else zeros) with w [2 C, 3, C] and bias [2 C], channel half i written
+// to frame y_frame0 + 2 t + i of y [N, y_frames, H, W, C]. C % 256 == 0.
+bool time_up_supported(int C);
+cudaError_t time_up_launch(const wan_bf16* x, const wan_bf16* cache_in, const wan_bf16* w, const wan_bf16* bias,
+                           wan_bf16* y, int N, int nf, int H, int W, int C, int a_frames, int y_frames, int y_frame0,
+                           int sms, unsigned* err, cudaStream_t stream);
 // cache_out[n, j] = ([cache_in or zeros; a])[n, T + j], j = 0, 1.
 cudaError_t cache_update_launch(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out,
                                 int N, int T, int H, int W, int C, int sms, cudaStream_t stream);
