@@ -41,13 +41,16 @@ constexpr int kTuN = 256;                    // output channels per item (both C
 constexpr int kTuBOffset = kTuAStages * kTuAStage;
 constexpr int kTuBarOffset = kTuBOffset + kTuBStages * kTuBStage;
 constexpr int kTuSmem = kTuBarOffset + 256 + 1024;  // + barriers, + 1024-byte alignment slack
-constexpr int kTuThreads = 192;              // producer, MMA issuer, 4 epilogue warps
+constexpr int kTuThreads = 320;              // producer, MMA issuer, 4 epilogue warps per accumulator
 static_assert(kTuSmem <= 232448, "shared memory per CTA");
 static_assert(kTuAStage % 1024 == 0 && kTuBStage % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
 
 struct TuArgs {
   int N, nf, H, W, C;            // input frames of the chunk (nf), channels C; output channels 2 C
   int tiles_w, tiles, tile_pairs, frame_pairs, n_blks, items;
+  // Scheduling units: item i < split0 is one unit (both output frames), items from split0 on are
+  // two (one output frame each): units = split0 + 2 (items - split0).
+  int units, split0;
   int has_cache;
   int y_frames, y_frame0;        // y: [N, y_frames, H, W, C]
   const wan_bf16* bias;          // [2 C] or null
@@ -78,12 +81,22 @@ __device__ __forceinline__ TuItem tu_decode(const TuArgs& a, int item, int which
   return it;
 }
 
-// Snake order of items over the CTA pairs; -1 once this pair has no item in round r.
-__device__ __forceinline__ int tu_item_of(const TuArgs& a, int r, int cluster, int nclusters) {
+// Snake order of units over the CTA pairs; -1 once this pair has no unit in round r.
+__device__ __forceinline__ int tu_unit_of(const TuArgs& a, int r, int cluster, int nclusters) {
   const int base = r * nclusters;
-  if (base >= a.items) return -1;
-  const int item = base + ((r & 1) ? nclusters - 1 - cluster : cluster);
-  return item < a.items ? item : -2;
+  if (base >= a.units) return -1;
+  const int unit = base + ((r & 1) ? nclusters - 1 - cluster : cluster);
+  return unit < a.units ? unit : -2;
+}
+
+// Unit -> item, and which of its output frames the unit computes (-1: both).
+__device__ __forceinline__ int tu_unit_item(const TuArgs& a, int unit, int& sub) {
+  if (unit < a.split0) {
+    sub = -1;
+    return unit;
+  }
+  sub = (unit - a.split0) & 1;
+  return a.split0 + ((unit - a.split0) >> 1);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTuThreads, 1)
@@ -116,7 +129,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTuThreads, 1)
       mbar_init(&empty_b[s], 1);
     }
     mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 8);  // 4 epilogue warps in each CTA of the pair
+    mbar_init(tmem_empty, 16);  // 8 epilogue warps in each CTA of the pair
     mbar_init(mma_done, 1);
     fence_mbarrier_init();
     prefetch_tensormap(&tm_x);
@@ -142,10 +155,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTuThreads, 1)
     uint32_t armed = 0, parity = 0;  // stages whose barriers the even CTA armed: A in bits 0-1, B in 2-3
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int item = tu_item_of(args, r, cluster, nclusters);
-      if (item == -1) break;
-      if (item < 0) continue;
-      const TuItem me = tu_decode(args, item, (int)rank);
+      const int unit = tu_unit_of(args, r, cluster, nclusters);
+      if (unit == -1) break;
+      if (unit < 0) continue;
+      int sub;
+      const TuItem me = tu_decode(args, tu_unit_item(args, unit, sub), (int)rank);
       const int brow = me.nb * kTuN + (int)rank * 128;
       for (int kb = 0; ok && kb < kblocks; ++kb) {
         // the three taps' weights of this K block
@@ -205,11 +219,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTuThreads, 1)
     uint32_t pha = 0, phb = 0, acc_phase = 0;
     bool ok = true;
     for (int r = 0; ok; ++r) {
-      const int item = tu_item_of(args, r, cluster, nclusters);
-      if (item == -1) break;
-      if (item < 0) continue;
-      // the second output frame exists for both tiles of the pair or for neither (same frames)
-      const bool second = tu_decode(args, item, 0).second;
+      const int unit = tu_unit_of(args, r, cluster, nclusters);
+      if (unit == -1) break;
+      if (unit < 0) continue;
+      int sub;
+      const int item = tu_unit_item(args, unit, sub);
+      // the second output frame exists for both tiles of the pair or for neither (same frames); a
+      // unit of one frame accumulates frame f0 + sub into accumulator 0 from frames sub .. sub + 2
+      const bool second = sub < 0 && tu_decode(args, item, 0).second;
+      const uint32_t first_off = sub > 0 ? (uint32_t)(kTuFrameBytes >> 4) : 0u;
       if (!mbar_wait_cluster(tmem_empty, acc_phase ^ 1, args.err, kDevErrTimeoutMma)) break;
       tc_fence_after();
       for (int kb = 0; kb < kblocks; ++kb) {
@@ -223,7 +241,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTuThreads, 1)
 #pragma unroll
         for (int kt = 0; kt < 3; ++kt) {
           const uint64_t bk = b0 + (uint64_t)kt * (kTuTapBytes >> 4);
-          const uint64_t af = a0 + (uint64_t)kt * (kTuFrameBytes >> 4);  // frame f0 - 2 + kt
+          const uint64_t af = a0 + first_off + (uint64_t)kt * (kTuFrameBytes >> 4);  // frame f0 - 2 + kt (+ sub)
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             mma_bf16_pair(tmem_base, af + 2 * k, bk + 2 * k, idesc, (kb == 0 && kt == 0 && k == 0) ? 0u : 1u);
@@ -253,24 +271,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTuThreads, 1)
     mbar_wait(mma_done, 0, args.err, kDevErrTimeoutDrain);
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue (both CTAs, own 128 rows)
-    const int quarter = warp & 3, row = quarter * 32 + lane;
+    // Warps 2-5 drain accumulator 0 and warps 6-9 accumulator 1 (a warp reaches the TMEM lanes of
+    // quarter warp % 4), so an item's two output frames are written at the same time.
+    const int quarter = warp & 3, row = quarter * 32 + lane, o = (warp - 2) / 4;
     const uint32_t leader_empty = mapa_shared(smem_u32(tmem_empty), 0);
     uint32_t acc_phase = 0;
     for (int r = 0;; ++r) {
-      const int item = tu_item_of(args, r, cluster, nclusters);
-      if (item == -1) break;
-      if (item < 0) continue;
-      const TuItem t = tu_decode(args, item, (int)rank);
+      const int unit = tu_unit_of(args, r, cluster, nclusters);
+      if (unit == -1) break;
+      if (unit < 0) continue;
+      int sub;
+      const TuItem t = tu_decode(args, tu_unit_item(args, unit, sub), (int)rank);
+      // accumulator o holds output frame f0 + o of a whole unit; a unit of one frame has it in
+      // accumulator 0 (accumulator 1's warps only hand the accumulators back)
+      const int frame = sub < 0 ? t.f0 + o : t.f0 + sub;
+      const bool writes = sub < 0 ? (o == 0 || t.second) : (o == 0 && (sub == 0 || t.second));
       const int hh = t.h0 + (row & 7), ww = t.w0 + row / 8;  // TMEM row = h + 8 w
       const bool valid = t.valid && hh < args.H && ww < args.W;
       const int half = t.nb * kTuN / args.C;  // the N block's channel half: output frame 2 t + half
       const int cy = t.nb * kTuN - half * args.C;
       if (!mbar_wait_cluster(tmem_full, acc_phase, args.err, kDevErrTimeoutEpilogue)) break;
       tc_fence_after();
-      for (int o = 0; o < (t.second ? 2 : 1); ++o) {
-        const int fy = args.y_frame0 + 2 * (t.f0 + o) + half;
+      if (writes) {
+        const int fy = args.y_frame0 + 2 * frame + half;
         wan_bf16* yrow = args.y + ((((size_t)t.n * args.y_frames + fy) * args.H + hh) * args.W + ww) * args.C + cy;
-        const uint32_t taddr = tmem_base + (uint32_t)(o * kTuN) + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t taddr = tmem_base + (uint32_t)((sub < 0 ? o : 0) * kTuN) + ((uint32_t)(quarter * 32) << 16);
         uint32_t rn[16];
         __syncwarp();
         tmem_ld16_issue(taddr, rn);
@@ -414,7 +439,17 @@ cudaError_t time_up_launch(const wan_bf16* x, const wan_bf16* cache_in, const wa
     max_clusters[dev] = n;
   }
   int clusters = (dev >= 0 && dev < 64) ? max_clusters[dev] : sms / 2;
-  if (clusters > args.items) clusters = args.items;
+  if (clusters < 1) clusters = 1;
+  // A last round of at most half the pairs' worth of items runs as twice as many units of one
+  // output frame each (half the MMAs).
+  const int rem = args.items % clusters;
+  args.split0 = args.items;
+  args.units = args.items;
+  if (rem > 0 && 2 * rem <= clusters) {
+    args.split0 = args.items - rem;
+    args.units = args.items + rem;
+  }
+  if (clusters > args.units) clusters = args.units;
   if (clusters < 1) clusters = 1;
   time_up_kernel<<<2 * clusters, kTuThreads, kTuSmem, stream>>>(tx, tc, tw, args);
   return cudaGetLastError();
