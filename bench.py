@@ -745,6 +745,9 @@ def main():
                     help="frames of the head's input (smaller values make a case small enough for ncu --set full)")
     ap.add_argument("--case", default="all", choices=CASES,
                     help="time one part of the step only (profiling captures); the default is the whole step")
+    ap.add_argument("--adjacent-only", action="store_true",
+                    help="time only the steps next to the ResBlock (profiling captures of those kernels); prints "
+                         "their figures, not the step's line")
     ap.add_argument("--one-thread-sample", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.one_thread_sample:
@@ -766,6 +769,11 @@ def main():
     dev = torch.device("cuda", local)
     from video_vae_decoder_gb300 import binding
     binding.lib()
+    if args.adjacent_only:
+        if rank == 0:
+            torch.cuda.set_device(dev)
+            print(json.dumps({"adjacent_steps": time_adjacent(dev)}), flush=True)
+        return
     out = run_ours(args, rank, world, dev)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
