@@ -81,6 +81,20 @@ def test_time_upsample_decode_size_sampled(wan):
     conv_close(oracle.round_to_bf16(out), ref, "time upsample, sampled")
 
 
+def test_time_upsample_bench_size_every_element(wan):
+    # The adjacent-step shape bench.py times, [1, 4, 44, 78, 1024] -> [1, 8, 44, 78, 1024] with
+    # history: every output element against the oracle (its two frames per CTA, the split last round).
+    shape = (1, 4, 44, 78, 1024)
+    x, w, b, c = tu_inputs(shape, "tu/bench")
+    c_out = torch.empty((1, 2, 44, 78, 1024), dtype=torch.bfloat16, device="cuda")
+    y = wan.wan_time_upsample(to_dev(x), to_dev(w), to_dev(b), False, to_dev(c), c_out)
+    torch.cuda.synchronize()
+    assert wan.wan_device_status() == 0
+    ref, c_ref = oracle.time_upsample(x, w, b, c, False)
+    conv_close(bits(y), ref, "time upsample, bench size")
+    assert np.array_equal(bits(c_out), c_ref)
+
+
 @pytest.mark.parametrize("shape,Cout", [((1, 2, 12, 33, 128), 256), ((2, 3, 9, 17, 256), 512),
                                         ((1, 2, 7, 19, 192), 256)])  # an odd count of 64-channel blocks
 def test_conv1x1_matches_oracle(wan, shape, Cout):
