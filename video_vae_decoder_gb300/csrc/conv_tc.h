@@ -19,7 +19,8 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
                              int a_frames = 0, int y_frames = 0, int y_frame0 = 0, wan_bf16* cache_out = nullptr);
 // Modes of conv_pair_launch beyond conv_launch's: 2, the causal 3x1x1 time conv to Cout = 2 C
 // channels (w [Cout, 3, Cin]) whose output frame t, channel half i lands in frame
-// y_frame0 + 2 t + i of y ([N, y_frames, H, W, Cout / 2]; Cout % 512 == 0, no residual);
+// y_frame0 + 2 t + i of y ([N, y_frames, H, W, Cout / 2]; Cout % 512 == 0, no residual), one
+// output frame per CTA (wan_time_upsample runs time_up_launch below, two frames per CTA);
 // 3, the 1x1x1 conv (w [Cout, Cin], no cache). a_frames: frames per n of the tensor `a` points
 // into (0: T), so `a` may start at a later frame of a longer video.
 // coef (optional, mode 0): GroupNorm + SiLU of `a` applied to the conv's operand tiles as they
