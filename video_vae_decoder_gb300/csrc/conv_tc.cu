@@ -28,6 +28,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "tma_host.h"
 #include "conv_tc.h"
 
 namespace wan {
@@ -323,22 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 bool make_map_5d(CUtensorMap* m, const void* base, int C, int W, int H, int T, int N, int box_w,
                  int box_h) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   const cuuint64_t dims[5] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)N};
   const cuuint64_t e = 2;
@@ -352,7 +340,7 @@ bool make_map_5d(CUtensorMap* m, const void* base, int C, int W, int H, int T, i
 }
 
 bool make_map_w(CUtensorMap* m, const void* base, int K, int Cout, int P, int BN) {
-  auto fn = encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)Cout, (cuuint64_t)P};
   const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)K * Cout * 2};

@@ -51,6 +51,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "tma_host.h"
 #include "conv_tc.h"
 
 namespace wan {
@@ -924,24 +925,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kKind>::kThreads
   if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn2() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 // Activations [N, T, H, W, C] addressed as (c, h, w, t, n): H is listed before W, so a box of
 // 8 rows x 18 columns lands in shared memory column by column (row m = h + 8 w).
 // T frames per n are mapped; consecutive n are n_frames frames apart (n_frames >= T).
 bool map_act_hw(CUtensorMap* m, const void* base, int C, int W, int H, int T, int N, int box_h = kTileH,
                 int n_frames = 0) {
-  auto fn = encode_fn2();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   if (n_frames < T) n_frames = T;
   const cuuint64_t dims[5] = {(cuuint64_t)C, (cuuint64_t)H, (cuuint64_t)W, (cuuint64_t)T, (cuuint64_t)N};
@@ -958,7 +947,7 @@ bool map_act_hw(CUtensorMap* m, const void* base, int C, int W, int H, int T, in
 // The same activations addressed as (c, w, h, t, n) for the 16 x 8 tiles: a box of 18 rows x 10
 // columns lands in shared memory row by row (row m = w + 10 h).
 bool map_act_wh(CUtensorMap* m, const void* base, int C, int W, int H, int T, int N, int n_frames = 0) {
-  auto fn = encode_fn2();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   if (n_frames < T) n_frames = T;
   const cuuint64_t dims[5] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)N};
@@ -974,7 +963,7 @@ bool map_act_wh(CUtensorMap* m, const void* base, int C, int W, int H, int T, in
 
 // Weights [P][Cout][K] addressed as (k, cout, p); a box is 64 K x `rows` output channels.
 bool map_w_half(CUtensorMap* m, const void* base, int K, int Cout, int P, int rows) {
-  auto fn = encode_fn2();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)Cout, (cuuint64_t)P};
   const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)K * Cout * 2};

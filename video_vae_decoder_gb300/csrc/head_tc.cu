@@ -30,6 +30,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "tma_host.h"
 #include "conv_tc.h"
 
 namespace wan {
@@ -580,21 +581,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc_pair(tmem_base, kTmemCols);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn_head() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 bool make_row_map(CUtensorMap* m, const void* base, int C, int W, int H, int T, int N) {
-  auto fn = encode_fn_head();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   const cuuint64_t dims[5] = {(cuuint64_t)C, (cuuint64_t)W, (cuuint64_t)H, (cuuint64_t)T, (cuuint64_t)N};
   const cuuint64_t e = 2;

@@ -24,6 +24,7 @@
 #include <stdint.h>
 
 #include "common.cuh"
+#include "tma_host.h"
 #include "conv_tc.h"
 
 namespace wan {
@@ -343,23 +344,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTuThreads, 1)
   if (warp == 1) tmem_dealloc_pair(tmem_base, 512);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tu_encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 // Activations [N, ., H, W, C] addressed as (c, h, w, t, n) with `frames` frames mapped per n
 // (n_frames apart): a box of 64 channels x 8 rows x 16 columns of one frame lands column by column
 // (row m = h + 8 w). Coordinates outside the map read zeros.
 bool tu_map_act(CUtensorMap* m, const void* base, int C, int W, int H, int frames, int N, int n_frames) {
-  auto fn = tu_encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   const cuuint64_t dims[5] = {(cuuint64_t)C, (cuuint64_t)H, (cuuint64_t)W, (cuuint64_t)frames, (cuuint64_t)N};
   const cuuint64_t e = 2;
@@ -374,7 +363,7 @@ bool tu_map_act(CUtensorMap* m, const void* base, int C, int W, int H, int frame
 
 // Weights [2 C][3 C] (output channel, tap * C + input channel) as (k, cout): boxes of 64 K x 128 rows.
 bool tu_map_w(CUtensorMap* m, const void* base, int K, int Cout) {
-  auto fn = tu_encode_fn();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)Cout, 1};
   const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)K * Cout * 2};

@@ -34,6 +34,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "tma_host.h"
 #include "winograd.h"
 
 namespace wan {
@@ -529,21 +530,9 @@ __global__ void __launch_bounds__(256) wino_output_kernel(const WinoOutArgs a) {
 // ------------------------------------------------------------------------------------------------
 // host side
 // ------------------------------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn_w() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
-  return fn;
-}
-
 // A [P][rows][K] fp16 tensor addressed as (k, row, p); a box is 64 K x 128 rows, 128-byte swizzle.
 bool map_f16_3d(CUtensorMap* m, const void* base, long long K, long long rows, int P) {
-  auto fn = encode_fn_w();
+  auto fn = tensor_map_encoder();
   if (!fn) return false;
   const cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)P};
   const cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)(K * rows * 2)};
