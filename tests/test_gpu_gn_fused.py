@@ -191,3 +191,19 @@ def test_resblock_chain_with_statistics_matches_oracle(wan):
             state[i] = (c1o, c2o)
         ref.append(h)
     conv_close(np.concatenate(outs, 1), np.concatenate(ref, 1), "resblock chain with statistics")
+
+
+def test_coefficients_from_statistics_of_other_sizes_are_refused(wan):
+    # Statistics written for 24 x 40 frames (36 records per frame and group) read as those of
+    # 12 x 20 frames (16 or 12): refused, the coefficients untouched.
+    x, g, be, w, b, c = prologue_inputs((1, 2, 24, 40, 256), 256, "gninst/other")
+    xd = to_dev(x)
+    coef = wan.wan_gn_silu_coefficients(xd, f32_dev(g), f32_dev(be), 32, EPS)
+    _, st = wan.wan_causal_conv3d_gn_input_stats(xd, coef, to_dev(w), 32, to_dev(b), None, to_dev(c))
+    torch.cuda.synchronize()
+    assert wan.wan_device_status() == 0
+    k = torch.full((1 * 2 * 256 * 16,), 7, dtype=torch.uint8, device="cuda")
+    g2, be2 = norm_params(256, "gninst/other/n2")
+    wan.wan_gn_silu_coefficients_from_stats(st, f32_dev(g2), f32_dev(be2), (1, 2, 12, 20, 256), 32, EPS, k)
+    assert wan.wan_device_status() == 1  # WAN_ERR_INVALID_ARG
+    assert bool((k == 7).all())
