@@ -42,7 +42,7 @@ constexpr int kTuN = 256;                    // output channels per item (both C
 constexpr int kTuBOffset = kTuAStages * kTuAStage;
 constexpr int kTuBarOffset = kTuBOffset + kTuBStages * kTuBStage;
 constexpr int kTuSmem = kTuBarOffset + 256 + 1024;  // + barriers, + 1024-byte alignment slack
-constexpr int kTuThreads = 320;              // producer, MMA issuer, 4 epilogue warps per accumulator
+constexpr int kTuThreads = 576;              // producer, MMA issuer, 8 epilogue warps per accumulator
 static_assert(kTuSmem <= 232448, "shared memory per CTA");
 static_assert(kTuAStage % 1024 == 0 && kTuBStage % 1024 == 0, "stages keep the 1024-byte swizzle alignment");
 
@@ -130,7 +130,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTuThreads, 1)
       mbar_init(&empty_b[s], 1);
     }
     mbar_init(tmem_full, 1);
-    mbar_init(tmem_empty, 16);  // 8 epilogue warps in each CTA of the pair
+    mbar_init(tmem_empty, 32);  // 16 epilogue warps in each CTA of the pair
     mbar_init(mma_done, 1);
     fence_mbarrier_init();
     prefetch_tensormap(&tm_x);
@@ -272,9 +272,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTuThreads, 1)
     mbar_wait(mma_done, 0, args.err, kDevErrTimeoutDrain);
   } else if (warp >= 2) {
     // ------------------------------------------------------------ epilogue (both CTAs, own 128 rows)
-    // Warps 2-5 drain accumulator 0 and warps 6-9 accumulator 1 (a warp reaches the TMEM lanes of
-    // quarter warp % 4), so an item's two output frames are written at the same time.
-    const int quarter = warp & 3, row = quarter * 32 + lane, o = (warp - 2) / 4;
+    // Warps 2-9 drain accumulator 0 and warps 10-17 accumulator 1, each warp 128 of its 256 columns
+    // for the TMEM lanes of quarter warp % 4, so an item's two output frames are written at once.
+    const int quarter = warp & 3, row = quarter * 32 + lane, o = (warp - 2) / 8;
+    const int col0 = (((warp - 2) >> 2) & 1) * (kTuN / 2);
     const uint32_t leader_empty = mapa_shared(smem_u32(tmem_empty), 0);
     uint32_t acc_phase = 0;
     for (int r = 0;; ++r) {
@@ -296,24 +297,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTuThreads, 1)
       if (writes) {
         const int fy = args.y_frame0 + 2 * frame + half;
         wan_bf16* yrow = args.y + ((((size_t)t.n * args.y_frames + fy) * args.H + hh) * args.W + ww) * args.C + cy;
-        const uint32_t taddr = tmem_base + (uint32_t)((sub < 0 ? o : 0) * kTuN) + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t taddr =
+            tmem_base + (uint32_t)((sub < 0 ? o : 0) * kTuN + col0) + ((uint32_t)(quarter * 32) << 16);
         uint32_t rn[16];
         __syncwarp();
         tmem_ld16_issue(taddr, rn);
         tmem_ld16_wait(rn);
 #pragma unroll 1
-        for (int c0 = 0; c0 < kTuN; c0 += 16) {
+        for (int c0 = 0; c0 < kTuN / 2; c0 += 16) {
           float v[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(rn[i]);
-          if (c0 + 16 < kTuN) {
+          if (c0 + 16 < kTuN / 2) {
             __syncwarp();
             tmem_ld16_issue(taddr + c0 + 16, rn);
           }
           if (valid) {
             if (args.bias) {
-              const uint4 b0 = __ldg(reinterpret_cast<const uint4*>(args.bias + t.nb * kTuN + c0));
-              const uint4 b1 = __ldg(reinterpret_cast<const uint4*>(args.bias + t.nb * kTuN + c0 + 8));
+              const uint4 b0 = __ldg(reinterpret_cast<const uint4*>(args.bias + t.nb * kTuN + col0 + c0));
+              const uint4 b1 = __ldg(reinterpret_cast<const uint4*>(args.bias + t.nb * kTuN + col0 + c0 + 8));
               const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
@@ -324,10 +326,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTuThreads, 1)
             uint32_t ov[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) ov[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-            *reinterpret_cast<uint4*>(yrow + c0) = make_uint4(ov[0], ov[1], ov[2], ov[3]);
-            *reinterpret_cast<uint4*>(yrow + c0 + 8) = make_uint4(ov[4], ov[5], ov[6], ov[7]);
+            *reinterpret_cast<uint4*>(yrow + col0 + c0) = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+            *reinterpret_cast<uint4*>(yrow + col0 + c0 + 8) = make_uint4(ov[4], ov[5], ov[6], ov[7]);
           }
-          if (c0 + 16 < kTuN) tmem_ld16_wait(rn);
+          if (c0 + 16 < kTuN / 2) tmem_ld16_wait(rn);
         }
       }
       // This warp is done with both accumulators: one arrival per warp on the even CTA's barrier.
