@@ -200,6 +200,7 @@ size_t wan_workspace_size(wan_op op, int N, int T, int H, int W, int Cin, int Co
 
 wan_status wan_gn_silu(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta, int N, int T,
                        int H, int W, int C, int groups, float eps, void* ws, size_t ws_bytes, void* stream) {
+  WAN_CALL_RANGE();
   wan_status st = check_gn(x, y, gamma, beta, N, T, H, W, C, groups, eps);
   if (st != WAN_OK) return st;
   const size_t bytes = (size_t)N * T * H * W * C * sizeof(wan_bf16);
@@ -213,6 +214,7 @@ wan_status wan_gn_silu(const wan_bf16* x, wan_bf16* y, const float* gamma, const
 
 wan_status wan_gn_silu_clip(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta, int N, int T,
                             int H, int W, int C, int groups, float eps, void* ws, size_t ws_bytes, void* stream) {
+  WAN_CALL_RANGE();
   wan_status st = check_gn(x, y, gamma, beta, N, T, H, W, C, groups, eps);
   if (st != WAN_OK) return st;
   const size_t bytes = (size_t)N * T * H * W * C * sizeof(wan_bf16);
@@ -228,6 +230,7 @@ wan_status wan_gn_silu_clip(const wan_bf16* x, wan_bf16* y, const float* gamma, 
 wan_status wan_gn_silu_from_stats(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta, int N,
                                   int T, int H, int W, int C, int groups, float eps, const void* stats,
                                   size_t stats_bytes, void* ws, size_t ws_bytes, void* stream) {
+  WAN_CALL_RANGE();
   wan_status st = check_gn(x, y, gamma, beta, N, T, H, W, C, groups, eps);
   if (st != WAN_OK) return st;
   if (!stats) return WAN_ERR_INVALID_ARG;
@@ -256,6 +259,7 @@ wan_status wan_gn_silu_from_stats(const wan_bf16* x, wan_bf16* y, const float* g
 wan_status wan_gn_silu_coefficients_from_stats(const void* stats, size_t stats_bytes, const float* gamma,
                                                const float* beta, int N, int T, int H, int W, int C, int groups,
                                                float eps, void* coef, void* stream) {
+  WAN_CALL_RANGE();
   if (!stats || !gamma || !beta || !coef) return WAN_ERR_INVALID_ARG;
   if (!positive(N, T, H, W, C) || groups <= 0 || C % groups != 0) return WAN_ERR_INVALID_ARG;
   if (!(eps > 0.0f) || eps != eps || eps > 3.0e38f) return WAN_ERR_INVALID_ARG;  // as check_gn
@@ -348,6 +352,7 @@ wan_status wan_causal_conv3d(const wan_bf16* a, const wan_bf16* cache_in, wan_bf
                              const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y,
                              int N, int T, int H, int W, int Cin, int Cout, void* ws, size_t ws_bytes,
                              void* stream) {
+  WAN_CALL_RANGE();
   (void)ws;
   (void)ws_bytes;
   return causal_conv(a, cache_in, cache_out, w, bias, residual, y, N, T, H, W, Cin, Cout, nullptr, 0, stream);
@@ -357,6 +362,7 @@ wan_status wan_causal_conv3d_gn_stats(const wan_bf16* a, const wan_bf16* cache_i
                                       const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y,
                                       int N, int T, int H, int W, int Cin, int Cout, int groups, void* stats,
                                       size_t stats_bytes, void* stream) {
+  WAN_CALL_RANGE();
   if (!stats || groups <= 0) return WAN_ERR_INVALID_ARG;
   if (!positive(N, T, H, W, Cin) || Cout <= 0) return WAN_ERR_INVALID_ARG;
   if (!conv_gn_stats_supported(Cout, groups)) return WAN_ERR_UNSUPPORTED_SHAPE;
@@ -369,6 +375,7 @@ wan_status wan_gn_silu_causal_conv3d(const wan_bf16* x, const float* gamma, cons
                                      float eps, const wan_bf16* cache_in, wan_bf16* cache_out, const wan_bf16* w,
                                      const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H,
                                      int W, int Cin, int Cout, void* ws, size_t ws_bytes, void* stream) {
+  WAN_CALL_RANGE();
   wan_status st = check_gn(x, y, gamma, beta, N, T, H, W, Cin, groups, eps);
   if (st != WAN_OK) return st;
   st = check_conv(x, w, y, N, T, H, W, Cin, Cout);
@@ -394,6 +401,7 @@ wan_status wan_gn_silu_causal_conv3d(const wan_bf16* x, const float* gamma, cons
 wan_status wan_gn_silu_coefficients(const wan_bf16* x, const float* gamma, const float* beta, int N, int T, int H,
                                     int W, int C, int groups, float eps, void* coef, void* ws, size_t ws_bytes,
                                     void* stream) {
+  WAN_CALL_RANGE();
   wan_status st = check_gn(x, coef, gamma, beta, N, T, H, W, C, groups, eps);
   if (st != WAN_OK) return st;
   if (C % 64 != 0) return WAN_ERR_UNSUPPORTED_SHAPE;
@@ -461,6 +469,7 @@ extern "C" {
 wan_status wan_causal_conv3d_gn_input(const wan_bf16* x, const void* coef, const wan_bf16* cache_in, wan_bf16* cache_out,
                                       const wan_bf16* w, const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y,
                                       int N, int T, int H, int W, int Cin, int Cout, void* stream) {
+  WAN_CALL_RANGE();
   return gn_input_conv(x, coef, cache_in, cache_out, w, bias, residual, y, N, T, H, W, Cin, Cout, 0, nullptr, 0,
                        stream);
 }
@@ -469,6 +478,7 @@ wan_status wan_causal_conv3d_gn_input_stats(const wan_bf16* x, const void* coef,
                                             wan_bf16* cache_out, const wan_bf16* w, const wan_bf16* bias,
                                             const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W, int Cin,
                                             int Cout, int groups, void* stats, size_t stats_bytes, void* stream) {
+  WAN_CALL_RANGE();
   if (!stats) return WAN_ERR_INVALID_ARG;
   return gn_input_conv(x, coef, cache_in, cache_out, w, bias, residual, y, N, T, H, W, Cin, Cout, groups, stats,
                        stats_bytes, stream);
@@ -476,6 +486,7 @@ wan_status wan_causal_conv3d_gn_input_stats(const wan_bf16* x, const void* coef,
 
 wan_status wan_gn_silu_cache_update(const wan_bf16* x, const void* coef, const wan_bf16* cache_in, wan_bf16* cache_out,
                                     int N, int T, int H, int W, int C, void* stream) {
+  WAN_CALL_RANGE();
   if (!x || !coef || !cache_out) return WAN_ERR_INVALID_ARG;
   if (!positive(N, T, H, W, C)) return WAN_ERR_INVALID_ARG;
   if (C % 64 != 0 || C > 2048 || !fits(N, T, H, W, C)) return WAN_ERR_UNSUPPORTED_SHAPE;
@@ -491,6 +502,7 @@ wan_status wan_gn_silu_cache_update(const wan_bf16* x, const void* coef, const w
 
 wan_status wan_cache_update(const wan_bf16* a, const wan_bf16* cache_in, wan_bf16* cache_out, int N, int T, int H,
                             int W, int C, void* stream) {
+  WAN_CALL_RANGE();
   if (!a || !cache_out) return WAN_ERR_INVALID_ARG;
   if (!positive(N, T, H, W, C)) return WAN_ERR_INVALID_ARG;
   if (C % 8 != 0 || !fits(N, T, H, W, C)) return WAN_ERR_UNSUPPORTED_SHAPE;
@@ -503,6 +515,7 @@ wan_status wan_cache_update(const wan_bf16* a, const wan_bf16* cache_in, wan_bf1
 }
 
 wan_status wan_upsample_phase_weights(const wan_bf16* w3, wan_bf16* wp, int Cin, int Cout, void* stream) {
+  WAN_CALL_RANGE();
   if (!w3 || !wp || Cin <= 0 || Cout <= 0) return WAN_ERR_INVALID_ARG;
   if ((long long)Cin * Cout * 16 >= (1LL << 40)) return WAN_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(w3) || !aligned16(wp)) return WAN_ERR_MISALIGNED;
@@ -512,6 +525,7 @@ wan_status wan_upsample_phase_weights(const wan_bf16* w3, wan_bf16* wp, int Cin,
 
 wan_status wan_upsample_phase_conv(const wan_bf16* x, const wan_bf16* wp, const wan_bf16* bias, wan_bf16* y,
                                    int N, int T, int H, int W, int Cin, int Cout, void* stream) {
+  WAN_CALL_RANGE();
   wan_status st = check_conv(x, wp, y, N, T, 2 * H, 2 * W, Cin, Cout);
   if (st != WAN_OK) return st;
   if (bias && !aligned16(bias)) return WAN_ERR_MISALIGNED;
@@ -526,6 +540,7 @@ wan_status wan_upsample_phase_conv(const wan_bf16* x, const wan_bf16* wp, const 
 wan_status wan_resblock(const wan_bf16* x, wan_bf16* out, const wan_resblock_params* p, wan_bf16* cache1,
                         wan_bf16* cache2, int cache_valid, int N, int T, int H, int W, int C, void* ws,
                         size_t ws_bytes, void* stream) {
+  WAN_CALL_RANGE();
   if (!p || !cache1 || !cache2) return WAN_ERR_INVALID_ARG;
   wan_status st = check_gn(x, out, p->gamma1, p->beta1, N, T, H, W, C, p->groups, p->eps);
   if (st != WAN_OK) return st;
@@ -564,6 +579,7 @@ wan_status wan_resblock(const wan_bf16* x, wan_bf16* out, const wan_resblock_par
 wan_status wan_time_upsample(const wan_bf16* x, const wan_bf16* cache_in, wan_bf16* cache_out, const wan_bf16* w,
                              const wan_bf16* bias, wan_bf16* y, int N, int T, int H, int W, int C, int first,
                              void* stream) {
+  WAN_CALL_RANGE();
   if (!x || !w || !y) return WAN_ERR_INVALID_ARG;
   if (!positive(N, T, H, W, C)) return WAN_ERR_INVALID_ARG;
   if (C % 256 != 0 || !fits(N, 2 * T, H, W, C)) return WAN_ERR_UNSUPPORTED_SHAPE;
@@ -607,6 +623,7 @@ wan_status wan_time_upsample(const wan_bf16* x, const wan_bf16* cache_in, wan_bf
 
 wan_status wan_conv1x1(const wan_bf16* x, const wan_bf16* w, wan_bf16* y, int N, int T, int H, int W, int Cin,
                        int Cout, void* stream) {
+  WAN_CALL_RANGE();
   wan_status st = check_conv(x, w, y, N, T, H, W, Cin, Cout);
   if (st != WAN_OK) return st;
   if (!conv_pair_supported(Cout)) return WAN_ERR_UNSUPPORTED_SHAPE;
@@ -618,6 +635,7 @@ wan_status wan_conv1x1(const wan_bf16* x, const wan_bf16* w, wan_bf16* y, int N,
 }
 
 wan_status wan_fold_bias(const wan_bf16* b2, const wan_bf16* b_shortcut, wan_bf16* out, int C, void* stream) {
+  WAN_CALL_RANGE();
   if (!b2 || !b_shortcut || !out || C <= 0) return WAN_ERR_INVALID_ARG;
   return cuda_status(fold_bias_launch(b2, b_shortcut, out, C, static_cast<cudaStream_t>(stream)));
 }
@@ -625,6 +643,7 @@ wan_status wan_fold_bias(const wan_bf16* b2, const wan_bf16* b_shortcut, wan_bf1
 wan_status wan_resblock_shortcut(const wan_bf16* x, wan_bf16* out, const wan_resblock_params* p, const wan_bf16* w_sc,
                                  wan_bf16* cache1, wan_bf16* cache2, int cache_valid, int N, int T, int H, int W,
                                  int Cin, int Cout, void* ws, size_t ws_bytes, void* stream) {
+  WAN_CALL_RANGE();
   if (!p || !cache1 || !cache2 || !w_sc) return WAN_ERR_INVALID_ARG;
   wan_status st = check_gn(x, out, p->gamma1, p->beta1, N, T, H, W, Cin, p->groups, p->eps);
   if (st != WAN_OK) return st;
@@ -669,6 +688,7 @@ wan_status wan_resblock_shortcut(const wan_bf16* x, wan_bf16* out, const wan_res
 }
 
 wan_status wan_winograd_weights(const wan_bf16* w, wan_fp16* u, int Cin, int Cout, void* stream) {
+  WAN_CALL_RANGE();
   if (!w || !u || Cin <= 0 || Cout <= 0) return WAN_ERR_INVALID_ARG;
   if (!wino_supported(Cin, Cout) || (long long)Cin * Cout * 27 >= (1LL << 40)) return WAN_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(w) || !aligned16(u)) return WAN_ERR_MISALIGNED;
@@ -680,6 +700,7 @@ wan_status wan_causal_conv3d_winograd(const wan_bf16* a, const void* coef, const
                                       wan_bf16* cache_out, const wan_fp16* u, const wan_bf16* bias,
                                       const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W, int Cin,
                                       int Cout, void* ws, size_t ws_bytes, void* stream) {
+  WAN_CALL_RANGE();
   wan_status st = check_conv(a, u, y, N, T, H, W, Cin, Cout);
   if (st != WAN_OK) return st;
   if (!wino_supported(Cin, Cout) || Cin > 2048) return WAN_ERR_UNSUPPORTED_SHAPE;
@@ -716,6 +737,7 @@ wan_status wan_causal_conv3d_winograd(const wan_bf16* a, const void* coef, const
 wan_status wan_resblock_winograd(const wan_bf16* x, wan_bf16* out, const wan_resblock_params* p, const wan_fp16* u1,
                                  const wan_fp16* u2, wan_bf16* cache1, wan_bf16* cache2, int cache_valid, int N, int T,
                                  int H, int W, int C, void* ws, size_t ws_bytes, void* stream) {
+  WAN_CALL_RANGE();
   if (!p || !cache1 || !cache2 || !u1 || !u2) return WAN_ERR_INVALID_ARG;
   wan_status st = check_gn(x, out, p->gamma1, p->beta1, N, T, H, W, C, p->groups, p->eps);
   if (st != WAN_OK) return st;
@@ -759,6 +781,7 @@ wan_status wan_resblock_winograd(const wan_bf16* x, wan_bf16* out, const wan_res
 }
 
 wan_status wan_device_status(void* stream) {
+  WAN_CALL_RANGE();
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return WAN_ERR_CUDA;
   unsigned v = 0;
   if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return WAN_ERR_CUDA;

@@ -2,6 +2,7 @@
 // implements an extern "C" call so that all of them validate arguments the same way.
 #pragma once
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 #include <stddef.h>
 
 #include "wan.h"
@@ -16,4 +17,17 @@ wan_status cuda_status(cudaError_t e);
 // The argument checks of wan_gn_silu: pointers, sizes, groups, eps, supported shape, alignment.
 wan_status check_gn(const void* x, const void* y, const float* gamma, const float* beta, int N, int T, int H, int W,
                     int C, int groups, float eps);
+
+// An NVTX range named after the entry point, open for the whole call (validation, workspace
+// layout and every launch it enqueues): timeline profilers show each call by name, and ncu can
+// select the kernels of one call (`--nvtx --nvtx-include "wan_resblock/"`). With no tool
+// attached a push or pop is one test of a function pointer.
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
 }  // namespace wan
+
+#define WAN_CALL_RANGE() const ::wan::CallRange wan_call_range_(__func__)

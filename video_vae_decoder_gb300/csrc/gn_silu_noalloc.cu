@@ -49,6 +49,7 @@ void* scratch_address() {
 
 extern "C" wan_status wan_gn_silu_noalloc(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta,
                                           int N, int T, int H, int W, int C, int groups, float eps, void* stream) {
+  WAN_CALL_RANGE();
   using namespace wan;
   wan_status st = check_gn(x, y, gamma, beta, N, T, H, W, C, groups, eps);
   if (st != WAN_OK) return st;

@@ -27,7 +27,6 @@
 #include <stdint.h>
 
 #include <algorithm>
-#include <vector>
 
 #include "common.cuh"
 #include "tma_host.h"
@@ -648,6 +647,8 @@ cudaError_t head_launch(const wan_bf16* a, const wan_bf16* cache_in, const wan_b
     }
     slots = max_clusters[dev];
   }
+  constexpr int kMaxSlots = 512;  // the per-pair load table below lives on the stack
+  slots = std::max(1, std::min(slots, kMaxSlots));
   // Rows per band and item order. First the fewest rounds over the CTA pairs, counting the two halo
   // rows of a band; then, among band counts within 10% of that, the schedule whose busiest pair
   // has the least work, counting a quad's real taps (frames before a chunk without history have
@@ -671,14 +672,14 @@ cudaError_t head_launch(const wan_bf16* a, const wan_bf16* cache_in, const wan_b
   }
   long long best_max = -1;
   int best_bands = 1, best_order = 0;
-  std::vector<long long> load(slots);
+  long long load[kMaxSlots];
   for (int bands = 1; bands <= H && bands <= 256; ++bands) {
     if (rounds_cost(bands) * 10 > min_cost * 11) continue;
     const int rows = cdiv(H, bands);
     const int nb = cdiv(H, rows);
     const long long items = base * nb;
     for (int order = 0; order < 2; ++order) {
-      std::fill(load.begin(), load.end(), 0);
+      std::fill(load, load + slots, 0LL);
       for (long long r = 0; r * slots < items; ++r)
         for (int c = 0; c < slots; ++c) {
           const long long off = order ? (c + r) % slots : ((r & 1) ? slots - 1 - c : c);
@@ -689,7 +690,7 @@ cudaError_t head_launch(const wan_bf16* a, const wan_bf16* cache_in, const wan_b
           const int nrows = std::min(h1, H - 1) - std::max(h0 - 1, 0) + 1;
           load[c] += (long long)nrows * (q < 64 ? quad_taps[q] : 3 * kFrames);
         }
-      const long long mx = *std::max_element(load.begin(), load.end());
+      const long long mx = *std::max_element(load, load + slots);
       if (best_max < 0 || mx < best_max) {
         best_max = mx;
         best_bands = nb;

@@ -37,6 +37,7 @@ extern "C" wan_status wan_selftest_wait_timeout(int which, long long wait_cycles
                                                 const float* gamma, const float* beta, int N, int T, int H, int W,
                                                 int C, int groups, float eps, void* ws, size_t ws_bytes,
                                                 void* stream) {
+  WAN_CALL_RANGE();
   using namespace wan;
   if (wait_cycles < 1000 || wait_cycles > 100000000LL || (which != 0 && which != 1)) return WAN_ERR_INVALID_ARG;
   if (which == 0) {
