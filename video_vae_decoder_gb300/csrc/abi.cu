@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <stdint.h>
 #include <string.h>
 
@@ -31,15 +32,15 @@ int current_device() {
 }  // namespace
 
 int sm_count() {
-  static int cached[kMaxDevices] = {0};
+  static std::atomic<int> cached[kMaxDevices];  // 0 until queried; every query gives the same answer
   const int d = current_device();
   if (d < 0 || d >= kMaxDevices) return 148;
-  if (!cached[d]) {
-    int n = 0;
+  int n = cached[d].load(std::memory_order_relaxed);
+  if (!n) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess || n <= 0) n = 148;
-    cached[d] = n;
+    cached[d].store(n, std::memory_order_relaxed);
   }
-  return cached[d];
+  return n;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -982,23 +982,7 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tc, const CUte
   constexpr int kSmem = Cfg<kKind>::kSmemTotal, kThr = Cfg<kKind>::kThreads;
   cudaError_t e = cudaFuncSetAttribute(conv_tc2_kernel<kKind>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  static int max_clusters[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && max_clusters[dev] == 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
-    cfg.blockDim = dim3(kThr, 1, 1);
-    cfg.dynamicSmemBytes = kSmem;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, conv_tc2_kernel<kKind>, &cfg) != cudaSuccess || n <= 0) {
-      cudaGetLastError();
-      n = sms / 2;
-    }
-    max_clusters[dev] = n;
-  }
-  int clusters = (dev >= 0 && dev < 64) ? max_clusters[dev] : sms / 2;
-  if (clusters < 1) clusters = 1;
+  int clusters = resident_pairs(reinterpret_cast<const void*>(conv_tc2_kernel<kKind>), kThr, kSmem, sms);
   // A last round of at most half the pairs' worth of items runs as twice as many 128-channel
   // halves (with the epilogue statistics only while a half holds whole windows of 4 groups).
   const int rem = args.items % clusters;

@@ -628,25 +628,7 @@ cudaError_t head_launch(const wan_bf16* a, const wan_bf16* cache_in, const wan_b
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTotal);
   if (e != cudaSuccess) return e;
   // CTA pairs the GPU can hold at once (a pair lives in one GPC).
-  static int max_clusters[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  int slots = sms / 2;
-  if (dev >= 0 && dev < 64) {
-    if (max_clusters[dev] == 0) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
-      cfg.blockDim = dim3(kThreads, 1, 1);
-      cfg.dynamicSmemBytes = kSmemTotal;
-      int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
-        cudaGetLastError();
-        n = sms / 2;
-      }
-      max_clusters[dev] = n;
-    }
-    slots = max_clusters[dev];
-  }
+  int slots = resident_pairs(reinterpret_cast<const void*>(kern), kThreads, kSmemTotal, sms);
   constexpr int kMaxSlots = 512;  // the per-pair load table below lives on the stack
   slots = std::max(1, std::min(slots, kMaxSlots));
   // Rows per band and item order. First the fewest rounds over the CTA pairs, counting the two halo

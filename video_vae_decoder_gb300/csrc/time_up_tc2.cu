@@ -414,23 +414,7 @@ cudaError_t time_up_launch(const wan_bf16* x, const wan_bf16* cache_in, const wa
   if (!tu_map_w(&tw, w, 3 * C, 2 * C)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(time_up_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTuSmem);
   if (e != cudaSuccess) return e;
-  static int max_clusters[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && max_clusters[dev] == 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
-    cfg.blockDim = dim3(kTuThreads, 1, 1);
-    cfg.dynamicSmemBytes = kTuSmem;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, time_up_kernel, &cfg) != cudaSuccess || n <= 0) {
-      cudaGetLastError();
-      n = sms / 2;
-    }
-    max_clusters[dev] = n;
-  }
-  int clusters = (dev >= 0 && dev < 64) ? max_clusters[dev] : sms / 2;
-  if (clusters < 1) clusters = 1;
+  int clusters = resident_pairs(reinterpret_cast<const void*>(time_up_kernel), kTuThreads, kTuSmem, sms);
   // A last round of at most half the pairs' worth of items runs as twice as many units of one
   // output frame each (half the MMAs).
   const int rem = args.items % clusters;

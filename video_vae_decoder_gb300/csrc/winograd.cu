@@ -637,22 +637,7 @@ cudaError_t wino_conv_launch(const wan_bf16* a, const float4* coef, const wan_bf
   if (!map_f16_3d(&tu, u, 3LL * Cin, Cout, 16)) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(wino_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem);
   if (e != cudaSuccess) return e;
-  static int max_clusters[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && max_clusters[dev] == 0) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
-    cfg.blockDim = dim3(kWThreads, 1, 1);
-    cfg.dynamicSmemBytes = kWSmem;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, wino_gemm_kernel, &cfg) != cudaSuccess || n <= 0) {
-      cudaGetLastError();
-      n = sms / 2;
-    }
-    max_clusters[dev] = n;
-  }
-  int clusters = (dev >= 0 && dev < 64) ? max_clusters[dev] : sms / 2;
+  int clusters = resident_pairs(reinterpret_cast<const void*>(wino_gemm_kernel), kWThreads, kWSmem, sms);
   if (clusters > ga.items) clusters = ga.items;
   if (clusters < 1) clusters = 1;
   wino_gemm_kernel<<<2 * clusters, kWThreads, kWSmem, s>>>(tv, tu, ga);
