@@ -32,6 +32,8 @@ def same(a, b):
     ((1, 1, 8, 16, 256), False, True),     # one frame: the history shifts by one
     ((1, 1, 8, 16, 256), True, False),     # the first chunk of one frame: only the pass-through
     ((1, 2, 12, 33, 512), False, False),   # no history, two N blocks per channel half
+    ((1, 2, 1, 1, 256), False, True),      # 1 x 1 frames with history
+    ((1, 3, 1, 5, 256), True, False),      # one-pixel-high frames, first chunk
 ])
 def test_time_upsample_matches_oracle(wan, shape, first, history):
     x, w, b, c = tu_inputs(shape, f"tu/{shape}/{first}/{history}")

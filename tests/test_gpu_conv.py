@@ -43,6 +43,11 @@ def run(wan, a, w, b, r, c, with_cache_out=True):
     ((1, 4, 8, 16, 64), 512, False, False, True),     # exactly one tile per frame, two N blocks
     ((1, 1, 3, 50, 64), 256, True, False, False),     # one frame, fewer rows than a tile, 4 tiles wide
     ((2, 2, 12, 33, 64), 256, True, True, True),      # batch 2: tile pairs that cross batch items
+    # degenerate frames: every tile mostly outside the frame, only some taps inside it
+    ((1, 2, 1, 1, 64), 256, True, True, True),        # 1 x 1 frames on the CTA-pair path: the centre taps
+    ((1, 3, 1, 9, 64), 256, True, False, True),       # one-pixel-high frames
+    ((1, 2, 9, 1, 64), 256, False, True, True),       # one-pixel-wide frames
+    ((1, 2, 1, 1, 64), 64, True, True, True),         # 1 x 1 frames on the one-CTA kernel
 ])
 def test_conv_small(wan, shape, Cout, bias, residual, cache):
     a, w, b, r, c = make(shape, Cout, f"conv/{shape}/{Cout}", bias, residual, cache)

@@ -72,6 +72,9 @@ def test_fused_equals_unfused(wan, shape, Cout, history, residual):
     ((1, 2, 9, 17, 256), 256),     # 8 channels per group
     ((1, 2, 9, 17, 1024), 1024),   # the widest stage's Cin: 16 K blocks per tap, 32 channels per group
     ((1, 3, 8, 20, 1024), 256),
+    ((1, 2, 1, 1, 64), 256),       # 1 x 1 frames: each group of a frame holds 2 values
+    ((1, 2, 1, 9, 256), 256),      # one-pixel-high frames: the tiles' boxes mostly zero padding
+    ((1, 2, 9, 1, 256), 256),      # one-pixel-wide frames
 ])
 def test_fused_matches_oracle(wan, shape, Cout):
     x, g, be, w, b, c, _ = inputs(shape, Cout, f"gnconv/oracle/{shape}/{Cout}")

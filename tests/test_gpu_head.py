@@ -37,6 +37,8 @@ def f64(x):
     ((1, 8, 9, 40, 128), True, False, False),
     ((1, 4, 6, 50, 192), False, False, True),
     ((1, 8, 5, 20, 64), False, True, True),
+    ((1, 3, 1, 1, 64), True, False, True),          # 1 x 1 frames: only the centre stencil term
+    ((1, 2, 7, 1, 128), False, True, False),        # one-pixel-wide frames
 ])
 def test_head_small(wan, shape, bias, residual, cache):
     a, w, b, r, c = make(shape, f"head/{shape}", bias, residual, cache)

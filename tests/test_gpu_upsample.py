@@ -22,6 +22,8 @@ def test_phase_weights_bit_exact(wan):
     ((2, 2, 5, 7, 64), 320, True),
     ((1, 2, 19, 40, 64), 256, True),    # CTA-pair path: ragged 8 x 16 tiles, 3 tiles wide
     ((1, 1, 9, 17, 128), 512, False),   # CTA-pair path: two N blocks
+    ((1, 2, 1, 1, 64), 256, True),      # a 1 x 1 input: a 2 x 2 output, each phase one tap inside
+    ((1, 1, 1, 7, 64), 256, False),     # a one-row input
 ])
 def test_upsample_small(wan, shape, Cout, bias):
     Cin = shape[-1]

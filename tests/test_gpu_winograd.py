@@ -70,6 +70,9 @@ def run_wino(wan, x, w, g, be, c, b, r, cache_out=True):
     ((1, 5, 20, 40, 256), 256, True, False, True, False),    # 1000 rows: 4 pair tiles, the last partial
     ((1, 2, 7, 9, 1024), 256, True, True, True, True),       # 16 K blocks per tap
     ((1, 2, 11, 91, 64), 256, True, True, False, False),     # 46 tiles wide: two column blocks of the transform
+    ((1, 2, 1, 1, 64), 256, True, True, True, True),         # a 1 x 1 frame: one tile, 3 of its outputs outside
+    ((1, 3, 1, 3, 64), 256, True, False, True, False),       # one-pixel-high frames
+    ((1, 2, 3, 1, 128), 256, False, True, False, True),      # one-pixel-wide frames
 ])
 def test_winograd_conv_matches_oracle(wan, shape, Cout, coef, cache, bias, residual):
     name = f"wino/conv/{shape}/{Cout}"
