@@ -91,6 +91,7 @@ def test_gn_rejects_invalid(L):
     assert call(T=0) == 1
     assert call(G=24) == 1            # does not divide 64
     assert call(C=60, G=4) == 2       # C % 8 != 0
+    assert call(C=2112, G=32) == 2    # wider than the 2048 channels the kernel supports
     assert call(eps=0.0) == 1
     assert call(x=MIS) == 3
     assert call(y=A) == 1             # y overlaps x

@@ -32,6 +32,8 @@ def run_case(wan, shape, groups, mean, std, name, seed=0):
     ((1, 2, 10, 10, 64), 16),      # 4 per group
     ((1, 1, 1, 1, 512), 32),       # a single pixel
     ((1, 2, 33, 47, 1024), 32),    # 32 per group
+    ((1, 2, 9, 13, 2048), 32),     # the widest C supported: 64 per group
+    ((1, 1, 5, 7, 2048), 256),     # the widest C in 256 groups of 8
 ])
 def test_gn_small(wan, shape, groups):
     mx, _, _ = run_case(wan, shape, groups, 0.5, np.sqrt(2.0), f"gn/{shape}")

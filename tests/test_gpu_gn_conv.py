@@ -75,6 +75,7 @@ def test_fused_equals_unfused(wan, shape, Cout, history, residual):
     ((1, 2, 1, 1, 64), 256),       # 1 x 1 frames: each group of a frame holds 2 values
     ((1, 2, 1, 9, 256), 256),      # one-pixel-high frames: the tiles' boxes mostly zero padding
     ((1, 2, 9, 1, 256), 256),      # one-pixel-wide frames
+    ((1, 2, 5, 9, 2048), 256),     # the widest Cin the norm takes: 32 K blocks per tap
 ])
 def test_fused_matches_oracle(wan, shape, Cout):
     x, g, be, w, b, c, _ = inputs(shape, Cout, f"gnconv/oracle/{shape}/{Cout}")

@@ -73,6 +73,7 @@ def run_wino(wan, x, w, g, be, c, b, r, cache_out=True):
     ((1, 2, 1, 1, 64), 256, True, True, True, True),         # a 1 x 1 frame: one tile, 3 of its outputs outside
     ((1, 3, 1, 3, 64), 256, True, False, True, False),       # one-pixel-high frames
     ((1, 2, 3, 1, 128), 256, False, True, False, True),      # one-pixel-wide frames
+    ((1, 2, 5, 7, 2048), 256, True, True, True, True),       # the widest Cin with the norm applied
 ])
 def test_winograd_conv_matches_oracle(wan, shape, Cout, coef, cache, bias, residual):
     name = f"wino/conv/{shape}/{Cout}"
