@@ -384,6 +384,12 @@ typedef struct wan_resblock_params {
  *                overwritten; 1: they hold the history left by the previous chunk.
  *   C % 64 == 0 and the GroupNorm conditions of wan_gn_silu.
  *   ws           >= wan_workspace_size(WAN_OP_RESBLOCK, N, T, H, W, C, C, groups) bytes.
+ * Cost of the in/out caches: with cache_valid = 1 a conv must read the old history before the
+ * new one replaces it, so each conv is followed by a pass that normalises its input's last two
+ * frames into the cache again (about 5% of a C = 256 conv at 176 x 312). Where the caller keeps
+ * two buffers per cache and swaps them, the steps of this call (wan_gn_silu_coefficients,
+ * wan_causal_conv3d_gn_input with cache_out apart from cache_in) let the conv write the new
+ * history itself, and the result is the same bits.
  */
 wan_status wan_resblock(const wan_bf16* x, wan_bf16* out, const wan_resblock_params* p,
                         wan_bf16* cache1, wan_bf16* cache2, int cache_valid,
