@@ -35,6 +35,14 @@
 // output elements with the same sequence of K steps as the whole item, so the split changes no
 // result.
 //
+// Modes (run time) and kinds (compile time, Cfg below). Mode 0 is the causal 3x3x3 conv, 1 the
+// phase convs, 2 the causal 3x1x1 time conv with one output frame per CTA (the time upsample call
+// has a kernel of its own, time_up_tc2.cu), and 3 the 1x1x1 conv of a channel-changing shortcut.
+// Kind 0 is the plain kernel on 8 x 16 tiles. Kind 1 adds the GroupNorm + SiLU operand prologue
+// and takes tall 10 x 18 boxes, one box holding a tap column's three kernel rows. Kind 2 is the
+// phase convs with one tall box per K block. Kind 3 is kind 1 on 16 x 8 tiles, with 18 x 10 boxes
+// stored row by row.
+//
 // MMA issue. One thread issues every MMA of the pair, and its issue rate, not the tensor pipe, was
 // the limit: with a wait, a fence and a stage release per tap inside a run-time loop, each MMA
 // took ~160 cycles to issue against 128 to execute (M256 x N256 x K16), whatever N was. Each A box
