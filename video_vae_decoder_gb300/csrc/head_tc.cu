@@ -15,10 +15,13 @@
 //     leaves room for an 8-deep TMA ring of input strips (one resident copy of all of W' would
 //     leave room for 3, and the MMAs would wait on load latency). One thread of the even CTA
 //     issues the M256 x N112 MMAs; the odd CTA's loads complete on the even CTA's barriers.
-//   * Each pair owns (batch item, pair of output frames t and t+1, two neighbouring 128-pixel
-//     strips, band of image rows) and walks the rows of its band. A frame pair shares the input
-//     frames t-1 and t, so 4 input rows feed 2 output rows; the two accumulators (2 x 112 TMEM
-//     columns) are double-buffered so the epilogue of row r overlaps the MMAs of row r+1.
+//   * Each pair owns (batch item, 4 output frames t .. t+3, two neighbouring 128-pixel strips,
+//     band of image rows) and walks the rows of its band. Per row it loads the 6 input frames
+//     t-2 .. t+3 once (1.5 input rows per output row instead of 3), and each input frame feeds the
+//     accumulators of the output frames that use it (4 x 112 of the 512 TMEM columns, one barrier
+//     pair per output frame), so one frame's epilogue runs while the MMAs of the others go on.
+//     Two epilogue warpgroups take two frames each; a frame's epilogue applies the 3x3 stencil and
+//     carries two partial output rows from one image row to the next.
 // Reduction order per output is fixed (taps, then the 9 stencil terms), independent of the
 // band/strip/pair placement and of chunking along T.
 #include <cuda.h>
