@@ -9,12 +9,14 @@
 // two grid barriers (bounded waits; a barrier that times out records an error and the kernel
 // winds down):
 //   A  statistics: work items are (frame, pixel span of ~64 KB), dealt round-robin to the CTAs.
-//      x streams through shared memory: each CTA keeps six 16 KB pieces in flight with bulk async
+//      x streams through shared memory: each CTA keeps three 32 KB pieces in flight with bulk async
 //      copies (cp.async.bulk, completion on an mbarrier). Every thread owns one 16-byte
 //      vector of 8 channels (so its groups are fixed) and accumulates, per channel, sum(d) and
 //      sum(d^2) of d = x - s, where s is one value of the channel's group in the frame (its
-//      first pixel). Both sums are fp32 pairs (hi, lo): sum(d) with Knuth's TwoSum, sum(d^2)
-//      (non-negative terms) with Dekker's Fast2Sum, two channels per packed fp32x2 instruction.
+//      first pixel). A thread first sums its run of up to 8 pixels of a piece in plain fp32
+//      (d^2 by FMA), then adds each run sum into fp32 pairs (hi, lo): sum(d) with Knuth's
+//      TwoSum, sum(d^2) (non-negative terms) with Dekker's Fast2Sum, two channels per packed
+//      fp32x2 instruction. A run sum is exact unless the run mixes values about 12 binades apart.
 //      The CTA merges its threads' pairs per group (float-float adds, fixed order) and writes
 //      one partial per (frame, span, group).
 //   B  finalize: one warp per (frame, group) adds the span partials as float-float pairs in a
