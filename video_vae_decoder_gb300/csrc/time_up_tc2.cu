@@ -12,6 +12,9 @@
 // issues 24 MMAs, taps kt into accumulator 0 reading frame kt and into accumulator 1 reading frame
 // kt + 1. Per K16 step and SM that is 4 KB of A and 4 KB of B read by the tensor core per MMA
 // and 4.7 KB written by the TMA unit, against 8 KB written for one output frame at a time.
+// Eight epilogue warps drain each accumulator, four lane quarters by two column halves. When the
+// last round holds at most half as many items as there are pairs, its items run as single-frame
+// units, each on its own pair (one accumulator, half the MMAs).
 //
 // Pair protocol (all waits bounded), as conv_tc2.cu: the odd CTA's loads complete on the even
 // CTA's full barriers; MMAs are issued by one thread of the even CTA; stage releases and the
