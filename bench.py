@@ -542,7 +542,7 @@ def run_ours(args, rank, world, dev):
     traffic = {"conv_c256": 172.575744e6 + 125.743872e6, "gn_coef_c256": 112.540416e6 + 3.522304e6,
                "gn_coef_c1024": 28.202496e6, "conv_c1024_winograd": (42.893824e6 + 120.870912e6) +
                (270.27328e6 + 182.016512e6) + (253.05728e6 + 4.976128e6),
-               "upsample_phase_conv": 22.552064e6 + 4.372736e6, "gn_silu_decode_mid": 68.827392e6 + 11.028992e6,
+               "upsample_phase_conv": 22.554112e6 + 4.61184e6, "gn_silu_decode_mid": 68.827392e6 + 11.028992e6,
                "head_256_to_12": 9.9e9 + 0.343e9}
     rooflines = []
     for name, k in kernels.items():
