@@ -200,6 +200,10 @@ class Workload:
                                                           0), dtype=torch.uint8, device=dev)
         self.rbw_ws = torch.empty(wan.wan_workspace_size(wan.WAN_OP_RESBLOCK_WINOGRAD, *self.x5.shape, self.x5.shape[-1],
                                                          GROUPS), dtype=torch.uint8, device=dev)
+        # GroupNorm statistics written by the C=1024 stage's Winograd convs with their outputs (h,
+        # then the block's output) for the norm that reads them next
+        st_bytes = wan.wan_workspace_size(wan.WAN_OP_GN_STATS_WINOGRAD, *self.x5.shape, self.x5.shape[-1], GROUPS)
+        self.st5 = [torch.empty(st_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
         need = max(wan.wan_workspace_size(wan.WAN_OP_GN_SILU, *t.shape, 0, GROUPS)
                    for t in (self.gn_x, self.x4, self.x5))
         self.gn_ws = torch.empty(need, dtype=torch.uint8, device=dev)
@@ -234,34 +238,53 @@ class Workload:
             # (GroupNorm + SiLU into each conv): the norm's coefficients (one pass over its input),
             # then the conv normalising its operand tiles as they arrive (or its input as it is
             # transformed), which also writes the conv's new history: each conv has two history
-            # buffers, reads one and writes the other, and they swap every step.
+            # buffers, reads one and writes the other, and they swap every step. On the Winograd
+            # stage every norm after the first takes its coefficients from the statistics that the
+            # conv which wrote its input emitted (the stage's first norm reads x with a pass).
             cur = x
+            st = self.st5 if us is not None else None
             for i, (p, (c1, c2), out) in enumerate(zip(blocks, caches, outs)):
                 h1 = [c1, alt[2 * i]]      # conv 1's history: [read, write]
                 h2 = [c2, alt[2 * i + 1]]  # conv 2's
+                chained_in = st is not None and i > 0          # cur's statistics from the previous block
+                emit_out = st is not None and i + 1 < len(blocks)  # out's, for the next block
 
-                def n1(cur=cur, p=p):
-                    wan.wan_gn_silu_coefficients(cur, p["gamma1"], p["beta1"], GROUPS, EPS, coef, self.gn_ws)
+                def n1(cur=cur, p=p, chained_in=chained_in):
+                    if chained_in:
+                        wan.wan_gn_silu_coefficients_from_stats(st[1], p["gamma1"], p["beta1"], cur.shape, GROUPS, EPS,
+                                                                coef)
+                    else:
+                        wan.wan_gn_silu_coefficients(cur, p["gamma1"], p["beta1"], GROUPS, EPS, coef, self.gn_ws)
 
                 def k1(cur=cur, p=p, hb=h1, i=i):
-                    if us is not None:
+                    if st is not None:
+                        wan.wan_causal_conv3d_winograd_stats(cur, us[i][0], GROUPS, coef, p["b1"], None, hb[0], hb[1], h,
+                                                             st[0], self.wino_ws)
+                    elif us is not None:
                         wan.wan_causal_conv3d_winograd(cur, us[i][0], coef, p["b1"], None, hb[0], hb[1], h, self.wino_ws)
                     else:
                         wan.wan_causal_conv3d_gn_input(cur, coef, p["w1"], p["b1"], None, hb[0], h, cache_out=hb[1])
                     hb.reverse()
 
                 def n2(p=p):
-                    wan.wan_gn_silu_coefficients(h, p["gamma2"], p["beta2"], GROUPS, EPS, coef, self.gn_ws)
+                    if st is not None:
+                        wan.wan_gn_silu_coefficients_from_stats(st[0], p["gamma2"], p["beta2"], h.shape, GROUPS, EPS,
+                                                                coef)
+                    else:
+                        wan.wan_gn_silu_coefficients(h, p["gamma2"], p["beta2"], GROUPS, EPS, coef, self.gn_ws)
 
-                def k2(cur=cur, p=p, hb=h2, out=out, i=i):
-                    if us is not None:
+                def k2(cur=cur, p=p, hb=h2, out=out, i=i, emit_out=emit_out):
+                    if emit_out:
+                        wan.wan_causal_conv3d_winograd_stats(h, us[i][1], GROUPS, coef, p["b2"], cur, hb[0], hb[1], out,
+                                                             st[1], self.wino_ws)
+                    elif us is not None:
                         wan.wan_causal_conv3d_winograd(h, us[i][1], coef, p["b2"], cur, hb[0], hb[1], out, self.wino_ws)
                     else:
                         wan.wan_causal_conv3d_gn_input(h, coef, p["w2"], p["b2"], cur, hb[0], out, cache_out=hb[1])
                     hb.reverse()
                 kc = 3 if us is not None else 1  # Winograd: input transform, component GEMMs, output transform
-                calls.extend([(f"{tag}.coef", 1, n1), (f"{tag}.conv", kc, k1),
-                              (f"{tag}.coef", 1, n2), (f"{tag}.conv", kc, k2)])
+                calls.extend([(f"{tag}.coefst" if chained_in else f"{tag}.coef", 1, n1), (f"{tag}.conv", kc, k1),
+                              (f"{tag}.coefst" if st is not None else f"{tag}.coef", 1, n2), (f"{tag}.conv", kc, k2)])
                 cur = out
 
         if want("c256"):
@@ -520,7 +543,9 @@ def run_ours(args, rank, world, dev):
         tensor_kernel("conv_c1024_winograd", cm, wino_flops(1, 4, 44, 78, 1024, 1024), tot("c1024.conv"))
         kernels["conv_c1024_winograd"]["direct_equivalent_tflops"] = conv_flops(1, 4, 44, 78, 1024, 1024) / cm / 1e9
         hbm_kernel("gn_coef_c1024", per_launch("c1024.coef"), 2.0 * wl.x5.numel(), tot("c1024.coef"))
-        kernels["resblock_c1024_ms"] = (tot("c1024.coef") + tot("c1024.conv")) / 2.0
+        # the later norms' coefficients from the statistics the Winograd convs emitted
+        kernels["gn_coef_from_stats_c1024"] = {"ms": per_launch("c1024.coefst"), "total_ms": tot("c1024.coefst")}
+        kernels["resblock_c1024_ms"] = (tot("c1024.coef") + tot("c1024.coefst") + tot("c1024.conv")) / 2.0
     if "head.conv" in per_tag:
         # Bound by whichever takes longer at the measured peaks: its useful MMAs or its HBM bytes.
         hm = per_launch("head.conv")
@@ -540,8 +565,7 @@ def run_ours(args, rank, world, dev):
     # each kernel (profiles/); the head's from a single-pass capture of the 16-frame launch; the
     # Winograd conv's is its three kernels' sum.
     traffic = {"conv_c256": 172.575744e6 + 125.743872e6, "gn_coef_c256": 112.540416e6 + 3.522304e6,
-               "gn_coef_c1024": 28.202496e6, "conv_c1024_winograd": (42.893824e6 + 120.870912e6) +
-               (270.27328e6 + 182.016512e6) + (253.05728e6 + 4.976128e6),
+               "gn_coef_c1024": 28.202496e6, "conv_c1024_winograd": None,
                "upsample_phase_conv": 22.554112e6 + 4.61184e6, "gn_silu_decode_mid": 68.827392e6 + 11.028992e6,
                "head_256_to_12": 9.9e9 + 0.343e9}
     rooflines = []

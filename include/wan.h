@@ -60,7 +60,8 @@ typedef enum wan_op {
   WAN_OP_GN_SILU_CONV3D = 5,     /* wan_gn_silu_causal_conv3d (Cin, Cout, groups) */
   WAN_OP_RESBLOCK_SHORTCUT = 6,  /* wan_resblock_shortcut (Cin, Cout, groups) */
   WAN_OP_WINOGRAD_CONV3D = 7,    /* wan_causal_conv3d_winograd (Cin, Cout) */
-  WAN_OP_RESBLOCK_WINOGRAD = 8   /* wan_resblock_winograd (Cin = C, groups) */
+  WAN_OP_RESBLOCK_WINOGRAD = 8,  /* wan_resblock_winograd (Cin = C, groups) */
+  WAN_OP_GN_STATS_WINOGRAD = 9   /* statistics buffer of wan_causal_conv3d_winograd_stats (Cout, groups) */
 } wan_op;
 
 /* Human-readable name of a status (static storage, never NULL). */
@@ -199,8 +200,11 @@ wan_status wan_causal_conv3d_gn_stats(const wan_bf16* a, const wan_bf16* cache_i
  *
  *   x, y, gamma, beta, groups, eps, ws  as wan_gn_silu (ws >= wan_workspace_size(WAN_OP_GN_SILU,
  *              N, T, H, W, C, 0, groups)).
- *   stats      the buffer filled by wan_causal_conv3d_gn_stats for this x (Cout = C, same groups);
- *              stats_bytes >= wan_workspace_size(WAN_OP_GN_STATS, ...) (else WAN_ERR_INVALID_ARG).
+ *   stats      the buffer filled by wan_causal_conv3d_gn_stats, wan_causal_conv3d_gn_input_stats or
+ *              wan_causal_conv3d_winograd_stats for this x (Cout = C, same groups); stats_bytes at
+ *              least the size that call required. Below the smallest size any of them writes for
+ *              these sizes the call returns WAN_ERR_INVALID_ARG; a buffer whose header names more
+ *              records than stats_bytes holds is reported by wan_device_status.
  */
 wan_status wan_gn_silu_from_stats(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta,
                                   int N, int T, int H, int W, int C, int groups, float eps,
@@ -477,9 +481,23 @@ wan_status wan_resblock_shortcut(const wan_bf16* x, wan_bf16* out, const wan_res
  *   Values: the transformed input and weights must fit fp16 (|values| below about 16000 at the
  *   input, which GroupNorm + SiLU outputs are for any gamma, beta of moderate size).
  *
+ * wan_causal_conv3d_winograd_stats: wan_causal_conv3d_winograd (y and cache_out bit for bit the
+ *   same) whose output transform also writes the GroupNorm statistics of y for `groups` groups:
+ *   per (frame, group, 2x2 output tile) the float-float sums of d and d^2 of d = y - s over the
+ *   tile's pixels and the group's channels, s being one value of the group there, with s and the
+ *   count, and a header with the number of tiles. As with wan_causal_conv3d_gn_stats the layout
+ *   is private: pass the buffer to wan_gn_silu_from_stats or wan_gn_silu_coefficients_from_stats
+ *   with the same N, T, H, W, C = Cout and groups.
+ *     groups  divides Cout; the channels per group are a power of two from 4 to 64 (else
+ *             WAN_ERR_UNSUPPORTED_SHAPE).
+ *     stats   >= wan_workspace_size(WAN_OP_GN_STATS_WINOGRAD, N, T, H, W, Cin, Cout, groups) bytes,
+ *             16-byte aligned, caller-owned; it may not overlap the tensors, coef or ws.
+ *
  * wan_resblock_winograd: wan_resblock with both convolutions through Winograd (u1, u2 from
  *   wan_winograd_weights of w1, w2; p->w1 and p->w2 are not read). Same definition, caches and
- *   conditions as wan_resblock, and C % 256 == 0.
+ *   conditions as wan_resblock, and C % 256 == 0. The second norm's coefficients come from the
+ *   statistics conv 1 writes with h (as wan_gn_silu_coefficients_from_stats computes them) when
+ *   C / groups is a power of two from 4 to 64, else from a pass over h.
  *     ws  >= wan_workspace_size(WAN_OP_RESBLOCK_WINOGRAD, N, T, H, W, C, C, groups) bytes.
  */
 wan_status wan_winograd_weights(const wan_bf16* w, wan_fp16* u, int Cin, int Cout, void* stream);
@@ -487,6 +505,11 @@ wan_status wan_causal_conv3d_winograd(const wan_bf16* a, const void* coef, const
                                       wan_bf16* cache_out, const wan_fp16* u, const wan_bf16* bias,
                                       const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W,
                                       int Cin, int Cout, void* ws, size_t ws_bytes, void* stream);
+wan_status wan_causal_conv3d_winograd_stats(const wan_bf16* a, const void* coef, const wan_bf16* cache_in,
+                                            wan_bf16* cache_out, const wan_fp16* u, const wan_bf16* bias,
+                                            const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W,
+                                            int Cin, int Cout, int groups, void* stats, size_t stats_bytes,
+                                            void* ws, size_t ws_bytes, void* stream);
 wan_status wan_resblock_winograd(const wan_bf16* x, wan_bf16* out, const wan_resblock_params* p,
                                  const wan_fp16* u1, const wan_fp16* u2, wan_bf16* cache1, wan_bf16* cache2,
                                  int cache_valid, int N, int T, int H, int W, int C, void* ws,

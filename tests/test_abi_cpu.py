@@ -68,6 +68,19 @@ def test_workspace_sizes(L):
     gn64 = b.wan_workspace_size(b.WAN_OP_GN_SILU, 1, 4, 16, 16, 64, 0, 32)
     assert b.wan_workspace_size(b.WAN_OP_GN_SILU_CONV3D, 1, 4, 16, 16, 64, 64, 32) == a256(gn64) + 4 * 16 * 16 * 64 * 2
     assert b.wan_workspace_size(b.WAN_OP_GN_SILU_CONV3D, 1, 4, 16, 16, 60, 64, 32) == 0  # groups do not divide Cin
+    # statistics from the Winograd output transform: a 256-byte header, then a float4 + float2 per
+    # (frame, group, 2x2 output tile); the Winograd ResBlock holds one such buffer for h
+    assert b.wan_workspace_size(b.WAN_OP_GN_STATS_WINOGRAD, 1, 4, 44, 78, 1024, 1024, 32) == 256 + 4 * 32 * (22 * 39) * 24
+    assert b.wan_workspace_size(b.WAN_OP_GN_STATS_WINOGRAD, 1, 2, 1, 1, 64, 256, 32) == 256 + 2 * 32 * 1 * 24
+    assert b.wan_workspace_size(b.WAN_OP_GN_STATS_WINOGRAD, 1, 4, 16, 16, 64, 320, 32) == 0    # Cout % 256 != 0
+    assert b.wan_workspace_size(b.WAN_OP_GN_STATS_WINOGRAD, 1, 4, 16, 16, 64, 256, 128) == 0   # 2 channels per group
+    assert b.wan_workspace_size(b.WAN_OP_GN_STATS_WINOGRAD, 1, 4, 16, 16, 64, 512, 4) == 0     # 128 channels per group
+    rbw = b.wan_workspace_size(b.WAN_OP_RESBLOCK_WINOGRAD, 1, 4, 44, 78, 1024, 1024, 32)
+    parts = (a256(4 * 44 * 78 * 1024 * 2) + a256(4 * 1024 * 16) +
+             a256(b.wan_workspace_size(b.WAN_OP_GN_STATS_WINOGRAD, 1, 4, 44, 78, 1024, 1024, 32)) +
+             a256(b.wan_workspace_size(b.WAN_OP_GN_SILU, 1, 4, 44, 78, 1024, 0, 32)) +
+             b.wan_workspace_size(b.WAN_OP_WINOGRAD_CONV3D, 1, 4, 44, 78, 1024, 1024, 0))
+    assert rbw == parts
     # the ResBlock: h, then the norm-into-conv workspace shared by its two convs
     assert b.wan_workspace_size(b.WAN_OP_RESBLOCK, 1, 4, 16, 16, 256, 256, 32) == \
         4 * 16 * 16 * 256 * 2 + b.wan_workspace_size(b.WAN_OP_GN_SILU_CONV3D, 1, 4, 16, 16, 256, 256, 32)
@@ -144,6 +157,29 @@ def test_fused_gn_statistics_calls_reject_invalid(L):
     assert g(*gn, 1, 2, 16, 16, 64, 32, 1e-6, A * 13, big, A * 11, big, None) == 2     # C % 256 != 0
     assert g(*gn, 1, 2, 16, 16, 256, 32, 1e-6, A * 13, 64, A * 11, big, None) == 1     # buffer too small
     assert g(*gn, 1, 2, 16, 16, 256, 32, 1e-6, A * 13, big, None, 0, None) == 4        # no workspace
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers are only passed where no GPU exists")
+def test_winograd_statistics_call_rejects_invalid(L):
+    f = L.wan_causal_conv3d_winograd_stats
+    # a, coef, cache_in, cache_out, u, bias, residual, y; then sizes, groups, stats, its bytes, ws, its bytes
+    ok = (A, None, None, None, A * 3, None, None, A * 5)
+    sz = (1, 2, 16, 16, 64, 256)
+    big = 1 << 30
+    st, ws = A * 64, A * 32
+    assert f(*ok, *sz, 32, st, big, ws, big, None) == 5       # every argument accepted: no device to run on
+    assert f(*ok, 1, 2, 16, 16, 64, 320, 32, st, big, ws, big, None) == 2   # Cout % 256 != 0
+    assert f(*ok, *sz, 128, st, big, ws, big, None) == 2      # 2 channels per group
+    assert f(*ok, *sz, 0, st, big, ws, big, None) == 1        # no groups
+    assert f(*ok, *sz, 32, None, big, ws, big, None) == 1     # no statistics buffer
+    assert f(*ok, *sz, 32, MIS, big, ws, big, None) == 3      # misaligned statistics buffer
+    assert f(*ok, *sz, 32, st, 64, ws, big, None) == 1        # statistics buffer too small
+    assert f(*ok, *sz, 32, A * 5, big, ws, big, None) == 1    # statistics overlapping y
+    assert f(*ok, *sz, 32, st, big, None, 0, None) == 4       # no workspace
+    g = L.wan_gn_silu_coefficients_from_stats
+    # 1 x 1 frames: the Winograd statistics (one record per frame and group) are the smallest
+    assert g(st, 256 + 2 * 32 * 24 - 1, A * 3, A * 5, 1, 2, 1, 1, 256, 32, 1e-6, A * 7, None) == 1
+    assert g(st, 256 + 2 * 32 * 24, A * 3, A * 5, 1, 2, 1, 1, 256, 32, 1e-6, A * 7, None) == 5
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers are only passed where no GPU exists")

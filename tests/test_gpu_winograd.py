@@ -135,3 +135,89 @@ def test_resblock_winograd_matches_oracle(wan):
     conv_close(np.concatenate([bits(o) for o in outs], 1), np.concatenate([r_a, r_b], 1), "winograd resblock")
     assert int(oracle.ulp_distance_bf16(bits(c1), r1).max()) <= 1
     cache2_close(bits(c2), r2, "winograd resblock cache 2")
+
+
+# ---- GroupNorm statistics from the output transform ----------------------------------------------
+
+def _coef_values(coef):
+    """The (S_hi, S_lo, B_hi, B_lo) quadruples as fp64 S = S_hi + S_lo, B = B_hi + B_lo."""
+    q = coef.view(torch.float32).cpu().numpy().astype(np.float64).reshape(-1, 4)
+    return q[:, 0] + q[:, 1], q[:, 2] + q[:, 3]
+
+
+def _norm(C, name):
+    return synth.normal_f32((C,), 0, f"{name}/gamma", 1.0, 0.1), synth.normal_f32((C,), 0, f"{name}/beta", 0.0, 0.1)
+
+
+@pytest.mark.parametrize("shape,Cout,groups,coef,cache,residual", [
+    ((1, 3, 9, 11, 64), 256, 32, True, True, False),      # odd H and W: tiles of 1 to 4 pixels; 8 per group
+    ((2, 2, 5, 7, 64), 512, 32, False, False, True),      # batch 2, 16 channels per group, residual
+    ((1, 2, 12, 20, 1024), 1024, 32, True, True, True),   # the widest stage's channels: 32 per group
+    ((1, 2, 6, 10, 64), 256, 64, True, False, False),     # 4 per group: one lane per group
+    ((1, 2, 6, 10, 64), 256, 4, True, False, False),      # 64 per group: 16 lanes per group
+    ((1, 2, 1, 1, 64), 256, 32, True, True, False),       # 1 x 1 frames: one record per frame and group
+])
+def test_winograd_statistics(wan, shape, Cout, groups, coef, cache, residual):
+    name = f"wino/stats/{shape}/{Cout}/{groups}"
+    x, w, g, be, c, b, r = make(shape, Cout, name, coef, cache, True, residual)
+    N, T, H, W, Cin = shape
+    xd, u = to_dev(x), wan.wan_winograd_weights(to_dev(w))
+    k1 = wan.wan_gn_silu_coefficients(xd, f32_dev(g), f32_dev(be), G, EPS) if coef else None
+    cd, bd, rd = (None if v is None else to_dev(v) for v in (c, b, r))
+    c_plain = torch.empty((N, 2, H, W, Cin), dtype=torch.bfloat16, device="cuda")
+    c_st = torch.empty_like(c_plain)
+    y_plain = wan.wan_causal_conv3d_winograd(xd, u, k1, bd, rd, cd, c_plain)
+    y, st = wan.wan_causal_conv3d_winograd_stats(xd, u, groups, k1, bd, rd, cd, c_st)
+    torch.cuda.synchronize()
+    assert wan.wan_device_status() == 0
+    assert torch.equal(y.view(torch.int16), y_plain.view(torch.int16))  # the statistics change nothing
+    assert torch.equal(c_st.view(torch.int16), c_plain.view(torch.int16))
+    # the next norm's coefficients from them against its own pass over y
+    g2, be2 = _norm(Cout, f"{name}/n2")
+    k_st = wan.wan_gn_silu_coefficients_from_stats(st, f32_dev(g2), f32_dev(be2), y.shape, groups, EPS)
+    k_pass = wan.wan_gn_silu_coefficients(y, f32_dev(g2), f32_dev(be2), groups, EPS)
+    torch.cuda.synchronize()
+    assert wan.wan_device_status() == 0
+    s_st, b_st = _coef_values(k_st)
+    s_p, b_p = _coef_values(k_pass)
+    assert np.max(np.abs(s_st - s_p) / np.abs(s_p)) < 1e-6
+    assert np.max(np.abs(b_st - b_p) / (np.abs(b_p) + np.abs(s_p))) < 1e-6
+    # the norm applied from them: within one bf16 ulp of the oracle's GroupNorm + SiLU of y
+    out = wan.wan_gn_silu_from_stats(y, f32_dev(g2), f32_dev(be2), groups, EPS, st)
+    torch.cuda.synchronize()
+    assert wan.wan_device_status() == 0
+    ref = oracle.gn_silu(bits(y), g2, be2, groups, EPS)
+    assert int(oracle.ulp_distance_bf16(bits(out), ref).max()) <= 1
+
+
+def test_winograd_statistics_chunked_equals_unchunked(wan):
+    shape, Cout, groups = (1, 6, 10, 14, 64), 256, 32
+    x, w, g, be, _, b, _ = make(shape, Cout, "wino/stats/chunks", True, False, True, False)
+    g2, be2 = _norm(Cout, "wino/stats/chunks/n2")
+    xd, u, bd = to_dev(x), wan.wan_winograd_weights(to_dev(w)), to_dev(b)
+
+    def call(xs, cin, cout):
+        k = wan.wan_gn_silu_coefficients(xs, f32_dev(g), f32_dev(be), G, EPS)
+        y, st = wan.wan_causal_conv3d_winograd_stats(xs, u, groups, k, bd, None, cin, cout)
+        return wan.wan_gn_silu_coefficients_from_stats(st, f32_dev(g2), f32_dev(be2), y.shape, groups, EPS)
+    full = call(xd, None, torch.empty((1, 2, 10, 14, 64), dtype=torch.bfloat16, device="cuda"))
+    caches = [torch.empty((1, 2, 10, 14, 64), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    parts = [call(xd[:, :3].contiguous(), None, caches[0]), call(xd[:, 3:].contiguous(), caches[0], caches[1])]
+    torch.cuda.synchronize()
+    assert wan.wan_device_status() == 0
+    assert torch.equal(torch.cat(parts), full)
+
+
+def test_winograd_statistics_of_other_sizes_are_refused(wan):
+    # Statistics of 24 x 40 frames (240 tiles per frame and group) read as those of 12 x 20
+    # frames: refused, the coefficients untouched.
+    x, w, g, be, _, b, _ = make((1, 2, 24, 40, 64), 256, "wino/stats/other", False, False, True, False)
+    _, st = wan.wan_causal_conv3d_winograd_stats(to_dev(x), wan.wan_winograd_weights(to_dev(w)), 32, None,
+                                                 to_dev(b))
+    torch.cuda.synchronize()
+    assert wan.wan_device_status() == 0
+    k = torch.full((1 * 2 * 256 * 16,), 7, dtype=torch.uint8, device="cuda")
+    g2, be2 = _norm(256, "wino/stats/other/n2")
+    wan.wan_gn_silu_coefficients_from_stats(st, f32_dev(g2), f32_dev(be2), (1, 2, 12, 20, 256), 32, EPS, k)
+    assert wan.wan_device_status() == 1  # WAN_ERR_INVALID_ARG
+    assert bool((k == 7).all())

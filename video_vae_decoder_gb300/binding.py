@@ -23,6 +23,7 @@ WAN_OP_GN_SILU_CONV3D = 5
 WAN_OP_RESBLOCK_SHORTCUT = 6
 WAN_OP_WINOGRAD_CONV3D = 7
 WAN_OP_RESBLOCK_WINOGRAD = 8
+WAN_OP_GN_STATS_WINOGRAD = 9
 
 STATUS = {0: "WAN_OK", 1: "WAN_ERR_INVALID_ARG", 2: "WAN_ERR_UNSUPPORTED_SHAPE", 3: "WAN_ERR_MISALIGNED",
           4: "WAN_ERR_WORKSPACE", 5: "WAN_ERR_CUDA", 6: "WAN_ERR_TIMEOUT"}
@@ -34,7 +35,8 @@ EXPORTS = ("wan_status_string", "wan_workspace_size", "wan_gn_silu", "wan_gn_sil
            "wan_causal_conv3d_gn_input_stats", "wan_gn_silu_coefficients_from_stats",
            "wan_time_upsample", "wan_conv1x1", "wan_fold_bias", "wan_resblock_shortcut",
            "wan_upsample_phase_weights", "wan_upsample_phase_conv", "wan_resblock", "wan_winograd_weights",
-           "wan_causal_conv3d_winograd", "wan_resblock_winograd", "wan_selftest_wait_timeout",
+           "wan_causal_conv3d_winograd", "wan_causal_conv3d_winograd_stats", "wan_resblock_winograd",
+           "wan_selftest_wait_timeout",
            "wan_device_status")
 
 
@@ -112,6 +114,8 @@ def lib() -> ctypes.CDLL:
     L.wan_winograd_weights.argtypes = [P, P, I, I, P]
     L.wan_causal_conv3d_winograd.restype = I
     L.wan_causal_conv3d_winograd.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, S, P]
+    L.wan_causal_conv3d_winograd_stats.restype = I
+    L.wan_causal_conv3d_winograd_stats.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, P, S, P, S, P]
     L.wan_resblock_winograd.restype = I
     L.wan_resblock_winograd.argtypes = [P, P, ctypes.POINTER(ResblockParams), P, P, P, P, I, I, I, I, I, I, P, S, P]
     L.wan_selftest_wait_timeout.restype = I
@@ -494,6 +498,30 @@ def wan_causal_conv3d_winograd(a, u, coef=None, bias=None, residual=None, cache_
                                             _ptr(residual), _ptr(y), N, T, H, W, Cin, Cout, _ptr(ws), need,
                                             _stream(stream)), "wan_causal_conv3d_winograd")
     return y
+
+
+def wan_causal_conv3d_winograd_stats(a, u, groups: int, coef=None, bias=None, residual=None, cache_in=None,
+                                     cache_out=None, y=None, stats=None, ws=None, stream=None):
+    """wan_causal_conv3d_winograd that also emits the GroupNorm statistics of y (for `groups` groups)
+    for wan_gn_silu_coefficients_from_stats / wan_gn_silu_from_stats. Returns (y, stats)."""
+    for t, n in ((a, "a"), (bias, "bias"), (residual, "residual"), (cache_in, "cache_in"), (cache_out, "cache_out")):
+        _need(t, torch.bfloat16, n)
+    _need(u, torch.float16, "u")
+    N, T, H, W, Cin = a.shape
+    Cout = u.shape[1]
+    y = torch.empty((N, T, H, W, Cout), dtype=torch.bfloat16, device=a.device) if y is None else y
+    _need(y, torch.bfloat16, "y")
+    need = wan_workspace_size(WAN_OP_WINOGRAD_CONV3D, N, T, H, W, Cin, Cout, 0)
+    ws = _workspace(need, a.device, ws)
+    st_need = wan_workspace_size(WAN_OP_GN_STATS_WINOGRAD, N, T, H, W, Cin, Cout, groups)
+    if st_need == 0:
+        raise WanError(2, "wan_causal_conv3d_winograd_stats")
+    stats = _workspace(st_need, a.device, stats)
+    _check(lib().wan_causal_conv3d_winograd_stats(_ptr(a), _ptr(coef), _ptr(cache_in), _ptr(cache_out), _ptr(u),
+                                                  _ptr(bias), _ptr(residual), _ptr(y), N, T, H, W, Cin, Cout, groups,
+                                                  _ptr(stats), stats.numel() * stats.element_size(), _ptr(ws), need,
+                                                  _stream(stream)), "wan_causal_conv3d_winograd_stats")
+    return y, stats
 
 
 def wan_resblock_winograd(x, params, u1, u2, cache1, cache2, cache_valid, groups: int, eps: float, out=None, ws=None,

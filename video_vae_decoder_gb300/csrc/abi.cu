@@ -182,11 +182,15 @@ size_t wan_workspace_size(wan_op op, int N, int T, int H, int W, int Cin, int Co
     case WAN_OP_WINOGRAD_CONV3D:
       if (!wino_supported(Cin, Cout)) return 0;
       return wino_workspace(N, T, H, W, Cin, Cout);
-    case WAN_OP_RESBLOCK_WINOGRAD: {  // h, the coefficients, the norm's workspace, the conv's
+    case WAN_OP_RESBLOCK_WINOGRAD: {  // h, the coefficients, h's statistics, the norm's workspace, the conv's
       if (groups <= 0 || Cin % groups || !gn_silu_supported(Cin, groups) || !wino_supported(Cin, Cin)) return 0;
       return align256((size_t)N * T * H * W * Cin * sizeof(wan_bf16)) + align256((size_t)N * T * Cin * 16) +
+             (wino_gn_stats_supported(Cin, groups) ? align256(wino_gn_stats_bytes(N, T, H, W, groups)) : 0) +
              align256(gn_silu_workspace(N, T, H, W, Cin, groups, sm_count())) + wino_workspace(N, T, H, W, Cin, Cin);
     }
+    case WAN_OP_GN_STATS_WINOGRAD:
+      if (!wino_gn_stats_supported(Cout, groups)) return 0;
+      return wino_gn_stats_bytes(N, T, H, W, groups);
     case WAN_OP_RESBLOCK_SHORTCUT: {  // h, the shortcut, then the norm-into-conv workspace
       if (Cout <= 0 || groups <= 0 || Cin % groups || Cout % groups || !gn_silu_supported(Cin, groups) ||
           !gn_silu_supported(Cout, groups))
@@ -228,6 +232,24 @@ wan_status wan_gn_silu_clip(const wan_bf16* x, wan_bf16* y, const float* gamma, 
                                     static_cast<cudaStream_t>(stream), true, nullptr, true));
 }
 
+}  // extern "C"
+
+namespace {
+
+// The smallest statistics buffer a producer (the pair conv in either tiling, or the Winograd
+// output transform) writes for these sizes; the finalize kernel checks the record count in the
+// header against the buffer's length before it reads a record.
+size_t gn_stats_min_bytes(int N, int T, int H, int W, int groups) {
+  int q_a, q_b;
+  conv_gn_stats_records(H, W, &q_a, &q_b);
+  const int q = std::min(std::min(q_a, q_b), wino_gn_stats_records(H, W));
+  return kGnStatsHeader + (size_t)N * T * groups * q * (sizeof(float4) + sizeof(float2));
+}
+
+}  // namespace
+
+extern "C" {
+
 wan_status wan_gn_silu_from_stats(const wan_bf16* x, wan_bf16* y, const float* gamma, const float* beta, int N,
                                   int T, int H, int W, int C, int groups, float eps, const void* stats,
                                   size_t stats_bytes, void* ws, size_t ws_bytes, void* stream) {
@@ -237,7 +259,7 @@ wan_status wan_gn_silu_from_stats(const wan_bf16* x, wan_bf16* y, const float* g
   if (!stats) return WAN_ERR_INVALID_ARG;
   if (!conv_gn_stats_supported(C, groups)) return WAN_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(stats)) return WAN_ERR_MISALIGNED;
-  if (stats_bytes < conv_gn_stats_bytes(N, T, H, W, C, groups)) return WAN_ERR_INVALID_ARG;
+  if (stats_bytes < gn_stats_min_bytes(N, T, H, W, groups)) return WAN_ERR_INVALID_ARG;
   const size_t bytes = (size_t)N * T * H * W * C * sizeof(wan_bf16);
   if (overlap(x, bytes, y, bytes)) return WAN_ERR_INVALID_ARG;
   const size_t need = wan_workspace_size(WAN_OP_GN_SILU, N, T, H, W, C, 0, groups);
@@ -267,7 +289,7 @@ wan_status wan_gn_silu_coefficients_from_stats(const void* stats, size_t stats_b
   if (!conv_gn_stats_supported(C, groups) || !gn_silu_supported(C, groups) || !fits(N, T, H, W, C))
     return WAN_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(stats) || !aligned16(coef) || !aligned16(gamma) || !aligned16(beta)) return WAN_ERR_MISALIGNED;
-  if (stats_bytes < conv_gn_stats_bytes(N, T, H, W, C, groups)) return WAN_ERR_INVALID_ARG;
+  if (stats_bytes < gn_stats_min_bytes(N, T, H, W, groups)) return WAN_ERR_INVALID_ARG;
   const size_t cbytes = (size_t)N * T * C * 16;
   if (overlap(stats, stats_bytes, coef, cbytes)) return WAN_ERR_INVALID_ARG;
   unsigned* err = device_error_word();
@@ -697,11 +719,16 @@ wan_status wan_winograd_weights(const wan_bf16* w, wan_fp16* u, int Cin, int Cou
   return cuda_status(wino_weights_launch(w, u, Cin, Cout, sm_count(), static_cast<cudaStream_t>(stream)));
 }
 
-wan_status wan_causal_conv3d_winograd(const wan_bf16* a, const void* coef, const wan_bf16* cache_in,
-                                      wan_bf16* cache_out, const wan_fp16* u, const wan_bf16* bias,
-                                      const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W, int Cin,
-                                      int Cout, void* ws, size_t ws_bytes, void* stream) {
-  WAN_CALL_RANGE();
+}  // extern "C"
+
+namespace {
+
+// The Winograd conv behind wan_causal_conv3d_winograd and wan_causal_conv3d_winograd_stats
+// (stats: null, or a statistics buffer of stats_bytes for `groups` groups, checked here).
+wan_status winograd_conv(const wan_bf16* a, const void* coef, const wan_bf16* cache_in, wan_bf16* cache_out,
+                         const wan_fp16* u, const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T,
+                         int H, int W, int Cin, int Cout, void* ws, size_t ws_bytes, void* stats, size_t stats_bytes,
+                         int groups, void* stream) {
   wan_status st = check_conv(a, u, y, N, T, H, W, Cin, Cout);
   if (st != WAN_OK) return st;
   if (!wino_supported(Cin, Cout) || Cin > 2048) return WAN_ERR_UNSUPPORTED_SHAPE;
@@ -719,6 +746,15 @@ wan_status wan_causal_conv3d_winograd(const wan_bf16* a, const void* coef, const
     return WAN_ERR_INVALID_ARG;
   if (!ws || ws_bytes < need) return WAN_ERR_WORKSPACE;
   if (!aligned16(ws)) return WAN_ERR_MISALIGNED;
+  if (stats) {
+    if (!wino_gn_stats_supported(Cout, groups)) return WAN_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned16(stats)) return WAN_ERR_MISALIGNED;
+    if (stats_bytes < wino_gn_stats_bytes(N, T, H, W, groups) || overlap(stats, stats_bytes, a, abytes) ||
+        overlap(stats, stats_bytes, y, ybytes) || overlap(stats, stats_bytes, residual, ybytes) ||
+        overlap(stats, stats_bytes, cache_in, cbytes) || overlap(stats, stats_bytes, cache_out, cbytes) ||
+        overlap(stats, stats_bytes, ws, need) || overlap(stats, stats_bytes, coef, (size_t)N * T * Cin * 16))
+      return WAN_ERR_INVALID_ARG;
+  }
   unsigned* err = device_error_word();
   if (!err) return WAN_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -729,10 +765,34 @@ wan_status wan_causal_conv3d_winograd(const wan_bf16* a, const void* coef, const
   if (direct && T == 1) e = cache_keep_last(cache_in, cache_out, N, H, W, Cin, s);
   if (e == cudaSuccess)
     e = wino_conv_launch(a, cf, cache_in, u, bias, residual, y, N, T, H, W, Cin, Cout, ws, sm_count(), err, s,
-                         direct ? cache_out : nullptr);
+                         direct ? cache_out : nullptr, stats, groups);
   if (e != cudaSuccess || !cache_out || direct) return cuda_status(e);
   if (cf) return cuda_status(gn_cache_update(a, cf, cache_in, cache_out, N, T, H, W, Cin, sm_count(), s));
   return cuda_status(cache_update_launch(a, cache_in, cache_out, N, T, H, W, Cin, sm_count(), s));
+}
+
+}  // namespace
+
+extern "C" {
+
+wan_status wan_causal_conv3d_winograd(const wan_bf16* a, const void* coef, const wan_bf16* cache_in,
+                                      wan_bf16* cache_out, const wan_fp16* u, const wan_bf16* bias,
+                                      const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W, int Cin,
+                                      int Cout, void* ws, size_t ws_bytes, void* stream) {
+  WAN_CALL_RANGE();
+  return winograd_conv(a, coef, cache_in, cache_out, u, bias, residual, y, N, T, H, W, Cin, Cout, ws, ws_bytes,
+                       nullptr, 0, 0, stream);
+}
+
+wan_status wan_causal_conv3d_winograd_stats(const wan_bf16* a, const void* coef, const wan_bf16* cache_in,
+                                            wan_bf16* cache_out, const wan_fp16* u, const wan_bf16* bias,
+                                            const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W,
+                                            int Cin, int Cout, int groups, void* stats, size_t stats_bytes, void* ws,
+                                            size_t ws_bytes, void* stream) {
+  WAN_CALL_RANGE();
+  if (!stats || groups <= 0) return WAN_ERR_INVALID_ARG;
+  return winograd_conv(a, coef, cache_in, cache_out, u, bias, residual, y, N, T, H, W, Cin, Cout, ws, ws_bytes,
+                       stats, stats_bytes, groups, stream);
 }
 
 wan_status wan_resblock_winograd(const wan_bf16* x, wan_bf16* out, const wan_resblock_params* p, const wan_fp16* u1,
@@ -764,18 +824,27 @@ wan_status wan_resblock_winograd(const wan_bf16* x, wan_bf16* out, const wan_res
   char* base = static_cast<char*>(ws);
   wan_bf16* h = reinterpret_cast<wan_bf16*>(base);
   float4* coef = reinterpret_cast<float4*>(base + align256(bytes));
-  void* gws = base + align256(bytes) + align256((size_t)N * T * C * 16);
+  char* stats = base + align256(bytes) + align256((size_t)N * T * C * 16);
+  const bool chain = wino_gn_stats_supported(C, p->groups);  // h's statistics from conv 1
+  const size_t stats_bytes = chain ? wino_gn_stats_bytes(N, T, H, W, p->groups) : 0;
+  void* gws = stats + align256(stats_bytes);
   void* wws = static_cast<char*>(gws) + align256(gn_silu_workspace(N, T, H, W, C, p->groups, sms));
   const wan_bf16* c1_in = cache_valid ? cache1 : nullptr;
   const wan_bf16* c2_in = cache_valid ? cache2 : nullptr;
   // Each norm's coefficients, the Winograd conv applying them to its input tiles, then the
-  // norm's last two frames into that conv's cache (after the conv has read the old ones).
+  // norm's last two frames into that conv's cache (after the conv has read the old ones). The
+  // second norm's coefficients come from the statistics conv 1's output transform wrote with h.
   cudaError_t e = gn_silu_launch(x, nullptr, p->gamma1, p->beta1, N, T, H, W, C, p->groups, p->eps, gws, sms, s,
                                  false, coef);
-  if (e == cudaSuccess) e = wino_conv_launch(x, coef, c1_in, u1, p->b1, nullptr, h, N, T, H, W, C, C, wws, sms, err, s);
+  if (e == cudaSuccess)
+    e = wino_conv_launch(x, coef, c1_in, u1, p->b1, nullptr, h, N, T, H, W, C, C, wws, sms, err, s, nullptr,
+                         chain ? stats : nullptr, p->groups);
   if (e == cudaSuccess) e = gn_cache_update(x, coef, c1_in, cache1, N, T, H, W, C, sms, s);
   if (e == cudaSuccess)
-    e = gn_silu_launch(h, nullptr, p->gamma2, p->beta2, N, T, H, W, C, p->groups, p->eps, gws, sms, s, false, coef);
+    e = chain ? gn_coef_from_stats_launch(stats, stats_bytes, p->gamma2, p->beta2, N, T, H, W, C, p->groups, p->eps,
+                                          coef, true, err, s)
+              : gn_silu_launch(h, nullptr, p->gamma2, p->beta2, N, T, H, W, C, p->groups, p->eps, gws, sms, s, false,
+                               coef);
   if (e == cudaSuccess) e = wino_conv_launch(h, coef, c2_in, u2, p->b2, x, out, N, T, H, W, C, C, wws, sms, err, s);
   if (e == cudaSuccess) e = gn_cache_update(h, coef, c2_in, cache2, N, T, H, W, C, sms, s);
   return cuda_status(e);

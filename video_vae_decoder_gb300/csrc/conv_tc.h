@@ -31,7 +31,8 @@ cudaError_t conv_pair_launch(int mode, const wan_bf16* a, const wan_bf16* cache_
 // GroupNorm statistics of the causal conv's output, emitted by the CTA-pair kernel's epilogue
 // (Cout a multiple of 256, channels per group a power of two from 4 to 64; with or without the
 // operand prologue). The buffer: a header of kGnStatsHeader bytes whose first int is q, the
-// records per (frame, group) (pixel tiles x 4 epilogue warps of the launch that wrote them), then
+// records per (frame, group) (pixel tiles x 4 epilogue warps of the launch that wrote them; the
+// Winograd output transform writes the same layout with one record per 2x2 output tile), then
 // per (frame, group, part < q) the float-float sums of d and d^2 of d = y - s as a float4, then
 // the (s, count) pairs as float2 in the same order.
 constexpr size_t kGnStatsHeader = 256;

@@ -44,6 +44,7 @@
 #include "common.cuh"
 #include "conv_tc.h"
 #include "gn_silu.h"
+#include "winograd.h"
 
 namespace wan {
 
@@ -535,7 +536,8 @@ __global__ void __launch_bounds__(kThreads + 32, 2) gn_silu_kernel(const GnArgs 
   }
 }
 
-// Coefficients from the conv epilogue's statistics: one CTA per (frame, group). Its threads take
+// Coefficients from the statistics a conv emitted with its output (the pair conv's epilogue or the
+// Winograd output transform; the same record layout): one CTA per (frame, group). Its threads take
 // the group's records q = t, t + 256, ... in order, each moved exactly to record 0's shift s in
 // float-float (dl = s_q - s by TwoSum, n dl by an FMA product error):
 //   sum (x - s) = S1_q + n dl,  sum (x - s)^2 = S2_q + dl (2 S1_q + n dl),
@@ -545,13 +547,14 @@ constexpr int kStatThreads = 256;
 constexpr int kStatBatch = 8;  // records in flight per thread
 
 __global__ void __launch_bounds__(kStatThreads) gn_coef_from_stats_kernel(const char* __restrict__ stats, int q_max,
-                                                                          int q_a, int q_b, const float* __restrict__ gamma,
+                                                                          int q_a, int q_b, int q_c,
+                                                                          const float* __restrict__ gamma,
                                                                           const float* __restrict__ beta, float4* coef,
                                                                           int F, int C, int G, double inv_len, float eps,
                                                                           int blocked, unsigned* err) {
   __shared__ float red[kStatThreads / 32][4];
   const int q = __ldcg(reinterpret_cast<const int*>(stats));
-  if (q <= 0 || q > q_max || (q != q_a && q != q_b)) {  // not statistics of these sizes
+  if (q <= 0 || q > q_max || (q != q_a && q != q_b && q != q_c)) {  // not statistics of these sizes
     if (threadIdx.x == 0) atomicOr(err, kDevErrBadStats);
     return;
   }
@@ -738,11 +741,12 @@ cudaError_t gn_coef_from_stats_launch(const void* stats, size_t stats_bytes, con
   const long long F = (long long)N * T;
   const long long pairs = F * G;
   if (pairs >= (1LL << 31) || stats_bytes < kGnStatsHeader) return cudaErrorInvalidValue;
-  int q_a, q_b;  // the record counts of the two tilings the conv may have used
+  int q_a, q_b;  // the record counts of the two tilings the pair conv may have used
   conv_gn_stats_records(H, W, &q_a, &q_b);
+  const int q_c = wino_gn_stats_records(H, W);  // and of the Winograd output transform
   const long long q_max = (long long)((stats_bytes - kGnStatsHeader) / ((size_t)pairs * (sizeof(float4) + sizeof(float2))));
   gn_coef_from_stats_kernel<<<(unsigned)pairs, kStatThreads, 0, stream>>>(
-      static_cast<const char*>(stats), (int)std::min<long long>(q_max, 1 << 30), q_a, q_b, gamma, beta, coef, (int)F, C,
+      static_cast<const char*>(stats), (int)std::min<long long>(q_max, 1 << 30), q_a, q_b, q_c, gamma, beta, coef, (int)F, C,
       G, 1.0 / ((double)H * W * (C / G)), eps, blocked ? 1 : 0, err);
   return cudaGetLastError();
 }

@@ -34,6 +34,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "conv_tc.h"
 #include "tma_host.h"
 #include "winograd.h"
 
@@ -446,10 +447,27 @@ struct WinoOutArgs {
   wan_bf16* y;
   int H, W, Cout, Wt, tiles;
   long long mrows, total;   // mrows = N T tiles; total = mrows Cout / 4
+  // GroupNorm statistics of y (optional): per (frame, group, tile) the float-float sums of d and
+  // d^2 of d = y - s over the tile's pixels and the group's 2^st_lg channels (st_rec), and (s,
+  // count) (st_meta), s the group's first channel at the tile's first pixel; st_hdr receives the
+  // records per (frame, group), the tile count.
+  float4* st_rec;
+  float2* st_meta;
+  int* st_hdr;
+  int st_lg, st_groups;
 };
 
-__global__ void __launch_bounds__(256) wino_output_kernel(const WinoOutArgs a) {
+// kStats: the launch writes the GroupNorm statistics of y (a.st_rec set). The plain instance fits
+// three CTAs per SM in 80 registers; the statistics instance takes two, in 115 registers: held to
+// 80 it spilled 150 bytes a thread and ran 12 us slower at [1, 4, 44, 78, 1024], against 1.5 us
+// for the lower occupancy.
+template <bool kStats>
+__global__ void __launch_bounds__(256, kStats ? 2 : 3) wino_output_kernel(const WinoOutArgs a) {
   const int cq = a.Cout / 4;
+  const int lane = threadIdx.x & 31;
+  if (kStats && blockIdx.x == 0 && threadIdx.x == 0) *a.st_hdr = a.tiles;
+  // A warp's 32 threads take 32 consecutive channel quads of one tile (cq is a multiple of 32 and
+  // so is every index the loop visits), so a group's quads are neighbouring lanes of one warp.
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < a.total;
        idx += (long long)gridDim.x * blockDim.x) {
     const int q = (int)(idx % cq);
@@ -489,6 +507,14 @@ __global__ void __launch_bounds__(256) wino_output_kernel(const WinoOutArgs a) {
       bv[2] = bf16lo_to_f32(b.y);
       bv[3] = bf16hi_to_f32(b.y);
     }
+    // GroupNorm statistics of the stored values (kStats): each lane sums d and d^2 over its 4
+    // channels of the tile's pixels in fp32 as it stores them (a sum of at most 16 deviations of
+    // bf16 values, exact unless they lie about 12 binades apart); sh is the group's first channel
+    // at the tile's first pixel, which every tile has.
+    const int lpg = kStats ? (1 << a.st_lg) >> 2 : 1;  // lanes per group
+    const int first = lane & ~(lpg - 1);
+    float sh = 0.f, s1 = 0.f, s2 = 0.f;
+    int npx = 0;
 #pragma unroll
     for (int pa = 0; pa < 2; ++pa) {
       const int hh = 2 * ti + pa;
@@ -520,8 +546,36 @@ __global__ void __launch_bounds__(256) wino_output_kernel(const WinoOutArgs a) {
           v[2] += bf16lo_to_f32(r.y);
           v[3] += bf16hi_to_f32(r.y);
         }
-        *reinterpret_cast<uint2*>(a.y + px * a.Cout + (size_t)q * 4) =
-            make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+        const uint2 o = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+        *reinterpret_cast<uint2*>(a.y + px * a.Cout + (size_t)q * 4) = o;
+        if (kStats) {
+          if (pa == 0 && pb == 0) sh = __shfl_sync(0xffffffffu, bf16lo_to_f32(o.x), first);
+          ++npx;
+          const float d[4] = {bf16lo_to_f32(o.x) - sh, bf16hi_to_f32(o.x) - sh, bf16lo_to_f32(o.y) - sh,
+                              bf16hi_to_f32(o.y) - sh};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            s1 += d[k];
+            s2 = fmaf(d[k], d[k], s2);
+          }
+        }
+      }
+    }
+    if (kStats) {
+      // The group's lanes add their sums as float-float pairs in a fixed butterfly order; the
+      // group's first lane writes the record.
+      float h1 = s1, l1 = 0.f, h2 = s2, l2 = 0.f;
+      for (int off = 1; off < lpg; off <<= 1) {
+        const float oh1 = __shfl_xor_sync(0xffffffffu, h1, off), ol1 = __shfl_xor_sync(0xffffffffu, l1, off);
+        const float oh2 = __shfl_xor_sync(0xffffffffu, h2, off), ol2 = __shfl_xor_sync(0xffffffffu, l2, off);
+        ff_add(h1, l1, oh1, ol1);
+        ff_add(h2, l2, oh2, ol2);
+      }
+      if (lane == first) {
+        const int g = (4 * q) >> a.st_lg;
+        const size_t rec = ((size_t)f * a.st_groups + g) * a.tiles + tile;
+        __stcg(a.st_rec + rec, make_float4(h1, l1, h2, l2));
+        __stcg(a.st_meta + rec, make_float2(sh, (float)(npx << a.st_lg)));
       }
     }
   }
@@ -572,6 +626,18 @@ int grid_for(long long work, int sms, int per_sm) {
 
 bool wino_supported(int Cin, int Cout) { return Cin > 0 && Cout > 0 && Cin % 64 == 0 && Cout % kWN == 0; }
 
+bool wino_gn_stats_supported(int Cout, int groups) {
+  if (groups <= 0 || Cout <= 0 || Cout % kWN != 0 || Cout % groups != 0) return false;
+  const int cg = Cout / groups;  // a group's quads are 1 .. 16 neighbouring lanes of a warp
+  return cg >= 4 && cg <= 64 && (cg & (cg - 1)) == 0;
+}
+
+int wino_gn_stats_records(int H, int W) { return ((H + 1) / 2) * ((W + 1) / 2); }
+
+size_t wino_gn_stats_bytes(int N, int T, int H, int W, int groups) {
+  return kGnStatsHeader + (size_t)N * T * groups * wino_gn_stats_records(H, W) * (sizeof(float4) + sizeof(float2));
+}
+
 size_t wino_workspace(int N, int T, int H, int W, int Cin, int Cout) {
   const WinoPlan p = wplan(N, T, H, W, Cin, Cout);
   return p.v_bytes + p.m_bytes;
@@ -587,8 +653,9 @@ cudaError_t wino_weights_launch(const wan_bf16* w, uint16_t* u, int Cin, int Cou
 cudaError_t wino_conv_launch(const wan_bf16* a, const float4* coef, const wan_bf16* cache_in, const uint16_t* u,
                              const wan_bf16* bias, const wan_bf16* residual, wan_bf16* y, int N, int T, int H, int W,
                              int Cin, int Cout, void* ws, int sms, unsigned* err, cudaStream_t s,
-                             wan_bf16* cache_out) {
+                             wan_bf16* cache_out, void* st_buf, int st_groups) {
   if (!wino_supported(Cin, Cout) || (cache_out && cache_out == cache_in)) return cudaErrorInvalidValue;
+  if (st_buf && !wino_gn_stats_supported(Cout, st_groups)) return cudaErrorInvalidValue;
   const WinoPlan p = wplan(N, T, H, W, Cin, Cout);
   uint16_t* v = static_cast<uint16_t*>(ws);
   float* mbuf = reinterpret_cast<float*>(static_cast<char*>(ws) + p.v_bytes);
@@ -656,7 +723,22 @@ cudaError_t wino_conv_launch(const wan_bf16* a, const float4* coef, const wan_bf
   oa.tiles = p.tiles;
   oa.mrows = p.mrows;
   oa.total = p.mrows * (Cout / 4);
-  wino_output_kernel<<<grid_for(oa.total, sms, 8), 256, 0, s>>>(oa);
+  oa.st_rec = nullptr;
+  oa.st_meta = nullptr;
+  oa.st_hdr = nullptr;
+  oa.st_lg = 0;
+  oa.st_groups = 0;
+  if (st_buf) {
+    oa.st_hdr = static_cast<int*>(st_buf);
+    oa.st_rec = reinterpret_cast<float4*>(static_cast<char*>(st_buf) + kGnStatsHeader);
+    oa.st_meta = reinterpret_cast<float2*>(oa.st_rec + (size_t)N * T * st_groups * p.tiles);
+    oa.st_groups = st_groups;
+    while ((1 << oa.st_lg) < Cout / st_groups) ++oa.st_lg;
+  }
+  if (st_buf)
+    wino_output_kernel<true><<<grid_for(oa.total, sms, 8), 256, 0, s>>>(oa);
+  else
+    wino_output_kernel<false><<<grid_for(oa.total, sms, 8), 256, 0, s>>>(oa);
   return cudaGetLastError();
 }
 
