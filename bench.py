@@ -563,9 +563,10 @@ def run_ours(args, rank, world, dev):
         hbm_kernel("gn_silu_decode_mid", per_launch("gn"), wl.gn_bytes, tot("gn"))
     # DRAM bytes (read + write) per launch from `ncu --set full` captures of the current build of
     # each kernel (profiles/); the head's from a single-pass capture of the 16-frame launch; the
-    # Winograd conv's is its three kernels' sum.
+    # Winograd conv's is its three kernels' sum, averaged over the stage's four calls (three of
+    # them writing statistics, two with the residual).
     traffic = {"conv_c256": 172.575744e6 + 125.743872e6, "gn_coef_c256": 112.540416e6 + 3.522304e6,
-               "gn_coef_c1024": 28.202496e6, "conv_c1024_winograd": None,
+               "gn_coef_c1024": 28.202496e6, "conv_c1024_winograd": 161.323e6 + 447.922e6 + 243.859e6,
                "upsample_phase_conv": 22.554112e6 + 4.61184e6, "gn_silu_decode_mid": 68.827392e6 + 11.028992e6,
                "head_256_to_12": 9.9e9 + 0.343e9}
     rooflines = []
