@@ -81,6 +81,11 @@ def test_workspace_sizes(L):
              a256(b.wan_workspace_size(b.WAN_OP_GN_SILU, 1, 4, 44, 78, 1024, 0, 32)) +
              b.wan_workspace_size(b.WAN_OP_WINOGRAD_CONV3D, 1, 4, 44, 78, 1024, 1024, 0))
     assert rbw == parts
+    # 2 channels per group: no statistics buffer (its second norm takes a pass over h)
+    rbw2 = b.wan_workspace_size(b.WAN_OP_RESBLOCK_WINOGRAD, 1, 4, 44, 78, 256, 256, 128)
+    assert rbw2 == (a256(4 * 44 * 78 * 256 * 2) + a256(4 * 256 * 16) +
+                    a256(b.wan_workspace_size(b.WAN_OP_GN_SILU, 1, 4, 44, 78, 256, 0, 128)) +
+                    b.wan_workspace_size(b.WAN_OP_WINOGRAD_CONV3D, 1, 4, 44, 78, 256, 256, 0))
     # the ResBlock: h, then the norm-into-conv workspace shared by its two convs
     assert b.wan_workspace_size(b.WAN_OP_RESBLOCK, 1, 4, 16, 16, 256, 256, 32) == \
         4 * 16 * 16 * 256 * 2 + b.wan_workspace_size(b.WAN_OP_GN_SILU_CONV3D, 1, 4, 16, 16, 256, 256, 32)

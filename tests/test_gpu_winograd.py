@@ -118,7 +118,12 @@ def test_winograd_chunked_equals_unchunked(wan):
     assert wan.wan_device_status() == 0
 
 
-def test_resblock_winograd_matches_oracle(wan):
+@pytest.mark.parametrize("groups", [
+    32,    # 8 channels per group: the second norm from conv 1's statistics
+    64,    # 4 per group: the statistics with one lane per group
+    128,   # 2 per group: no statistics at this width, the second norm from a pass over h
+])
+def test_resblock_winograd_matches_oracle(wan, groups):
     # Two chunks (2 + 2 frames) of a C=256 ResBlock with both convs through Winograd.
     x = synth.normal_bf16((1, 4, 12, 20, 256), 0, "wino/rb/x")
     p = synth.resblock_params(256, 0, "wino/rb")
@@ -126,12 +131,12 @@ def test_resblock_winograd_matches_oracle(wan):
     u1, u2 = wan.wan_winograd_weights(pd["w1"]), wan.wan_winograd_weights(pd["w2"])
     c1 = torch.zeros((1, 2, 12, 20, 256), dtype=torch.bfloat16, device="cuda")
     c2 = torch.zeros_like(c1)
-    outs = [wan.wan_resblock_winograd(to_dev(np.ascontiguousarray(x[:, s:s + 2])), pd, u1, u2, c1, c2, s > 0, G, EPS)
-            for s in (0, 2)]
+    outs = [wan.wan_resblock_winograd(to_dev(np.ascontiguousarray(x[:, s:s + 2])), pd, u1, u2, c1, c2, s > 0, groups,
+                                      EPS) for s in (0, 2)]
     torch.cuda.synchronize()
     assert wan.wan_device_status() == 0
-    r_a, r1, r2 = oracle.resblock(x[:, :2], p, G, EPS)
-    r_b, r1, r2 = oracle.resblock(x[:, 2:], p, G, EPS, r1, r2)
+    r_a, r1, r2 = oracle.resblock(x[:, :2], p, groups, EPS)
+    r_b, r1, r2 = oracle.resblock(x[:, 2:], p, groups, EPS, r1, r2)
     conv_close(np.concatenate([bits(o) for o in outs], 1), np.concatenate([r_a, r_b], 1), "winograd resblock")
     assert int(oracle.ulp_distance_bf16(bits(c1), r1).max()) <= 1
     cache2_close(bits(c2), r2, "winograd resblock cache 2")
@@ -156,6 +161,7 @@ def _norm(C, name):
     ((1, 2, 6, 10, 64), 256, 64, True, False, False),     # 4 per group: one lane per group
     ((1, 2, 6, 10, 64), 256, 4, True, False, False),      # 64 per group: 16 lanes per group
     ((1, 2, 1, 1, 64), 256, 32, True, True, False),       # 1 x 1 frames: one record per frame and group
+    ((1, 1, 6, 10, 64), 256, 32, True, True, True),       # one frame with history and residual
 ])
 def test_winograd_statistics(wan, shape, Cout, groups, coef, cache, residual):
     name = f"wino/stats/{shape}/{Cout}/{groups}"
