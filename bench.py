@@ -543,8 +543,14 @@ def run_ours(args, rank, world, dev):
         tensor_kernel("conv_c1024_winograd", cm, wino_flops(1, 4, 44, 78, 1024, 1024), tot("c1024.conv"))
         kernels["conv_c1024_winograd"]["direct_equivalent_tflops"] = conv_flops(1, 4, 44, 78, 1024, 1024) / cm / 1e9
         hbm_kernel("gn_coef_c1024", per_launch("c1024.coef"), 2.0 * wl.x5.numel(), tot("c1024.coef"))
-        # the later norms' coefficients from the statistics the Winograd convs emitted
-        kernels["gn_coef_from_stats_c1024"] = {"ms": per_launch("c1024.coefst"), "total_ms": tot("c1024.coefst")}
+        # the later norms' coefficients from the statistics the Winograd convs emitted: one CTA per
+        # (frame, group) reading its records (24 B each, one per 2x2 tile), bound by latency rather
+        # than by a roofline, so it stays out of `rooflines`
+        sm = per_launch("c1024.coefst")
+        st_bytes = 24.0 * wl.x5.shape[0] * wl.x5.shape[1] * GROUPS * ((wl.x5.shape[2] + 1) // 2) * \
+            ((wl.x5.shape[3] + 1) // 2)
+        kernels["gn_coef_from_stats_c1024"] = {"ms": sm, "gbs": st_bytes / sm / 1e6 if sm else 0.0,
+                                               "total_ms": tot("c1024.coefst"), "bound": "latency"}
         kernels["resblock_c1024_ms"] = (tot("c1024.coef") + tot("c1024.coefst") + tot("c1024.conv")) / 2.0
     if "head.conv" in per_tag:
         # Bound by whichever takes longer at the measured peaks: its useful MMAs or its HBM bytes.
