@@ -795,9 +795,10 @@ def main():
         return
 
     import torch
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)  # before the process group, so every rank's NCCL work uses its own GPU
     if world > 1:
         torch.distributed.init_process_group("nccl")
-    dev = torch.device("cuda", local)
     from video_vae_decoder_gb300 import binding
     binding.lib()
     if args.adjacent_only:
