@@ -227,3 +227,27 @@ def test_winograd_statistics_of_other_sizes_are_refused(wan):
     wan.wan_gn_silu_coefficients_from_stats(st, f32_dev(g2), f32_dev(be2), (1, 2, 12, 20, 256), 32, EPS, k)
     assert wan.wan_device_status() == 1  # WAN_ERR_INVALID_ARG
     assert bool((k == 7).all())
+
+
+def test_winograd_statistics_with_a_large_mean(wan):
+    # Outputs around 1000 (a bias of mean 1000) against a spread of about one: the sums only stay
+    # exact because every record is taken around a value of its own group and moved to one shift.
+    shape, Cout, groups = (1, 2, 9, 11, 64), 256, 32
+    x, w, g, be, c, _, _ = make(shape, Cout, "wino/stats/mean", True, True, False, False)
+    b = synth.normal_bf16((Cout,), 0, "wino/stats/mean/b", 1000.0, 1.0)
+    xd, u = to_dev(x), wan.wan_winograd_weights(to_dev(w))
+    k1 = wan.wan_gn_silu_coefficients(xd, f32_dev(g), f32_dev(be), G, EPS)
+    y, st = wan.wan_causal_conv3d_winograd_stats(xd, u, groups, k1, to_dev(b), None, to_dev(c))
+    g2, be2 = _norm(Cout, "wino/stats/mean/n2")
+    k_st = wan.wan_gn_silu_coefficients_from_stats(st, f32_dev(g2), f32_dev(be2), y.shape, groups, EPS)
+    k_pass = wan.wan_gn_silu_coefficients(y, f32_dev(g2), f32_dev(be2), groups, EPS)
+    out = wan.wan_gn_silu_from_stats(y, f32_dev(g2), f32_dev(be2), groups, EPS, st)
+    torch.cuda.synchronize()
+    assert wan.wan_device_status() == 0
+    assert float(oracle.bf16_to_f64(bits(y)).mean()) > 900.0
+    s_st, b_st = _coef_values(k_st)
+    s_p, b_p = _coef_values(k_pass)
+    assert np.max(np.abs(s_st - s_p) / np.abs(s_p)) < 1e-6
+    assert np.max(np.abs(b_st - b_p) / (np.abs(b_p) + np.abs(s_p))) < 1e-6
+    ref = oracle.gn_silu(bits(y), g2, be2, groups, EPS)
+    assert int(oracle.ulp_distance_bf16(bits(out), ref).max()) <= 1
