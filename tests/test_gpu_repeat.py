@@ -36,6 +36,23 @@ def test_repeat_resblock_c256_chunk(wan):
     assert wan.wan_device_status() == 0
 
 
+def test_repeat_resblock_winograd_c1024(wan):
+    # The widest stage's block through Winograd, its second norm from conv 1's statistics.
+    C = 1024
+    x = n((1, 4, 44, 78, C), "rep/w/x")
+    p = {k: (torch.from_numpy(v).cuda() if v.dtype == np.float32 else
+             torch.from_numpy(v.view(np.int16).copy()).view(torch.bfloat16).cuda())
+         for k, v in synth.resblock_params(C, 0, "rep/w/block").items()}
+    u1, u2 = wan.wan_winograd_weights(p["w1"]), wan.wan_winograd_weights(p["w2"])
+    c = n((1, 2, 44, 78, C), "rep/w/c")
+
+    def run():
+        c1, c2 = c.clone(), c.clone()
+        return wan.wan_resblock_winograd(x, p, u1, u2, c1, c2, True, 32, EPS)
+    assert same(run)
+    assert wan.wan_device_status() == 0
+
+
 def test_repeat_conv_c1024_split(wan):
     C = 1024
     x = n((1, 4, 44, 78, C), "rep/x5")
